@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 FP32 SGEMM: GFLOP/s on the 2048^3 workload.
+
+One step is one sgemm_run call (C = A*B, row-major FP32, 2*M*N*K flops) on
+inputs already resident in HBM.  L2 is flushed (a 256 MiB write) before every
+step and each GEMM is timed with CUDA events on the stream it runs on.  The
+line printed also carries:
+  roofline      the GEMM kernel against the FP32 FFMA peak (alu bound), with
+                the same-run FFMA probe beside it;
+  e2e           the same metric through sgemm_run_host: host->device copies of
+                A and B, the GEMM and the device->host copy of C, per step;
+  cpu_baseline  the CPU oracle timed on this host's cores on a bounded sample
+                of the same workload;
+  secondary     the 4092^3 (alpha=0.5, beta=2) workload, timed the same way;
+  clocks        SM clocks sampled with nvidia-smi during the timed region.
+
+--impl reference times the CPU oracle instead (rank 0 only).
+Several GPUs (torchrun) run independent replicas: no data exchange.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import datagen  # noqa: E402
+
+WORKLOADS = {
+    "s2_2048": "sgemm 2048x2048x2048 fp32 row-major alpha=1 beta=0 A,B U[-1,1)",
+    "s3_4092": "sgemm 4092x4092x4092 fp32 row-major alpha=0.5 beta=2 A,B,C U[-1,1)",
+    "s4_rect": "sgemm 8192x6144x2048 fp32 row-major alpha=1 beta=0 A,B N(0,1)",
+    "s5_odd": "sgemm 1023x1025x513 fp32 row-major alpha=1 beta=0 A,B N(0,1)",
+    "s6_skinny": "sgemm 16x8192x8192 fp32 row-major alpha=1 beta=0 A,B U[-1,1)",
+    "s1_128": "sgemm 128x128x128 fp32 row-major alpha=1 beta=0 A,B U[-1,1)",
+}
+METRIC = "SGEMM GFLOP/s at 4092^3 and 2048^3 FP32; % of GB300 FP32 FFMA peak"
+SMS_GB300 = 152
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2070.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def nominal_fp32_tflops(sms=SMS_GB300, mhz=SM_MAX_MHZ):
+    return sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def flops_of(cfg):
+    return 2.0 * cfg["M"] * cfg["N"] * cfg["K"]
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline object)
+# --------------------------------------------------------------------------
+
+def time_oracle(name, budget_s=12.0, threads=0):
+    """Time the oracle on the first R rows of workload `name`, R grown until
+    about budget_s of wall time is spent (or the whole matrix is done)."""
+    import oracle
+
+    cfg, A, B, C = datagen.config_inputs(name)
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    nthreads = threads or oracle.default_threads()
+    rows = min(M, max(nthreads, 1))
+    total_rows = 0
+    elapsed = 0.0
+    start_row = 0
+    while elapsed < budget_s and start_row < M:
+        take = min(rows, M - start_row)
+        idx = np.arange(start_row, start_row + take)
+        t0 = time.perf_counter()
+        oracle.sgemm_ref_flat(M, N, K, cfg["alpha"], A, K, B, N, cfg["beta"], C, N,
+                              rows=idx, threads=nthreads, want_absprod=False)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        total_rows += take
+        start_row += take
+        if dt < budget_s / 8:
+            rows = min(M, rows * 2)
+    gflops = 2.0 * total_rows * N * K / elapsed / 1e9
+    return {
+        "value": round(gflops, 3), "unit": "GFLOP/s", "cores": int(nthreads), "kind": "oracle",
+        "sample": f"first {total_rows} of {M} rows of {name} ({M}x{N}x{K}), fp64 triple loop, "
+                  f"{elapsed:.1f} s wall on {nthreads} threads",
+    }
+
+
+# --------------------------------------------------------------------------
+# Clock sampling
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.out = None
+        self.gpu_index = gpu_index
+
+    def __enter__(self):
+        try:
+            import tempfile
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.flush()
+        self.out.seek(0)
+        lines = [l.strip() for l in self.out.read().splitlines() if l.strip()]
+        path = self.out.name
+        self.out.close()
+        try:
+            os.remove(path)
+        except OSError:
+            pass
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = sorted(sm)[len(sm) // 2:] or sm  # upper half: the samples under load
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def gpu_arm(args, ws, rank, local):
+    import torch
+
+    import dense_fp32_sgemm_gb300 as sg
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sg.build()
+    sg.library()
+
+    def device_inputs(name):
+        cfg, A, B, C = datagen.config_inputs(name)
+        M, N, K = cfg["M"], cfg["N"], cfg["K"]
+        dA = torch.from_numpy(A).to(dev)
+        dB = torch.from_numpy(B).to(dev)
+        dC = torch.from_numpy(C).to(dev) if C is not None else torch.zeros(M * N, device=dev)
+        return cfg, A, B, C, dA, dB, dC
+
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(cfg, dA, dB, dC):
+        st = sg.sgemm_run(cfg["M"], cfg["N"], cfg["K"], cfg["alpha"], dA.data_ptr(), cfg["K"],
+                          dB.data_ptr(), cfg["N"], cfg["beta"], dC.data_ptr(), cfg["N"],
+                          stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError("sgemm_run: " + sg.status_string(st))
+
+    def timed(cfg, dA, dB, dC, steps, warmup, C0=None):
+        for _ in range(warmup):
+            step(cfg, dA, dB, dC)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for e0, e1 in evs:
+            flush.fill_(1.0)  # evict A, B and C from L2 between steps
+            e0.record(stream)
+            step(cfg, dA, dB, dC)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        if ws > 1:
+            torch.distributed.barrier()
+        st = sg.device_status(stream)
+        if st != 0:
+            raise RuntimeError("device status: " + sg.status_string(st))
+        durs = [e0.elapsed_time(e1) / 1e3 for e0, e1 in evs]
+        return durs, wall
+
+    def ffma_probe(seconds_target, paired):
+        sink = torch.zeros(4096, device=dev)
+        blocks = SMS_GB300 * 4
+        iters = 200
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # calibrate
+        sg.probe_ffma(paired, iters, blocks, sink.data_ptr(), stream)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        fl = sg.probe_ffma(paired, iters, blocks, sink.data_ptr(), stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dt = e0.elapsed_time(e1) / 1e3
+        iters = max(200, int(iters * min(seconds_target, 2.0) / max(dt, 1e-6)))
+        best = 0.0
+        rates = []
+        t_end = time.perf_counter() + seconds_target
+        while True:
+            e0.record(stream)
+            fl = sg.probe_ffma(paired, iters, blocks, sink.data_ptr(), stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            r = fl / (e0.elapsed_time(e1) / 1e3) / 1e12
+            rates.append(r)
+            best = max(best, r)
+            if time.perf_counter() > t_end:
+                break
+        return {"burst": round(best, 3), "sustained": round(statistics.median(rates), 3)}
+
+    gpu_index = 0
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis and vis.split(",")[local].strip().isdigit():
+        gpu_index = int(vis.split(",")[local])
+
+    # ---- primary workload ----
+    name = args.workload
+    cfg, A, B, C, dA, dB, dC = device_inputs(name)
+    flops = flops_of(cfg)
+    with ClockSampler(gpu_index) as clk:
+        durs, wall = timed(cfg, dA, dB, dC, args.steps, args.warmup)
+    clocks = clk.summary()
+    mean_s = sum(durs) / len(durs)
+    # max over ranks of the summed GEMM time
+    total = torch.tensor([sum(durs)], device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(total, op=torch.distributed.ReduceOp.MAX)
+    value = ws * args.steps * flops / float(total.item()) / 1e9
+
+    plan = sg.plan_describe(cfg["M"], cfg["N"], cfg["K"], a_addr=dA.data_ptr(),
+                            b_addr=dB.data_ptr(), c_addr=dC.data_ptr(), beta=cfg["beta"])
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean_s * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOADS[name], "M": cfg["M"], "N": cfg["N"], "K": cfg["K"],
+                   "alpha": cfg["alpha"], "beta": cfg["beta"], "seed": datagen.CONFIG_SEEDS[name],
+                   "l2": "flushed before every step (256 MiB write); GEMM timed per step "
+                         "with CUDA events",
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "plan": plan.get("variant"), "grid": int(plan.get("grid", 0))},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if args.quick:
+        return result, rank
+
+    # ---- probes: same process, run as long as the timed GEMMs ----
+    probe_s = max(2.0, min(10.0, 2.0 * wall))
+    ffma = ffma_probe(probe_s, False)
+    ffma2 = ffma_probe(probe_s, True)
+    probe_peak = max(ffma["sustained"], ffma2["sustained"])
+    achieved = flops / mean_s / 1e12
+    peak = nominal_fp32_tflops()
+    result["roofline"] = {
+        "bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
+        "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+        "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz (max SM clock)",
+        "probe": {"ffma_tflops": ffma, "ffma2_tflops": ffma2,
+                  "frac_of_probe": round(achieved / probe_peak, 4)},
+        "kernel": "sgemm_tile_kernel" if plan.get("variant") in ("tile", "streamk")
+        else plan.get("variant"),
+    }
+
+    # ---- secondary workload: 4092^3 ----
+    if name != "s3_4092" and not args.no_secondary:
+        cfg2, _, _, C2, dA2, dB2, dC2 = device_inputs("s3_4092")
+        C2dev = dC2.clone()
+        durs2, _ = timed(cfg2, dA2, dB2, dC2, max(3, args.steps // 4), args.warmup)
+        m2 = sum(durs2) / len(durs2)
+        a2 = flops_of(cfg2) / m2 / 1e12
+        result["secondary"] = {
+            "workload": WORKLOADS["s3_4092"], "value": round(flops_of(cfg2) / m2 / 1e9, 2),
+            "unit": "GFLOP/s", "ms_per_step": round(m2 * 1e3, 4),
+            "frac_of_peak": round(a2 / peak, 4), "frac_of_probe": round(a2 / probe_peak, 4),
+            "note": "C is updated in place each step (beta=2), so values grow; the timing "
+                    "is unaffected",
+        }
+        del dA2, dB2, dC2, C2dev
+
+    # ---- end to end through the host entry point ----
+    pA = torch.from_numpy(A.reshape(cfg["M"], cfg["K"])).pin_memory()
+    pB = torch.from_numpy(B.reshape(cfg["K"], cfg["N"])).pin_memory()
+    pC = torch.zeros(cfg["M"], cfg["N"]).pin_memory()
+    for _ in range(2):
+        sg.run_host(pA, pB, pC, cfg["alpha"], cfg["beta"])
+    e2e_steps = max(3, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        sg.run_host(pA, pB, pC, cfg["alpha"], cfg["beta"])
+    e2e_wall = time.perf_counter() - t0
+    h2d = 4 * (cfg["M"] * cfg["K"] + cfg["K"] * cfg["N"]
+               + (cfg["M"] * cfg["N"] if cfg["beta"] != 0 else 0))
+    result["e2e"] = {"value": round(e2e_steps * flops / e2e_wall / 1e9, 2), "unit": "GFLOP/s",
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * cfg["M"] * cfg["N"],
+                     "steps": e2e_steps, "api": "sgemm_run_host (pinned host buffers)"}
+
+    # ---- CPU baseline (rank 0 only) ----
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = time_oracle(name, budget_s=args.cpu_seconds)
+    return result, rank
+
+
+def reference_arm(args, ws, rank):
+    if rank != 0:
+        return None
+    name = args.workload
+    cfg = datagen.CONFIGS[name]
+    samples = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        info = time_oracle(name, budget_s=max(1.0, args.cpu_seconds / max(args.steps, 1)))
+        if i >= args.warmup:
+            samples.append(info["value"])
+    value = statistics.mean(samples)
+    flops = flops_of(cfg)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(flops / (value * 1e9) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOADS[name], "M": cfg["M"], "N": cfg["N"], "K": cfg["K"],
+                   "alpha": cfg["alpha"], "beta": cfg["beta"],
+                   "note": "each step times a bounded row sample of the workload; "
+                           "ms_per_step is extrapolated to the whole product"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GFLOP/s", "cores": info["cores"],
+                         "kind": "oracle", "sample": info["sample"]},
+        "e2e": {"value": round(value, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="s2_2048")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the 4092^3 line")
+    ap.add_argument("--quick", action="store_true",
+                    help="only the timed GEMM steps (for profiler runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch
+        import torch.distributed as tdist
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+        else:
+            torch.cuda.set_device(local)
+            tdist.init_process_group("nccl")
+
+    if args.impl == "reference":
+        out = reference_arm(args, ws, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+
+    result, rank = gpu_arm(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as tdist
+        tdist.barrier()
+        tdist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

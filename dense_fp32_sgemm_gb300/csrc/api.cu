@@ -1,0 +1,410 @@
+// C ABI of the SGEMM library (declared in include/sgemm.h): argument checks,
+// per-device state, workspace, TMA descriptors and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/sgemm.h"
+#include "../../include/sgemm_probe.h"
+#include "kernels.h"
+#include "plan.h"
+
+namespace sgemm {
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // one second
+
+std::atomic<int> g_force_variant{-1};
+std::atomic<int> g_force_splits{0};
+std::atomic<unsigned long long> g_timeout_ns{0};
+std::atomic<int> g_skip_loads_from{-1};
+std::atomic<int> g_fma_mode{kFmaPairDupA};
+std::atomic<int> g_stages{3};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct Workspace {
+    float *partials = nullptr;
+    size_t partial_bytes = 0;
+    int *counters = nullptr;
+    size_t counter_count = 0;
+};
+
+struct HostBuffers {
+    float *A = nullptr, *B = nullptr, *C = nullptr;
+    size_t a_bytes = 0, b_bytes = 0, c_bytes = 0;
+};
+
+struct DeviceState {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    int *err = nullptr;  // device error word
+    std::map<cudaStream_t, Workspace> ws;
+    HostBuffers host;
+    unsigned configured = 0;  // bit per (fma_mode, stages) tile configuration
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_dev;
+EncodeTiledFn g_encode = nullptr;
+
+sgemm_status_t status_from(cudaError_t e) { return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH; }
+
+// Per-device state, created on first use with that device current.
+sgemm_status_t device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_NO_DEVICE;
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SGEMM_ERR_NO_DEVICE;
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        if (d.supported) {
+            if (cudaMalloc(&d.err, sizeof(int)) != cudaSuccess) return SGEMM_ERR_ALLOC;
+            if (cudaMemset(d.err, 0, sizeof(int)) != cudaSuccess) return SGEMM_ERR_ALLOC;
+        }
+        d.ready = true;
+    }
+    if (!d.supported) return SGEMM_ERR_NO_DEVICE;
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return SGEMM_ERR_TMA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *out = &d;
+    return SGEMM_OK;
+}
+
+sgemm_status_t ensure_workspace(DeviceState &d, cudaStream_t stream, size_t partial_bytes,
+                                size_t counters, Workspace **out) {
+    Workspace &w = d.ws[stream];
+    if (w.partial_bytes < partial_bytes) {
+        if (w.partials) cudaFree(w.partials);
+        w.partials = nullptr;
+        w.partial_bytes = 0;
+        if (cudaMalloc(&w.partials, partial_bytes) != cudaSuccess) return SGEMM_ERR_ALLOC;
+        w.partial_bytes = partial_bytes;
+    }
+    if (w.counter_count < counters) {
+        if (w.counters) cudaFree(w.counters);
+        w.counters = nullptr;
+        w.counter_count = 0;
+        if (cudaMalloc(&w.counters, counters * sizeof(int)) != cudaSuccess) return SGEMM_ERR_ALLOC;
+        if (cudaMemset(w.counters, 0, counters * sizeof(int)) != cudaSuccess) return SGEMM_ERR_ALLOC;
+        w.counter_count = counters;
+    }
+    *out = &w;
+    return SGEMM_OK;
+}
+
+// Row-major rows x cols FP32 matrix with leading dimension ld (elements),
+// box of box_rows x box_cols, zero fill outside the matrix.
+sgemm_status_t encode_2d(CUtensorMap *map, const float *base, int64_t rows, int64_t cols,
+                         int64_t ld, int box_cols, int box_rows) {
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SGEMM_OK : SGEMM_ERR_TMA;
+}
+
+sgemm_status_t validate(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                        const float *B, int64_t ldb, float beta, const float *C, int64_t ldc) {
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+        return SGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (!C || (reinterpret_cast<uintptr_t>(C) & 3u)) return SGEMM_ERR_INVALID_ARG;
+    if (K > 0 && alpha != 0.0f) {
+        if (!A || !B) return SGEMM_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(B) & 3u))
+            return SGEMM_ERR_INVALID_ARG;
+    }
+    (void)beta;
+    return SGEMM_OK;
+}
+
+sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                          int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                          int64_t ldc, cudaStream_t stream, DeviceState &d) {
+    PlanInput in;
+    in.M = M; in.N = N; in.K = K; in.lda = lda; in.ldb = ldb; in.ldc = ldc;
+    in.a_addr = reinterpret_cast<uintptr_t>(A);
+    in.b_addr = reinterpret_cast<uintptr_t>(B);
+    in.c_addr = reinterpret_cast<uintptr_t>(C);
+    in.alpha = alpha; in.beta = beta;
+    in.num_sms = d.num_sms;
+    in.force_variant = g_force_variant.load();
+    in.force_splits = g_force_splits.load();
+    Plan pl;
+    if (make_plan(in, &pl) != 0) return SGEMM_ERR_INVALID_ARG;
+
+    switch (pl.variant) {
+        case kVarNone:
+            return SGEMM_OK;
+        case kVarScale:
+            return status_from(launch_scale((int)M, (int)N, beta, C, ldc, stream));
+        case kVarGeneric: {
+            GenericParams gp;
+            gp.M = (int)M; gp.N = (int)N; gp.K = (int)K;
+            gp.alpha = alpha; gp.beta = beta;
+            gp.A = A; gp.lda = lda; gp.B = B; gp.ldb = ldb; gp.C = C; gp.ldc = ldc;
+            return status_from(launch_generic(gp, stream));
+        }
+        case kVarTile:
+        case kVarStreamK: {
+            const int fm = g_fma_mode.load(), st = g_stages.load();
+            const unsigned bit = 1u << (fm * 8 + st);
+            if (!(d.configured & bit)) {
+                if (tile_configure(fm, st) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+                d.configured |= bit;
+            }
+            CUtensorMap mapA, mapB;
+            sgemm_status_t s = encode_2d(&mapA, A, M, K, lda, kTileBK, kTileBM);
+            if (s != SGEMM_OK) return s;
+            s = encode_2d(&mapB, B, K, N, ldb, kTileBN, kTileBK);
+            if (s != SGEMM_OK) return s;
+            TileParams tp;
+            tp.M = (int)M; tp.N = (int)N; tp.K = (int)K;
+            tp.tiles_m = pl.tiles_m; tp.tiles_n = pl.tiles_n; tp.kt_total = pl.kt_total;
+            tp.dp_tiles = pl.dp_tiles; tp.sk_tiles = pl.sk_tiles; tp.sk_share = pl.sk_share;
+            tp.group_m = pl.group_m;
+            tp.alpha = alpha; tp.beta = beta; tp.C = C; tp.ldc = ldc; tp.c_vec4 = pl.c_vec4;
+            tp.partials = nullptr; tp.counters = nullptr;
+            tp.err = d.err;
+            const unsigned long long to = g_timeout_ns.load();
+            tp.timeout_ns = to ? to : kDefaultTimeoutNs;
+            tp.skip_loads_from = g_skip_loads_from.load();
+            if (pl.sk_tiles > 0) {
+                Workspace *w = nullptr;
+                const size_t pbytes = (size_t)2 * pl.grid * kTileBM * kTileBN * sizeof(float);
+                s = ensure_workspace(d, stream, pbytes, (size_t)pl.sk_tiles, &w);
+                if (s != SGEMM_OK) return s;
+                tp.partials = w->partials;
+                tp.counters = w->counters;
+            }
+            return status_from(launch_tile(fm, st, mapA, mapB, tp, pl.grid, stream));
+        }
+        default:
+            return SGEMM_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+}  // namespace sgemm
+
+using namespace sgemm;
+
+extern "C" {
+
+sgemm_status_t sgemm_run(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                         int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                         int64_t ldc, void *stream) {
+    const sgemm_status_t v = validate(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    if (v != SGEMM_OK) return v;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState *d = nullptr;
+    const sgemm_status_t s = device_state(&d);
+    if (s != SGEMM_OK) return s;
+    return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                      static_cast<cudaStream_t>(stream), *d);
+}
+
+sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                              int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                              int64_t ldc, void *stream) {
+    sgemm_status_t v = validate(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    if (v != SGEMM_OK) return v;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState *d = nullptr;
+    sgemm_status_t s = device_state(&d);
+    if (s != SGEMM_OK) return s;
+    HostBuffers &hb = d->host;
+    const bool need_ab = K > 0 && alpha != 0.0f;
+    // Device copies use tight leading dimensions (the row lengths, rounded up
+    // to 4 elements so rows stay 16-byte aligned).
+    const int64_t dlda = (K + 3) / 4 * 4, dldb = (N + 3) / 4 * 4, dldc = (N + 3) / 4 * 4;
+    auto grow = [](float **p, size_t *have, size_t want) -> bool {
+        if (*have >= want) return true;
+        if (*p) cudaFree(*p);
+        *p = nullptr;
+        *have = 0;
+        if (cudaMalloc(p, want) != cudaSuccess) return false;
+        *have = want;
+        return true;
+    };
+    const size_t a_bytes = need_ab ? (size_t)M * dlda * 4 : 0;
+    const size_t b_bytes = need_ab ? (size_t)K * dldb * 4 : 0;
+    const size_t c_bytes = (size_t)M * dldc * 4;
+    if (!grow(&hb.A, &hb.a_bytes, a_bytes ? a_bytes : 16) ||
+        !grow(&hb.B, &hb.b_bytes, b_bytes ? b_bytes : 16) || !grow(&hb.C, &hb.c_bytes, c_bytes))
+        return SGEMM_ERR_ALLOC;
+    if (need_ab) {
+        if (cudaMemcpy2DAsync(hb.A, dlda * 4, A, lda * 4, K * 4, M, cudaMemcpyHostToDevice, st) !=
+                cudaSuccess ||
+            cudaMemcpy2DAsync(hb.B, dldb * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice, st) !=
+                cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
+    }
+    if (beta != 0.0f &&
+        cudaMemcpy2DAsync(hb.C, dldc * 4, C, ldc * 4, N * 4, M, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    s = run_locked(M, N, K, alpha, hb.A, dlda, hb.B, dldb, beta, hb.C, dldc, st, *d);
+    if (s != SGEMM_OK) return s;
+    if (cudaMemcpy2DAsync(C, ldc * 4, hb.C, dldc * 4, N * 4, M, cudaMemcpyDeviceToHost, st) !=
+        cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    return status_from(cudaStreamSynchronize(st));
+}
+
+const char *sgemm_status_string(sgemm_status_t status) {
+    switch (status) {
+        case SGEMM_OK: return "SGEMM_OK";
+        case SGEMM_ERR_INVALID_ARG: return "SGEMM_ERR_INVALID_ARG";
+        case SGEMM_ERR_ALLOC: return "SGEMM_ERR_ALLOC";
+        case SGEMM_ERR_TMA: return "SGEMM_ERR_TMA";
+        case SGEMM_ERR_LAUNCH: return "SGEMM_ERR_LAUNCH";
+        case SGEMM_ERR_DEVICE_TIMEOUT: return "SGEMM_ERR_DEVICE_TIMEOUT";
+        case SGEMM_ERR_NO_DEVICE: return "SGEMM_ERR_NO_DEVICE";
+        case SGEMM_ERR_UNSUPPORTED: return "SGEMM_ERR_UNSUPPORTED";
+        default: return "SGEMM_ERR_UNKNOWN";
+    }
+}
+
+sgemm_status_t sgemm_device_status(void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState *d = nullptr;
+    sgemm_status_t s = device_state(&d);
+    if (s != SGEMM_OK) return s;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    int word = 0;
+    if (cudaMemcpy(&word, d->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    if (word == 0) return SGEMM_OK;
+    // A kernel gave up: clear the word and every arrival counter, so the
+    // stream-K tickets of the abandoned call do not leak into the next one.
+    if (cudaMemset(d->err, 0, sizeof(int)) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    for (auto &kv : d->ws)
+        if (kv.second.counters &&
+            cudaMemset(kv.second.counters, 0, kv.second.counter_count * sizeof(int)) != cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    return SGEMM_ERR_DEVICE_TIMEOUT;
+}
+
+sgemm_status_t sgemm_plan_describe(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                   int64_t ldc, uint64_t a_addr, uint64_t b_addr, uint64_t c_addr,
+                                   float beta, int num_sms, char *buf, size_t len) {
+    if (M < 0 || N < 0 || K < 0 || lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) ||
+        ldc < (N > 1 ? N : 1) || !buf || len == 0)
+        return SGEMM_ERR_INVALID_ARG;
+    if (num_sms <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SGEMM_ERR_NO_DEVICE;
+    }
+    PlanInput in;
+    in.M = M; in.N = N; in.K = K; in.lda = lda; in.ldb = ldb; in.ldc = ldc;
+    in.a_addr = a_addr; in.b_addr = b_addr; in.c_addr = c_addr;
+    in.alpha = 1.0f; in.beta = beta;
+    in.num_sms = num_sms;
+    in.force_variant = g_force_variant.load();
+    in.force_splits = g_force_splits.load();
+    Plan pl;
+    if (make_plan(in, &pl) != 0) return SGEMM_ERR_INVALID_ARG;
+    describe_plan(pl, buf, len);
+    return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_set_plan_override(int variant, int splits) {
+    if (variant < -1 || variant > SGEMM_VARIANT_SKINNY || splits < 0) return SGEMM_ERR_INVALID_ARG;
+    g_force_variant.store(variant);
+    g_force_splits.store(splits);
+    return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns, int skip_loads_from) {
+    if (skip_loads_from < -1) return SGEMM_ERR_INVALID_ARG;
+    g_timeout_ns.store(timeout_ns);
+    g_skip_loads_from.store(skip_loads_from);
+    return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages) {
+    if (tile_smem_bytes(fma_mode, stages) == 0) return SGEMM_ERR_INVALID_ARG;
+    g_fma_mode.store(fma_mode);
+    g_stages.store(stages);
+    return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_release_workspace(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int prev = 0;
+    cudaGetDevice(&prev);
+    for (auto &kv : g_dev) {
+        DeviceState &d = kv.second;
+        if (!d.supported) continue;
+        cudaSetDevice(kv.first);
+        cudaDeviceSynchronize();
+        for (auto &w : d.ws) {
+            if (w.second.partials) cudaFree(w.second.partials);
+            if (w.second.counters) cudaFree(w.second.counters);
+        }
+        d.ws.clear();
+        if (d.host.A) cudaFree(d.host.A);
+        if (d.host.B) cudaFree(d.host.B);
+        if (d.host.C) cudaFree(d.host.C);
+        d.host = HostBuffers();
+    }
+    cudaSetDevice(prev);
+    return SGEMM_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+sgemm_status_t sgemm_probe_ffma(int paired, int64_t iters, int blocks, float *sink, void *stream) {
+    if (iters < 1 || blocks < 1 || !sink) return SGEMM_ERR_INVALID_ARG;
+    return status_from(launch_ffma_probe(paired, iters, blocks, sink,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+sgemm_status_t sgemm_probe_read(const float *buf, int64_t n_floats, float *sink, int blocks,
+                                void *stream) {
+    if (!buf || !sink || blocks < 1 || n_floats < 4 || (n_floats & 3) ||
+        (reinterpret_cast<uintptr_t>(buf) & 15u))
+        return SGEMM_ERR_INVALID_ARG;
+    return status_from(launch_read_probe(reinterpret_cast<const float4 *>(buf), n_floats / 4, sink,
+                                         blocks, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

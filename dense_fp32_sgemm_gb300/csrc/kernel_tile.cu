@@ -1,0 +1,610 @@
+// Tiled SIMT FP32 GEMM for sm_103a: C = alpha * A * B + beta * C, row-major.
+//
+// One CTA of 256 threads owns a 128 x 256 tile of C and walks K in slices of
+// 32.  Each thread keeps a 16 x 8 micro-tile of running sums in registers and
+// updates it with an outer product per k: 16 values of A and 8 of B feed 128
+// multiply-adds ("Optimizing Matrix Multiply on CUDA, Part 2", section
+// "Increasing the Outputs per Thread": the 16 x 8 patch and 128 x 256 tile).
+//
+// Global -> shared staging uses TMA tiled copies into a ring of STAGES
+// buffers completed on mbarriers.  A's slice arrives as stored (k fastest);
+// the threads then rewrite it k-major ("transposed") into a second buffer so
+// that a thread's A values for one k are adjacent and come in with 128-bit
+// shared loads ("Optimizing CUDA matmul, steps 4 to 6", section "Two ladders,
+// one kernel": the transposed tile and the fill's derived 2-way store
+// conflict; "Part 2", section "Reducing the Slice Depth": 4-8 store passes).
+// Here the fill reads four 16-byte rows and writes four 16-byte columns per
+// thread, and the 16-byte chunk index of the transposed tile is XOR-ed with
+// (k / 4) mod 8, so both the fill and the inner-loop reads are free of bank
+// conflicts.
+//
+// B is read in two groups of four columns 32 apart per thread ("Part 2",
+// section "Changing the Shared-Memory Access Pattern"), so the eight threads
+// of a quarter-warp cover 32 consecutive banks.
+//
+// Work distribution ("Part 2", sections "Choosing Tiles" and "Distributing
+// the Partially Filled Wave"): a persistent grid computes the first dp_tiles
+// tiles whole, round-robin, then shares the k-iterations of the remaining
+// tiles evenly (stream-K).  A CTA whose range covers only part of a tile
+// writes its partial sums to a fixed slot and takes a ticket; the CTA that
+// arrives last adds the pieces in CTA order (so the result does not depend on
+// arrival order) and applies the epilogue.  No CTA ever waits for another.
+//
+// The multiply-add is IEEE FP32 fma with round-to-nearest, either one product
+// per instruction or two per instruction through the packed form (__ffma2_rn,
+// identical per-component arithmetic); FmaMode picks how the pairs are formed.
+
+#include "device_common.cuh"
+#include "kernels.h"
+
+namespace sgemm {
+namespace {
+
+constexpr int BM = kTileBM;
+constexpr int BN = kTileBN;
+constexpr int BK = kTileBK;
+constexpr int NT = kTileThreads;
+constexpr int TM = 16;
+constexpr int TN = 8;
+constexpr int A_STAGE_FLOATS = BM * BK;
+constexpr int B_STAGE_FLOATS = BK * BN;
+constexpr int STAGE_FLOATS = A_STAGE_FLOATS + B_STAGE_FLOATS;
+constexpr uint32_t STAGE_TX_BYTES = STAGE_FLOATS * 4;
+constexpr int TILE_FLOATS = BM * BN;
+static_assert(NT * TM * TN == TILE_FLOATS, "threads x micro-tile must cover the tile");
+static_assert(BK == 32 && BM == 128, "the transposing fill assumes 32 x 128 A slices");
+
+template <int FM>
+struct AtRow {
+    static constexpr int value = (FM == kFmaPairDupA) ? 2 * BM : BM;
+};
+
+template <int FM, int STAGES>
+struct SmemLayout {
+    static constexpr size_t stage_bytes = size_t(STAGE_FLOATS) * 4;
+    static constexpr size_t at_bytes = size_t(BK) * AtRow<FM>::value * 4;
+    static constexpr size_t at_off = STAGES * stage_bytes;
+    static constexpr size_t bar_off = at_off + 2 * at_bytes;
+    static constexpr size_t flag_off = bar_off + STAGES * 8;
+    static constexpr size_t total = flag_off + 16;
+};
+
+// ----- accumulators --------------------------------------------------------
+template <int FM>
+struct Acc;
+
+template <>
+struct Acc<kFmaScalar> {
+    float v[TM][TN];
+    __device__ __forceinline__ float &at(int i, int j) { return v[i][j]; }
+};
+
+struct AccPairN {  // v[i][jp] = (C[i][2jp], C[i][2jp+1])
+    float2 v[TM][TN / 2];
+    __device__ __forceinline__ float &at(int i, int j) {
+        return (j & 1) ? v[i][j >> 1].y : v[i][j >> 1].x;
+    }
+};
+template <>
+struct Acc<kFmaPairMovA> : AccPairN {};
+template <>
+struct Acc<kFmaPairDupA> : AccPairN {};
+
+template <>
+struct Acc<kFmaPairMovB> {  // v[ip][j] = (C[2ip][j], C[2ip+1][j])
+    float2 v[TM / 2][TN];
+    __device__ __forceinline__ float &at(int i, int j) {
+        return (i & 1) ? v[i >> 1][j].y : v[i >> 1][j].x;
+    }
+};
+
+template <int FM>
+__device__ __forceinline__ void acc_zero(Acc<FM> &acc) {
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc.at(i, j) = 0.0f;
+}
+
+// ----- fragments -------------------------------------------------------------
+// A fragment for one k: thread rows r*16 + ty*4 + (0..3), r = 0..3.
+// B fragment for one k: thread columns c*32 + tx*4 + (0..3), c = 0..1.
+template <int FM>
+struct Frag {
+    float4 a[FM == kFmaPairDupA ? 8 : 4];
+    float4 b[2];
+};
+
+__device__ __forceinline__ float comp(const float4 &v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// Per-thread shared-memory offsets (in floats) for the rows of one block of
+// four k values (the swizzle is constant over such a block).
+struct FragPtrs {
+    int a0, a1;  // A: two XOR-ed chunk bases (see load_frag)
+    int b;       // B: first column group
+};
+
+template <int FM>
+__device__ __forceinline__ FragPtrs frag_ptrs(int kblk, int wm, int wn, int ty, int tx) {
+    constexpr int ROW = AtRow<FM>::value;
+    const int swz = (kblk >> 2) & 7;
+    FragPtrs f;
+    if (FM == kFmaPairDupA) {
+        // chunk(r, p) = wm*32 + r*8 + ty*2 + p; the XOR touches only the low
+        // three bits, (2*ty + p).
+        const int x0 = (2 * ty) ^ swz;
+        f.a0 = kblk * ROW + (wm * 32 + x0) * 4;
+        f.a1 = kblk * ROW + (wm * 32 + (x0 ^ 1)) * 4;
+    } else {
+        // chunk(r) = wm*16 + r*4 + ty; low three bits are (r&1)*4 + ty.
+        const int x0 = ty ^ swz;
+        f.a0 = kblk * ROW + (wm * 16 + x0) * 4;
+        f.a1 = kblk * ROW + (wm * 16 + (x0 ^ 4)) * 4;
+    }
+    f.b = kblk * BN + wn * 64 + tx * 4;
+    return f;
+}
+
+template <int FM>
+__device__ __forceinline__ void load_frag(const float *at, const float *bs, const FragPtrs &fp,
+                                          int j, Frag<FM> &f) {
+    constexpr int ROW = AtRow<FM>::value;
+    const float *pa0 = at + fp.a0 + j * ROW;
+    const float *pa1 = at + fp.a1 + j * ROW;
+    if (FM == kFmaPairDupA) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            f.a[2 * r + 0] = ld_shared_f4(pa0 + r * 32);
+            f.a[2 * r + 1] = ld_shared_f4(pa1 + r * 32);
+        }
+    } else {
+        f.a[0] = ld_shared_f4(pa0);
+        f.a[1] = ld_shared_f4(pa1);
+        f.a[2] = ld_shared_f4(pa0 + 32);
+        f.a[3] = ld_shared_f4(pa1 + 32);
+    }
+    const float *pb = bs + fp.b + j * BN;
+    f.b[0] = ld_shared_f4(pb);
+    f.b[1] = ld_shared_f4(pb + 32);
+}
+
+template <int FM>
+__device__ __forceinline__ void fma_frag(const Frag<FM> &f, Acc<FM> &acc) {
+    if (FM == kFmaScalar) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const float a = comp(f.a[i >> 2], i & 3);
+#pragma unroll
+            for (int j = 0; j < TN; ++j)
+                acc.at(i, j) = __fmaf_rn(a, comp(f.b[j >> 2], j & 3), acc.at(i, j));
+        }
+    } else if (FM == kFmaPairMovA || FM == kFmaPairDupA) {
+        auto &v = reinterpret_cast<AccPairN &>(acc).v;
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            float2 a2;
+            if (FM == kFmaPairDupA) {
+                const float4 &d = f.a[i >> 1];
+                a2 = (i & 1) ? make_float2(d.z, d.w) : make_float2(d.x, d.y);
+            } else {
+                const float a = comp(f.a[i >> 2], i & 3);
+                a2 = make_float2(a, a);
+            }
+#pragma unroll
+            for (int jp = 0; jp < TN / 2; ++jp) {
+                const float4 &b = f.b[jp >> 1];
+                const float2 b2 = (jp & 1) ? make_float2(b.z, b.w) : make_float2(b.x, b.y);
+                v[i][jp] = __ffma2_rn(a2, b2, v[i][jp]);
+            }
+        }
+    } else {  // kFmaPairMovB
+        auto &v = reinterpret_cast<Acc<kFmaPairMovB> &>(acc).v;
+#pragma unroll
+        for (int ip = 0; ip < TM / 2; ++ip) {
+            const float4 &a = f.a[ip >> 1];
+            const float2 a2 = (ip & 1) ? make_float2(a.z, a.w) : make_float2(a.x, a.y);
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const float b = comp(f.b[j >> 2], j & 3);
+                v[ip][j] = __ffma2_rn(a2, make_float2(b, b), v[ip][j]);
+            }
+        }
+    }
+}
+
+// One K slice (32 k) of outer products from the transposed A slice `at` and
+// the B slice `bs`.  Fragments are double-buffered in registers: the loads
+// for k+1 are issued before the multiply-adds of k.
+template <int FM>
+__device__ __forceinline__ void compute_slice(const float *at, const float *bs, Acc<FM> &acc,
+                                              int wm, int wn, int ty, int tx) {
+    Frag<FM> f[2];
+    FragPtrs cur = frag_ptrs<FM>(0, wm, wn, ty, tx);
+    load_frag<FM>(at, bs, cur, 0, f[0]);
+#pragma unroll 1
+    for (int kb = 0; kb < BK; kb += 4) {
+        // The last prefetch of the slice wraps to row 0: in bounds, unused.
+        const FragPtrs nxt = frag_ptrs<FM>((kb + 4) & (BK - 1), wm, wn, ty, tx);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < 3)
+                load_frag<FM>(at, bs, cur, j + 1, f[(j + 1) & 1]);
+            else
+                load_frag<FM>(at, bs, nxt, 0, f[(j + 1) & 1]);
+            fma_frag<FM>(f[j & 1], acc);
+        }
+        cur = nxt;
+    }
+}
+
+// Rewrite the TMA-loaded A slice (BM rows x BK k, k fastest) k-major into
+// `at`, XOR-swizzling the 16-byte chunk index with (k / 4) mod 8.  Thread t
+// moves the 4 x 4 block rows 4*(t/8).., k 4*(t%8)..: the eight threads of a
+// quarter-warp read eight different chunks of one 128-byte row and write
+// eight different bank groups.
+template <int FM>
+__device__ __forceinline__ void transpose_slice(const float *raw, float *at, int tid) {
+    constexpr int ROW = AtRow<FM>::value;
+    const int kc = tid & 7;
+    const int mb = tid >> 3;
+    float4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = ld_shared_f4(raw + (4 * mb + i) * BK + 4 * kc);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        float *row = at + (4 * kc + kk) * ROW;
+        const float e0 = comp(v[0], kk), e1 = comp(v[1], kk);
+        const float e2 = comp(v[2], kk), e3 = comp(v[3], kk);
+        if (FM == kFmaPairDupA) {
+            st_shared_f4(row + ((2 * mb) ^ kc) * 4, make_float4(e0, e0, e1, e1));
+            st_shared_f4(row + ((2 * mb + 1) ^ kc) * 4, make_float4(e2, e2, e3, e3));
+        } else {
+            st_shared_f4(row + (mb ^ kc) * 4, make_float4(e0, e1, e2, e3));
+        }
+    }
+}
+
+__device__ __forceinline__ void tile_coords(const TileParams &p, int t, int &tm, int &tn) {
+    // Grouped rasterisation: runs of group_m tile-rows are walked column by
+    // column so CTAs that run together share A rows and B columns in L2.
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int rows = min(p.tiles_m - first_m, p.group_m);
+    const int r = t - g * per_group;
+    tm = first_m + r % rows;
+    tn = r / rows;
+}
+
+// Iterates the units (tile, k-range) of one CTA: its round-robin share of
+// the whole tiles, then its contiguous range of stream-K iterations.
+struct UnitIter {
+    int dp_next;
+    int sk_u, sk_end;
+    __device__ __forceinline__ void init(const TileParams &p, int cta) {
+        dp_next = cta;
+        const int sk_total = p.sk_tiles * p.kt_total;
+        sk_u = min(cta * p.sk_share, sk_total);
+        sk_end = min(sk_u + p.sk_share, sk_total);
+    }
+    __device__ __forceinline__ bool next(const TileParams &p, int G, int &tile, int &k0, int &k1) {
+        if (dp_next < p.dp_tiles) {
+            tile = dp_next;
+            k0 = 0;
+            k1 = p.kt_total;
+            dp_next += G;
+            return true;
+        }
+        if (sk_u < sk_end) {
+            const int t = sk_u / p.kt_total;
+            k0 = sk_u - t * p.kt_total;
+            k1 = min(p.kt_total, k0 + (sk_end - sk_u));
+            tile = p.dp_tiles + t;
+            sk_u += k1 - k0;
+            return true;
+        }
+        return false;
+    }
+};
+
+template <int FM>
+__device__ __forceinline__ void store_tile(Acc<FM> &acc, const TileParams &p, int tm, int tn,
+                                           int wm, int wn, int ty, int tx) {
+    const int m_base = tm * BM + wm * 64 + ty * 4;
+    const int n_base = tn * BN + wn * 64 + tx * 4;
+    const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int m = m_base + r * 16 + i;
+            if (m >= p.M) continue;
+            float *crow = p.C + (long long)m * p.ldc;
+            const int ti = r * 4 + i;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int n = n_base + c * 32;
+                if (p.c_vec4 && n + 3 < p.N) {
+                    float4 o;
+                    o.x = alpha * acc.at(ti, c * 4 + 0);
+                    o.y = alpha * acc.at(ti, c * 4 + 1);
+                    o.z = alpha * acc.at(ti, c * 4 + 2);
+                    o.w = alpha * acc.at(ti, c * 4 + 3);
+                    if (beta != 0.0f) {
+                        const float4 cv = *reinterpret_cast<const float4 *>(crow + n);
+                        o.x = __fmaf_rn(beta, cv.x, o.x);
+                        o.y = __fmaf_rn(beta, cv.y, o.y);
+                        o.z = __fmaf_rn(beta, cv.z, o.z);
+                        o.w = __fmaf_rn(beta, cv.w, o.w);
+                    }
+                    *reinterpret_cast<float4 *>(crow + n) = o;
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        if (n + jj < p.N) {
+                            float o = alpha * acc.at(ti, c * 4 + jj);
+                            if (beta != 0.0f) o = __fmaf_rn(beta, crow[n + jj], o);
+                            crow[n + jj] = o;
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Partial tiles use a thread-linear layout: float4 number e4 of thread tid
+// sits at slot[(e4 * NT + tid) * 4], element order (row ti, columns c*4..).
+template <int FM>
+__device__ __forceinline__ void write_partial(float *slot, Acc<FM> &acc, int tid) {
+#pragma unroll
+    for (int e4 = 0; e4 < TILE_FLOATS / NT / 4; ++e4) {
+        const int ti = e4 >> 1, c = e4 & 1;
+        const float4 v = make_float4(acc.at(ti, c * 4 + 0), acc.at(ti, c * 4 + 1),
+                                     acc.at(ti, c * 4 + 2), acc.at(ti, c * 4 + 3));
+        __stcg(reinterpret_cast<float4 *>(slot) + e4 * NT + tid, v);
+    }
+}
+
+__device__ __forceinline__ int partial_slot(const TileParams &p, int cta, int t_sk) {
+    const int tile_start = t_sk * p.kt_total;
+    const int k0 = max(cta * p.sk_share, tile_start) - tile_start;
+    return 2 * cta + (k0 == 0 ? 1 : 0);
+}
+
+// Sum the pieces of stream-K tile t_sk, CTAs c_first..c_last, in CTA order;
+// this CTA's own piece is taken from registers.
+template <int FM>
+__device__ __forceinline__ void reduce_pieces(Acc<FM> &acc, const TileParams &p, int cta,
+                                              int t_sk, int c_first, int c_last, int tid) {
+#pragma unroll
+    for (int e4 = 0; e4 < TILE_FLOATS / NT / 4; ++e4) {
+        const int ti = e4 >> 1, c = e4 & 1;
+        const float4 own = make_float4(acc.at(ti, c * 4 + 0), acc.at(ti, c * 4 + 1),
+                                       acc.at(ti, c * 4 + 2), acc.at(ti, c * 4 + 3));
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int cc = c_first; cc <= c_last; ++cc) {
+            float4 v;
+            if (cc == cta) {
+                v = own;
+            } else {
+                const float *slot =
+                    p.partials + (size_t)partial_slot(p, cc, t_sk) * TILE_FLOATS;
+                v = __ldcg(reinterpret_cast<const float4 *>(slot) + e4 * NT + tid);
+            }
+            if (cc == c_first) {
+                s = v;
+            } else {
+                s.x += v.x;
+                s.y += v.y;
+                s.z += v.z;
+                s.w += v.w;
+            }
+        }
+        acc.at(ti, c * 4 + 0) = s.x;
+        acc.at(ti, c * 4 + 1) = s.y;
+        acc.at(ti, c * 4 + 2) = s.z;
+        acc.at(ti, c * 4 + 3) = s.w;
+    }
+}
+
+template <int FM, int STAGES>
+__global__ void __launch_bounds__(NT, 1)
+    sgemm_tile_kernel(const __grid_constant__ CUtensorMap mapA,
+                      const __grid_constant__ CUtensorMap mapB, const TileParams p) {
+    using L = SmemLayout<FM, STAGES>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    float *stages = reinterpret_cast<float *>(smem);
+    float *at_buf = reinterpret_cast<float *>(smem + L::at_off);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off);
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + L::flag_off);
+    constexpr int AT_FLOATS = BK * AtRow<FM>::value;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int wm = warp >> 2, wn = warp & 3;
+    const int ty = lane >> 3, tx = lane & 7;
+    const int G = gridDim.x, cta = blockIdx.x;
+
+    // Number of k-iterations this CTA runs, over all its units.
+    const int n_dp = cta < p.dp_tiles ? (p.dp_tiles - 1 - cta) / G + 1 : 0;
+    const int sk_total = p.sk_tiles * p.kt_total;
+    const int sk_begin = min(cta * p.sk_share, sk_total);
+    const int sk_end = min(sk_begin + p.sk_share, sk_total);
+    const int q_total = n_dp * p.kt_total + (sk_end - sk_begin);
+    if (q_total == 0) return;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        flags[0] = 0;
+        flags[1] = 0;
+        fence_barrier_init();
+        prefetch_tensormap(&mapA);
+        prefetch_tensormap(&mapB);
+    }
+    __syncthreads();
+
+    // ---- copy producer state (used by thread 0 only) ----
+    UnitIter prod;
+    prod.init(p, cta);
+    int pq = 0, p_tm = 0, p_tn = 0, p_k = 0, p_k1 = 0;
+    auto issue_next = [&]() {
+        if (pq >= q_total) return;
+        if (p.skip_loads_from >= 0 && pq >= p.skip_loads_from) return;
+        if (p_k >= p_k1) {
+            int tile;
+            prod.next(p, G, tile, p_k, p_k1);
+            tile_coords(p, tile, p_tm, p_tn);
+        }
+        const int s = pq % STAGES;
+        float *sa = stages + s * STAGE_FLOATS;
+        float *sb = sa + A_STAGE_FLOATS;
+        mbar_arrive_expect_tx(&full[s], STAGE_TX_BYTES);
+        tma_load_2d(sa, &mapA, &full[s], p_k * BK, p_tm * BM);
+        tma_load_2d(sb, &mapB, &full[s], p_tn * BN, p_k * BK);
+        ++p_k;
+        ++pq;
+    };
+    if (tid == 0)
+        for (int s = 0; s < STAGES; ++s) issue_next();
+
+    // ---- consumers (all threads) ----
+    UnitIter cons;
+    cons.init(p, cta);
+    int q = 0;
+    bool aborted = false;
+
+    if (!mbar_wait_bounded(&full[0], 0, p.timeout_ns)) {
+        flags[0] = 1;
+        atomicOr(p.err, kErrWaitTimeout);
+    }
+    transpose_slice<FM>(stages, at_buf, tid);
+    __syncthreads();
+    if (flags[0]) aborted = true;
+
+    int tile, k0, k1;
+    while (!aborted && cons.next(p, G, tile, k0, k1)) {
+        int tm, tn;
+        tile_coords(p, tile, tm, tn);
+        Acc<FM> acc;
+        acc_zero<FM>(acc);
+
+        for (int kt = k0; kt < k1; ++kt, ++q) {
+            const int s = q % STAGES;
+            if (q + 1 < q_total) {
+                const int s1 = (q + 1) % STAGES;
+                if (!mbar_wait_bounded(&full[s1], ((q + 1) / STAGES) & 1, p.timeout_ns)) {
+                    flags[0] = 1;
+                    atomicOr(p.err, kErrWaitTimeout);
+                }
+                transpose_slice<FM>(stages + s1 * STAGE_FLOATS, at_buf + ((q + 1) & 1) * AT_FLOATS,
+                                    tid);
+            }
+            compute_slice<FM>(at_buf + (q & 1) * AT_FLOATS, stages + s * STAGE_FLOATS + A_STAGE_FLOATS,
+                              acc, wm, wn, ty, tx);
+            __syncthreads();
+            if (flags[0]) {
+                aborted = true;
+                ++q;
+                break;
+            }
+            if (tid == 0) issue_next();
+        }
+        if (aborted) break;
+
+        if (k0 == 0 && k1 == p.kt_total) {
+            store_tile<FM>(acc, p, tm, tn, wm, wn, ty, tx);
+        } else {
+            const int t_sk = tile - p.dp_tiles;
+            float *slot = p.partials + (size_t)partial_slot(p, cta, t_sk) * TILE_FLOATS;
+            write_partial<FM>(slot, acc, tid);
+            __threadfence();
+            __syncthreads();
+            const int c_first = (t_sk * p.kt_total) / p.sk_share;
+            const int c_last = (t_sk * p.kt_total + p.kt_total - 1) / p.sk_share;
+            if (tid == 0) {
+                const int old = atomicAdd(&p.counters[t_sk], 1);
+                flags[1] = (old == c_last - c_first) ? 1 : 0;
+            }
+            __syncthreads();
+            if (flags[1]) {
+                __threadfence();
+                reduce_pieces<FM>(acc, p, cta, t_sk, c_first, c_last, tid);
+                if (tid == 0) p.counters[t_sk] = 0;
+                store_tile<FM>(acc, p, tm, tn, wm, wn, ty, tx);
+            }
+        }
+    }
+
+    if (aborted && tid == 0) {
+        // Wait (bounded) for every copy issued but not yet consumed, so none
+        // lands in shared memory after this CTA has exited.  q is the first
+        // position not yet transposed; positions [q, pq) may be in flight.
+        for (int j = q; j < pq; ++j) {
+            if (!mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1, 1000000000ull)) {
+                atomicOr(p.err, kErrDrainTimeout);
+                break;
+            }
+        }
+    }
+}
+
+template <int FM, int STAGES>
+cudaError_t launch_impl(const CUtensorMap &mapA, const CUtensorMap &mapB, const TileParams &p,
+                        int grid, cudaStream_t stream) {
+    using L = SmemLayout<FM, STAGES>;
+    sgemm_tile_kernel<FM, STAGES><<<grid, NT, L::total, stream>>>(mapA, mapB, p);
+    return cudaGetLastError();
+}
+
+template <int FM, int STAGES>
+cudaError_t configure_impl() {
+    using L = SmemLayout<FM, STAGES>;
+    return cudaFuncSetAttribute(sgemm_tile_kernel<FM, STAGES>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::total);
+}
+
+}  // namespace
+
+size_t tile_smem_bytes(int fma_mode, int stages) {
+#define SGEMM_TILE_CASE(FM, S) \
+    if (fma_mode == FM && stages == S) return SmemLayout<FM, S>::total;
+    SGEMM_TILE_CASE(kFmaScalar, 3)
+    SGEMM_TILE_CASE(kFmaScalar, 4)
+    SGEMM_TILE_CASE(kFmaPairMovA, 3)
+    SGEMM_TILE_CASE(kFmaPairMovA, 4)
+    SGEMM_TILE_CASE(kFmaPairDupA, 3)
+    SGEMM_TILE_CASE(kFmaPairMovB, 3)
+    SGEMM_TILE_CASE(kFmaPairMovB, 4)
+#undef SGEMM_TILE_CASE
+    return 0;
+}
+
+#define SGEMM_TILE_DISPATCH(CALL)                                              \
+    switch (fma_mode * 10 + stages) {                                          \
+        case kFmaScalar * 10 + 3: return CALL(kFmaScalar, 3);                  \
+        case kFmaScalar * 10 + 4: return CALL(kFmaScalar, 4);                  \
+        case kFmaPairMovA * 10 + 3: return CALL(kFmaPairMovA, 3);              \
+        case kFmaPairMovA * 10 + 4: return CALL(kFmaPairMovA, 4);              \
+        case kFmaPairDupA * 10 + 3: return CALL(kFmaPairDupA, 3);              \
+        case kFmaPairMovB * 10 + 3: return CALL(kFmaPairMovB, 3);              \
+        case kFmaPairMovB * 10 + 4: return CALL(kFmaPairMovB, 4);              \
+        default: return cudaErrorInvalidValue;                                 \
+    }
+
+cudaError_t launch_tile(int fma_mode, int stages, const CUtensorMap &mapA, const CUtensorMap &mapB,
+                        const TileParams &p, int grid, cudaStream_t stream) {
+#define SGEMM_LAUNCH(FM, S) launch_impl<FM, S>(mapA, mapB, p, grid, stream)
+    SGEMM_TILE_DISPATCH(SGEMM_LAUNCH)
+#undef SGEMM_LAUNCH
+}
+
+cudaError_t tile_configure(int fma_mode, int stages) {
+#define SGEMM_CONF(FM, S) configure_impl<FM, S>()
+    SGEMM_TILE_DISPATCH(SGEMM_CONF)
+#undef SGEMM_CONF
+}
+
+}  // namespace sgemm

@@ -1,0 +1,120 @@
+// Kernel parameter blocks and launch wrappers shared by the host planner
+// (api.cu) and the kernel translation units.  Host-visible only: no device
+// code here.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sgemm {
+
+// ---------------------------------------------------------------------------
+// Tiled FFMA kernel (TMA + mbarrier pipeline, in-CTA transposed A tile).
+// Block tile BM x BN = 128 x 256, K slice BK = 32, 256 threads, each thread
+// a 16 x 8 micro-tile.
+// ---------------------------------------------------------------------------
+constexpr int kTileBM = 128;
+constexpr int kTileBN = 256;
+constexpr int kTileBK = 32;
+constexpr int kTileThreads = 256;
+
+// Inner-product form of the micro-tile update (see kernel_tile.cu).
+enum FmaMode : int {
+    kFmaScalar = 0,    // one FFMA per product
+    kFmaPairMovA = 1,  // packed pairs along n, A value duplicated in registers
+    kFmaPairDupA = 2,  // packed pairs along n, A stored duplicated in shared memory
+    kFmaPairMovB = 3,  // packed pairs along m, B value duplicated in registers
+};
+
+struct TileParams {
+    int M, N, K;
+    int tiles_m, tiles_n;
+    int kt_total;       // ceil(K / BK): k-iterations of a whole tile
+    int dp_tiles;       // tiles [0, dp_tiles) are computed whole, round-robin
+    int sk_tiles;       // tiles [dp_tiles, dp_tiles + sk_tiles) are stream-K
+    int sk_share;       // k-iterations each CTA takes in the stream-K region
+    int group_m;        // tile rasterisation: tiles_m grouped by this many rows
+    float alpha, beta;
+    float *C;
+    long long ldc;
+    int c_vec4;         // C and ldc allow 16-byte accesses
+    float *partials;    // 2 * gridDim.x slots of BM*BN floats (stream-K)
+    int *counters;      // one arrival counter per stream-K tile, zero at rest
+    int *err;           // device error word
+    unsigned long long timeout_ns;
+    int skip_loads_from;  // testing hook, -1 = off
+};
+
+cudaError_t launch_tile(int fma_mode, int stages, const CUtensorMap &mapA,
+                        const CUtensorMap &mapB, const TileParams &p, int grid,
+                        cudaStream_t stream);
+size_t tile_smem_bytes(int fma_mode, int stages);
+cudaError_t tile_configure(int fma_mode, int stages);
+
+// ---------------------------------------------------------------------------
+// Generic kernel: any alignment and leading dimension, bounds-checked loads.
+// ---------------------------------------------------------------------------
+constexpr int kGenBM = 64;
+constexpr int kGenBN = 64;
+constexpr int kGenBK = 16;
+
+struct GenericParams {
+    int M, N, K;
+    float alpha, beta;
+    const float *A;
+    long long lda;
+    const float *B;
+    long long ldb;
+    float *C;
+    long long ldc;
+};
+
+cudaError_t launch_generic(const GenericParams &p, cudaStream_t stream);
+
+// C = beta * C (beta == 0 writes zeros without reading C).
+cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc,
+                         cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Skinny-M kernel: streams B once through a TMA ring, A resident in shared
+// memory, stream-K over (column slab, k) with a fixed-order reduction.
+// ---------------------------------------------------------------------------
+constexpr int kSkinnyBN = 256;   // columns per slab
+constexpr int kSkinnyBK = 32;    // B rows per TMA stage
+constexpr int kSkinnyMaxM = 32;
+constexpr int kSkinnyThreads = 256;
+
+struct SkinnyParams {
+    int M, N, K;
+    int slabs;            // ceil(N / BN)
+    int kt_total;         // ceil(K / BK)
+    int share;            // k-iterations per CTA over the (slab, k) space
+    float alpha, beta;
+    const float *A;
+    long long lda;
+    float *C;
+    long long ldc;
+    int c_vec4;
+    float *partials;      // 2 * gridDim.x slots of kSkinnyMaxM * BN floats
+    int *counters;        // one per slab
+    int *err;
+    unsigned long long timeout_ns;
+    int skip_loads_from;
+};
+
+cudaError_t launch_skinny(int m_tile, const CUtensorMap &mapB, const SkinnyParams &p,
+                          int grid, cudaStream_t stream);
+size_t skinny_smem_bytes(int m_tile, int share);
+cudaError_t skinny_configure(int m_tile);
+constexpr int kSkinnyStages = 6;
+
+// ---------------------------------------------------------------------------
+// Measurement probes (same library, used by the benchmark).
+// ---------------------------------------------------------------------------
+cudaError_t launch_ffma_probe(int paired, long long iters, int blocks, float *sink,
+                              cudaStream_t stream);
+cudaError_t launch_read_probe(const float4 *buf, long long n4, float *sink, int blocks,
+                              cudaStream_t stream);
+
+}  // namespace sgemm

@@ -1,0 +1,52 @@
+// Host-side planner: picks the kernel variant and the work split for one
+// SGEMM call.  Pure host code (no CUDA calls), so it can be exercised on a
+// machine without a GPU through sgemm_plan_describe().
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sgemm {
+
+enum Variant : int {
+    kVarNone = -2,      // nothing to do (M == 0 or N == 0)
+    kVarScale = -3,     // alpha == 0 or K == 0: C = beta * C
+    kVarGeneric = 0,
+    kVarTile = 1,       // data-parallel only
+    kVarStreamK = 2,    // data-parallel waves + stream-K tail
+    kVarSkinny = 3,
+};
+
+struct PlanInput {
+    int64_t M, N, K, lda, ldb, ldc;
+    uint64_t a_addr, b_addr, c_addr;
+    float alpha, beta;
+    int num_sms;
+    int force_variant;  // -1 = automatic
+    int force_splits;   // 0 = automatic
+};
+
+struct Plan {
+    int variant;
+    // tile / stream-K
+    int tiles_m, tiles_n, kt_total;
+    int dp_tiles, sk_tiles, sk_share;
+    int group_m;
+    int grid;
+    int c_vec4;
+    // skinny
+    int m_tile, slabs;
+    double cost;  // estimated busiest-SM work, in k-iterations of one tile
+    const char *reason;
+};
+
+// Returns 0 and fills `out`, or a negative value for arguments no variant
+// can take (the caller has validated sizes already).
+int make_plan(const PlanInput &in, Plan *out);
+
+// Writes a one-line key=value description of `plan`.
+int describe_plan(const Plan &plan, char *buf, size_t len);
+
+const char *variant_name(int variant);
+
+}  // namespace sgemm

@@ -1,0 +1,168 @@
+/*
+ * sgemm.h -- C ABI of the GB300 (sm_103a) single-precision GEMM library.
+ *
+ * The operation is C = alpha * A * B + beta * C on row-major FP32 matrices,
+ * computed with plain FP32 fused multiply-add (no tensor cores, no TF32):
+ * - "Optimizing Matrix Multiply on CUDA, Part 1", section "Counting the Work":
+ *   C[i][j] is the dot product of row i of A and column j of B.
+ * - "GEMM from Scratch", Module 02 ("One Thread Per Output"): row-major
+ *   operands A[x*K+i], B[i*N+y], C[x*N+y] and the epilogue
+ *   alpha*tmp + beta*C[x*N+y].
+ * - "Optimizing CUDA matmul, steps 4 to 6", section "The honest target":
+ *   plain FP32 in, FP32 accumulate, FP32 out, no TF32 path.
+ *
+ * Layout: element (i, j) of a row-major matrix X with leading dimension ldx
+ * lives at X[i * ldx + j]; ldx counts elements and may exceed the row length.
+ * A is M x K (lda >= max(1, K)), B is K x N (ldb >= max(1, N)), C is M x N
+ * (ldc >= max(1, N)).
+ *
+ * Conventions the pages leave open (BLAS practice):
+ * - beta == 0: C is write-only; whatever C held (NaN included) is ignored.
+ * - alpha == 0 or K == 0: A and B are not read; C = beta * C.
+ * - M == 0 or N == 0: nothing is done.
+ * - Any summation order of the K products is allowed; for a given shape,
+ *   leading dimensions and pointer alignment the result is bitwise
+ *   reproducible from call to call.
+ *
+ * All entry points return an sgemm_status_t.  Validation errors are returned
+ * before any work is queued.  Calls are asynchronous with respect to the
+ * host; results are ready once the given stream has been synchronised.
+ */
+#ifndef GB300_SGEMM_H
+#define GB300_SGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SGEMM_API __attribute__((visibility("default")))
+#else
+#define SGEMM_API
+#endif
+
+typedef int sgemm_status_t;
+
+enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_ARG = 1,    /* a size, leading dimension or pointer is invalid  */
+    SGEMM_ERR_ALLOC = 2,          /* internal workspace could not be allocated        */
+    SGEMM_ERR_TMA = 3,            /* a TMA tensor map could not be encoded            */
+    SGEMM_ERR_LAUNCH = 4,         /* a kernel launch or CUDA runtime call failed      */
+    SGEMM_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait gave up (see below)   */
+    SGEMM_ERR_NO_DEVICE = 6,      /* no CUDA device, or it is not sm_103              */
+    SGEMM_ERR_UNSUPPORTED = 7     /* the request names something this build lacks     */
+};
+
+/*
+ * sgemm_run -- C = alpha * A * B + beta * C on the GPU.
+ *
+ * A, B, C: device pointers owned by the caller.  A and B are only read; C is
+ *   read (when beta != 0) and written.  C must not overlap A or B.  Any
+ *   4-byte-aligned pointers are accepted; 16-byte-aligned pointers with
+ *   leading dimensions that are multiples of 4 take the fastest path.
+ * stream: a cudaStream_t (NULL = the legacy default stream).  All work is
+ *   queued on it; the call does not synchronise.
+ * Internal workspace (partial tiles for K-split schedules) is allocated by
+ *   the library on first use per (device, stream) and kept until
+ *   sgemm_release_workspace().  Concurrent calls on one stream are ordered by
+ *   the stream; calls on different streams use different workspaces.
+ * Returns SGEMM_ERR_INVALID_ARG if M, N or K < 0, a leading dimension is below
+ *   its minimum, or a pointer the operation must dereference is NULL or not
+ *   4-byte aligned; SGEMM_ERR_LAUNCH if a launch fails.  A bounded device wait
+ *   that gave up is reported by sgemm_device_status().
+ */
+SGEMM_API sgemm_status_t sgemm_run(int64_t M, int64_t N, int64_t K, float alpha,
+                         const float *A, int64_t lda, const float *B, int64_t ldb,
+                         float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * sgemm_run_host -- the same operation on HOST matrices.
+ *
+ * A, B, C are host pointers (pinned memory gives full copy bandwidth).  The
+ * call copies A, B (and C when beta != 0) to device buffers it owns, runs
+ * sgemm_run on `stream`, copies C back and synchronises `stream` before
+ * returning, so C holds the result on return.  Device buffers are kept for
+ * reuse until sgemm_release_workspace().
+ */
+SGEMM_API sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha,
+                              const float *A, int64_t lda, const float *B, int64_t ldb,
+                              float beta, float *C, int64_t ldc, void *stream);
+
+/* Human-readable name of a status code (a static string). */
+SGEMM_API const char *sgemm_status_string(sgemm_status_t status);
+
+/*
+ * sgemm_device_status -- synchronise `stream`, then read and clear the
+ * library's device error word on the current device.  Returns
+ * SGEMM_ERR_DEVICE_TIMEOUT if any kernel since the last call gave up a
+ * bounded wait (its output is then undefined; the library resets its own
+ * workspace counters so later calls are valid), SGEMM_ERR_LAUNCH if the
+ * stream reports a CUDA error, else SGEMM_OK.
+ */
+SGEMM_API sgemm_status_t sgemm_device_status(void *stream);
+
+/*
+ * sgemm_plan_describe -- host-only: write into buf (NUL-terminated, at most
+ * len bytes) the plan sgemm_run would choose for these sizes, leading
+ * dimensions and pointer addresses on a GPU with `num_sms` SMs (0 = query the
+ * current device).  The text is one line of key=value pairs: kernel variant,
+ * tile, grid, data-parallel tiles, stream-K tiles and share, estimated
+ * busiest-SM cost.  Touches no device memory.  Returns SGEMM_ERR_INVALID_ARG
+ * on bad sizes, SGEMM_ERR_NO_DEVICE if num_sms == 0 and no device is present.
+ */
+SGEMM_API sgemm_status_t sgemm_plan_describe(int64_t M, int64_t N, int64_t K,
+                                   int64_t lda, int64_t ldb, int64_t ldc,
+                                   uint64_t a_addr, uint64_t b_addr, uint64_t c_addr,
+                                   float beta, int num_sms, char *buf, size_t len);
+
+/*
+ * sgemm_set_plan_override -- testing and benchmarking hook, process-wide.
+ * variant: -1 = automatic; otherwise one of SGEMM_VARIANT_*.
+ * splits: for the stream-K variants, 0 = automatic, else the number of
+ *   k-iterations each CTA takes in the stream-K region is chosen so that
+ *   tiles split into about `splits` pieces.
+ * Returns SGEMM_ERR_INVALID_ARG for an unknown variant.
+ */
+enum {
+    SGEMM_VARIANT_AUTO = -1,
+    SGEMM_VARIANT_GENERIC = 0,   /* any alignment: 64x64 tile, bounds-checked loads  */
+    SGEMM_VARIANT_TILE = 1,      /* TMA + FFMA2 128x256 tile, whole tiles only        */
+    SGEMM_VARIANT_STREAMK = 2,   /* same kernel, data-parallel waves + stream-K tail  */
+    SGEMM_VARIANT_SKINNY = 3     /* small-M streaming kernel (HBM-bound shapes)       */
+};
+SGEMM_API sgemm_status_t sgemm_set_plan_override(int variant, int splits);
+
+/*
+ * sgemm_set_wait_timeout_ns -- testing hook: the limit (nanoseconds of GPU
+ * global time) every bounded device-side wait uses; 0 restores the default
+ * (one second).  skip_loads_from >= 0 makes the copy producer of the tiled
+ * kernels stop issuing loads at that k-iteration of each CTA, so the waits
+ * for them run out (a flag that nothing sets); -1 disables it.
+ */
+SGEMM_API sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns, int skip_loads_from);
+
+/*
+ * sgemm_set_tile_config -- tuning hook, process-wide: the form of the
+ * multiply-add in the tiled kernel and its number of TMA ring stages.
+ * fma_mode: 0 = one FFMA per product; 1 = packed pairs along n with the A
+ *   value duplicated in registers; 2 = packed pairs along n with A stored
+ *   duplicated in shared memory (default); 3 = packed pairs along m with the
+ *   B value duplicated in registers.
+ * stages: 3 or 4 (mode 2 supports 3 only).
+ * All forms compute the same IEEE FP32 products and sums.  Returns
+ * SGEMM_ERR_INVALID_ARG for a combination this build does not contain.
+ */
+SGEMM_API sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages);
+
+/* Free every workspace and host-path buffer the library holds on all devices. */
+SGEMM_API sgemm_status_t sgemm_release_workspace(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_SGEMM_H */

@@ -1,0 +1,243 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+Floating point is judged elementwise by
+|C_gpu - C_ref| <= 2*K*2^-24*(|alpha|(|A||B|)_ij + |beta||C_ij|) (K >= 3);
+integer-valued inputs whose partial sums stay below 2^24 must match exactly.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import datagen
+import dense_fp32_sgemm_gb300 as sg
+import oracle
+from tests.checks import assert_within
+from tests.gpu_harness import run_gemm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sg.build()
+    sg.set_plan_override(-1, 0)
+    sg.set_wait_timeout_ns(0, -1)
+    yield
+    sg.set_plan_override(-1, 0)
+    sg.set_wait_timeout_ns(0, -1)
+
+
+def inputs(dist, seed, M, N, K, lda=None, ldb=None, ldc=None, with_c=True):
+    lda, ldb, ldc = lda or max(K, 1), ldb or max(N, 1), ldc or max(N, 1)
+    A = datagen.matrix(dist, seed, "A", M, K, ld=lda) if M * K else np.zeros(max(M * lda, 1), np.float32)
+    B = datagen.matrix(dist, seed, "B", K, N, ld=ldb) if K * N else np.zeros(max(K * ldb, 1), np.float32)
+    C = datagen.matrix(dist, seed, "C", M, N, ld=ldc) if with_c else None
+    return A, lda, B, ldb, C, ldc
+
+
+def reference(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, rows=None):
+    ref, absprod = oracle.sgemm_ref_flat(M, N, K, alpha, A, lda, B, ldb, beta,
+                                         C if beta != 0 else None, ldc, rows=rows)
+    rows_idx = np.arange(M) if rows is None else np.asarray(rows)
+    Cm = C.reshape(M, ldc)[rows_idx, :N] if (C is not None and beta != 0) else None
+    return ref, oracle.error_bound(absprod, Cm, alpha, beta, K)
+
+
+def check(M, N, K, alpha, beta, dist="uniform", seed=1, lda=None, ldb=None, ldc=None,
+          variant=-1, splits=0, offsets=(0, 0, 0), rows=None, label=""):
+    A, lda, B, ldb, C, ldc = inputs(dist, seed, M, N, K, lda, ldb, ldc, with_c=True)
+    out, _ = run_gemm(M, N, K, alpha, beta, A, lda, B, ldb, C if beta != 0 else None, ldc,
+                      offsets=offsets, variant=variant, splits=splits,
+                      c_fill=None if beta != 0 else float("nan"))
+    ref, bound = reference(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, rows=rows)
+    got = out if rows is None else out[np.asarray(rows)]
+    assert_within(got, ref, bound, label or f"{M}x{N}x{K} variant={variant} splits={splits}")
+    return out
+
+
+def sample_rows(M, count, seed):
+    """Rows spread over the matrix, always including both ends and the rows
+    on either side of 128-row tile boundaries near them."""
+    rng = np.random.default_rng(seed)
+    fixed = {0, 1, 127, 128, 129, M // 2, M - 129, M - 128, M - 2, M - 1}
+    fixed = {r for r in fixed if 0 <= r < M}
+    extra = rng.choice(M, size=min(M, count), replace=False).tolist()
+    return sorted(fixed | set(extra))
+
+
+# ----- the six workloads at full size, launched as the benchmark launches them ---
+
+@pytest.mark.parametrize("name,sample", [
+    ("s1_128", None), ("s2_2048", 192), ("s3_4092", 64), ("s4_rect", 48),
+    ("s5_odd", None), ("s6_skinny", None),
+])
+def test_workload_full_size(name, sample):
+    cfg, A, B, C = datagen.config_inputs(name)
+    M, N, K, alpha, beta = cfg["M"], cfg["N"], cfg["K"], cfg["alpha"], cfg["beta"]
+    out, _ = run_gemm(M, N, K, alpha, beta, A, K, B, N, C, N,
+                      c_fill=None if beta != 0 else float("nan"))
+    rows = None if sample is None else sample_rows(M, sample, 7)
+    ref, bound = reference(M, N, K, alpha, beta, A, K, B, N, C, N, rows=rows)
+    got = out if rows is None else out[np.asarray(rows)]
+    assert np.isfinite(out).all()
+    assert_within(got, ref, bound, name)
+
+
+# ----- exact integer inputs: every variant must be bit-exact ---------------------
+
+@pytest.mark.parametrize("variant,splits", [(0, 0), (1, 0), (2, 2), (2, 3), (2, 4), (-1, 0)])
+@pytest.mark.parametrize("M,N,K", [(64, 64, 64), (300, 520, 64), (129, 257, 40)])
+def test_small_integers_bit_exact(variant, splits, M, N, K):
+    Kp = (K + 3) // 4 * 4
+    Np = (N + 3) // 4 * 4
+    A, lda, B, ldb, C, ldc = inputs("ints", 3, M, N, K, lda=Kp, ldb=Np, ldc=Np)
+    out, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc, variant=variant, splits=splits)
+    Ai = A.reshape(M, lda)[:, :K].astype(np.int64)
+    Bi = B.reshape(K, ldb)[:, :N].astype(np.int64)
+    Ci = C.reshape(M, ldc)[:, :N].astype(np.int64)
+    want = Ai @ Bi + Ci
+    assert np.array_equal(out.astype(np.int64), want)
+
+
+# ----- ragged shapes, leading dimensions, alignment -----------------------------
+
+SIZES = [1, 3, 8, 31, 33, 127, 129, 255, 257]
+
+
+@pytest.mark.parametrize("M", [1, 33, 129, 257])
+@pytest.mark.parametrize("N", [1, 31, 255, 257])
+@pytest.mark.parametrize("K", [1, 8, 127])
+def test_ragged_shapes_aligned_ld(M, N, K):
+    Kp, Np = (K + 3) // 4 * 4 + 4, (N + 3) // 4 * 4 + 8
+    check(M, N, K, 0.5, 2.0, dist="normal", seed=M * 7 + N * 3 + K, lda=Kp, ldb=Np, ldc=Np)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 5, 7), (33, 255, 31), (257, 129, 127), (130, 300, 65)])
+def test_ragged_shapes_odd_ld(M, N, K):
+    check(M, N, K, 1.0, 0.0, dist="uniform", seed=5, lda=K + 1, ldb=N + 3, ldc=N + 5)
+
+
+@pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 1)])
+def test_misaligned_pointers(offsets):
+    check(200, 300, 100, 1.0, 1.0, seed=6, offsets=offsets, lda=104, ldb=300, ldc=300)
+
+
+@pytest.mark.parametrize("splits", [2, 3, 4, 5])
+def test_stream_k_forced_splits(splits):
+    check(640, 1024, 1000, 1.0, 0.5, seed=8, variant=2, splits=splits)
+
+
+def test_generic_forced_matches_bound():
+    check(300, 400, 500, -1.5, 0.25, seed=9, variant=0)
+
+
+# ----- conventions ---------------------------------------------------------------
+
+def test_beta_zero_ignores_nan_in_c():
+    M, N, K = 150, 260, 70
+    A, lda, B, ldb, _, _ = inputs("uniform", 10, M, N, K, ldb=260, lda=72)
+    out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, c_fill=float("nan"))
+    assert np.isfinite(out).all()
+
+
+@pytest.mark.parametrize("alpha,K", [(0.0, 64), (1.0, 0)])
+def test_alpha_zero_or_k_zero_scales_c(alpha, K):
+    M, N = 70, 90
+    A, lda, B, ldb, C, ldc = inputs("uniform", 11, M, N, K, lda=max(K, 4), ldb=92, ldc=92)
+    out, _ = run_gemm(M, N, K, alpha, -2.0, A, lda, B, ldb, C, ldc)
+    want = (np.float32(-2.0) * C.reshape(M, ldc)[:, :N]).astype(np.float32)
+    assert np.array_equal(out, want)
+    out0, _ = run_gemm(M, N, K, alpha, 0.0, A, lda, B, ldb, None, ldc, c_fill=float("nan"))
+    assert np.array_equal(out0, np.zeros((M, N), np.float32))
+
+
+def test_stream_k_is_bitwise_deterministic():
+    M, N, K = 512, 2048, 2048
+    A, lda, B, ldb, _, _ = inputs("uniform", 12, M, N, K)
+    first, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, variant=2, splits=3)
+    for _ in range(4):
+        again, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, variant=2, splits=3)
+        assert np.array_equal(first, again)
+
+
+def test_fma_forms_are_bitwise_identical():
+    # Every form issues the same fma sequence per output; only the packing differs.
+    M, N, K = 256, 512, 300
+    A, lda, B, ldb, _, _ = inputs("normal", 13, M, N, K, lda=300, ldb=512)
+    results = []
+    try:
+        for fm, st in [(0, 3), (1, 3), (2, 3), (3, 3), (0, 4)]:
+            sg.set_tile_config(fm, st)
+            out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, variant=1)
+            results.append(out)
+    finally:
+        sg.set_tile_config(2, 3)
+    for r in results[1:]:
+        assert np.array_equal(results[0], r)
+
+
+def test_host_entry_point():
+    M, N, K = 333, 444, 555
+    A, lda, B, ldb, C, ldc = inputs("uniform", 14, M, N, K)
+    Ah = A.reshape(M, K)
+    Bh = B.reshape(K, N)
+    Ch = C.reshape(M, N).copy()
+    sg.run_host(Ah, Bh, Ch, alpha=0.5, beta=2.0)
+    ref, bound = reference(M, N, K, 0.5, 2.0, A, lda, B, ldb, C, ldc)
+    assert_within(Ch, ref, bound, "sgemm_run_host")
+
+
+def test_torch_binding_with_strided_rows():
+    M, N, K = 200, 300, 96
+    A, _, B, _, _, _ = inputs("uniform", 15, M, N, K)
+    At = torch.zeros(M, K + 8, device="cuda")[:, :K]
+    At.copy_(torch.from_numpy(A.reshape(M, K)))
+    Bt = torch.from_numpy(B.reshape(K, N)).cuda()
+    Ct = torch.empty(M, N, device="cuda")
+    sg.run(At, Bt, Ct)
+    ref, bound = reference(M, N, K, 1.0, 0.0, A, K, B, N, None, N)
+    assert_within(Ct.cpu().numpy(), ref, bound, "torch binding")
+
+
+# ----- bounded waits --------------------------------------------------------------
+
+def test_wait_timeout_reports_and_recovers():
+    M, N, K = 512, 1024, 1024
+    A, lda, B, ldb, _, _ = inputs("uniform", 16, M, N, K)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.zeros(M * N, device="cuda")
+    stream = torch.cuda.current_stream()
+    # The producer stops issuing copies at k-iteration 5, so the consumers'
+    # wait for iteration 5 runs out after 2 ms; the kernel records the timeout
+    # and returns.
+    sg.set_wait_timeout_ns(2_000_000, 5)
+    try:
+        st = sg.sgemm_run(M, N, K, 1.0, dA.data_ptr(), lda, dB.data_ptr(), ldb, 0.0,
+                          dC.data_ptr(), N, stream.cuda_stream)
+        assert st == 0
+        assert sg.device_status(stream) == 5  # SGEMM_ERR_DEVICE_TIMEOUT
+    finally:
+        sg.set_wait_timeout_ns(0, -1)
+    assert sg.device_status(stream) == 0
+    # The context and the library still work.
+    out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
+    ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, rows=[0, 255, 511])
+    assert_within(out[[0, 255, 511]], ref, bound, "after timeout")
+
+
+# ----- probes ----------------------------------------------------------------------
+
+def test_probes_run():
+    sink = torch.zeros(4096, device="cuda")
+    buf = torch.ones(1 << 20, device="cuda")
+    stream = torch.cuda.current_stream()
+    for paired in (False, True):
+        flops = sg.probe_ffma(paired, 100, 152, sink.data_ptr(), stream)
+        assert flops == 152 * 512 * 100 * 128 * 2
+    nbytes = sg.probe_read(buf.data_ptr(), buf.numel(), sink.data_ptr(), 152, stream)
+    assert nbytes == 4 * buf.numel()
+    torch.cuda.synchronize()

@@ -1,0 +1,128 @@
+"""Host-side planner checks (no GPU): variant choice, wave arithmetic and the
+stream-K split, on a GPU described by its SM count (152 on GB300)."""
+import math
+
+import pytest
+
+import dense_fp32_sgemm_gb300 as sg
+
+SMS = 152
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    sg.build()
+    sg.set_plan_override(-1, 0)
+    yield
+    sg.set_plan_override(-1, 0)
+
+
+def ceil4(x):
+    return (x + 3) // 4 * 4
+
+
+def plan(M, N, K, aligned_ld=True, **kw):
+    if aligned_ld:
+        kw.setdefault("lda", ceil4(max(K, 1)))
+        kw.setdefault("ldb", ceil4(max(N, 1)))
+        kw.setdefault("ldc", ceil4(max(N, 1)))
+    kw.setdefault("a_addr", 1 << 20)
+    kw.setdefault("b_addr", 2 << 20)
+    kw.setdefault("c_addr", 3 << 20)
+    kw.setdefault("num_sms", SMS)
+    return sg.plan_describe(M, N, K, **kw)
+
+
+def ints(p, *keys):
+    return [int(p[k]) for k in keys]
+
+
+def test_quick_returns():
+    assert plan(0, 5, 7)["variant"] == "none"
+    assert plan(5, 0, 7)["variant"] == "none"
+    assert plan(5, 6, 0)["variant"] == "scale"
+
+
+def test_misaligned_operands_take_generic_kernel():
+    # 1023 x 1025 x 513: lda = 513 and ldb = 1025 break 16-byte row alignment.
+    p = plan(1023, 1025, 513, aligned_ld=False)
+    assert p["variant"] == "generic"
+    p = plan(256, 256, 256, a_addr=(1 << 20) + 4)
+    assert p["variant"] == "generic"
+
+
+def test_2048_cube_uses_stream_k_over_all_sms():
+    # 128 tiles of 128 x 256 would fill 128 of 152 SMs (one partial wave);
+    # stream-K shares their 128 * 64 k-iterations evenly.
+    p = plan(2048, 2048, 2048)
+    assert p["variant"] == "streamk"
+    tm, tn, kt, dp, sk, share, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles",
+                                           "sk_tiles", "sk_share", "grid")
+    assert (tm, tn, kt) == (16, 8, 64)
+    assert dp == 0 and sk == 128
+    assert share == math.ceil(128 * 64 / SMS)
+    assert grid == SMS
+    assert float(p["cost"]) < 64  # beats one whole tile per SM
+
+
+def test_4092_cube_keeps_full_waves_whole():
+    p = plan(4092, 4092, 4092, beta=2.0)
+    tm, tn, kt, dp, sk = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles", "sk_tiles")
+    assert (tm, tn, kt) == (32, 16, 128)
+    assert p["variant"] == "streamk"
+    assert dp % SMS == 0 and dp + sk == tm * tn
+    assert float(p["cost"]) < math.ceil(tm * tn / SMS) * kt
+
+
+def test_exact_waves_stay_data_parallel():
+    # 152 * 2 tiles: two full waves, nothing to balance.
+    p = plan(128 * 19, 256 * 16, 512)
+    assert p["variant"] == "tile"
+    assert ints(p, "dp_tiles", "grid") == [304, SMS]
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (1000, 3000, 77), (8192, 6144, 2048),
+                                   (16, 8192, 8192), (4000, 300, 20000), (129, 257, 33),
+                                   (1, 1, 100000), (5000, 5000, 1)])
+def test_plan_invariants(M, N, K):
+    p = plan(M, N, K)
+    assert p["variant"] in ("tile", "streamk")
+    tm, tn, kt, dp, sk, share, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles",
+                                           "sk_tiles", "sk_share", "grid")
+    T = tm * tn
+    assert tm == math.ceil(M / 128) and tn == math.ceil(N / 256) and kt == math.ceil(K / 32)
+    assert dp + sk == T
+    assert 1 <= grid <= SMS
+    if sk:
+        assert dp % SMS == 0
+        # every stream-K iteration is owned by some CTA of the grid
+        assert share * grid >= sk * kt
+        # pieces per tile stay small
+        assert share >= math.ceil(kt / 4)
+    # the chosen cost never exceeds the data-parallel cost
+    assert float(p["cost"]) <= math.ceil(T / SMS) * kt + 1e-9
+
+
+def test_forced_split_count():
+    sg.set_plan_override(sg.VARIANT_STREAMK, 3)
+    try:
+        p = plan(256, 512, 960)
+        assert p["variant"] == "streamk"
+        kt, share = ints(p, "kt", "sk_share")
+        assert share == math.ceil(kt / 3)
+        # A split too fine for the grid is coarsened until every CTA has one range.
+        sg.set_plan_override(sg.VARIANT_STREAMK, 16)
+        p = plan(4096, 4096, 4096)
+        tm, tn, kt, dp, sk, share, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles",
+                                               "sk_tiles", "sk_share", "grid")
+        assert p["variant"] == "streamk" and share * grid >= sk * kt
+    finally:
+        sg.set_plan_override(-1, 0)
+
+
+def test_forced_generic():
+    sg.set_plan_override(sg.VARIANT_GENERIC, 0)
+    try:
+        assert plan(512, 512, 512)["variant"] == "generic"
+    finally:
+        sg.set_plan_override(-1, 0)
