@@ -24,7 +24,7 @@ std::atomic<int> g_force_variant{-1};
 std::atomic<int> g_force_splits{0};
 std::atomic<unsigned long long> g_timeout_ns{0};
 std::atomic<int> g_skip_loads_from{-1};
-std::atomic<int> g_fma_mode{kFmaPairDupA};
+std::atomic<int> g_fma_mode{kFmaPairMovB};
 std::atomic<int> g_stages{3};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -206,6 +206,34 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
                 tp.counters = w->counters;
             }
             return status_from(launch_tile(fm, st, mapA, mapB, tp, pl.grid, stream));
+        }
+        case kVarSkinny: {
+            const unsigned bit = 1u << (24 + pl.m_tile / 8);
+            if (!(d.configured & bit)) {
+                if (skinny_configure(pl.m_tile) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+                d.configured |= bit;
+            }
+            CUtensorMap mapA, mapB;
+            sgemm_status_t s = encode_2d(&mapA, A, M, K, lda, kSkinnyBK, pl.m_tile);
+            if (s != SGEMM_OK) return s;
+            s = encode_2d(&mapB, B, K, N, ldb, kSkinnyBN, kSkinnyBK);
+            if (s != SGEMM_OK) return s;
+            SkinnyParams sp;
+            sp.M = (int)M; sp.N = (int)N; sp.K = (int)K;
+            sp.slabs = pl.slabs; sp.kt_total = pl.kt_total; sp.share = pl.sk_share;
+            sp.alpha = alpha; sp.beta = beta;
+            sp.A = A; sp.lda = lda; sp.C = C; sp.ldc = ldc; sp.c_vec4 = 0;
+            sp.err = d.err;
+            const unsigned long long to = g_timeout_ns.load();
+            sp.timeout_ns = to ? to : kDefaultTimeoutNs;
+            sp.skip_loads_from = g_skip_loads_from.load();
+            Workspace *w = nullptr;
+            const size_t pbytes = (size_t)2 * pl.grid * kSkinnyMaxM * kSkinnyBN * sizeof(float);
+            s = ensure_workspace(d, stream, pbytes, (size_t)pl.slabs, &w);
+            if (s != SGEMM_OK) return s;
+            sp.partials = w->partials;
+            sp.counters = w->counters;
+            return status_from(launch_skinny(pl.m_tile, mapA, mapB, sp, pl.grid, stream));
         }
         default:
             return SGEMM_ERR_UNSUPPORTED;

@@ -67,6 +67,7 @@ struct SmemLayout {
     static constexpr size_t bar_off = at_off + 2 * at_bytes;
     static constexpr size_t flag_off = bar_off + STAGES * 8;
     static constexpr size_t total = flag_off + 16;
+    static_assert(total <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 };
 
 // ----- accumulators --------------------------------------------------------

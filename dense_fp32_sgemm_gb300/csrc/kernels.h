@@ -77,8 +77,9 @@ cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc,
                          cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
-// Skinny-M kernel: streams B once through a TMA ring, A resident in shared
-// memory, stream-K over (column slab, k) with a fixed-order reduction.
+// Skinny-M kernel (M <= 16): streams B once through a TMA ring together with
+// the matching 32-column slices of A, stream-K over (column slab, k) with a
+// fixed-order reduction.
 // ---------------------------------------------------------------------------
 constexpr int kSkinnyBN = 256;   // columns per slab
 constexpr int kSkinnyBK = 32;    // B rows per TMA stage
@@ -103,11 +104,11 @@ struct SkinnyParams {
     int skip_loads_from;
 };
 
-cudaError_t launch_skinny(int m_tile, const CUtensorMap &mapB, const SkinnyParams &p,
-                          int grid, cudaStream_t stream);
+cudaError_t launch_skinny(int m_tile, const CUtensorMap &mapA, const CUtensorMap &mapB,
+                          const SkinnyParams &p, int grid, cudaStream_t stream);
 size_t skinny_smem_bytes(int m_tile, int share);
 cudaError_t skinny_configure(int m_tile);
-constexpr int kSkinnyStages = 6;
+constexpr int kSkinnyStages = 5;
 
 // ---------------------------------------------------------------------------
 // Measurement probes (same library, used by the benchmark).

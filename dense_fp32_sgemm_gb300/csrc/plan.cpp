@@ -128,8 +128,37 @@ int make_plan(const PlanInput &in, Plan *pl) {
                         in.ldb % 4 == 0 && in.lda < (int64_t(1) << 37) &&
                         in.ldb < (int64_t(1) << 37);
     int want = in.force_variant;
-    if (want == kVarSkinny) want = -1;  // skinny kernel not in this build yet
-    if ((want == kVarTile || want == kVarStreamK) && !tma_ok) return -2;
+    if ((want == kVarTile || want == kVarStreamK || want == kVarSkinny) && !tma_ok) return -2;
+    if (want == kVarSkinny && in.M > kSkinnyMaxM / 2) return -3;
+
+    // M <= 16: every B element feeds at most 16 products, so the product is
+    // bound by streaming B; a 128-row tile would spend 8x the multiply-adds.
+    if (tma_ok && (want == kVarSkinny || (want < 0 && in.M <= kSkinnyMaxM / 2))) {
+        const int64_t G = in.num_sms > 0 ? in.num_sms : 1;
+        const int64_t slabs = ceil_div(in.N, kSkinnyBN);
+        const int64_t KT = ceil_div(in.K, kSkinnyBK);
+        const int64_t total = slabs * KT;
+        if (total < (int64_t(1) << 30)) {
+            int64_t share = ceil_div(total, G);
+            if (in.force_splits > 0) {
+                const int64_t w = ceil_div(KT, in.force_splits);
+                share = w > share ? w : share;
+            }
+            p.variant = kVarSkinny;
+            p.m_tile = in.M <= 8 ? 8 : 16;
+            p.slabs = (int)slabs;
+            p.tiles_n = (int)slabs;
+            p.tiles_m = 1;
+            p.kt_total = (int)KT;
+            p.sk_share = (int)share;
+            p.grid = (int)ceil_div(total, share);
+            p.c_vec4 = 0;
+            p.cost = (double)share;
+            p.reason = "small M: stream B once";
+            *pl = p;
+            return 0;
+        }
+    }
 
     if (want == kVarGeneric || (want < 0 && !tma_ok)) {
         p.variant = kVarGeneric;
@@ -150,9 +179,9 @@ int make_plan(const PlanInput &in, Plan *pl) {
 int describe_plan(const Plan &p, char *buf, size_t len) {
     return snprintf(buf, len,
                     "variant=%s tiles_m=%d tiles_n=%d kt=%d dp_tiles=%d sk_tiles=%d sk_share=%d "
-                    "grid=%d group_m=%d c_vec4=%d cost=%.2f reason=%s",
+                    "grid=%d group_m=%d c_vec4=%d m_tile=%d cost=%.2f reason=%s",
                     variant_name(p.variant), p.tiles_m, p.tiles_n, p.kt_total, p.dp_tiles,
-                    p.sk_tiles, p.sk_share, p.grid, p.group_m, p.c_vec4, p.cost,
+                    p.sk_tiles, p.sk_share, p.grid, p.group_m, p.c_vec4, p.m_tile, p.cost,
                     p.reason ? p.reason : "");
 }
 

@@ -150,9 +150,9 @@ SGEMM_API sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns, int skip
  * multiply-add in the tiled kernel and its number of TMA ring stages.
  * fma_mode: 0 = one FFMA per product; 1 = packed pairs along n with the A
  *   value duplicated in registers; 2 = packed pairs along n with A stored
- *   duplicated in shared memory (default); 3 = packed pairs along m with the
- *   B value duplicated in registers.
- * stages: 3 or 4 (mode 2 supports 3 only).
+ *   duplicated in shared memory; 3 = packed pairs along m with the B value
+ *   duplicated in registers (default).
+ * stages: 3 or 4 (mode 2 supports 3 only; default 3).
  * All forms compute the same IEEE FP32 products and sums.  Returns
  * SGEMM_ERR_INVALID_ARG for a combination this build does not contain.
  */

@@ -12,6 +12,13 @@ GUARD = 1024          # floats of canary before and after every buffer
 CANARY = 12345.678    # float32-exact enough to compare bitwise after a round trip
 
 
+def same_bits(a, b) -> bool:
+    """Bitwise equality (NaN canaries compare equal to themselves)."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    return a.shape == b.shape and bool(np.array_equal(a.view(np.uint32), b.view(np.uint32)))
+
+
 class DeviceMatrix:
     """rows x ld float32 buffer on the GPU at a chosen float offset from a
     256-byte aligned allocation, surrounded by canaries."""
@@ -44,8 +51,8 @@ class DeviceMatrix:
         host = self.to_host() if host is None else host
         lo = host[:GUARD + self.offset]
         hi = host[GUARD + self.offset + self.n:]
-        return bool(np.array_equal(lo, self.host_init[:GUARD + self.offset])
-                    and np.array_equal(hi, self.host_init[GUARD + self.offset + self.n:]))
+        return bool(same_bits(lo, self.host_init[:GUARD + self.offset])
+                    and same_bits(hi, self.host_init[GUARD + self.offset + self.n:]))
 
 
 def run_gemm(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, offsets=(0, 0, 0),
@@ -72,5 +79,5 @@ def run_gemm(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, offsets=(0, 0, 0),
     if ldc > N and M > 0:
         gap = out[:, N:]
         init = dC.region(dC.host_init)[:M * ldc].reshape(M, ldc)[:, N:]
-        assert np.array_equal(gap, init), "C's leading-dimension gap was written"
+        assert same_bits(gap, init), "C's leading-dimension gap was written"
     return out[:, :N].copy(), dC

@@ -98,5 +98,5 @@ def test_hooks_validate(lib):
     with pytest.raises(sg.SgemmError):
         sg.set_wait_timeout_ns(0, -5)
     sg.set_plan_override(-1, 0)
-    sg.set_tile_config(2, 3)
+    sg.set_tile_config(3, 3)
     sg.set_wait_timeout_ns(0, -1)

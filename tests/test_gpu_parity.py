@@ -174,7 +174,7 @@ def test_fma_forms_are_bitwise_identical():
             out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, variant=1)
             results.append(out)
     finally:
-        sg.set_tile_config(2, 3)
+        sg.set_tile_config(3, 3)
     for r in results[1:]:
         assert np.array_equal(results[0], r)
 
@@ -241,3 +241,55 @@ def test_probes_run():
     nbytes = sg.probe_read(buf.data_ptr(), buf.numel(), sink.data_ptr(), 152, stream)
     assert nbytes == 4 * buf.numel()
     torch.cuda.synchronize()
+
+
+# ----- skinny-M streaming kernel ---------------------------------------------------
+
+def ceil4(x):
+    return (x + 3) // 4 * 4
+
+
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 16])
+@pytest.mark.parametrize("N,K", [(256, 32), (300, 70), (1030, 1000), (4096, 513)])
+def test_skinny_shapes(M, N, K):
+    check(M, N, K, 0.5, 2.0, dist="normal", seed=M + N + K, lda=ceil4(K), ldb=ceil4(N),
+          ldc=N + 1, label=f"skinny {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("splits", [0, 2, 3, 7])
+def test_skinny_integers_bit_exact(splits):
+    M, N, K = 16, 1024, 96
+    A, lda, B, ldb, C, ldc = inputs("ints", 17, M, N, K)
+    out, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc, variant=3, splits=splits)
+    want = (A.reshape(M, K).astype(np.int64) @ B.reshape(K, N).astype(np.int64)
+            + C.reshape(M, N).astype(np.int64))
+    assert np.array_equal(out.astype(np.int64), want)
+
+
+def test_skinny_is_bitwise_deterministic():
+    M, N, K = 16, 2048, 4096
+    A, lda, B, ldb, _, _ = inputs("uniform", 18, M, N, K)
+    first, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
+    for _ in range(3):
+        again, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
+        assert np.array_equal(first, again)
+
+
+def test_skinny_wait_timeout_reports_and_recovers():
+    M, N, K = 16, 1024, 4096
+    A, lda, B, ldb, _, _ = inputs("uniform", 19, M, N, K)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.zeros(M * N, device="cuda")
+    stream = torch.cuda.current_stream()
+    sg.set_wait_timeout_ns(2_000_000, 3)
+    try:
+        st = sg.sgemm_run(M, N, K, 1.0, dA.data_ptr(), lda, dB.data_ptr(), ldb, 0.0,
+                          dC.data_ptr(), N, stream.cuda_stream)
+        assert st == 0
+        assert sg.device_status(stream) == 5
+    finally:
+        sg.set_wait_timeout_ns(0, -1)
+    out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
+    ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
+    assert_within(out, ref, bound, "skinny after timeout")

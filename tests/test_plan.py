@@ -82,8 +82,8 @@ def test_exact_waves_stay_data_parallel():
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (1000, 3000, 77), (8192, 6144, 2048),
-                                   (16, 8192, 8192), (4000, 300, 20000), (129, 257, 33),
-                                   (1, 1, 100000), (5000, 5000, 1)])
+                                   (17, 8192, 8192), (4000, 300, 20000), (129, 257, 33),
+                                   (40, 1, 100000), (5000, 5000, 1)])
 def test_plan_invariants(M, N, K):
     p = plan(M, N, K)
     assert p["variant"] in ("tile", "streamk")
@@ -126,3 +126,23 @@ def test_forced_generic():
         assert plan(512, 512, 512)["variant"] == "generic"
     finally:
         sg.set_plan_override(-1, 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 8192, 8192), (1, 4096, 4096), (9, 300, 70),
+                                   (8, 100000, 64)])
+def test_skinny_plan(M, N, K):
+    # M <= 16: the streaming kernel over 256-column slabs and 32-row k-steps,
+    # its (slab, k) plane shared evenly over the grid.
+    p = plan(M, N, K)
+    assert p["variant"] == "skinny"
+    slabs, kt, share, grid, m_tile = ints(p, "tiles_n", "kt", "sk_share", "grid", "m_tile")
+    assert slabs == math.ceil(N / 256) and kt == math.ceil(K / 32)
+    assert m_tile == (8 if M <= 8 else 16)
+    assert share == math.ceil(slabs * kt / SMS)
+    assert grid == math.ceil(slabs * kt / share) and grid <= SMS
+
+
+def test_skinny_16x8192x8192_split():
+    # 32 slabs x 256 k-steps over 152 SMs: 54 k-steps each, about 5 pieces a slab.
+    p = plan(16, 8192, 8192)
+    assert ints(p, "tiles_n", "kt", "sk_share", "grid") == [32, 256, 54, 152]
