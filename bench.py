@@ -64,6 +64,21 @@ def flops_of(cfg):
     return 2.0 * cfg["M"] * cfg["N"] * cfg["K"]
 
 
+def algorithmic_bytes(cfg):
+    """Read A and B once, read C if beta != 0, write C once (FP32)."""
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    return 4 * (M * K + K * N + M * N * (2 if cfg["beta"] != 0 else 1))
+
+
+def measured_hbm_peak():
+    """Copy bandwidth measured by the pool's driver on GB300, else the fallback."""
+    try:
+        v = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"]
+        return float(v), "MEASURED_PEAKS.json hbm_gbs (copy, of measured)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback 6.8 TB/s (of fallback)"
+
+
 # --------------------------------------------------------------------------
 # CPU oracle timing (the reference arm and the cpu_baseline object)
 # --------------------------------------------------------------------------
@@ -277,6 +292,20 @@ def gpu_arm(args, ws, rank, local):
                 break
         return {"burst": round(best, 3), "sustained": round(statistics.median(rates), 3)}
 
+    def read_probe():
+        sink = torch.zeros(4096, device=dev)
+        buf = torch.ones(1 << 28, device=dev)  # 1 GiB, 8x the L2
+        best = 0.0
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            nb = sg.probe_read(buf.data_ptr(), buf.numel(), sink.data_ptr(), SMS_GB300 * 4, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            best = max(best, nb / (e0.elapsed_time(e1) / 1e3) / 1e9)
+        del buf
+        return round(best, 1)
+
     gpu_index = 0
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     if vis and vis.split(",")[local].strip().isdigit():
@@ -318,37 +347,69 @@ def gpu_arm(args, ws, rank, local):
 
     # ---- probes: same process, run as long as the timed GEMMs ----
     probe_s = max(2.0, min(10.0, 2.0 * wall))
+    read_probe_gbs = read_probe()
     ffma = ffma_probe(probe_s, False)
     ffma2 = ffma_probe(probe_s, True)
     probe_peak = max(ffma["sustained"], ffma2["sustained"])
     achieved = flops / mean_s / 1e12
     peak = nominal_fp32_tflops()
-    result["roofline"] = {
-        "bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
-        "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-        "traffic": recorded_traffic("sgemm_tile_kernel", name),
-        "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz (max SM clock)",
-        "probe": {"ffma_tflops": ffma, "ffma2_tflops": ffma2,
-                  "frac_of_probe": round(achieved / probe_peak, 4)},
-        "kernel": "sgemm_tile_kernel" if plan.get("variant") in ("tile", "streamk")
-        else plan.get("variant"),
-    }
-
-    # ---- secondary workload: 4092^3 ----
-    if name != "s3_4092" and not args.no_secondary:
-        cfg2, _, _, C2, dA2, dB2, dC2 = device_inputs("s3_4092")
-        C2dev = dC2.clone()
-        durs2, _ = timed(cfg2, dA2, dB2, dC2, max(3, args.steps // 4), args.warmup)
-        m2 = sum(durs2) / len(durs2)
-        a2 = flops_of(cfg2) / m2 / 1e12
-        result["secondary"] = {
-            "workload": WORKLOADS["s3_4092"], "value": round(flops_of(cfg2) / m2 / 1e9, 2),
-            "unit": "GFLOP/s", "ms_per_step": round(m2 * 1e3, 4),
-            "frac_of_peak": round(a2 / peak, 4), "frac_of_probe": round(a2 / probe_peak, 4),
-            "note": "C is updated in place each step (beta=2), so values grow; the timing "
-                    "is unaffected",
+    hbm_peak, hbm_src = measured_hbm_peak()
+    kernel = {"tile": "sgemm_tile_kernel", "streamk": "sgemm_tile_kernel",
+              "skinny": "sgemm_skinny_kernel", "generic": "sgemm_generic_kernel"}.get(
+                  plan.get("variant"), plan.get("variant"))
+    if plan.get("variant") == "skinny":
+        nbytes = algorithmic_bytes(cfg)
+        result["roofline"] = {
+            "bound": "hbm", "achieved": round(nbytes / mean_s / 1e9, 1), "peak": hbm_peak,
+            "unit": "GB/s", "frac": round(nbytes / mean_s / 1e9 / hbm_peak, 4),
+            "traffic": recorded_traffic(kernel, name), "peak_source": hbm_src,
+            "bytes_per_launch": nbytes, "read_probe_gbs": read_probe_gbs, "kernel": kernel,
+            "fp32": {"achieved_tflops": round(achieved, 3),
+                     "frac_of_probe": round(achieved / probe_peak, 4)},
         }
-        del dA2, dB2, dC2, C2dev
+    else:
+        result["roofline"] = {
+            "bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic(kernel, name),
+            "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz (max SM clock)",
+            "probe": {"ffma_tflops": ffma, "ffma2_tflops": ffma2,
+                      "frac_of_probe": round(achieved / probe_peak, 4)},
+            "kernel": kernel,
+        }
+
+    # ---- the other workloads, timed the same way (fewer steps) ----
+    if not args.no_secondary:
+        others = []
+        for other in ("s3_4092", "s4_rect", "s5_odd", "s6_skinny", "s1_128"):
+            if other == name:
+                continue
+            cfgo, _, _, _, dAo, dBo, dCo = device_inputs(other)
+            durso, _ = timed(cfgo, dAo, dBo, dCo, max(5, args.steps // 10), args.warmup)
+            mo = statistics.median(durso)
+            po = sg.plan_describe(cfgo["M"], cfgo["N"], cfgo["K"], a_addr=dAo.data_ptr(),
+                                  b_addr=dBo.data_ptr(), c_addr=dCo.data_ptr(),
+                                  beta=cfgo["beta"])
+            ent = {"workload": WORKLOADS[other], "plan": po.get("variant"),
+                   "value": round(flops_of(cfgo) / mo / 1e9, 2), "unit": "GFLOP/s",
+                   "ms_per_step": round(mo * 1e3, 4)}
+            ao = flops_of(cfgo) / mo / 1e12
+            if other == "s6_skinny":
+                nbytes = algorithmic_bytes(cfgo)
+                ent["roofline"] = {"bound": "hbm", "achieved": round(nbytes / mo / 1e9, 1),
+                                   "peak": hbm_peak, "unit": "GB/s",
+                                   "frac": round(nbytes / mo / 1e9 / hbm_peak, 4),
+                                   "peak_source": hbm_src, "bytes_per_launch": nbytes,
+                                   "read_probe_gbs": read_probe_gbs}
+            else:
+                ent["frac_of_peak"] = round(ao / peak, 4)
+                ent["frac_of_probe"] = round(ao / probe_peak, 4)
+            if other == "s3_4092":
+                result["secondary"] = dict(ent, note="the second size the metric is quoted at")
+            else:
+                others.append(ent)
+            del dAo, dBo, dCo
+        result["other_workloads"] = others
 
     # ---- end to end through the host entry point ----
     pA = torch.from_numpy(A.reshape(cfg["M"], cfg["K"])).pin_memory()
