@@ -28,7 +28,7 @@ __all__ = [
 STATUS = {
     0: "SGEMM_OK", 1: "SGEMM_ERR_INVALID_ARG", 2: "SGEMM_ERR_ALLOC",
     3: "SGEMM_ERR_TMA", 4: "SGEMM_ERR_LAUNCH", 5: "SGEMM_ERR_DEVICE_TIMEOUT",
-    6: "SGEMM_ERR_NO_DEVICE", 7: "SGEMM_ERR_UNSUPPORTED",
+    6: "SGEMM_ERR_NO_DEVICE", 7: "SGEMM_ERR_UNSUPPORTED", 8: "SGEMM_ERR_SCRATCH_LIMIT",
 }
 VARIANT_AUTO, VARIANT_GENERIC, VARIANT_TILE, VARIANT_STREAMK, VARIANT_SKINNY = -1, 0, 1, 2, 3
 
@@ -38,6 +38,8 @@ _i64, _f32, _vp, _int = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.
 _SIGNATURES = {
     "sgemm_run": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
     "sgemm_run_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
+    "sgemm_run_skinny_noalloc": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp,
+                                        _i64, _vp]),
     "sgemm_status_string": (ctypes.c_char_p, [_int]),
     "sgemm_device_status": (_int, [_vp]),
     "sgemm_plan_describe": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_uint64,

@@ -321,6 +321,7 @@ const char *sgemm_status_string(sgemm_status_t status) {
         case SGEMM_ERR_DEVICE_TIMEOUT: return "SGEMM_ERR_DEVICE_TIMEOUT";
         case SGEMM_ERR_NO_DEVICE: return "SGEMM_ERR_NO_DEVICE";
         case SGEMM_ERR_UNSUPPORTED: return "SGEMM_ERR_UNSUPPORTED";
+        case SGEMM_ERR_SCRATCH_LIMIT: return "SGEMM_ERR_SCRATCH_LIMIT";
         default: return "SGEMM_ERR_UNKNOWN";
     }
 }

@@ -54,7 +54,8 @@ enum {
     SGEMM_ERR_LAUNCH = 4,         /* a kernel launch or CUDA runtime call failed      */
     SGEMM_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait gave up (see below)   */
     SGEMM_ERR_NO_DEVICE = 6,      /* no CUDA device, or it is not sm_103              */
-    SGEMM_ERR_UNSUPPORTED = 7     /* the request names something this build lacks     */
+    SGEMM_ERR_UNSUPPORTED = 7,    /* the request names something this build lacks     */
+    SGEMM_ERR_SCRATCH_LIMIT = 8   /* beyond what sgemm_run_skinny_noalloc's fixed buffer takes */
 };
 
 /*
@@ -91,6 +92,37 @@ SGEMM_API sgemm_status_t sgemm_run(int64_t M, int64_t N, int64_t K, float alpha,
 SGEMM_API sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha,
                               const float *A, int64_t lda, const float *B, int64_t ldb,
                               float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * sgemm_run_skinny_noalloc -- the skinny-M product (M <= 16) with no device
+ * allocation at all.  (The pages have no counterpart; this is a library
+ * convenience.)
+ *
+ * For callers that cannot call cudaMalloc: code running while a framework's
+ * caching allocator owns the device memory, loops that must not allocate after
+ * start-up, or code that must not put a synchronising allocation between
+ * queued work.  sgemm_run allocates its stream-K workspace on first use; this
+ * entry point takes partial sums, tickets and its error word from one fixed
+ * 10 MiB + 16 KiB buffer compiled into the library as a __device__ array,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ * Same arguments, layout and conventions as sgemm_run (device pointers owned
+ * by the caller, queued on `stream`, no host synchronisation), with limits:
+ * M <= 16; N <= 1,048,576 (4096 slabs of 256 columns); a grid of at most 160
+ * CTAs (one per SM); A and B 16-byte aligned with lda and ldb multiples of 4.
+ * Requests beyond them return SGEMM_ERR_SCRATCH_LIMIT before any work is
+ * queued.  The first call on each device looks up the buffer's device address
+ * (no work is queued by that set-up, but make the first call before any stream
+ * capture).  Every call shares the one buffer: calls that overlap on the GPU
+ * (different streams, or concurrent host threads) race and must be ordered by
+ * the caller.  Each call clears the tickets and error word it uses.  A bounded
+ * device wait that gives up is recorded in the buffer's own error word, not
+ * in the word sgemm_device_status() reads.
+ */
+SGEMM_API sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                                  const float *A, int64_t lda, const float *B,
+                                                  int64_t ldb, float beta, float *C, int64_t ldc,
+                                                  void *stream);
 
 /* Human-readable name of a status code (a static string). */
 SGEMM_API const char *sgemm_status_string(sgemm_status_t status);
