@@ -47,7 +47,7 @@ _SIGNATURES = {
                                    ctypes.c_char_p, ctypes.c_size_t]),
     "sgemm_set_plan_override": (_int, [_int, _int]),
     "sgemm_set_wait_timeout_ns": (_int, [ctypes.c_uint64, _int]),
-    "sgemm_set_tile_config": (_int, [_int, _int]),
+    "sgemm_set_tile_config": (_int, [_int, _int, _int]),
     "sgemm_release_workspace": (_int, []),
     "sgemm_probe_ffma": (_int, [_int, _i64, _int, _vp, _vp]),
     "sgemm_probe_read": (_int, [_vp, _i64, _vp, _int, _vp]),
@@ -213,8 +213,9 @@ def set_wait_timeout_ns(timeout_ns: int = 0, skip_loads_from: int = -1) -> None:
            "sgemm_set_wait_timeout_ns")
 
 
-def set_tile_config(fma_mode: int, stages: int) -> None:
-    _check(library().sgemm_set_tile_config(int(fma_mode), int(stages)), "sgemm_set_tile_config")
+def set_tile_config(fma_mode: int = 3, stages: int = 3, micro_m: int = 16) -> None:
+    _check(library().sgemm_set_tile_config(int(fma_mode), int(stages), int(micro_m)),
+           "sgemm_set_tile_config")
 
 
 def release_workspace() -> None:

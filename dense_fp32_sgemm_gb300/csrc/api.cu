@@ -8,6 +8,7 @@
 #include <atomic>
 #include <map>
 #include <mutex>
+#include <set>
 #include <utility>
 
 #include "../../include/sgemm.h"
@@ -26,6 +27,7 @@ std::atomic<unsigned long long> g_timeout_ns{0};
 std::atomic<int> g_skip_loads_from{-1};
 std::atomic<int> g_fma_mode{kFmaPairMovB};
 std::atomic<int> g_stages{3};
+std::atomic<int> g_micro_m{16};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -51,7 +53,8 @@ struct DeviceState {
     int *err = nullptr;  // device error word
     std::map<cudaStream_t, Workspace> ws;
     HostBuffers host;
-    unsigned configured = 0;  // bit per (fma_mode, stages) tile configuration
+    unsigned configured = 0;            // skinny configurations set up
+    std::set<int> configured_tiles;     // tile configurations set up
 };
 
 std::mutex g_mu;
@@ -118,14 +121,15 @@ sgemm_status_t ensure_workspace(DeviceState &d, cudaStream_t stream, size_t part
 // Row-major rows x cols FP32 matrix with leading dimension ld (elements),
 // box of box_rows x box_cols, zero fill outside the matrix.
 sgemm_status_t encode_2d(CUtensorMap *map, const float *base, int64_t rows, int64_t cols,
-                         int64_t ld, int box_cols, int box_rows) {
+                         int64_t ld, int box_cols, int box_rows,
+                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
     const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
                                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? SGEMM_OK : SGEMM_ERR_TMA;
 }
@@ -175,11 +179,11 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
         }
         case kVarTile:
         case kVarStreamK: {
-            const int fm = g_fma_mode.load(), st = g_stages.load();
-            const unsigned bit = 1u << (fm * 8 + st);
-            if (!(d.configured & bit)) {
-                if (tile_configure(fm, st) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-                d.configured |= bit;
+            const int fm = g_fma_mode.load(), st = g_stages.load(), tm = g_micro_m.load();
+            const int key = (fm * 10 + st) * 100 + tm;
+            if (!d.configured_tiles.count(key)) {
+                if (tile_configure(fm, st, tm) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+                d.configured_tiles.insert(key);
             }
             CUtensorMap mapA, mapB;
             sgemm_status_t s = encode_2d(&mapA, A, M, K, lda, kTileBK, kTileBM);
@@ -205,7 +209,7 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
                 tp.partials = w->partials;
                 tp.counters = w->counters;
             }
-            return status_from(launch_tile(fm, st, mapA, mapB, tp, pl.grid, stream));
+            return status_from(launch_tile(fm, st, tm, mapA, mapB, tp, pl.grid, stream));
         }
         case kVarSkinny: {
             const unsigned bit = 1u << (24 + pl.m_tile / 8);
@@ -214,7 +218,8 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
                 d.configured |= bit;
             }
             CUtensorMap mapA, mapB;
-            sgemm_status_t s = encode_2d(&mapA, A, M, K, lda, kSkinnyBK, pl.m_tile);
+            sgemm_status_t s = encode_2d(&mapA, A, M, K, lda, kSkinnyBK, pl.m_tile,
+                                         CU_TENSOR_MAP_SWIZZLE_128B);
             if (s != SGEMM_OK) return s;
             s = encode_2d(&mapB, B, K, N, ldb, kSkinnyBN, kSkinnyBK);
             if (s != SGEMM_OK) return s;
@@ -387,10 +392,11 @@ sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns, int skip_loads_fro
     return SGEMM_OK;
 }
 
-sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages) {
-    if (tile_smem_bytes(fma_mode, stages) == 0) return SGEMM_ERR_INVALID_ARG;
+sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages, int micro_m) {
+    if (tile_smem_bytes(fma_mode, stages, micro_m) == 0) return SGEMM_ERR_INVALID_ARG;
     g_fma_mode.store(fma_mode);
     g_stages.store(stages);
+    g_micro_m.store(micro_m);
     return SGEMM_OK;
 }
 

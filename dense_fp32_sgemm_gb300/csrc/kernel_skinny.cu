@@ -8,14 +8,22 @@
 // Work: N is cut into slabs of 256 columns; the (slab, k) plane is shared
 // out in equal contiguous ranges of 32-row k-iterations to a persistent grid
 // (stream-K over the slabs).  For each k-iteration a TMA copy brings the
-// 32 x 256 block of B and the M x 32 block of A into a ring of shared-memory
-// stages completed on mbarriers, several stages ahead, so enough bytes are in
-// flight to keep HBM busy.  The threads rewrite A's block k-major with each
-// value duplicated, (a, a), so a 128-bit shared load gives two packed
-// operands for __ffma2_rn; a lane owns 8 columns (two groups of four, 128
-// apart) and the eight warps take the 32 rows of a block round-robin.
+// 32 x 256 block of B and the M x 32 block of A (128-byte swizzled rows) into
+// a ring of shared-memory stages completed on mbarriers, several stages
+// ahead, so enough bytes are in flight to keep HBM busy.
 //
-// After a unit the eight warps' partial sums are added in warp order through
+// 8 warps: lane l of every warp owns columns 4l .. 4l+3 and 128+4l .. 128+4l+3
+// of the slab (two groups of four, 128 apart, so a quarter-warp's 128-bit
+// loads cover 32 consecutive banks); warp g takes rows g, g + 8, g + 16,
+// g + 24 of each block.  Six 128-bit shared loads (16 A values, 8 B values)
+// feed 64 packed multiply-adds per row.  A warp rewrites only
+// the four A columns it needs k-major into its own corner of shared memory,
+// so no CTA-wide barrier is needed inside a unit: warps run through the
+// stages independently, and the last warp to finish with a stage (a counter
+// in shared memory) refills it.  The update is the packed FP32 fma
+// (__ffma2_rn) on pairs along m: (a_m, a_m+1) * (b_n, b_n).
+//
+// After a unit the eight row groups' sums are added in group order through
 // shared memory; a unit covering part of a slab writes them to a fixed slot
 // and the last CTA to arrive adds the pieces in CTA order (no CTA waits for
 // another), then applies alpha and beta.
@@ -26,47 +34,33 @@
 namespace sgemm {
 namespace {
 
-constexpr int SBN = kSkinnyBN;      // 256 columns per slab
-constexpr int SBK = kSkinnyBK;      // 32 rows of B per stage
+constexpr int SBN = kSkinnyBN;       // 256 columns per slab
+constexpr int SBK = kSkinnyBK;       // 32 rows of B per stage
 constexpr int SNT = kSkinnyThreads;  // 256 threads
 constexpr int SSTAGES = kSkinnyStages;
 constexpr int WARPS = SNT / 32;
-constexpr int CPL = 8;  // columns per lane
-static_assert(32 * CPL == SBN, "one warp covers a slab row");
+constexpr int GROUPS = WARPS;              // row groups: one per warp
+constexpr int RPW = SBK / GROUPS;          // rows of a block per warp
+constexpr int CPL = 8;                     // columns per lane
+static_assert(RPW == 4 && GROUPS == 8 && 32 * CPL == SBN, "warp layout assumes 8 warps");
 
 template <int MT>
 struct SkinnyLayout {
-    static constexpr int a_floats = MT * SBK;
+    static constexpr int a_floats = MT * SBK;  // M x 32, 128-byte rows, swizzled
     static constexpr int b_floats = SBK * SBN;
     static constexpr int stage_floats = a_floats + b_floats;
     static constexpr size_t stage_bytes = size_t(stage_floats) * 4;
-    static constexpr int at_floats = SBK * 2 * MT;  // duplicated, k-major
-    static constexpr int red_floats = WARPS * 4 * SBN;  // 4 rows of M per round
+    static_assert(stage_bytes % 1024 == 0, "stages must keep 1024-byte alignment");
+    static constexpr int at_floats = RPW * MT;  // per warp: 4 k x MT m
+    static constexpr int red_floats = GROUPS * 4 * SBN;
     static constexpr size_t at_off = SSTAGES * stage_bytes;
-    static constexpr size_t red_off = at_off + 2 * size_t(at_floats) * 4;
+    static constexpr size_t red_off = at_off + size_t(WARPS) * at_floats * 4;
     static constexpr size_t bar_off = red_off + size_t(red_floats) * 4;
-    static constexpr size_t flag_off = bar_off + SSTAGES * 8;
+    static constexpr size_t cnt_off = bar_off + SSTAGES * 8;
+    static constexpr size_t flag_off = cnt_off + SSTAGES * 4 * 2;
     static constexpr size_t total = flag_off + 16;
     static constexpr uint32_t tx_bytes = stage_floats * 4;
     static_assert(total <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
-};
-
-// One unit of work: k-iterations [k0, k1) of slab `slab`.
-struct SkinnyIter {
-    int u, end;
-    __device__ __forceinline__ void init(const SkinnyParams &p, int cta) {
-        const int total = p.slabs * p.kt_total;
-        u = min(cta * p.share, total);
-        end = min(u + p.share, total);
-    }
-    __device__ __forceinline__ bool next(const SkinnyParams &p, int &slab, int &k0, int &k1) {
-        if (u >= end) return false;
-        slab = u / p.kt_total;
-        k0 = u - slab * p.kt_total;
-        k1 = min(p.kt_total, k0 + (end - u));
-        u += k1 - k0;
-        return true;
-    }
 };
 
 __device__ __forceinline__ int skinny_slot(const SkinnyParams &p, int cta, int slab) {
@@ -75,17 +69,10 @@ __device__ __forceinline__ int skinny_slot(const SkinnyParams &p, int cta, int s
     return 2 * cta + (k0 == 0 ? 1 : 0);
 }
 
-// A block (MT rows x 32 k, k fastest) -> k-major duplicated pairs.
-template <int MT>
-__device__ __forceinline__ void skinny_transpose(const float *raw, float *at, int tid) {
-    if (tid < MT * (SBK / 4)) {
-        const int m = tid / (SBK / 4), kc = tid % (SBK / 4);
-        const float4 v = ld_shared_f4(raw + m * SBK + kc * 4);
-        const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<float2 *>(at + (kc * 4 + i) * 2 * MT + 2 * m) = make_float2(e[i], e[i]);
-    }
+// Element (m, k) of the TMA-loaded A block: rows of 32 floats whose 16-byte
+// chunks are XOR-swizzled with (row mod 8).
+__device__ __forceinline__ float a_elem(const float *raw, int m, int k) {
+    return raw[m * SBK + ((((k >> 2) ^ (m & 7)) << 2) | (k & 3))];
 }
 
 template <int MT>
@@ -95,21 +82,41 @@ __global__ void __launch_bounds__(SNT, 1)
     using L = SkinnyLayout<MT>;
     extern __shared__ __align__(1024) uint8_t smem[];
     float *stages = reinterpret_cast<float *>(smem);
-    float *at_buf = reinterpret_cast<float *>(smem + L::at_off);
     float *red = reinterpret_cast<float *>(smem + L::red_off);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off);
+    int *release = reinterpret_cast<int *>(smem + L::cnt_off);
+    volatile int *issued = reinterpret_cast<volatile int *>(smem + L::cnt_off + SSTAGES * 4);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + L::flag_off);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = warp;
     const int cta = blockIdx.x;
+    float *at_w = reinterpret_cast<float *>(smem + L::at_off) + warp * L::at_floats;
 
-    SkinnyIter it0;
-    it0.init(p, cta);
-    const int q_total = it0.end - it0.u;
+    const int total = p.slabs * p.kt_total;
+    const int u0 = min(cta * p.share, total);
+    const int q_total = min(u0 + p.share, total) - u0;
     if (q_total <= 0) return;
 
+    // Copy of position q (the CTA's q-th k-iteration) into stage q % SSTAGES.
+    auto issue = [&](int q) {
+        if (p.skip_loads_from >= 0 && q >= p.skip_loads_from) return;
+        const int s = q % SSTAGES;
+        const int u = u0 + q;
+        const int slab = u / p.kt_total, k = u - slab * p.kt_total;
+        float *sa = stages + s * L::stage_floats;
+        issued[s] = q;
+        mbar_arrive_expect_tx(&full[s], L::tx_bytes);
+        tma_load_2d(sa, &mapA, &full[s], k * SBK, 0);
+        tma_load_2d(sa + L::a_floats, &mapB, &full[s], slab * SBN, k * SBK);
+    };
+
     if (tid == 0) {
-        for (int s = 0; s < SSTAGES; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < SSTAGES; ++s) {
+            mbar_init(&full[s], 1);
+            release[s] = 0;
+            issued[s] = -1;
+        }
         flags[0] = 0;
         flags[1] = 0;
         fence_barrier_init();
@@ -117,116 +124,133 @@ __global__ void __launch_bounds__(SNT, 1)
         prefetch_tensormap(&mapB);
     }
     __syncthreads();
-
-    // ---- copy producer (thread 0) ----
-    SkinnyIter prod = it0;
-    int pq = 0, p_slab = 0, p_k = 0, p_k1 = 0;
-    auto issue_next = [&]() {
-        if (pq >= q_total) return;
-        if (p.skip_loads_from >= 0 && pq >= p.skip_loads_from) return;
-        if (p_k >= p_k1) prod.next(p, p_slab, p_k, p_k1);
-        const int s = pq % SSTAGES;
-        float *sa = stages + s * L::stage_floats;
-        float *sb = sa + L::a_floats;
-        mbar_arrive_expect_tx(&full[s], L::tx_bytes);
-        tma_load_2d(sa, &mapA, &full[s], p_k * SBK, 0);
-        tma_load_2d(sb, &mapB, &full[s], p_slab * SBN, p_k * SBK);
-        ++p_k;
-        ++pq;
-    };
     if (tid == 0)
-        for (int s = 0; s < SSTAGES; ++s) issue_next();
+        for (int q = 0; q < SSTAGES && q < q_total; ++q) issue(q);
 
-    SkinnyIter cons = it0;
     int q = 0;
     bool aborted = false;
-    if (!mbar_wait_bounded(&full[0], 0, p.timeout_ns)) {
-        flags[0] = 1;
-        atomicOr(p.err, kErrWaitTimeout);
-    }
-    skinny_transpose<MT>(stages, at_buf, tid);
-    __syncthreads();
-    if (flags[0]) aborted = true;
+    int timed_out = 0;  // this thread saw a wait run out (made uniform at unit end)
+    while (q < q_total && !aborted) {
+        const int u = u0 + q;
+        const int slab = u / p.kt_total;
+        const int k0 = u - slab * p.kt_total;
+        const int k1 = min(p.kt_total, k0 + (q_total - q));
 
-    int slab, k0, k1;
-    while (!aborted && cons.next(p, slab, k0, k1)) {
-        float2 acc[MT][CPL / 2];
+        float2 acc[MT / 2][CPL];  // acc[ip][j] = (C[2ip][n_j], C[2ip+1][n_j])
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
+        for (int i = 0; i < MT / 2; ++i)
 #pragma unroll
-            for (int j = 0; j < CPL / 2; ++j) acc[m][j] = make_float2(0.f, 0.f);
+            for (int j = 0; j < CPL; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
         for (int kt = k0; kt < k1; ++kt, ++q) {
             const int s = q % SSTAGES;
-            if (q + 1 < q_total) {
-                const int s1 = (q + 1) % SSTAGES;
-                if (!mbar_wait_bounded(&full[s1], ((q + 1) / SSTAGES) & 1, p.timeout_ns)) {
-                    flags[0] = 1;
-                    atomicOr(p.err, kErrWaitTimeout);
-                }
-                skinny_transpose<MT>(stages + s1 * L::stage_floats,
-                                     at_buf + ((q + 1) & 1) * L::at_floats, tid);
+            // After a timeout anywhere in the CTA (flags[0], a hint) the
+            // remaining waits are skipped; the garbage computed is discarded.
+            if (!timed_out && !flags[0] &&
+                !mbar_wait_bounded(&full[s], (q / SSTAGES) & 1, p.timeout_ns)) {
+                timed_out = 1;
+                flags[0] = 1;
+                atomicOr(p.err, kErrWaitTimeout);
             }
-            const float *at = at_buf + (q & 1) * L::at_floats;
-            const float *bs = stages + s * L::stage_floats + L::a_floats;
+            const float *raw = stages + s * L::stage_floats;
+            const float *bs = raw + L::a_floats;
+            // This warp's A columns k = g + 8 * kk, k-major: at_w[kk * MT + m].
 #pragma unroll
-            for (int r = 0; r < SBK / WARPS; ++r) {
-                const int k = warp + r * WARPS;
-                const float4 b0 = ld_shared_f4(bs + k * SBN + lane * 4);
-                const float4 b1 = ld_shared_f4(bs + k * SBN + 128 + lane * 4);
-                const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                                      make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+            for (int e = lane; e < RPW * MT; e += 32) {
+                const int m = e % MT, kk = e / MT;
+                at_w[kk * MT + m] = a_elem(raw, m, g + GROUPS * kk);
+            }
+            __syncwarp();
+
+            const float *bcol = bs + lane * 4;
+            float4 bf[2][2];
+            float4 af[2][MT / 4];
+            bf[0][0] = ld_shared_f4(bcol + g * SBN);
+            bf[0][1] = ld_shared_f4(bcol + g * SBN + 128);
 #pragma unroll
-                for (int m2 = 0; m2 < MT / 2; ++m2) {
-                    const float4 a = ld_shared_f4(at + k * 2 * MT + m2 * 4);
-                    const float2 a0 = make_float2(a.x, a.y), a1 = make_float2(a.z, a.w);
+            for (int r = 0; r < MT / 4; ++r) af[0][r] = ld_shared_f4(at_w + r * 4);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        acc[2 * m2][j] = __ffma2_rn(a0, bp[j], acc[2 * m2][j]);
-                        acc[2 * m2 + 1][j] = __ffma2_rn(a1, bp[j], acc[2 * m2 + 1][j]);
+            for (int kk = 0; kk < RPW; ++kk) {
+                const int cur = kk & 1, nxt = cur ^ 1;
+                if (kk + 1 < RPW) {
+                    const float *brow = bcol + (g + GROUPS * (kk + 1)) * SBN;
+                    bf[nxt][0] = ld_shared_f4(brow);
+                    bf[nxt][1] = ld_shared_f4(brow + 128);
+#pragma unroll
+                    for (int r = 0; r < MT / 4; ++r)
+                        af[nxt][r] = ld_shared_f4(at_w + (kk + 1) * MT + r * 4);
+                }
+                const float b[CPL] = {bf[cur][0].x, bf[cur][0].y, bf[cur][0].z, bf[cur][0].w,
+                                      bf[cur][1].x, bf[cur][1].y, bf[cur][1].z, bf[cur][1].w};
+#pragma unroll
+                for (int r = 0; r < MT / 4; ++r) {
+                    const float2 a01 = make_float2(af[cur][r].x, af[cur][r].y);
+                    const float2 a23 = make_float2(af[cur][r].z, af[cur][r].w);
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) {
+                        const float2 bb = make_float2(b[j], b[j]);
+                        acc[2 * r][j] = __ffma2_rn(a01, bb, acc[2 * r][j]);
+                        acc[2 * r + 1][j] = __ffma2_rn(a23, bb, acc[2 * r + 1][j]);
                     }
                 }
             }
-            __syncthreads();
-            if (flags[0]) {
-                aborted = true;
-                ++q;
-                break;
+            __syncwarp();
+            // Release the stage; the last of the 16 warps refills it.
+            if (lane == 0) {
+                __threadfence_block();
+                const int old = atomicAdd(&release[s], 1);
+                if (old == WARPS - 1) {
+                    release[s] = 0;
+                    if (q + SSTAGES < q_total && !flags[0]) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        issue(q + SSTAGES);
+                    }
+                }
             }
-            if (tid == 0) issue_next();
         }
-        if (aborted) break;
 
-        // ---- add the eight warps' sums in warp order; thread t owns column t ----
+        // Abort uniformly if any thread of the CTA gave up a wait in this unit.
+        if (__syncthreads_or(timed_out)) {
+            aborted = true;
+            break;
+        }
+
+        // ---- add the eight row groups' sums in group order ----
+        // Thread t owns column t and all MT rows.
         float fin[MT];
 #pragma unroll
-        for (int mr = 0; mr < MT / 4; ++mr) {
+        for (int r = 0; r < MT / 4; ++r) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int m = mr * 4 + i;
-                float *dst = red + (warp * 4 + i) * SBN;
-                *reinterpret_cast<float4 *>(dst + lane * 4) =
-                    make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
-                *reinterpret_cast<float4 *>(dst + 128 + lane * 4) =
-                    make_float4(acc[m][2].x, acc[m][2].y, acc[m][3].x, acc[m][3].y);
+                const int m = 4 * r + i;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float4 v;
+                    v.x = (m & 1) ? acc[m >> 1][4 * h + 0].y : acc[m >> 1][4 * h + 0].x;
+                    v.y = (m & 1) ? acc[m >> 1][4 * h + 1].y : acc[m >> 1][4 * h + 1].x;
+                    v.z = (m & 1) ? acc[m >> 1][4 * h + 2].y : acc[m >> 1][4 * h + 2].x;
+                    v.w = (m & 1) ? acc[m >> 1][4 * h + 3].y : acc[m >> 1][4 * h + 3].x;
+                    *reinterpret_cast<float4 *>(red + (g * 4 + i) * SBN + h * 128 + lane * 4) = v;
+                }
             }
             __syncthreads();
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                float sum = red[(0 * 4 + i) * SBN + tid];
+                float sum = red[i * SBN + tid];
 #pragma unroll
-                for (int w = 1; w < WARPS; ++w) sum += red[(w * 4 + i) * SBN + tid];
-                fin[mr * 4 + i] = sum;
+                for (int gg = 1; gg < GROUPS; ++gg) sum += red[(gg * 4 + i) * SBN + tid];
+                fin[4 * r + i] = sum;
             }
             __syncthreads();
         }
 
-        const int n = slab * SBN + tid;
+        const int col = tid;
+        const int n = slab * SBN + col;
         bool write_c = true;
         if (!(k0 == 0 && k1 == p.kt_total)) {
             float *slot = p.partials + (size_t)skinny_slot(p, cta, slab) * (kSkinnyMaxM * SBN);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) __stcg(slot + m * SBN + tid, fin[m]);
+            for (int m = 0; m < MT; ++m) __stcg(slot + m * SBN + col, fin[m]);
             __threadfence();
             __syncthreads();
             const int c_first = (slab * p.kt_total) / p.share;
@@ -241,19 +265,20 @@ __global__ void __launch_bounds__(SNT, 1)
                 __threadfence();
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    float s = 0.f;
+                    float sum = 0.f;
                     for (int cc = c_first; cc <= c_last; ++cc) {
                         const float v =
                             (cc == cta) ? fin[m]
                                         : __ldcg(p.partials +
                                                  (size_t)skinny_slot(p, cc, slab) * (kSkinnyMaxM * SBN) +
-                                                 m * SBN + tid);
-                        s = (cc == c_first) ? v : s + v;
+                                                 m * SBN + col);
+                        sum = (cc == c_first) ? v : sum + v;
                     }
-                    fin[m] = s;
+                    fin[m] = sum;
                 }
                 if (tid == 0) p.counters[slab] = 0;
             }
+            __syncthreads();  // flags[1] is rewritten by the next unit
         }
         if (write_c && n < p.N) {
 #pragma unroll
@@ -269,8 +294,12 @@ __global__ void __launch_bounds__(SNT, 1)
     }
 
     if (aborted && tid == 0) {
-        for (int j = q; j < pq; ++j) {
-            if (!mbar_wait_bounded(&full[j % SSTAGES], (j / SSTAGES) & 1, 1000000000ull)) {
+        // Wait (bounded) for the last copy issued into every stage, so none
+        // lands in shared memory after this CTA has exited.
+        for (int s = 0; s < SSTAGES; ++s) {
+            const int last = issued[s];
+            if (last < 0) continue;
+            if (!mbar_wait_bounded(&full[s], (last / SSTAGES) & 1, 1000000000ull)) {
                 atomicOr(p.err, kErrDrainTimeout);
                 break;
             }

@@ -43,16 +43,30 @@ namespace {
 constexpr int BM = kTileBM;
 constexpr int BN = kTileBN;
 constexpr int BK = kTileBK;
-constexpr int NT = kTileThreads;
-constexpr int TM = 16;
 constexpr int TN = 8;
 constexpr int A_STAGE_FLOATS = BM * BK;
 constexpr int B_STAGE_FLOATS = BK * BN;
 constexpr int STAGE_FLOATS = A_STAGE_FLOATS + B_STAGE_FLOATS;
 constexpr uint32_t STAGE_TX_BYTES = STAGE_FLOATS * 4;
 constexpr int TILE_FLOATS = BM * BN;
-static_assert(NT * TM * TN == TILE_FLOATS, "threads x micro-tile must cover the tile");
+constexpr int FILL_THREADS = BM * BK / 16;  // one 4 x 4 block of the A slice each
 static_assert(BK == 32 && BM == 128, "the transposing fill assumes 32 x 128 A slices");
+
+// Thread organisation for a micro-tile of TM rows x 8 columns.  A warp is 4
+// (rows) x 8 (columns) threads; a thread's rows come in groups of four, 16
+// apart, its columns in two groups of four, 32 apart.  TM = 16: 8 warps of
+// 64 x 64 (two warps per scheduler, up to 255 registers); TM = 8: 16 warps of
+// 32 x 64 (four per scheduler, at most 128 registers).
+template <int TM_>
+struct Cfg {
+    static constexpr int TM = TM_;
+    static constexpr int NT = TILE_FLOATS / (TM * TN);
+    static constexpr int WARP_M = 4 * TM;
+    static constexpr int WARP_N = 8 * TN;
+    static constexpr int WARPS_N = BN / WARP_N;
+    static constexpr int RG = TM / 4;  // row groups
+    static_assert(NT % 32 == 0 && NT >= FILL_THREADS, "bad thread count");
+};
 
 template <int FM>
 struct AtRow {
@@ -66,41 +80,51 @@ struct SmemLayout {
     static constexpr size_t at_off = STAGES * stage_bytes;
     static constexpr size_t bar_off = at_off + 2 * at_bytes;
     static constexpr size_t flag_off = bar_off + STAGES * 8;
-    static constexpr size_t total = flag_off + 16;
+    static constexpr size_t prod_off = flag_off + 16;
+    static constexpr size_t total = prod_off + 32;
     static_assert(total <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 };
 
 // ----- accumulators --------------------------------------------------------
-template <int FM>
-struct Acc;
-
-template <>
-struct Acc<kFmaScalar> {
+template <int TM>
+struct AccScalar {
     float v[TM][TN];
     __device__ __forceinline__ float &at(int i, int j) { return v[i][j]; }
 };
 
+template <int TM>
 struct AccPairN {  // v[i][jp] = (C[i][2jp], C[i][2jp+1])
     float2 v[TM][TN / 2];
     __device__ __forceinline__ float &at(int i, int j) {
         return (j & 1) ? v[i][j >> 1].y : v[i][j >> 1].x;
     }
 };
-template <>
-struct Acc<kFmaPairMovA> : AccPairN {};
-template <>
-struct Acc<kFmaPairDupA> : AccPairN {};
 
-template <>
-struct Acc<kFmaPairMovB> {  // v[ip][j] = (C[2ip][j], C[2ip+1][j])
+template <int TM>
+struct AccPairM {  // v[ip][j] = (C[2ip][j], C[2ip+1][j])
     float2 v[TM / 2][TN];
     __device__ __forceinline__ float &at(int i, int j) {
         return (i & 1) ? v[i >> 1][j].y : v[i >> 1][j].x;
     }
 };
 
-template <int FM>
-__device__ __forceinline__ void acc_zero(Acc<FM> &acc) {
+template <int FM, int TM>
+struct AccSel {
+    using type = AccPairN<TM>;
+};
+template <int TM>
+struct AccSel<kFmaScalar, TM> {
+    using type = AccScalar<TM>;
+};
+template <int TM>
+struct AccSel<kFmaPairMovB, TM> {
+    using type = AccPairM<TM>;
+};
+template <int FM, int TM>
+using Acc = typename AccSel<FM, TM>::type;
+
+template <int FM, int TM>
+__device__ __forceinline__ void acc_zero(Acc<FM, TM> &acc) {
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -108,11 +132,11 @@ __device__ __forceinline__ void acc_zero(Acc<FM> &acc) {
 }
 
 // ----- fragments -------------------------------------------------------------
-// A fragment for one k: thread rows r*16 + ty*4 + (0..3), r = 0..3.
+// A fragment for one k: thread rows r*16 + ty*4 + (0..3), r < TM/4.
 // B fragment for one k: thread columns c*32 + tx*4 + (0..3), c = 0..1.
-template <int FM>
+template <int FM, int TM>
 struct Frag {
-    float4 a[FM == kFmaPairDupA ? 8 : 4];
+    float4 a[FM == kFmaPairDupA ? TM / 2 : TM / 4];
     float4 b[2];
 };
 
@@ -127,52 +151,51 @@ struct FragPtrs {
     int b;       // B: first column group
 };
 
-template <int FM>
+template <int FM, int TM>
 __device__ __forceinline__ FragPtrs frag_ptrs(int kblk, int wm, int wn, int ty, int tx) {
     constexpr int ROW = AtRow<FM>::value;
     const int swz = (kblk >> 2) & 7;
     FragPtrs f;
     if (FM == kFmaPairDupA) {
-        // chunk(r, p) = wm*32 + r*8 + ty*2 + p; the XOR touches only the low
-        // three bits, (2*ty + p).
+        // chunk(r, p) = wm*2*TM + r*8 + ty*2 + p; the XOR touches only the
+        // low three bits, (2*ty + p).
         const int x0 = (2 * ty) ^ swz;
-        f.a0 = kblk * ROW + (wm * 32 + x0) * 4;
-        f.a1 = kblk * ROW + (wm * 32 + (x0 ^ 1)) * 4;
+        f.a0 = kblk * ROW + (wm * 2 * TM + x0) * 4;
+        f.a1 = kblk * ROW + (wm * 2 * TM + (x0 ^ 1)) * 4;
     } else {
-        // chunk(r) = wm*16 + r*4 + ty; low three bits are (r&1)*4 + ty.
+        // chunk(r) = wm*TM + r*4 + ty; low three bits are (r&1)*4 + ty.
         const int x0 = ty ^ swz;
-        f.a0 = kblk * ROW + (wm * 16 + x0) * 4;
-        f.a1 = kblk * ROW + (wm * 16 + (x0 ^ 4)) * 4;
+        f.a0 = kblk * ROW + (wm * TM + x0) * 4;
+        f.a1 = kblk * ROW + (wm * TM + (x0 ^ 4)) * 4;
     }
     f.b = kblk * BN + wn * 64 + tx * 4;
     return f;
 }
 
-template <int FM>
+template <int FM, int TM>
 __device__ __forceinline__ void load_frag(const float *at, const float *bs, const FragPtrs &fp,
-                                          int j, Frag<FM> &f) {
+                                          int j, Frag<FM, TM> &f) {
     constexpr int ROW = AtRow<FM>::value;
     const float *pa0 = at + fp.a0 + j * ROW;
     const float *pa1 = at + fp.a1 + j * ROW;
     if (FM == kFmaPairDupA) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < TM / 4; ++r) {
             f.a[2 * r + 0] = ld_shared_f4(pa0 + r * 32);
             f.a[2 * r + 1] = ld_shared_f4(pa1 + r * 32);
         }
     } else {
-        f.a[0] = ld_shared_f4(pa0);
-        f.a[1] = ld_shared_f4(pa1);
-        f.a[2] = ld_shared_f4(pa0 + 32);
-        f.a[3] = ld_shared_f4(pa1 + 32);
+#pragma unroll
+        for (int r = 0; r < TM / 4; ++r)
+            f.a[r] = ld_shared_f4(((r & 1) ? pa1 : pa0) + (r >> 1) * 32);
     }
     const float *pb = bs + fp.b + j * BN;
     f.b[0] = ld_shared_f4(pb);
     f.b[1] = ld_shared_f4(pb + 32);
 }
 
-template <int FM>
-__device__ __forceinline__ void fma_frag(const Frag<FM> &f, Acc<FM> &acc) {
+template <int FM, int TM>
+__device__ __forceinline__ void fma_frag(const Frag<FM, TM> &f, Acc<FM, TM> &acc) {
     if (FM == kFmaScalar) {
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
@@ -182,7 +205,7 @@ __device__ __forceinline__ void fma_frag(const Frag<FM> &f, Acc<FM> &acc) {
                 acc.at(i, j) = __fmaf_rn(a, comp(f.b[j >> 2], j & 3), acc.at(i, j));
         }
     } else if (FM == kFmaPairMovA || FM == kFmaPairDupA) {
-        auto &v = reinterpret_cast<AccPairN &>(acc).v;
+        auto &v = reinterpret_cast<AccPairN<TM> &>(acc).v;
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
             float2 a2;
@@ -201,7 +224,7 @@ __device__ __forceinline__ void fma_frag(const Frag<FM> &f, Acc<FM> &acc) {
             }
         }
     } else {  // kFmaPairMovB
-        auto &v = reinterpret_cast<Acc<kFmaPairMovB> &>(acc).v;
+        auto &v = reinterpret_cast<AccPairM<TM> &>(acc).v;
 #pragma unroll
         for (int ip = 0; ip < TM / 2; ++ip) {
             const float4 &a = f.a[ip >> 1];
@@ -216,27 +239,25 @@ __device__ __forceinline__ void fma_frag(const Frag<FM> &f, Acc<FM> &acc) {
 }
 
 // One K slice (32 k) of outer products from the transposed A slice `at` and
-// the B slice `bs`.  Fragments are double-buffered in registers: the loads
-// for k+1 are issued before the multiply-adds of k.
-template <int FM>
-__device__ __forceinline__ void compute_slice(const float *at, const float *bs, Acc<FM> &acc,
+// the B slice `bs`, fully unrolled: fragments are double-buffered in
+// registers (the loads for k+1 are issued before the multiply-adds of k) and
+// every shared-memory offset but the per-thread base is a constant, which
+// gives the instruction scheduler the whole slice to interleave.  (Measured
+// on GB300: 4-k blocks in a loop ran about 8% slower.)
+template <int FM, int TM>
+__device__ __forceinline__ void compute_slice(const float *at, const float *bs, Acc<FM, TM> &acc,
                                               int wm, int wn, int ty, int tx) {
-    Frag<FM> f[2];
-    FragPtrs cur = frag_ptrs<FM>(0, wm, wn, ty, tx);
-    load_frag<FM>(at, bs, cur, 0, f[0]);
-#pragma unroll 1
-    for (int kb = 0; kb < BK; kb += 4) {
-        // The last prefetch of the slice wraps to row 0: in bounds, unused.
-        const FragPtrs nxt = frag_ptrs<FM>((kb + 4) & (BK - 1), wm, wn, ty, tx);
+    Frag<FM, TM> f[2];
+    load_frag<FM, TM>(at, bs, frag_ptrs<FM, TM>(0, wm, wn, ty, tx), 0, f[0]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (j < 3)
-                load_frag<FM>(at, bs, cur, j + 1, f[(j + 1) & 1]);
-            else
-                load_frag<FM>(at, bs, nxt, 0, f[(j + 1) & 1]);
-            fma_frag<FM>(f[j & 1], acc);
+    for (int k = 0; k < BK; ++k) {
+        if (k + 1 < BK) {
+            // Row k+1 sits in the 4-row block starting at (k+1) & ~3, whose
+            // swizzle the pointers carry.
+            const FragPtrs fp = frag_ptrs<FM, TM>((k + 1) & ~3, wm, wn, ty, tx);
+            load_frag<FM, TM>(at, bs, fp, (k + 1) & 3, f[(k + 1) & 1]);
         }
-        cur = nxt;
+        fma_frag<FM, TM>(f[k & 1], acc);
     }
 }
 
@@ -248,6 +269,7 @@ __device__ __forceinline__ void compute_slice(const float *at, const float *bs, 
 template <int FM>
 __device__ __forceinline__ void transpose_slice(const float *raw, float *at, int tid) {
     constexpr int ROW = AtRow<FM>::value;
+    if (tid >= FILL_THREADS) return;
     const int kc = tid & 7;
     const int mb = tid >> 3;
     float4 v[4];
@@ -310,14 +332,19 @@ struct UnitIter {
     }
 };
 
-template <int FM>
-__device__ __forceinline__ void store_tile(Acc<FM> &acc, const TileParams &p, int tm, int tn,
+struct ProducerState {
+    UnitIter it;
+    int pq, tm, tn, k, k1;  // next position to issue; its tile and k-range
+};
+
+template <int FM, int TM>
+__device__ __forceinline__ void store_tile(Acc<FM, TM> &acc, const TileParams &p, int tm, int tn,
                                            int wm, int wn, int ty, int tx) {
-    const int m_base = tm * BM + wm * 64 + ty * 4;
+    const int m_base = tm * BM + wm * Cfg<TM>::WARP_M + ty * 4;
     const int n_base = tn * BN + wn * 64 + tx * 4;
     const float alpha = p.alpha, beta = p.beta;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < TM / 4; ++r) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int m = m_base + r * 16 + i;
@@ -358,8 +385,9 @@ __device__ __forceinline__ void store_tile(Acc<FM> &acc, const TileParams &p, in
 
 // Partial tiles use a thread-linear layout: float4 number e4 of thread tid
 // sits at slot[(e4 * NT + tid) * 4], element order (row ti, columns c*4..).
-template <int FM>
-__device__ __forceinline__ void write_partial(float *slot, Acc<FM> &acc, int tid) {
+template <int FM, int TM>
+__device__ __forceinline__ void write_partial(float *slot, Acc<FM, TM> &acc, int tid) {
+    constexpr int NT = Cfg<TM>::NT;
 #pragma unroll
     for (int e4 = 0; e4 < TILE_FLOATS / NT / 4; ++e4) {
         const int ti = e4 >> 1, c = e4 & 1;
@@ -377,9 +405,10 @@ __device__ __forceinline__ int partial_slot(const TileParams &p, int cta, int t_
 
 // Sum the pieces of stream-K tile t_sk, CTAs c_first..c_last, in CTA order;
 // this CTA's own piece is taken from registers.
-template <int FM>
-__device__ __forceinline__ void reduce_pieces(Acc<FM> &acc, const TileParams &p, int cta,
+template <int FM, int TM>
+__device__ __forceinline__ void reduce_pieces(Acc<FM, TM> &acc, const TileParams &p, int cta,
                                               int t_sk, int c_first, int c_last, int tid) {
+    constexpr int NT = Cfg<TM>::NT;
 #pragma unroll
     for (int e4 = 0; e4 < TILE_FLOATS / NT / 4; ++e4) {
         const int ti = e4 >> 1, c = e4 & 1;
@@ -411,11 +440,12 @@ __device__ __forceinline__ void reduce_pieces(Acc<FM> &acc, const TileParams &p,
     }
 }
 
-template <int FM, int STAGES>
-__global__ void __launch_bounds__(NT, 1)
+template <int FM, int STAGES, int TM>
+__global__ void __launch_bounds__(Cfg<TM>::NT, 1)
     sgemm_tile_kernel(const __grid_constant__ CUtensorMap mapA,
                       const __grid_constant__ CUtensorMap mapB, const TileParams p) {
     using L = SmemLayout<FM, STAGES>;
+    using C = Cfg<TM>;
     extern __shared__ __align__(1024) uint8_t smem[];
     float *stages = reinterpret_cast<float *>(smem);
     float *at_buf = reinterpret_cast<float *>(smem + L::at_off);
@@ -425,7 +455,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int wm = warp >> 2, wn = warp & 3;
+    const int wm = warp / C::WARPS_N, wn = warp % C::WARPS_N;
     const int ty = lane >> 3, tx = lane & 7;
     const int G = gridDim.x, cta = blockIdx.x;
 
@@ -439,7 +469,6 @@ __global__ void __launch_bounds__(NT, 1)
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
-        flags[0] = 0;
         flags[1] = 0;
         fence_barrier_init();
         prefetch_tensormap(&mapA);
@@ -447,10 +476,15 @@ __global__ void __launch_bounds__(NT, 1)
     }
     __syncthreads();
 
-    // ---- copy producer state (used by thread 0 only) ----
-    UnitIter prod;
-    prod.init(p, cta);
-    int pq = 0, p_tm = 0, p_tn = 0, p_k = 0, p_k1 = 0;
+    // ---- copy producer state: used by thread 0 only, so it lives in shared
+    // memory rather than in every thread's registers ----
+    ProducerState &ps = *reinterpret_cast<ProducerState *>(smem + L::prod_off);
+    UnitIter &prod = ps.it;
+    int &pq = ps.pq, &p_tm = ps.tm, &p_tn = ps.tn, &p_k = ps.k, &p_k1 = ps.k1;
+    if (tid == 0) {
+        prod.init(p, cta);
+        pq = p_tm = p_tn = p_k = p_k1 = 0;
+    }
     auto issue_next = [&]() {
         if (pq >= q_total) return;
         if (p.skip_loads_from >= 0 && pq >= p.skip_loads_from) return;
@@ -476,37 +510,36 @@ __global__ void __launch_bounds__(NT, 1)
     cons.init(p, cta);
     int q = 0;
     bool aborted = false;
+    int timed_out = 0;  // made uniform over the CTA by __syncthreads_or
 
     if (!mbar_wait_bounded(&full[0], 0, p.timeout_ns)) {
-        flags[0] = 1;
+        timed_out = 1;
         atomicOr(p.err, kErrWaitTimeout);
     }
     transpose_slice<FM>(stages, at_buf, tid);
-    __syncthreads();
-    if (flags[0]) aborted = true;
+    if (__syncthreads_or(timed_out)) aborted = true;
 
     int tile, k0, k1;
     while (!aborted && cons.next(p, G, tile, k0, k1)) {
         int tm, tn;
         tile_coords(p, tile, tm, tn);
-        Acc<FM> acc;
-        acc_zero<FM>(acc);
+        Acc<FM, TM> acc;
+        acc_zero<FM, TM>(acc);
 
         for (int kt = k0; kt < k1; ++kt, ++q) {
             const int s = q % STAGES;
             if (q + 1 < q_total) {
                 const int s1 = (q + 1) % STAGES;
                 if (!mbar_wait_bounded(&full[s1], ((q + 1) / STAGES) & 1, p.timeout_ns)) {
-                    flags[0] = 1;
+                    timed_out = 1;
                     atomicOr(p.err, kErrWaitTimeout);
                 }
                 transpose_slice<FM>(stages + s1 * STAGE_FLOATS, at_buf + ((q + 1) & 1) * AT_FLOATS,
                                     tid);
             }
-            compute_slice<FM>(at_buf + (q & 1) * AT_FLOATS, stages + s * STAGE_FLOATS + A_STAGE_FLOATS,
-                              acc, wm, wn, ty, tx);
-            __syncthreads();
-            if (flags[0]) {
+            compute_slice<FM, TM>(at_buf + (q & 1) * AT_FLOATS,
+                                  stages + s * STAGE_FLOATS + A_STAGE_FLOATS, acc, wm, wn, ty, tx);
+            if (__syncthreads_or(timed_out)) {
                 aborted = true;
                 ++q;
                 break;
@@ -516,11 +549,11 @@ __global__ void __launch_bounds__(NT, 1)
         if (aborted) break;
 
         if (k0 == 0 && k1 == p.kt_total) {
-            store_tile<FM>(acc, p, tm, tn, wm, wn, ty, tx);
+            store_tile<FM, TM>(acc, p, tm, tn, wm, wn, ty, tx);
         } else {
             const int t_sk = tile - p.dp_tiles;
             float *slot = p.partials + (size_t)partial_slot(p, cta, t_sk) * TILE_FLOATS;
-            write_partial<FM>(slot, acc, tid);
+            write_partial<FM, TM>(slot, acc, tid);
             __threadfence();
             __syncthreads();
             const int c_first = (t_sk * p.kt_total) / p.sk_share;
@@ -532,9 +565,9 @@ __global__ void __launch_bounds__(NT, 1)
             __syncthreads();
             if (flags[1]) {
                 __threadfence();
-                reduce_pieces<FM>(acc, p, cta, t_sk, c_first, c_last, tid);
+                reduce_pieces<FM, TM>(acc, p, cta, t_sk, c_first, c_last, tid);
                 if (tid == 0) p.counters[t_sk] = 0;
-                store_tile<FM>(acc, p, tm, tn, wm, wn, ty, tx);
+                store_tile<FM, TM>(acc, p, tm, tn, wm, wn, ty, tx);
             }
         }
     }
@@ -552,60 +585,63 @@ __global__ void __launch_bounds__(NT, 1)
     }
 }
 
-template <int FM, int STAGES>
+template <int FM, int STAGES, int TM>
 cudaError_t launch_impl(const CUtensorMap &mapA, const CUtensorMap &mapB, const TileParams &p,
                         int grid, cudaStream_t stream) {
     using L = SmemLayout<FM, STAGES>;
-    sgemm_tile_kernel<FM, STAGES><<<grid, NT, L::total, stream>>>(mapA, mapB, p);
+    sgemm_tile_kernel<FM, STAGES, TM><<<grid, Cfg<TM>::NT, L::total, stream>>>(mapA, mapB, p);
     return cudaGetLastError();
 }
 
-template <int FM, int STAGES>
+template <int FM, int STAGES, int TM>
 cudaError_t configure_impl() {
     using L = SmemLayout<FM, STAGES>;
-    return cudaFuncSetAttribute(sgemm_tile_kernel<FM, STAGES>,
+    return cudaFuncSetAttribute(sgemm_tile_kernel<FM, STAGES, TM>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::total);
 }
 
+// The instantiated configurations: (multiply-add form, ring stages, micro-tile rows).
+// (8-row micro-tiles with 4 warps per scheduler measured slower on GB300 and
+// spill at their 128-register limit, so they are not instantiated.)
+#define SGEMM_TILE_CONFIGS(X)       \
+    X(kFmaScalar, 3, 16)            \
+    X(kFmaPairMovA, 3, 16)          \
+    X(kFmaPairDupA, 3, 16)          \
+    X(kFmaPairMovB, 3, 16)          \
+    X(kFmaPairMovB, 4, 16)
+
+constexpr int config_key(int fm, int st, int tm) { return (fm * 10 + st) * 100 + tm; }
+
 }  // namespace
 
-size_t tile_smem_bytes(int fma_mode, int stages) {
-#define SGEMM_TILE_CASE(FM, S) \
-    if (fma_mode == FM && stages == S) return SmemLayout<FM, S>::total;
-    SGEMM_TILE_CASE(kFmaScalar, 3)
-    SGEMM_TILE_CASE(kFmaScalar, 4)
-    SGEMM_TILE_CASE(kFmaPairMovA, 3)
-    SGEMM_TILE_CASE(kFmaPairMovA, 4)
-    SGEMM_TILE_CASE(kFmaPairDupA, 3)
-    SGEMM_TILE_CASE(kFmaPairMovB, 3)
-    SGEMM_TILE_CASE(kFmaPairMovB, 4)
-#undef SGEMM_TILE_CASE
+size_t tile_smem_bytes(int fma_mode, int stages, int tm) {
+#define SGEMM_SMEM(FM, S, TM) \
+    if (config_key(fma_mode, stages, tm) == config_key(FM, S, TM)) return SmemLayout<FM, S>::total;
+    SGEMM_TILE_CONFIGS(SGEMM_SMEM)
+#undef SGEMM_SMEM
     return 0;
 }
 
-#define SGEMM_TILE_DISPATCH(CALL)                                              \
-    switch (fma_mode * 10 + stages) {                                          \
-        case kFmaScalar * 10 + 3: return CALL(kFmaScalar, 3);                  \
-        case kFmaScalar * 10 + 4: return CALL(kFmaScalar, 4);                  \
-        case kFmaPairMovA * 10 + 3: return CALL(kFmaPairMovA, 3);              \
-        case kFmaPairMovA * 10 + 4: return CALL(kFmaPairMovA, 4);              \
-        case kFmaPairDupA * 10 + 3: return CALL(kFmaPairDupA, 3);              \
-        case kFmaPairMovB * 10 + 3: return CALL(kFmaPairMovB, 3);              \
-        case kFmaPairMovB * 10 + 4: return CALL(kFmaPairMovB, 4);              \
-        default: return cudaErrorInvalidValue;                                 \
-    }
+int tile_threads(int tm) { return tm == 8 ? Cfg<8>::NT : Cfg<16>::NT; }
 
-cudaError_t launch_tile(int fma_mode, int stages, const CUtensorMap &mapA, const CUtensorMap &mapB,
-                        const TileParams &p, int grid, cudaStream_t stream) {
-#define SGEMM_LAUNCH(FM, S) launch_impl<FM, S>(mapA, mapB, p, grid, stream)
-    SGEMM_TILE_DISPATCH(SGEMM_LAUNCH)
+cudaError_t launch_tile(int fma_mode, int stages, int tm, const CUtensorMap &mapA,
+                        const CUtensorMap &mapB, const TileParams &p, int grid,
+                        cudaStream_t stream) {
+#define SGEMM_LAUNCH(FM, S, TM)                                       \
+    if (config_key(fma_mode, stages, tm) == config_key(FM, S, TM)) \
+        return launch_impl<FM, S, TM>(mapA, mapB, p, grid, stream);
+    SGEMM_TILE_CONFIGS(SGEMM_LAUNCH)
 #undef SGEMM_LAUNCH
+    return cudaErrorInvalidValue;
 }
 
-cudaError_t tile_configure(int fma_mode, int stages) {
-#define SGEMM_CONF(FM, S) configure_impl<FM, S>()
-    SGEMM_TILE_DISPATCH(SGEMM_CONF)
+cudaError_t tile_configure(int fma_mode, int stages, int tm) {
+#define SGEMM_CONF(FM, S, TM)                                         \
+    if (config_key(fma_mode, stages, tm) == config_key(FM, S, TM)) \
+        return configure_impl<FM, S, TM>();
+    SGEMM_TILE_CONFIGS(SGEMM_CONF)
 #undef SGEMM_CONF
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace sgemm

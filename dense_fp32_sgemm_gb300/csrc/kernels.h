@@ -11,13 +11,12 @@ namespace sgemm {
 
 // ---------------------------------------------------------------------------
 // Tiled FFMA kernel (TMA + mbarrier pipeline, in-CTA transposed A tile).
-// Block tile BM x BN = 128 x 256, K slice BK = 32, 256 threads, each thread
-// a 16 x 8 micro-tile.
+// Block tile BM x BN = 128 x 256, K slice BK = 32; each thread a TM x 8
+// micro-tile.
 // ---------------------------------------------------------------------------
 constexpr int kTileBM = 128;
 constexpr int kTileBN = 256;
 constexpr int kTileBK = 32;
-constexpr int kTileThreads = 256;
 
 // Inner-product form of the micro-tile update (see kernel_tile.cu).
 enum FmaMode : int {
@@ -46,11 +45,14 @@ struct TileParams {
     int skip_loads_from;  // testing hook, -1 = off
 };
 
-cudaError_t launch_tile(int fma_mode, int stages, const CUtensorMap &mapA,
+// tm: micro-tile rows, 16 (256 threads, 2 warps per scheduler) or 8 (512
+// threads, 4 warps per scheduler); both cover the 128 x 256 tile.
+cudaError_t launch_tile(int fma_mode, int stages, int tm, const CUtensorMap &mapA,
                         const CUtensorMap &mapB, const TileParams &p, int grid,
                         cudaStream_t stream);
-size_t tile_smem_bytes(int fma_mode, int stages);
-cudaError_t tile_configure(int fma_mode, int stages);
+size_t tile_smem_bytes(int fma_mode, int stages, int tm);
+cudaError_t tile_configure(int fma_mode, int stages, int tm);
+int tile_threads(int tm);
 
 // ---------------------------------------------------------------------------
 // Generic kernel: any alignment and leading dimension, bounds-checked loads.
@@ -78,8 +80,9 @@ cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc,
 
 // ---------------------------------------------------------------------------
 // Skinny-M kernel (M <= 16): streams B once through a TMA ring together with
-// the matching 32-column slices of A, stream-K over (column slab, k) with a
-// fixed-order reduction.
+// the matching 32-column slices of A (128-byte swizzled), stream-K over
+// (column slab, k) with a fixed-order reduction.  The A tensor map must use
+// CU_TENSOR_MAP_SWIZZLE_128B.
 // ---------------------------------------------------------------------------
 constexpr int kSkinnyBN = 256;   // columns per slab
 constexpr int kSkinnyBK = 32;    // B rows per TMA stage

@@ -59,14 +59,15 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 EncodeTiledFn g_encode_fn = nullptr;
 
 sgemm_status_t encode(CUtensorMap *map, const float *base, int64_t rows, int64_t cols, int64_t ld,
-                      int box_cols, int box_rows) {
+                      int box_cols, int box_rows,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
     const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode_fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                                    const_cast<float *>(base), dims, strides, box, estr,
-                                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? SGEMM_OK : SGEMM_ERR_TMA;
@@ -164,7 +165,7 @@ extern "C" sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t
         configured = true;
     }
     CUtensorMap mapA, mapB;
-    s = encode(&mapA, A, M, K, lda, kSkinnyBK, pl.m_tile);
+    s = encode(&mapA, A, M, K, lda, kSkinnyBK, pl.m_tile, CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != SGEMM_OK) return s;
     s = encode(&mapB, B, K, N, ldb, kSkinnyBN, kSkinnyBK);
     if (s != SGEMM_OK) return s;

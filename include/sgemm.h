@@ -179,16 +179,18 @@ SGEMM_API sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns, int skip
 
 /*
  * sgemm_set_tile_config -- tuning hook, process-wide: the form of the
- * multiply-add in the tiled kernel and its number of TMA ring stages.
+ * multiply-add in the tiled kernel, its number of TMA ring stages and the
+ * height of each thread's micro-tile.
  * fma_mode: 0 = one FFMA per product; 1 = packed pairs along n with the A
  *   value duplicated in registers; 2 = packed pairs along n with A stored
  *   duplicated in shared memory; 3 = packed pairs along m with the B value
  *   duplicated in registers (default).
- * stages: 3 or 4 (mode 2 supports 3 only; default 3).
+ * stages: 3 or 4 (default 3).
+ * micro_m: 16 (256 threads of 16 x 8); the only height this build contains.
  * All forms compute the same IEEE FP32 products and sums.  Returns
  * SGEMM_ERR_INVALID_ARG for a combination this build does not contain.
  */
-SGEMM_API sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages);
+SGEMM_API sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages, int micro_m);
 
 /* Free every workspace and host-path buffer the library holds on all devices. */
 SGEMM_API sgemm_status_t sgemm_release_workspace(void);

@@ -94,9 +94,13 @@ def test_hooks_validate(lib):
     with pytest.raises(sg.SgemmError):
         sg.set_plan_override(7, 0)
     with pytest.raises(sg.SgemmError):
-        sg.set_tile_config(2, 4)
+        sg.set_tile_config(2, 4, 16)
+    with pytest.raises(sg.SgemmError):
+        sg.set_tile_config(3, 3, 12)
+    with pytest.raises(sg.SgemmError):
+        sg.set_tile_config(3, 3, 8)
     with pytest.raises(sg.SgemmError):
         sg.set_wait_timeout_ns(0, -5)
     sg.set_plan_override(-1, 0)
-    sg.set_tile_config(3, 3)
+    sg.set_tile_config(3, 3, 16)
     sg.set_wait_timeout_ns(0, -1)

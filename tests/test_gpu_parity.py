@@ -130,6 +130,17 @@ def test_stream_k_forced_splits(splits):
     check(640, 1024, 1000, 1.0, 0.5, seed=8, variant=2, splits=splits)
 
 
+@pytest.mark.parametrize("stages", [3, 4])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_ring_depths(stages, splits):
+    try:
+        sg.set_tile_config(3, stages, 16)
+        check(700, 900, 1100, 0.5, 2.0, seed=20 + stages, variant=2 if splits else -1,
+              splits=splits, lda=1100, ldb=900, ldc=904)
+    finally:
+        sg.set_tile_config(3, 3, 16)
+
+
 def test_generic_forced_matches_bound():
     check(300, 400, 500, -1.5, 0.25, seed=9, variant=0)
 
@@ -169,12 +180,12 @@ def test_fma_forms_are_bitwise_identical():
     A, lda, B, ldb, _, _ = inputs("normal", 13, M, N, K, lda=300, ldb=512)
     results = []
     try:
-        for fm, st in [(0, 3), (1, 3), (2, 3), (3, 3), (0, 4)]:
-            sg.set_tile_config(fm, st)
+        for fm, st, tm in [(0, 3, 16), (1, 3, 16), (2, 3, 16), (3, 3, 16), (3, 4, 16)]:
+            sg.set_tile_config(fm, st, tm)
             out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, variant=1)
             results.append(out)
     finally:
-        sg.set_tile_config(3, 3)
+        sg.set_tile_config(3, 3, 16)
     for r in results[1:]:
         assert np.array_equal(results[0], r)
 
