@@ -263,18 +263,55 @@ __global__ void __launch_bounds__(SNT, 1)
             write_c = flags[1] != 0;
             if (write_c) {
                 __threadfence();
+                // Pieces are added in CTA order.  The loads of every other
+                // piece for a group of rows are issued together, so a group
+                // costs one L2 round trip (up to kFastPieces pieces; more
+                // take a plain loop).
+                constexpr int kFastPieces = 8;
+                const int npieces = c_last - c_first + 1;
+                if (npieces <= kFastPieces) {
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    float sum = 0.f;
-                    for (int cc = c_first; cc <= c_last; ++cc) {
-                        const float v =
-                            (cc == cta) ? fin[m]
-                                        : __ldcg(p.partials +
-                                                 (size_t)skinny_slot(p, cc, slab) * (kSkinnyMaxM * SBN) +
-                                                 m * SBN + col);
-                        sum = (cc == c_first) ? v : sum + v;
+                    for (int m0 = 0; m0 < MT; m0 += 4) {
+                        float v[kFastPieces][4];
+#pragma unroll
+                        for (int i = 0; i < kFastPieces; ++i) {
+                            const int cc = c_first + i;
+                            if (cc <= c_last && cc != cta) {
+                                const float *slot = p.partials +
+                                                    (size_t)skinny_slot(p, cc, slab) * (kSkinnyMaxM * SBN) +
+                                                    col;
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) v[i][r] = __ldcg(slot + (m0 + r) * SBN);
+                            }
+                        }
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const float own = fin[m0 + r];
+                            float sum = own;
+#pragma unroll
+                            for (int i = 0; i < kFastPieces; ++i) {
+                                const int cc = c_first + i;
+                                if (cc > c_last) break;
+                                const float x = (cc == cta) ? own : v[i][r];
+                                sum = (i == 0) ? x : sum + x;
+                            }
+                            fin[m0 + r] = sum;
+                        }
                     }
-                    fin[m] = sum;
+                } else {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        float sum = 0.f;
+                        for (int cc = c_first; cc <= c_last; ++cc) {
+                            const float v =
+                                (cc == cta) ? fin[m]
+                                            : __ldcg(p.partials +
+                                                     (size_t)skinny_slot(p, cc, slab) * (kSkinnyMaxM * SBN) +
+                                                     m * SBN + col);
+                            sum = (cc == c_first) ? v : sum + v;
+                        }
+                        fin[m] = sum;
+                    }
                 }
                 if (tid == 0) p.counters[slab] = 0;
             }

@@ -79,9 +79,15 @@ struct SmemLayout {
     static constexpr size_t at_bytes = size_t(BK) * AtRow<FM>::value * 4;
     static constexpr size_t at_off = STAGES * stage_bytes;
     static constexpr size_t bar_off = at_off + 2 * at_bytes;
-    static constexpr size_t flag_off = bar_off + STAGES * 8;
+    static constexpr size_t redbar_off = bar_off + STAGES * 8;  // fixup bulk copies
+    static constexpr size_t prebar_off = redbar_off + 8;        // partner prefetch, 2 parts
+    static constexpr size_t flag_off = prebar_off + 16;
     static constexpr size_t prod_off = flag_off + 16;
     static constexpr size_t total = prod_off + 32;
+    // The partner prefetch fills the two idle stages and then the last one.
+    static_assert(STAGES != 3 || 3 * stage_bytes >= size_t(TILE_FLOATS) * 4, "prefetch layout");
+    static_assert(STAGES * stage_bytes >= size_t(TILE_FLOATS) * 4,
+                  "the final-unit fixup stages a whole partial tile in the ring");
     static_assert(total <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
 };
 
@@ -440,6 +446,77 @@ __device__ __forceinline__ void reduce_pieces(Acc<FM, TM> &acc, const TileParams
     }
 }
 
+// The same sum for a CTA's final unit, when its TMA ring is idle: the other
+// pieces' partial tiles are pulled into the ring with bulk asynchronous
+// copies (one L2 round trip per round, no registers), then added from
+// shared memory in CTA order.  ROUNDS splits the tile so that all other
+// pieces of a round fit the ring: 1 other piece -> 1 round, 2 -> 2, 3 or 4
+// -> 4.  Returns false if a copy did not arrive in time (the error word is
+// set; the caller still waits for the copies before exiting).
+template <int FM, int TM, int ROUNDS>
+__device__ __forceinline__ bool reduce_pieces_staged(Acc<FM, TM> &acc, const TileParams &p,
+                                                     int cta, int t_sk, int c_first, int c_last,
+                                                     int tid, float *ring, uint64_t *bar,
+                                                     uint32_t &phase) {
+    constexpr int NT = Cfg<TM>::NT;
+    constexpr int E4 = TILE_FLOATS / NT / 4;
+    constexpr int E = E4 / ROUNDS;                    // float4 per thread per round
+    constexpr uint32_t CHUNK = uint32_t(E) * NT * 16;  // bytes per piece per round
+    const int others = c_last - c_first;
+    bool ok = true;
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+        if (tid == 0) {
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(bar, CHUNK * others);
+            int j = 0;
+            for (int cc = c_first; cc <= c_last; ++cc) {
+                if (cc == cta) continue;
+                const char *slot = reinterpret_cast<const char *>(
+                    p.partials + (size_t)partial_slot(p, cc, t_sk) * TILE_FLOATS);
+                bulk_load(reinterpret_cast<char *>(ring) + j * CHUNK, slot + r * CHUNK, CHUNK, bar);
+                ++j;
+            }
+        }
+        if (!mbar_wait_bounded(bar, phase, p.timeout_ns)) {
+            atomicOr(p.err, kErrWaitTimeout);
+            ok = false;
+        }
+        phase ^= 1u;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int e4 = r * E + e, ti = e4 >> 1, cg = e4 & 1;
+            const float4 own = make_float4(acc.at(ti, cg * 4 + 0), acc.at(ti, cg * 4 + 1),
+                                           acc.at(ti, cg * 4 + 2), acc.at(ti, cg * 4 + 3));
+            float4 sum = own;
+            int j = 0;
+            for (int cc = c_first; cc <= c_last; ++cc) {
+                float4 x;
+                if (cc == cta) {
+                    x = own;
+                } else {
+                    x = ld_shared_f4(ring + (size_t)j * (CHUNK / 4) + (e * NT + tid) * 4);
+                    ++j;
+                }
+                if (cc == c_first) {
+                    sum = x;
+                } else {
+                    sum.x += x.x;
+                    sum.y += x.y;
+                    sum.z += x.z;
+                    sum.w += x.w;
+                }
+            }
+            acc.at(ti, cg * 4 + 0) = sum.x;
+            acc.at(ti, cg * 4 + 1) = sum.y;
+            acc.at(ti, cg * 4 + 2) = sum.z;
+            acc.at(ti, cg * 4 + 3) = sum.w;
+        }
+        __syncthreads();  // the ring is read before the next round overwrites it
+    }
+    return ok;
+}
+
 template <int FM, int STAGES, int TM>
 __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
     sgemm_tile_kernel(const __grid_constant__ CUtensorMap mapA,
@@ -450,6 +527,10 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
     float *stages = reinterpret_cast<float *>(smem);
     float *at_buf = reinterpret_cast<float *>(smem + L::at_off);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off);
+    uint64_t *red_bar = reinterpret_cast<uint64_t *>(smem + L::redbar_off);
+    uint64_t *pre_bar = reinterpret_cast<uint64_t *>(smem + L::prebar_off);
+    uint32_t red_phase = 0;
+    bool prefetched = false;  // the partner prefetch was issued (uniform)
     volatile int *flags = reinterpret_cast<volatile int *>(smem + L::flag_off);
     constexpr int AT_FLOATS = BK * AtRow<FM>::value;
 
@@ -469,6 +550,9 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+        mbar_init(red_bar, 1);
+        mbar_init(&pre_bar[0], 1);
+        mbar_init(&pre_bar[1], 1);
         flags[1] = 0;
         fence_barrier_init();
         prefetch_tensormap(&mapA);
@@ -526,6 +610,22 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
         Acc<FM, TM> acc;
         acc_zero<FM, TM>(acc);
 
+        // A two-piece stream-K tile whose head piece is this CTA's final
+        // unit: the partner's piece is its first unit and normally finished
+        // long ago.  If its ticket is already in at the start of the last
+        // slice, its partial tile is prefetched into the ring stages that are
+        // already idle, and this CTA finishes the tile without writing a
+        // partial or taking a ticket.  (The sum is the same: this CTA's piece
+        // is the first in CTA order.)
+        const bool whole = (k0 == 0 && k1 == p.kt_total);
+        const int t_sk = tile - p.dp_tiles;
+        bool predict = false;
+        if (STAGES == 3 && !whole && k0 == 0 && q + (k1 - k0) == q_total) {
+            const int cf = (t_sk * p.kt_total) / p.sk_share;
+            const int cl = (t_sk * p.kt_total + p.kt_total - 1) / p.sk_share;
+            predict = (cf == cta && cl == cta + 1);
+        }
+
         for (int kt = k0; kt < k1; ++kt, ++q) {
             const int s = q % STAGES;
             if (q + 1 < q_total) {
@@ -537,9 +637,29 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
                 transpose_slice<FM>(stages + s1 * STAGE_FLOATS, at_buf + ((q + 1) & 1) * AT_FLOATS,
                                     tid);
             }
+            if (predict && kt == k1 - 1 && tid == 0) {
+                // Last slice: stage s is in use; the other two are idle.
+                int arrived;
+                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];"
+                             : "=r"(arrived)
+                             : "l"(p.counters + t_sk)
+                             : "memory");
+                flags[2] = arrived == 1;
+                if (arrived == 1) {
+                    fence_proxy_async_global();
+                    const char *src = reinterpret_cast<const char *>(
+                        p.partials + (size_t)partial_slot(p, cta + 1, t_sk) * TILE_FLOATS);
+                    constexpr uint32_t kStage = STAGE_FLOATS * 4;
+                    mbar_arrive_expect_tx(&pre_bar[0], 2 * kStage);
+                    bulk_load(stages + ((s + 1) % STAGES) * STAGE_FLOATS, src, kStage, &pre_bar[0]);
+                    bulk_load(stages + ((s + 2) % STAGES) * STAGE_FLOATS, src + kStage, kStage,
+                              &pre_bar[0]);
+                }
+            }
             compute_slice<FM, TM>(at_buf + (q & 1) * AT_FLOATS,
                                   stages + s * STAGE_FLOATS + A_STAGE_FLOATS, acc, wm, wn, ty, tx);
             if (__syncthreads_or(timed_out)) {
+                if (predict && kt == k1 - 1 && flags[2]) prefetched = true;
                 aborted = true;
                 ++q;
                 break;
@@ -548,10 +668,42 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
         }
         if (aborted) break;
 
-        if (k0 == 0 && k1 == p.kt_total) {
+        if (predict && flags[2]) {
+            // The last stage is idle now: bring in the rest of the partner's
+            // partial (the first two stages' worth is already on its way).
+            prefetched = true;
+            const int s_last = (q - 1) % STAGES;
+            constexpr uint32_t kStage = STAGE_FLOATS * 4;
+            constexpr uint32_t kRest = TILE_FLOATS * 4 - 2 * kStage;
+            if (tid == 0) {
+                const char *src = reinterpret_cast<const char *>(
+                    p.partials + (size_t)partial_slot(p, cta + 1, t_sk) * TILE_FLOATS);
+                mbar_arrive_expect_tx(&pre_bar[1], kRest);
+                bulk_load(stages + s_last * STAGE_FLOATS, src + 2 * kStage, kRest, &pre_bar[1]);
+            }
+            bool ok = mbar_wait_bounded(&pre_bar[0], 0, p.timeout_ns);
+            ok = mbar_wait_bounded(&pre_bar[1], 0, p.timeout_ns) && ok;
+            if (!ok) atomicOr(p.err, kErrWaitTimeout);
+            const float *part[3] = {stages + ((s_last + 1) % STAGES) * STAGE_FLOATS,
+                                    stages + ((s_last + 2) % STAGES) * STAGE_FLOATS,
+                                    stages + s_last * STAGE_FLOATS};
+            constexpr int NT = Cfg<TM>::NT;
+            constexpr int PER_STAGE = STAGE_FLOATS / 4 / NT;  // float4 rows per stage
+#pragma unroll
+            for (int e4 = 0; e4 < TILE_FLOATS / NT / 4; ++e4) {
+                const int ti = e4 >> 1, cg = e4 & 1;
+                const float4 x =
+                    ld_shared_f4(part[e4 / PER_STAGE] + ((e4 % PER_STAGE) * NT + tid) * 4);
+                acc.at(ti, cg * 4 + 0) += x.x;
+                acc.at(ti, cg * 4 + 1) += x.y;
+                acc.at(ti, cg * 4 + 2) += x.z;
+                acc.at(ti, cg * 4 + 3) += x.w;
+            }
+            if (tid == 0) p.counters[t_sk] = 0;
+            store_tile<FM, TM>(acc, p, tm, tn, wm, wn, ty, tx);
+        } else if (whole) {
             store_tile<FM, TM>(acc, p, tm, tn, wm, wn, ty, tx);
         } else {
-            const int t_sk = tile - p.dp_tiles;
             float *slot = p.partials + (size_t)partial_slot(p, cta, t_sk) * TILE_FLOATS;
             write_partial<FM, TM>(slot, acc, tid);
             __threadfence();
@@ -565,7 +717,26 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
             __syncthreads();
             if (flags[1]) {
                 __threadfence();
-                reduce_pieces<FM, TM>(acc, p, cta, t_sk, c_first, c_last, tid);
+                const int others = c_last - c_first;
+                // The final unit's ring is idle (every copy issued has been
+                // consumed): stage the other pieces there.
+                bool staged_ok = true;
+                if (q == q_total && others <= 4) {
+                    if (others == 1)
+                        staged_ok = reduce_pieces_staged<FM, TM, 1>(acc, p, cta, t_sk, c_first, c_last,
+                                                                    tid, stages, red_bar, red_phase);
+                    else if (others == 2)
+                        staged_ok = reduce_pieces_staged<FM, TM, 2>(acc, p, cta, t_sk, c_first, c_last,
+                                                                    tid, stages, red_bar, red_phase);
+                    else
+                        staged_ok = reduce_pieces_staged<FM, TM, 4>(acc, p, cta, t_sk, c_first, c_last,
+                                                                    tid, stages, red_bar, red_phase);
+                    if (!staged_ok && tid == 0 &&
+                        !mbar_wait_bounded(red_bar, red_phase ^ 1u, 1000000000ull))
+                        atomicOr(p.err, kErrDrainTimeout);
+                } else {
+                    reduce_pieces<FM, TM>(acc, p, cta, t_sk, c_first, c_last, tid);
+                }
                 if (tid == 0) p.counters[t_sk] = 0;
                 store_tile<FM, TM>(acc, p, tm, tn, wm, wn, ty, tx);
             }
@@ -576,6 +747,8 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
         // Wait (bounded) for every copy issued but not yet consumed, so none
         // lands in shared memory after this CTA has exited.  q is the first
         // position not yet transposed; positions [q, pq) may be in flight.
+        if (prefetched && !mbar_wait_bounded(&pre_bar[0], 0, 1000000000ull))
+            atomicOr(p.err, kErrDrainTimeout);
         for (int j = q; j < pq; ++j) {
             if (!mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1, 1000000000ull)) {
                 atomicOr(p.err, kErrDrainTimeout);
