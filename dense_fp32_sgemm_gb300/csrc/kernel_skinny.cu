@@ -12,11 +12,10 @@
 // a ring of shared-memory stages completed on mbarriers, several stages
 // ahead, so enough bytes are in flight to keep HBM busy.
 //
-// 8 warps: lane l of every warp owns columns 4l .. 4l+3 and 128+4l .. 128+4l+3
-// of the slab (two groups of four, 128 apart, so a quarter-warp's 128-bit
-// loads cover 32 consecutive banks); warp g takes rows g, g + 8, g + 16,
-// g + 24 of each block.  Six 128-bit shared loads (16 A values, 8 B values)
-// feed 64 packed multiply-adds per row.  A warp rewrites only
+// Lanes own groups of four columns (so a quarter-warp's 128-bit loads cover
+// 32 consecutive banks): with 8 columns per lane, 8 warps each cover the
+// whole 256-column row; with 4, 16 warps cover it in halves.  Row group g
+// (one per 8 rows) takes rows g, g + 8, g + 16, g + 24 of each block.  A warp rewrites only
 // the four A columns it needs k-major into its own corner of shared memory,
 // so no CTA-wide barrier is needed inside a unit: warps run through the
 // stages independently, and the last warp to finish with a stage (a counter
@@ -36,13 +35,14 @@ namespace {
 
 constexpr int SBN = kSkinnyBN;       // 256 columns per slab
 constexpr int SBK = kSkinnyBK;       // 32 rows of B per stage
-constexpr int SNT = kSkinnyThreads;  // 256 threads
+constexpr int SNT = kSkinnyThreads;
 constexpr int SSTAGES = kSkinnyStages;
+constexpr int CPL = kSkinnyCPL;            // columns per lane: 8 (8 warps) or 4 (16 warps)
+constexpr int HALVES = 8 / CPL;            // warps sharing one row of a block
 constexpr int WARPS = SNT / 32;
-constexpr int GROUPS = WARPS;              // row groups: one per warp
+constexpr int GROUPS = WARPS / HALVES;     // row groups
 constexpr int RPW = SBK / GROUPS;          // rows of a block per warp
-constexpr int CPL = 8;                     // columns per lane
-static_assert(RPW == 4 && GROUPS == 8 && 32 * CPL == SBN, "warp layout assumes 8 warps");
+static_assert(RPW == 4 && GROUPS == 8 && 32 * CPL * HALVES == SBN, "warp layout");
 
 template <int MT>
 struct SkinnyLayout {
@@ -52,7 +52,8 @@ struct SkinnyLayout {
     static constexpr size_t stage_bytes = size_t(stage_floats) * 4;
     static_assert(stage_bytes % 1024 == 0, "stages must keep 1024-byte alignment");
     static constexpr int at_floats = RPW * MT;  // per warp: 4 k x MT m
-    static constexpr int red_floats = GROUPS * 4 * SBN;
+    static constexpr int RED_ROWS = 2;  // rows of M per reduction round
+    static constexpr int red_floats = GROUPS * RED_ROWS * SBN;
     static constexpr size_t at_off = SSTAGES * stage_bytes;
     static constexpr size_t red_off = at_off + size_t(WARPS) * at_floats * 4;
     static constexpr size_t bar_off = red_off + size_t(red_floats) * 4;
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(SNT, 1)
     volatile int *flags = reinterpret_cast<volatile int *>(smem + L::flag_off);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = warp;
+    const int g = warp / HALVES, h = warp % HALVES;
     const int cta = blockIdx.x;
     float *at_w = reinterpret_cast<float *>(smem + L::at_off) + warp * L::at_floats;
 
@@ -162,30 +163,33 @@ __global__ void __launch_bounds__(SNT, 1)
             }
             __syncwarp();
 
-            const float *bcol = bs + lane * 4;
-            float4 bf[2][2];
-            float4 af[2][MT / 4];
-            bf[0][0] = ld_shared_f4(bcol + g * SBN);
-            bf[0][1] = ld_shared_f4(bcol + g * SBN + 128);
+            const float *bcol = bs + h * 128 + lane * 4;
+            float4 bf[2][CPL / 4];
 #pragma unroll
-            for (int r = 0; r < MT / 4; ++r) af[0][r] = ld_shared_f4(at_w + r * 4);
+            for (int c = 0; c < CPL / 4; ++c) bf[0][c] = ld_shared_f4(bcol + g * SBN + c * 128);
 #pragma unroll
             for (int kk = 0; kk < RPW; ++kk) {
                 const int cur = kk & 1, nxt = cur ^ 1;
                 if (kk + 1 < RPW) {
                     const float *brow = bcol + (g + GROUPS * (kk + 1)) * SBN;
-                    bf[nxt][0] = ld_shared_f4(brow);
-                    bf[nxt][1] = ld_shared_f4(brow + 128);
 #pragma unroll
-                    for (int r = 0; r < MT / 4; ++r)
-                        af[nxt][r] = ld_shared_f4(at_w + (kk + 1) * MT + r * 4);
+                    for (int c = 0; c < CPL / 4; ++c) bf[nxt][c] = ld_shared_f4(brow + c * 128);
                 }
-                const float b[CPL] = {bf[cur][0].x, bf[cur][0].y, bf[cur][0].z, bf[cur][0].w,
-                                      bf[cur][1].x, bf[cur][1].y, bf[cur][1].z, bf[cur][1].w};
+                float b[CPL];
+#pragma unroll
+                for (int c = 0; c < CPL / 4; ++c) {
+                    b[4 * c + 0] = bf[cur][c].x;
+                    b[4 * c + 1] = bf[cur][c].y;
+                    b[4 * c + 2] = bf[cur][c].z;
+                    b[4 * c + 3] = bf[cur][c].w;
+                }
+                // A values of this row: broadcast loads from the warp's own
+                // k-major copy.
 #pragma unroll
                 for (int r = 0; r < MT / 4; ++r) {
-                    const float2 a01 = make_float2(af[cur][r].x, af[cur][r].y);
-                    const float2 a23 = make_float2(af[cur][r].z, af[cur][r].w);
+                    const float4 a = ld_shared_f4(at_w + kk * MT + r * 4);
+                    const float2 a01 = make_float2(a.x, a.y);
+                    const float2 a23 = make_float2(a.z, a.w);
 #pragma unroll
                     for (int j = 0; j < CPL; ++j) {
                         const float2 bb = make_float2(b[j], b[j]);
@@ -217,40 +221,48 @@ __global__ void __launch_bounds__(SNT, 1)
 
         // ---- add the eight row groups' sums in group order ----
         // Thread t owns column t and all MT rows.
+        constexpr int RR = L::RED_ROWS;
         float fin[MT];
 #pragma unroll
-        for (int r = 0; r < MT / 4; ++r) {
+        for (int r = 0; r < MT / RR; ++r) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int m = 4 * r + i;
+            for (int i = 0; i < RR; ++i) {
+                const int m = RR * r + i;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int c = 0; c < CPL / 4; ++c) {
                     float4 v;
-                    v.x = (m & 1) ? acc[m >> 1][4 * h + 0].y : acc[m >> 1][4 * h + 0].x;
-                    v.y = (m & 1) ? acc[m >> 1][4 * h + 1].y : acc[m >> 1][4 * h + 1].x;
-                    v.z = (m & 1) ? acc[m >> 1][4 * h + 2].y : acc[m >> 1][4 * h + 2].x;
-                    v.w = (m & 1) ? acc[m >> 1][4 * h + 3].y : acc[m >> 1][4 * h + 3].x;
-                    *reinterpret_cast<float4 *>(red + (g * 4 + i) * SBN + h * 128 + lane * 4) = v;
+                    v.x = (m & 1) ? acc[m >> 1][4 * c + 0].y : acc[m >> 1][4 * c + 0].x;
+                    v.y = (m & 1) ? acc[m >> 1][4 * c + 1].y : acc[m >> 1][4 * c + 1].x;
+                    v.z = (m & 1) ? acc[m >> 1][4 * c + 2].y : acc[m >> 1][4 * c + 2].x;
+                    v.w = (m & 1) ? acc[m >> 1][4 * c + 3].y : acc[m >> 1][4 * c + 3].x;
+                    *reinterpret_cast<float4 *>(red + (g * RR + i) * SBN + h * 128 + c * 128 +
+                                                lane * 4) = v;
                 }
             }
             __syncthreads();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float sum = red[i * SBN + tid];
+            for (int i = 0; i < RR; ++i) {
+                const int col = tid & (SBN - 1);
+                float sum = red[i * SBN + col];
 #pragma unroll
-                for (int gg = 1; gg < GROUPS; ++gg) sum += red[(gg * 4 + i) * SBN + tid];
-                fin[4 * r + i] = sum;
+                for (int gg = 1; gg < GROUPS; ++gg) sum += red[(gg * RR + i) * SBN + col];
+                fin[RR * r + i] = sum;
             }
             __syncthreads();
         }
 
-        const int col = tid;
+        // With 512 threads the upper half repeats the lower half's sums and
+        // stores nothing.
+        const int col = tid & (SBN - 1);
+        const bool owner = tid < SBN;
         const int n = slab * SBN + col;
         bool write_c = true;
         if (!(k0 == 0 && k1 == p.kt_total)) {
             float *slot = p.partials + (size_t)skinny_slot(p, cta, slab) * (kSkinnyMaxM * SBN);
+            if (owner) {
 #pragma unroll
-            for (int m = 0; m < MT; ++m) __stcg(slot + m * SBN + col, fin[m]);
+                for (int m = 0; m < MT; ++m) __stcg(slot + m * SBN + col, fin[m]);
+            }
             __threadfence();
             __syncthreads();
             const int c_first = (slab * p.kt_total) / p.share;
@@ -267,12 +279,12 @@ __global__ void __launch_bounds__(SNT, 1)
                 // piece for a group of rows are issued together, so a group
                 // costs one L2 round trip (up to kFastPieces pieces; more
                 // take a plain loop).
-                constexpr int kFastPieces = 8;
+                constexpr int kFastPieces = 6;
                 const int npieces = c_last - c_first + 1;
                 if (npieces <= kFastPieces) {
 #pragma unroll
-                    for (int m0 = 0; m0 < MT; m0 += 4) {
-                        float v[kFastPieces][4];
+                    for (int m0 = 0; m0 < MT; m0 += 2) {
+                        float v[kFastPieces][2];
 #pragma unroll
                         for (int i = 0; i < kFastPieces; ++i) {
                             const int cc = c_first + i;
@@ -281,11 +293,11 @@ __global__ void __launch_bounds__(SNT, 1)
                                                     (size_t)skinny_slot(p, cc, slab) * (kSkinnyMaxM * SBN) +
                                                     col;
 #pragma unroll
-                                for (int r = 0; r < 4; ++r) v[i][r] = __ldcg(slot + (m0 + r) * SBN);
+                                for (int r = 0; r < 2; ++r) v[i][r] = __ldcg(slot + (m0 + r) * SBN);
                             }
                         }
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
+                        for (int r = 0; r < 2; ++r) {
                             const float own = fin[m0 + r];
                             float sum = own;
 #pragma unroll
@@ -317,7 +329,7 @@ __global__ void __launch_bounds__(SNT, 1)
             }
             __syncthreads();  // flags[1] is rewritten by the next unit
         }
-        if (write_c && n < p.N) {
+        if (write_c && owner && n < p.N) {
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 if (m < p.M) {

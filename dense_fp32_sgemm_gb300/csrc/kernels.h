@@ -87,7 +87,11 @@ cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc,
 constexpr int kSkinnyBN = 256;   // columns per slab
 constexpr int kSkinnyBK = 32;    // B rows per TMA stage
 constexpr int kSkinnyMaxM = 32;
-constexpr int kSkinnyThreads = 256;
+#ifndef SGEMM_SKINNY_CPL
+#define SGEMM_SKINNY_CPL 8
+#endif
+constexpr int kSkinnyCPL = SGEMM_SKINNY_CPL;          // columns per lane
+constexpr int kSkinnyThreads = 32 * 8 * (8 / kSkinnyCPL);
 
 struct SkinnyParams {
     int M, N, K;
@@ -111,7 +115,7 @@ cudaError_t launch_skinny(int m_tile, const CUtensorMap &mapA, const CUtensorMap
                           const SkinnyParams &p, int grid, cudaStream_t stream);
 size_t skinny_smem_bytes(int m_tile, int share);
 cudaError_t skinny_configure(int m_tile);
-constexpr int kSkinnyStages = 5;
+constexpr int kSkinnyStages = 6;
 
 // ---------------------------------------------------------------------------
 // Measurement probes (same library, used by the benchmark).
