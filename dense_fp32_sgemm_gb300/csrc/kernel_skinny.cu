@@ -12,20 +12,23 @@
 // a ring of shared-memory stages completed on mbarriers, several stages
 // ahead, so enough bytes are in flight to keep HBM busy.
 //
-// Lanes own groups of four columns (so a quarter-warp's 128-bit loads cover
-// 32 consecutive banks): with 8 columns per lane, 8 warps each cover the
-// whole 256-column row; with 4, 16 warps cover it in halves.  Row group g
-// (one per 8 rows) takes rows g, g + 8, g + 16, g + 24 of each block.  A warp rewrites only
-// the four A columns it needs k-major into its own corner of shared memory,
-// so no CTA-wide barrier is needed inside a unit: warps run through the
-// stages independently, and the last warp to finish with a stage (a counter
-// in shared memory) refills it.  The update is the packed FP32 fma
-// (__ffma2_rn) on pairs along m: (a_m, a_m+1) * (b_n, b_n).
+// With 4 warps a CTA (two CTAs per SM, three stages each) the two CTAs of an
+// SM run out of step, so one computes while the other waits for its next
+// block; with 8 warps (one CTA, six stages) all warps of the SM meet at the
+// same stage.  Each lane owns 8 columns (two groups of four, so a
+// quarter-warp's 128-bit loads cover 32 consecutive banks) and a warp the
+// whole 256-column row; warp w takes rows w, w + W, w + 2W, ... of each
+// block.  A warp rewrites only the A columns it needs k-major into its own
+// corner of shared memory, so no CTA-wide barrier is needed inside a unit:
+// warps run through the stages independently, and the last warp to finish
+// with a stage (a counter in shared memory) refills it.  The update is the
+// packed FP32 fma (__ffma2_rn) on pairs along m: (a_m, a_m+1) * (b_n, b_n).
 //
-// After a unit the eight row groups' sums are added in group order through
-// shared memory; a unit covering part of a slab writes them to a fixed slot
-// and the last CTA to arrive adds the pieces in CTA order (no CTA waits for
-// another), then applies alpha and beta.
+// After a unit the warps' sums are added in warp order through shared
+// memory; a unit covering part of a slab writes them to a fixed slot and the
+// last CTA to arrive adds the pieces in CTA order (no CTA waits for another),
+// then applies alpha and beta.  When that CTA has no copies outstanding (its
+// last unit) it fetches the other pieces with bulk copies into its idle ring.
 
 #include "device_common.cuh"
 #include "kernels.h"
@@ -35,14 +38,13 @@ namespace {
 
 constexpr int SBN = kSkinnyBN;       // 256 columns per slab
 constexpr int SBK = kSkinnyBK;       // 32 rows of B per stage
+constexpr int WARPS = kSkinnyWarps;  // 4 or 8
 constexpr int SNT = kSkinnyThreads;
 constexpr int SSTAGES = kSkinnyStages;
-constexpr int CPL = kSkinnyCPL;            // columns per lane: 8 (8 warps) or 4 (16 warps)
-constexpr int HALVES = 8 / CPL;            // warps sharing one row of a block
-constexpr int WARPS = SNT / 32;
-constexpr int GROUPS = WARPS / HALVES;     // row groups
-constexpr int RPW = SBK / GROUPS;          // rows of a block per warp
-static_assert(RPW == 4 && GROUPS == 8 && 32 * CPL * HALVES == SBN, "warp layout");
+constexpr int CPL = 8;               // columns per lane: a warp covers the row
+constexpr int RPW = SBK / WARPS;     // rows of a block per warp
+constexpr int OWN = SBN / SNT;       // adjacent columns a thread owns after the reduction
+static_assert(32 * CPL == SBN && RPW * WARPS == SBK && (OWN == 1 || OWN == 2), "warp layout");
 
 template <int MT>
 struct SkinnyLayout {
@@ -51,17 +53,22 @@ struct SkinnyLayout {
     static constexpr int stage_floats = a_floats + b_floats;
     static constexpr size_t stage_bytes = size_t(stage_floats) * 4;
     static_assert(stage_bytes % 1024 == 0, "stages must keep 1024-byte alignment");
-    static constexpr int at_floats = RPW * MT;  // per warp: 4 k x MT m
-    static constexpr int RED_ROWS = 2;  // rows of M per reduction round
-    static constexpr int red_floats = GROUPS * RED_ROWS * SBN;
+    static constexpr int at_floats = RPW * MT;  // per warp: RPW k x MT m
+    static constexpr int RED_ROWS = 2;          // rows of M per reduction round
+    static constexpr int red_floats = WARPS * RED_ROWS * SBN;
     static constexpr size_t at_off = SSTAGES * stage_bytes;
     static constexpr size_t red_off = at_off + size_t(WARPS) * at_floats * 4;
-    static constexpr size_t bar_off = red_off + size_t(red_floats) * 4;
-    static constexpr size_t cnt_off = bar_off + SSTAGES * 8;
+    static constexpr size_t bar_off = red_off + size_t(red_floats) * 4;  // SSTAGES + 1 barriers
+    static constexpr size_t cnt_off = bar_off + (SSTAGES + 1) * 8;
     static constexpr size_t flag_off = cnt_off + SSTAGES * 4 * 2;
     static constexpr size_t total = flag_off + 16;
     static constexpr uint32_t tx_bytes = stage_floats * 4;
+    // Fix-up through the idle ring: one piece is MT rows of a slot.
+    static constexpr uint32_t piece_bytes = uint32_t(MT) * SBN * 4;
+    static constexpr int ring_pieces = int(SSTAGES * stage_bytes / piece_bytes);
     static_assert(total <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
+    // The CTAs of one SM must fit its 228 KB together with 1 KB reserved each.
+    static_assert(kSkinnyCtasPerSm * (total + 1024) <= 233472, "CTAs per SM do not fit");
 };
 
 __device__ __forceinline__ int skinny_slot(const SkinnyParams &p, int cta, int slab) {
@@ -70,14 +77,44 @@ __device__ __forceinline__ int skinny_slot(const SkinnyParams &p, int cta, int s
     return 2 * cta + (k0 == 0 ? 1 : 0);
 }
 
+__device__ __forceinline__ const float *skinny_piece(const SkinnyParams &p, int cta, int slab) {
+    return p.partials + (size_t)skinny_slot(p, cta, slab) * (kSkinnyMaxM * SBN);
+}
+
 // Element (m, k) of the TMA-loaded A block: rows of 32 floats whose 16-byte
 // chunks are XOR-swizzled with (row mod 8).
 __device__ __forceinline__ float a_elem(const float *raw, int m, int k) {
     return raw[m * SBK + ((((k >> 2) ^ (m & 7)) << 2) | (k & 3))];
 }
 
+// N adjacent floats: shared-memory load, L2 load and L2 store.
+template <int N>
+struct Vec;
+template <>
+struct Vec<1> {
+    __device__ __forceinline__ static void load(const float *p, float *v) { v[0] = *p; }
+    __device__ __forceinline__ static void load_cg(const float *p, float *v) { v[0] = __ldcg(p); }
+    __device__ __forceinline__ static void store_cg(float *p, const float *v) { __stcg(p, v[0]); }
+};
+template <>
+struct Vec<2> {
+    __device__ __forceinline__ static void load(const float *p, float *v) {
+        const float2 x = *reinterpret_cast<const float2 *>(p);
+        v[0] = x.x;
+        v[1] = x.y;
+    }
+    __device__ __forceinline__ static void load_cg(const float *p, float *v) {
+        const float2 x = __ldcg(reinterpret_cast<const float2 *>(p));
+        v[0] = x.x;
+        v[1] = x.y;
+    }
+    __device__ __forceinline__ static void store_cg(float *p, const float *v) {
+        __stcg(reinterpret_cast<float2 *>(p), make_float2(v[0], v[1]));
+    }
+};
+
 template <int MT>
-__global__ void __launch_bounds__(SNT, 1)
+__global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
     sgemm_skinny_kernel(const __grid_constant__ CUtensorMap mapA,
                         const __grid_constant__ CUtensorMap mapB, const SkinnyParams p) {
     using L = SkinnyLayout<MT>;
@@ -85,12 +122,12 @@ __global__ void __launch_bounds__(SNT, 1)
     float *stages = reinterpret_cast<float *>(smem);
     float *red = reinterpret_cast<float *>(smem + L::red_off);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off);
+    uint64_t *fix_bar = full + SSTAGES;
     int *release = reinterpret_cast<int *>(smem + L::cnt_off);
     volatile int *issued = reinterpret_cast<volatile int *>(smem + L::cnt_off + SSTAGES * 4);
     volatile int *flags = reinterpret_cast<volatile int *>(smem + L::flag_off);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = warp / HALVES, h = warp % HALVES;
     const int cta = blockIdx.x;
     float *at_w = reinterpret_cast<float *>(smem + L::at_off) + warp * L::at_floats;
 
@@ -118,6 +155,7 @@ __global__ void __launch_bounds__(SNT, 1)
             release[s] = 0;
             issued[s] = -1;
         }
+        mbar_init(fix_bar, 1);
         flags[0] = 0;
         flags[1] = 0;
         fence_barrier_init();
@@ -130,7 +168,10 @@ __global__ void __launch_bounds__(SNT, 1)
 
     int q = 0;
     bool aborted = false;
+    bool fix_pending = false;  // a fix-up copy may still be in flight (after a timeout)
+    uint32_t fix_phase = 0;
     int timed_out = 0;  // this thread saw a wait run out (made uniform at unit end)
+    const int col0 = tid * OWN;  // first column this thread owns after the reduction
     while (q < q_total && !aborted) {
         const int u = u0 + q;
         const int slab = u / p.kt_total;
@@ -155,23 +196,23 @@ __global__ void __launch_bounds__(SNT, 1)
             }
             const float *raw = stages + s * L::stage_floats;
             const float *bs = raw + L::a_floats;
-            // This warp's A columns k = g + 8 * kk, k-major: at_w[kk * MT + m].
+            // This warp's A columns k = warp + WARPS * kk, k-major: at_w[kk * MT + m].
 #pragma unroll
             for (int e = lane; e < RPW * MT; e += 32) {
                 const int m = e % MT, kk = e / MT;
-                at_w[kk * MT + m] = a_elem(raw, m, g + GROUPS * kk);
+                at_w[kk * MT + m] = a_elem(raw, m, warp + WARPS * kk);
             }
             __syncwarp();
 
-            const float *bcol = bs + h * 128 + lane * 4;
+            const float *bcol = bs + lane * 4;
             float4 bf[2][CPL / 4];
 #pragma unroll
-            for (int c = 0; c < CPL / 4; ++c) bf[0][c] = ld_shared_f4(bcol + g * SBN + c * 128);
+            for (int c = 0; c < CPL / 4; ++c) bf[0][c] = ld_shared_f4(bcol + warp * SBN + c * 128);
 #pragma unroll
             for (int kk = 0; kk < RPW; ++kk) {
                 const int cur = kk & 1, nxt = cur ^ 1;
                 if (kk + 1 < RPW) {
-                    const float *brow = bcol + (g + GROUPS * (kk + 1)) * SBN;
+                    const float *brow = bcol + (warp + WARPS * (kk + 1)) * SBN;
 #pragma unroll
                     for (int c = 0; c < CPL / 4; ++c) bf[nxt][c] = ld_shared_f4(brow + c * 128);
                 }
@@ -199,7 +240,7 @@ __global__ void __launch_bounds__(SNT, 1)
                 }
             }
             __syncwarp();
-            // Release the stage; the last of the 16 warps refills it.
+            // Release the stage; the last warp to do so refills it.
             if (lane == 0) {
                 __threadfence_block();
                 const int old = atomicAdd(&release[s], 1);
@@ -219,10 +260,10 @@ __global__ void __launch_bounds__(SNT, 1)
             break;
         }
 
-        // ---- add the eight row groups' sums in group order ----
-        // Thread t owns column t and all MT rows.
+        // ---- add the warps' sums in warp order ----
+        // Thread t owns columns [OWN t, OWN t + OWN) and all MT rows.
         constexpr int RR = L::RED_ROWS;
-        float fin[MT];
+        float fin[MT][OWN];
 #pragma unroll
         for (int r = 0; r < MT / RR; ++r) {
 #pragma unroll
@@ -235,34 +276,31 @@ __global__ void __launch_bounds__(SNT, 1)
                     v.y = (m & 1) ? acc[m >> 1][4 * c + 1].y : acc[m >> 1][4 * c + 1].x;
                     v.z = (m & 1) ? acc[m >> 1][4 * c + 2].y : acc[m >> 1][4 * c + 2].x;
                     v.w = (m & 1) ? acc[m >> 1][4 * c + 3].y : acc[m >> 1][4 * c + 3].x;
-                    *reinterpret_cast<float4 *>(red + (g * RR + i) * SBN + h * 128 + c * 128 +
-                                                lane * 4) = v;
+                    *reinterpret_cast<float4 *>(red + (warp * RR + i) * SBN + c * 128 + lane * 4) = v;
                 }
             }
             __syncthreads();
 #pragma unroll
             for (int i = 0; i < RR; ++i) {
-                const int col = tid & (SBN - 1);
-                float sum = red[i * SBN + col];
+                float sum[OWN], x[OWN];
+                Vec<OWN>::load(red + i * SBN + col0, sum);
 #pragma unroll
-                for (int gg = 1; gg < GROUPS; ++gg) sum += red[(gg * RR + i) * SBN + col];
-                fin[RR * r + i] = sum;
+                for (int w = 1; w < WARPS; ++w) {
+                    Vec<OWN>::load(red + (w * RR + i) * SBN + col0, x);
+#pragma unroll
+                    for (int o = 0; o < OWN; ++o) sum[o] += x[o];
+                }
+#pragma unroll
+                for (int o = 0; o < OWN; ++o) fin[RR * r + i][o] = sum[o];
             }
             __syncthreads();
         }
 
-        // With 512 threads the upper half repeats the lower half's sums and
-        // stores nothing.
-        const int col = tid & (SBN - 1);
-        const bool owner = tid < SBN;
-        const int n = slab * SBN + col;
         bool write_c = true;
         if (!(k0 == 0 && k1 == p.kt_total)) {
             float *slot = p.partials + (size_t)skinny_slot(p, cta, slab) * (kSkinnyMaxM * SBN);
-            if (owner) {
 #pragma unroll
-                for (int m = 0; m < MT; ++m) __stcg(slot + m * SBN + col, fin[m]);
-            }
+            for (int m = 0; m < MT; ++m) Vec<OWN>::store_cg(slot + m * SBN + col0, fin[m]);
             __threadfence();
             __syncthreads();
             const int c_first = (slab * p.kt_total) / p.share;
@@ -275,76 +313,115 @@ __global__ void __launch_bounds__(SNT, 1)
             write_c = flags[1] != 0;
             if (write_c) {
                 __threadfence();
-                // Pieces are added in CTA order.  The loads of every other
-                // piece for a group of rows are issued together, so a group
-                // costs one L2 round trip (up to kFastPieces pieces; more
-                // take a plain loop).
-                constexpr int kFastPieces = 6;
-                const int npieces = c_last - c_first + 1;
-                if (npieces <= kFastPieces) {
+                float own[MT][OWN];
 #pragma unroll
-                    for (int m0 = 0; m0 < MT; m0 += 2) {
-                        float v[kFastPieces][2];
+                for (int m = 0; m < MT; ++m)
 #pragma unroll
-                        for (int i = 0; i < kFastPieces; ++i) {
-                            const int cc = c_first + i;
-                            if (cc <= c_last && cc != cta) {
-                                const float *slot = p.partials +
-                                                    (size_t)skinny_slot(p, cc, slab) * (kSkinnyMaxM * SBN) +
-                                                    col;
-#pragma unroll
-                                for (int r = 0; r < 2; ++r) v[i][r] = __ldcg(slot + (m0 + r) * SBN);
+                    for (int o = 0; o < OWN; ++o) own[m][o] = fin[m][o];
+                if (q == q_total) {
+                    // Last unit: no copies are outstanding, so the ring is
+                    // idle.  The other pieces come in with bulk copies, up to
+                    // ring_pieces at a time, and are added in CTA order.
+                    bool ok = true;
+                    int cc = c_first;
+                    while (cc <= c_last) {
+                        int cnt = 0, cc_end = cc;
+                        while (cc_end <= c_last && (cc_end == cta || cnt < L::ring_pieces)) {
+                            if (cc_end != cta) ++cnt;
+                            ++cc_end;
+                        }
+                        if (cnt > 0) {
+                            __syncthreads();  // the ring's previous contents are read
+                            if (tid == 0) {
+                                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                                fence_proxy_async_global();
+                                mbar_arrive_expect_tx(fix_bar, cnt * L::piece_bytes);
+                                int j = 0;
+                                for (int c = cc; c < cc_end; ++c) {
+                                    if (c == cta) continue;
+                                    bulk_load(reinterpret_cast<char *>(stages) + j * L::piece_bytes,
+                                              skinny_piece(p, c, slab), L::piece_bytes, fix_bar);
+                                    ++j;
+                                }
+                            }
+                            const bool got = mbar_wait_bounded(fix_bar, fix_phase, p.timeout_ns);
+                            fix_phase ^= 1u;
+                            if (__syncthreads_or(!got)) {
+                                // Stop issuing; the copies of this round are
+                                // waited for (bounded) before the CTA exits.
+                                ok = false;
+                                fix_pending = true;
+                                if (tid == 0) atomicOr(p.err, kErrWaitTimeout);
+                                break;
                             }
                         }
+                        int j = 0;
+                        for (int c = cc; c < cc_end; ++c) {
 #pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            const float own = fin[m0 + r];
-                            float sum = own;
+                            for (int m = 0; m < MT; ++m) {
+                                float x[OWN];
+                                if (c == cta) {
 #pragma unroll
-                            for (int i = 0; i < kFastPieces; ++i) {
-                                const int cc = c_first + i;
-                                if (cc > c_last) break;
-                                const float x = (cc == cta) ? own : v[i][r];
-                                sum = (i == 0) ? x : sum + x;
+                                    for (int o = 0; o < OWN; ++o) x[o] = own[m][o];
+                                } else {
+                                    Vec<OWN>::load(stages + (size_t)j * (MT * SBN) + m * SBN + col0, x);
+                                }
+#pragma unroll
+                                for (int o = 0; o < OWN; ++o)
+                                    fin[m][o] = (c == c_first) ? x[o] : fin[m][o] + x[o];
                             }
-                            fin[m0 + r] = sum;
+                            if (c != cta) ++j;
                         }
+                        cc = cc_end;
+                    }
+                    if (!ok) {  // uniform: set after a CTA-wide vote
+                        write_c = false;
+                        aborted = true;
                     }
                 } else {
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
-                        float sum = 0.f;
-                        for (int cc = c_first; cc <= c_last; ++cc) {
-                            const float v =
-                                (cc == cta) ? fin[m]
-                                            : __ldcg(p.partials +
-                                                     (size_t)skinny_slot(p, cc, slab) * (kSkinnyMaxM * SBN) +
-                                                     m * SBN + col);
-                            sum = (cc == c_first) ? v : sum + v;
+                        for (int c = c_first; c <= c_last; ++c) {
+                            float x[OWN];
+                            if (c == cta) {
+#pragma unroll
+                                for (int o = 0; o < OWN; ++o) x[o] = own[m][o];
+                            } else {
+                                Vec<OWN>::load_cg(skinny_piece(p, c, slab) + m * SBN + col0, x);
+                            }
+#pragma unroll
+                            for (int o = 0; o < OWN; ++o)
+                                fin[m][o] = (c == c_first) ? x[o] : fin[m][o] + x[o];
                         }
-                        fin[m] = sum;
                     }
                 }
                 if (tid == 0) p.counters[slab] = 0;
             }
             __syncthreads();  // flags[1] is rewritten by the next unit
         }
-        if (write_c && owner && n < p.N) {
+        if (write_c) {
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (m < p.M) {
-                    float *c = p.C + (long long)m * p.ldc + n;
-                    float o = p.alpha * fin[m];
-                    if (p.beta != 0.0f) o = __fmaf_rn(p.beta, *c, o);
-                    *c = o;
+            for (int o = 0; o < OWN; ++o) {
+                const int n = slab * SBN + col0 + o;
+                if (n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (m < p.M) {
+                            float *c = p.C + (long long)m * p.ldc + n;
+                            float out = p.alpha * fin[m][o];
+                            if (p.beta != 0.0f) out = __fmaf_rn(p.beta, *c, out);
+                            *c = out;
+                        }
+                    }
                 }
             }
         }
     }
 
     if (aborted && tid == 0) {
-        // Wait (bounded) for the last copy issued into every stage, so none
-        // lands in shared memory after this CTA has exited.
+        // Wait (bounded) for the last copy issued into every stage, and for a
+        // fix-up copy that timed out, so none lands in shared memory after
+        // this CTA has exited.
         for (int s = 0; s < SSTAGES; ++s) {
             const int last = issued[s];
             if (last < 0) continue;
@@ -353,7 +430,21 @@ __global__ void __launch_bounds__(SNT, 1)
                 break;
             }
         }
+        if (fix_pending && !mbar_wait_bounded(fix_bar, fix_phase ^ 1u, 1000000000ull))
+            atomicOr(p.err, kErrDrainTimeout);
     }
+}
+
+template <int MT>
+cudaError_t configure_impl() {
+    cudaError_t e = cudaFuncSetAttribute(sgemm_skinny_kernel<MT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SkinnyLayout<MT>::total);
+    if (e != cudaSuccess) return e;
+    // Two CTAs per SM need the whole unified L1 / shared array as shared memory.
+    return cudaFuncSetAttribute(sgemm_skinny_kernel<MT>,
+                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared);
 }
 
 }  // namespace
@@ -365,14 +456,8 @@ size_t skinny_smem_bytes(int m_tile, int /*share*/) {
 }
 
 cudaError_t skinny_configure(int m_tile) {
-    if (m_tile == 8)
-        return cudaFuncSetAttribute(sgemm_skinny_kernel<8>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)SkinnyLayout<8>::total);
-    if (m_tile == 16)
-        return cudaFuncSetAttribute(sgemm_skinny_kernel<16>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)SkinnyLayout<16>::total);
+    if (m_tile == 8) return configure_impl<8>();
+    if (m_tile == 16) return configure_impl<16>();
     return cudaErrorInvalidValue;
 }
 

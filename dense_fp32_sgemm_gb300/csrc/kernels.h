@@ -86,12 +86,17 @@ cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc,
 // ---------------------------------------------------------------------------
 constexpr int kSkinnyBN = 256;   // columns per slab
 constexpr int kSkinnyBK = 32;    // B rows per TMA stage
-constexpr int kSkinnyMaxM = 32;
-#ifndef SGEMM_SKINNY_CPL
-#define SGEMM_SKINNY_CPL 8
+constexpr int kSkinnyMaxM = 16;  // rows of C the kernel covers (partial slots hold this many)
+// Warps per CTA: 4 (two CTAs per SM, 3 ring stages each) or 8 (one CTA per
+// SM, 6 stages).  A build constant so that both can be timed.
+#ifndef SGEMM_SKINNY_WARPS
+#define SGEMM_SKINNY_WARPS 4
 #endif
-constexpr int kSkinnyCPL = SGEMM_SKINNY_CPL;          // columns per lane
-constexpr int kSkinnyThreads = 32 * 8 * (8 / kSkinnyCPL);
+constexpr int kSkinnyWarps = SGEMM_SKINNY_WARPS;
+static_assert(kSkinnyWarps == 4 || kSkinnyWarps == 8, "skinny kernel: 4 or 8 warps");
+constexpr int kSkinnyThreads = 32 * kSkinnyWarps;
+constexpr int kSkinnyCtasPerSm = kSkinnyWarps == 4 ? 2 : 1;
+constexpr int kSkinnyStages = kSkinnyWarps == 4 ? 3 : 6;
 
 struct SkinnyParams {
     int M, N, K;
@@ -115,7 +120,6 @@ cudaError_t launch_skinny(int m_tile, const CUtensorMap &mapA, const CUtensorMap
                           const SkinnyParams &p, int grid, cudaStream_t stream);
 size_t skinny_smem_bytes(int m_tile, int share);
 cudaError_t skinny_configure(int m_tile);
-constexpr int kSkinnyStages = 6;
 
 // ---------------------------------------------------------------------------
 // Measurement probes (same library, used by the benchmark).
@@ -124,5 +128,6 @@ cudaError_t launch_ffma_probe(int paired, long long iters, int blocks, float *si
                               cudaStream_t stream);
 cudaError_t launch_read_probe(const float4 *buf, long long n4, float *sink, int blocks,
                               cudaStream_t stream);
+cudaError_t launch_hold(unsigned long long ns, cudaStream_t stream);
 
 }  // namespace sgemm

@@ -12,8 +12,8 @@
 // file-scope __device__ array, created by the CUDA runtime on each GPU that
 // loads the library and held there until the process exits.
 //
-// Limits: M <= 16, at most kMaxGrid CTAs (the plan uses one CTA per SM, so
-// any GPU with up to 160 SMs), at most kMaxSlabs slabs of 256 columns
+// Limits: M <= 16, at most kMaxGrid CTAs (the plan fills every SM with
+// kSkinnyCtasPerSm CTAs: any GPU with up to 160 SMs), at most kMaxSlabs slabs of 256 columns
 // (N <= 1,048,576), A and B 16-byte aligned with leading dimensions that are
 // multiples of 4.  Anything else is rejected with SGEMM_ERR_SCRATCH_LIMIT
 // before any work is queued.
@@ -27,16 +27,16 @@
 namespace sgemm {
 namespace {
 
-constexpr int kMaxGrid = 160;
+constexpr int kMaxGrid = 160 * kSkinnyCtasPerSm;
 constexpr int kMaxSlabs = 4096;
 constexpr int kMaxDevices = 64;
 // The skinny kernel gives each CTA two partial slots of kSkinnyMaxM x 256
-// floats (32 KiB).
+// floats (16 KiB).
 constexpr size_t kSlotFloats = size_t(kSkinnyMaxM) * kSkinnyBN;
 constexpr size_t kPartialBytes = 2 * size_t(kMaxGrid) * kSlotFloats * sizeof(float);
 constexpr size_t kCounterBytes = size_t(kMaxSlabs) * sizeof(int);
 constexpr size_t kErrOffset = kPartialBytes + kCounterBytes;
-constexpr size_t kScratchBytes = kErrOffset + 256;  // 10 MiB + 16 KiB + 256 B
+constexpr size_t kScratchBytes = kErrOffset + 256;  // 10 MiB + 16 KiB + 256 B (two CTAs per SM)
 
 // The fixed scratch.  In host code this name is a host-side stand-in, not a
 // device address: the host only ever passes the address cudaGetSymbolAddress
@@ -131,7 +131,7 @@ extern "C" sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t
                     (reinterpret_cast<uintptr_t>(B) & 3u)))
         return SGEMM_ERR_INVALID_ARG;
     // Sizes and layouts this fixed buffer and kernel cannot take.
-    if (M > kSkinnyMaxM / 2) return SGEMM_ERR_SCRATCH_LIMIT;
+    if (M > kSkinnyMaxM) return SGEMM_ERR_SCRATCH_LIMIT;
     if ((N + kSkinnyBN - 1) / kSkinnyBN > kMaxSlabs) return SGEMM_ERR_SCRATCH_LIMIT;
     if (product && ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
                     lda % 4 != 0 || ldb % 4 != 0))

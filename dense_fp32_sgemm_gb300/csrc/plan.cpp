@@ -129,12 +129,13 @@ int make_plan(const PlanInput &in, Plan *pl) {
                         in.ldb < (int64_t(1) << 37);
     int want = in.force_variant;
     if ((want == kVarTile || want == kVarStreamK || want == kVarSkinny) && !tma_ok) return -2;
-    if (want == kVarSkinny && in.M > kSkinnyMaxM / 2) return -3;
+    if (want == kVarSkinny && in.M > kSkinnyMaxM) return -3;
 
     // M <= 16: every B element feeds at most 16 products, so the product is
     // bound by streaming B; a 128-row tile would spend 8x the multiply-adds.
-    if (tma_ok && (want == kVarSkinny || (want < 0 && in.M <= kSkinnyMaxM / 2))) {
-        const int64_t G = in.num_sms > 0 ? in.num_sms : 1;
+    if (tma_ok && (want == kVarSkinny || (want < 0 && in.M <= kSkinnyMaxM))) {
+        // Persistent grid: every CTA the SMs hold at once.
+        const int64_t G = (in.num_sms > 0 ? in.num_sms : 1) * kSkinnyCtasPerSm;
         const int64_t slabs = ceil_div(in.N, kSkinnyBN);
         const int64_t KT = ceil_div(in.K, kSkinnyBK);
         const int64_t total = slabs * KT;
@@ -160,14 +161,25 @@ int make_plan(const PlanInput &in, Plan *pl) {
         }
     }
 
-    if (want == kVarGeneric || (want < 0 && !tma_ok)) {
+    // A product with fewer 128 x 256 x 32 tile slices than SMs leaves most
+    // SMs idle under the tiled kernel, or splits its few tiles into pieces
+    // whose combination costs more than they balance; 64 x 64 tiles spread
+    // it over more SMs.
+    bool small = false;
+    if (want < 0 && tma_ok) {
+        const int64_t G = in.num_sms > 0 ? in.num_sms : 1;
+        const int64_t slices = ceil_div(in.M, kTileBM) * ceil_div(in.N, kTileBN) *
+                               ceil_div(in.K, kTileBK);
+        small = slices <= G;
+    }
+    if (want == kVarGeneric || (want < 0 && (!tma_ok || small))) {
         p.variant = kVarGeneric;
         p.tiles_m = (int)ceil_div(in.M, kGenBM);
         p.tiles_n = (int)ceil_div(in.N, kGenBN);
         p.kt_total = (int)ceil_div(in.K, kGenBK);
         p.grid = p.tiles_m * p.tiles_n;
         p.cost = 0;
-        p.reason = tma_ok ? "forced" : "operands not 16-byte aligned";
+        p.reason = !tma_ok ? "operands not 16-byte aligned" : small ? "small product" : "forced";
         *pl = p;
         return 0;
     }

@@ -107,12 +107,16 @@ def test_small_integers_bit_exact(variant, splits, M, N, K):
 SIZES = [1, 3, 8, 31, 33, 127, 129, 255, 257]
 
 
+# Automatic plan (small products take the 64 x 64 kernel), and the tiled
+# kernel whole (1) and split (2) on the same edges.
+@pytest.mark.parametrize("variant", [-1, 1, 2])
 @pytest.mark.parametrize("M", [1, 33, 129, 257])
 @pytest.mark.parametrize("N", [1, 31, 255, 257])
 @pytest.mark.parametrize("K", [1, 8, 127])
-def test_ragged_shapes_aligned_ld(M, N, K):
+def test_ragged_shapes_aligned_ld(M, N, K, variant):
     Kp, Np = (K + 3) // 4 * 4 + 4, (N + 3) // 4 * 4 + 8
-    check(M, N, K, 0.5, 2.0, dist="normal", seed=M * 7 + N * 3 + K, lda=Kp, ldb=Np, ldc=Np)
+    check(M, N, K, 0.5, 2.0, dist="normal", seed=M * 7 + N * 3 + K, lda=Kp, ldb=Np, ldc=Np,
+          variant=variant)
 
 
 @pytest.mark.parametrize("M,N,K", [(3, 5, 7), (33, 255, 31), (257, 129, 127), (130, 300, 65)])
@@ -252,6 +256,12 @@ def test_probes_run():
     nbytes = sg.probe_read(buf.data_ptr(), buf.numel(), sink.data_ptr(), 152, stream)
     assert nbytes == 4 * buf.numel()
     torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    sg.probe_hold(2_000_000, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert 1.9 <= e0.elapsed_time(e1) < 50.0
 
 
 # ----- skinny-M streaming kernel ---------------------------------------------------
@@ -293,7 +303,9 @@ def test_skinny_wait_timeout_reports_and_recovers():
     dB = torch.from_numpy(B).cuda()
     dC = torch.zeros(M * N, device="cuda")
     stream = torch.cuda.current_stream()
-    sg.set_wait_timeout_ns(2_000_000, 3)
+    # Every CTA has at least two k-steps here; the second one's copy is never issued.
+    assert int(sg.plan_describe(M, N, K)["sk_share"]) >= 2
+    sg.set_wait_timeout_ns(2_000_000, 1)
     try:
         st = sg.sgemm_run(M, N, K, 1.0, dA.data_ptr(), lda, dB.data_ptr(), ldb, 0.0,
                           dC.data_ptr(), N, stream.cuda_stream)

@@ -81,8 +81,8 @@ def test_exact_waves_stay_data_parallel():
     assert ints(p, "dp_tiles", "grid") == [304, SMS]
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (1000, 3000, 77), (8192, 6144, 2048),
-                                   (17, 8192, 8192), (4000, 300, 20000), (129, 257, 33),
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128 * 39), (1000, 3000, 77), (8192, 6144, 2048),
+                                   (17, 8192, 8192), (4000, 300, 20000), (129, 257, 33 * 40),
                                    (40, 1, 100000), (5000, 5000, 1)])
 def test_plan_invariants(M, N, K):
     p = plan(M, N, K)
@@ -101,6 +101,18 @@ def test_plan_invariants(M, N, K):
         assert share >= math.ceil(kt / 4)
     # the chosen cost never exceeds the data-parallel cost
     assert float(p["cost"]) <= math.ceil(T / SMS) * kt + 1e-9
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (129, 257, 33), (1024, 1024, 64),
+                                   (2048, 2048, 16), (300, 520, 64)])
+def test_small_products_take_the_64x64_kernel(M, N, K):
+    # No more 128 x 256 x 32 slices than SMs: the tiled kernel would idle
+    # most SMs, so the 64 x 64 kernel takes the product.
+    assert math.ceil(M / 128) * math.ceil(N / 256) * math.ceil(K / 32) <= SMS
+    p = plan(M, N, K)
+    assert p["variant"] == "generic" and p["reason"] == "small product"
+    # One more slice than SMs goes back to the tiled kernel.
+    assert plan(128 * 17, 256 * 9, 32)["variant"] in ("tile", "streamk")
 
 
 def test_forced_split_count():
@@ -138,11 +150,12 @@ def test_skinny_plan(M, N, K):
     slabs, kt, share, grid, m_tile = ints(p, "tiles_n", "kt", "sk_share", "grid", "m_tile")
     assert slabs == math.ceil(N / 256) and kt == math.ceil(K / 32)
     assert m_tile == (8 if M <= 8 else 16)
-    assert share == math.ceil(slabs * kt / SMS)
-    assert grid == math.ceil(slabs * kt / share) and grid <= SMS
+    # Two 4-warp CTAs per SM.
+    assert share == math.ceil(slabs * kt / (2 * SMS))
+    assert grid == math.ceil(slabs * kt / share) and grid <= 2 * SMS
 
 
 def test_skinny_16x8192x8192_split():
-    # 32 slabs x 256 k-steps over 152 SMs: 54 k-steps each, about 5 pieces a slab.
+    # 32 slabs x 256 k-steps over 2 x 152 CTAs: 27 k-steps each, about 10 pieces a slab.
     p = plan(16, 8192, 8192)
-    assert ints(p, "tiles_n", "kt", "sk_share", "grid") == [32, 256, 54, 152]
+    assert ints(p, "tiles_n", "kt", "sk_share", "grid") == [32, 256, 27, 304]
