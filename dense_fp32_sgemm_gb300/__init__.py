@@ -20,7 +20,7 @@ __all__ = [
     "SgemmError", "build", "library", "library_path", "sgemm_run", "sgemm_run_host",
     "run", "run_host", "status_string", "device_status", "plan_describe",
     "set_plan_override", "set_wait_timeout_ns", "set_tile_config",
-    "release_workspace", "probe_ffma", "probe_read", "EXPORTED_SYMBOLS",
+    "release_workspace", "probe_ffma", "probe_read", "probe_hold", "EXPORTED_SYMBOLS",
     "VARIANT_AUTO", "VARIANT_GENERIC", "VARIANT_TILE", "VARIANT_STREAMK",
     "VARIANT_SKINNY", "STATUS",
 ]
@@ -51,6 +51,7 @@ _SIGNATURES = {
     "sgemm_release_workspace": (_int, []),
     "sgemm_probe_ffma": (_int, [_int, _i64, _int, _vp, _vp]),
     "sgemm_probe_read": (_int, [_vp, _i64, _vp, _int, _vp]),
+    "sgemm_probe_hold": (_int, [_i64, _vp]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -197,10 +198,14 @@ def plan_describe(M, N, K, lda=None, ldb=None, ldc=None, a_addr=0, b_addr=0, c_a
                                          int(max(ldb, 1)), int(max(ldc, 1)), int(a_addr),
                                          int(b_addr), int(c_addr), float(beta), int(num_sms),
                                          buf, len(buf)), "sgemm_plan_describe")
+    # key=value pairs; the last one, reason, is free text.
+    head, sep, reason = buf.value.decode().partition(" reason=")
     out = {}
-    for kv in buf.value.decode().split():
+    for kv in head.split():
         k, _, v = kv.partition("=")
         out[k] = v
+    if sep:
+        out["reason"] = reason
     return out
 
 
@@ -236,3 +241,9 @@ def probe_read(buf_ptr: int, n_floats: int, sink_ptr: int, blocks: int, stream=N
     _check(library().sgemm_probe_read(buf_ptr, int(n_floats), sink_ptr, int(blocks), s),
            "sgemm_probe_read")
     return 4.0 * n_floats
+
+
+def probe_hold(ns: int, stream=None) -> None:
+    """Queue a kernel that keeps `stream` busy for `ns` nanoseconds."""
+    s = stream.cuda_stream if stream is not None else None
+    _check(library().sgemm_probe_hold(int(ns), s), "sgemm_probe_hold")

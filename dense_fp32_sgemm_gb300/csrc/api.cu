@@ -442,4 +442,9 @@ sgemm_status_t sgemm_probe_read(const float *buf, int64_t n_floats, float *sink,
                                          blocks, static_cast<cudaStream_t>(stream)));
 }
 
+sgemm_status_t sgemm_probe_hold(int64_t ns, void *stream) {
+    if (ns <= 0 || ns > 1000000000LL) return SGEMM_ERR_INVALID_ARG;
+    return status_from(launch_hold((unsigned long long)ns, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

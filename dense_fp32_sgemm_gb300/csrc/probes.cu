@@ -7,6 +7,9 @@
 //   as 16 scalar FFMA or 8 packed pairs per iteration; 2 flops per product.
 // - Read probe: a grid-stride 128-bit streaming read of a buffer, summed so
 //   the loads cannot be dropped.
+// - Hold: one thread that sleeps on the GPU global timer for a fixed time,
+//   so that the host can queue the next launches behind it and the device
+//   never waits for the host between them.
 
 #include "device_common.cuh"
 #include "kernels.h"
@@ -72,6 +75,11 @@ __global__ void read_probe_kernel(const float4 *__restrict__ buf, long long n4, 
     if (s == 1234.5f) sink[blockIdx.x] = s;
 }
 
+__global__ void hold_kernel(unsigned long long ns) {
+    const unsigned long long t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns) __nanosleep(2000);
+}
+
 }  // namespace
 
 // Products per thread per iteration: 8 rounds x 16 chains = 128 FMA.
@@ -87,6 +95,11 @@ cudaError_t launch_ffma_probe(int paired, long long iters, int blocks, float *si
 cudaError_t launch_read_probe(const float4 *buf, long long n4, float *sink, int blocks,
                               cudaStream_t stream) {
     read_probe_kernel<<<blocks, 512, 0, stream>>>(buf, n4, sink);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_hold(unsigned long long ns, cudaStream_t stream) {
+    hold_kernel<<<1, 1, 0, stream>>>(ns);
     return cudaGetLastError();
 }
 

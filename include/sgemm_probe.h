@@ -9,7 +9,7 @@
  *   under a sustained load the clock, and with it the peak, drops; the probe
  *   is therefore run for as long as the GEMM it is compared with.
  *
- * Both calls queue one kernel on `stream` (a cudaStream_t, NULL = legacy
+ * Each call queues one kernel on `stream` (a cudaStream_t, NULL = legacy
  * default stream) and return at once; the caller times them with events.
  */
 #ifndef GB300_SGEMM_PROBE_H
@@ -41,6 +41,16 @@ SGEMM_API sgemm_status_t sgemm_probe_ffma(int paired, int64_t iters, int blocks,
  */
 SGEMM_API sgemm_status_t sgemm_probe_read(const float *buf, int64_t n_floats, float *sink, int blocks,
                                 void *stream);
+
+/*
+ * sgemm_probe_hold -- one thread that sleeps on the GPU global timer for `ns`
+ * nanoseconds and does nothing else.  A benchmark queues it ahead of a batch
+ * of timed launches so that the host has queued the whole batch before the
+ * device reaches it: the device then never idles waiting for the host, and
+ * an event pair around one launch times that launch alone.  Returns
+ * SGEMM_ERR_INVALID_ARG unless 0 < ns <= 10^9 (one second).
+ */
+SGEMM_API sgemm_status_t sgemm_probe_hold(int64_t ns, void *stream);
 
 #ifdef __cplusplus
 }

@@ -88,6 +88,8 @@ def test_probe_argument_checks(lib):
     assert lib.sgemm_probe_ffma(0, 0, 1, 4096, None) == 1
     assert lib.sgemm_probe_read(4100, 16, 4096, 1, None) == 1
     assert lib.sgemm_probe_read(4096, 6, 4096, 1, None) == 1
+    assert lib.sgemm_probe_hold(0, None) == 1
+    assert lib.sgemm_probe_hold(1000000001, None) == 1
 
 
 def test_hooks_validate(lib):
