@@ -14,6 +14,8 @@ also carries:
   cpu_baseline  the CPU oracle timed on this host's cores on a bounded sample
                 of the same workload;
   secondary     the 4092^3 (alpha=0.5, beta=2) workload, timed the same way;
+  cublas_context  the same products through cuBLAS FP32 with TF32 off (context);
+  sets          the value over the first and the second half of the timed steps;
   clocks        SM clocks sampled with nvidia-smi during the timed region.
 
 --impl reference times the CPU oracle instead (rank 0 only).
@@ -283,6 +285,37 @@ def gpu_arm(args, ws, rank, local):
         durs = [e0.elapsed_time(e1) / 1e3 for e0, e1 in evs]
         return durs, wall
 
+    def timed_cublas(cfg, dA, dB, dC, steps, warmup):
+        """The same product through cuBLAS FP32 (torch.mm / addmm with TF32
+        off), timed like the GEMM: context for the reader, not a baseline."""
+        M, N, K = cfg["M"], cfg["N"], cfg["K"]
+        a, b = dA.view(M, K), dB.view(K, N)
+        c_in = dC.view(M, N)
+        out = torch.empty(M, N, device=dev)
+
+        def one():
+            if cfg["beta"] != 0:
+                torch.addmm(c_in, a, b, beta=cfg["beta"], alpha=cfg["alpha"], out=out)
+            elif cfg["alpha"] != 1:
+                torch.mm(a, b, out=out).mul_(cfg["alpha"])
+            else:
+                torch.mm(a, b, out=out)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for b0 in range(0, steps, HOLD_BATCH):
+            sg.probe_hold(20_000_000, stream)
+            for e0, e1 in evs[b0:b0 + HOLD_BATCH]:
+                flush_l2()
+                e0.record(stream)
+                one()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) / 1e3 for e0, e1 in evs]
+
     def ffma_probe(seconds_target, paired):
         sink = torch.zeros(4096, device=dev)
         blocks = SMS_GB300 * 4
@@ -345,6 +378,11 @@ def gpu_arm(args, ws, rank, local):
         torch.distributed.all_reduce(total, op=torch.distributed.ReduceOp.MAX)
     value = ws * args.steps * flops / float(total.item()) / 1e9
 
+    half = len(durs) // 2
+    drift = {"first_half": round(half * flops / sum(durs[:half]) / 1e9, 2),
+             "second_half": round((len(durs) - half) * flops / sum(durs[half:]) / 1e9, 2),
+             "unit": "GFLOP/s"} if half > 0 else None
+
     plan = sg.plan_describe(cfg["M"], cfg["N"], cfg["K"], a_addr=dA.data_ptr(),
                             b_addr=dB.data_ptr(), c_addr=dC.data_ptr(), beta=cfg["beta"])
 
@@ -361,6 +399,7 @@ def gpu_arm(args, ws, rank, local):
                          "so the device never waits for the host",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "plan": plan.get("variant"), "grid": int(plan.get("grid", 0))},
+        "sets": drift,
         "gpu_launches": args.steps + -(-args.steps // HOLD_BATCH),
         "gpu_launches_detail": {"sgemm (inside the event pairs)": args.steps,
                                 "hold (between batches)": -(-args.steps // HOLD_BATCH)},
@@ -435,6 +474,22 @@ def gpu_arm(args, ws, rank, local):
             del dAo, dBo, dCo
         result["other_workloads"] = others
 
+    # ---- cuBLAS FP32 on the same products (context, TF32 off) ----
+    if not args.no_cublas:
+        torch.backends.cuda.matmul.allow_tf32 = False
+        ctx = []
+        for cname in (name, "s3_4092", "s6_skinny"):
+            if any(e["workload"] == WORKLOADS[cname] for e in ctx):
+                continue
+            cfgc, _, _, _, dAc, dBc, dCc = device_inputs(cname)
+            steps_c = max(5, min(200, args.steps // 10))
+            dc = statistics.median(timed_cublas(cfgc, dAc, dBc, dCc, steps_c, 3))
+            ctx.append({"workload": WORKLOADS[cname], "api": "torch.mm/addmm, cuBLAS FP32, TF32 off",
+                        "value": round(flops_of(cfgc) / dc / 1e9, 2), "unit": "GFLOP/s",
+                        "ms_per_step": round(dc * 1e3, 4), "steps": steps_c})
+            del dAc, dBc, dCc
+        result["cublas_context"] = ctx
+
     # ---- end to end through the host entry point ----
     pA = torch.from_numpy(A.reshape(cfg["M"], cfg["K"])).pin_memory()
     pB = torch.from_numpy(B.reshape(cfg["K"], cfg["N"])).pin_memory()
@@ -455,6 +510,8 @@ def gpu_arm(args, ws, rank, local):
     # ---- CPU baseline (rank 0 only) ----
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = time_oracle(name, budget_s=args.cpu_seconds)
+        result["cpu_baseline"]["s1_128_one_thread_gflops"] = time_oracle("s1_128", budget_s=1.0,
+                                                                 threads=1)["value"]
     return result, rank
 
 
@@ -498,6 +555,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     ap.add_argument("--no-secondary", action="store_true", help="skip the 4092^3 line")
+    ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS context timings")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed GEMM steps (for profiler runs)")
     args = ap.parse_args()

@@ -17,7 +17,8 @@ import threading
 from . import _build
 
 __all__ = [
-    "SgemmError", "build", "library", "library_path", "sgemm_run", "sgemm_run_host",
+    "SgemmError", "build", "library", "library_path", "sgemm_run", "sgemm_run_epilogue",
+    "sgemm_run_host", "ACT_NONE", "ACT_RELU",
     "run", "run_host", "status_string", "device_status", "plan_describe",
     "set_plan_override", "set_wait_timeout_ns", "set_tile_config",
     "release_workspace", "probe_ffma", "probe_read", "probe_hold", "EXPORTED_SYMBOLS",
@@ -31,12 +32,15 @@ STATUS = {
     6: "SGEMM_ERR_NO_DEVICE", 7: "SGEMM_ERR_UNSUPPORTED", 8: "SGEMM_ERR_SCRATCH_LIMIT",
 }
 VARIANT_AUTO, VARIANT_GENERIC, VARIANT_TILE, VARIANT_STREAMK, VARIANT_SKINNY = -1, 0, 1, 2, 3
+ACT_NONE, ACT_RELU = 0, 1
 
 _i64, _f32, _vp, _int = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
 
 # name -> (restype, argtypes); one entry per function declared in include/*.h
 _SIGNATURES = {
     "sgemm_run": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
+    "sgemm_run_epilogue": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
+                                  _vp, _int, _vp]),
     "sgemm_run_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
     "sgemm_run_skinny_noalloc": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp,
                                         _i64, _vp]),
@@ -109,6 +113,14 @@ def sgemm_run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
                                float(beta), C, int(ldc), stream)
 
 
+def sgemm_run_epilogue(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias=None,
+                       activation=ACT_NONE, stream=None) -> int:
+    """Raw C-ABI call of C = act(alpha*A*B + beta*C + bias); returns the status."""
+    return library().sgemm_run_epilogue(int(M), int(N), int(K), float(alpha), A, int(lda), B,
+                                        int(ldb), float(beta), C, int(ldc), bias,
+                                        int(activation), stream)
+
+
 def sgemm_run_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
     """Raw C-ABI call with integer host addresses; returns the status."""
     return library().sgemm_run_host(int(M), int(N), int(K), float(alpha), A, int(lda), B,
@@ -127,12 +139,15 @@ def _matrix_args(t, name):
     return t.data_ptr(), max(ld, cols, 1)
 
 
-def run(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
-    """C = alpha * A @ B + beta * C in place on CUDA float32 tensors.
+def run(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, bias=None,
+        activation: int = ACT_NONE):
+    """C = act(alpha * A @ B + beta * C + bias) in place on CUDA float32 tensors.
 
     Tensors are row-major with unit column stride; a row stride larger than
-    the row length is passed on as the leading dimension.  ``stream`` is a
-    torch.cuda.Stream (default: the current stream).  Returns C.
+    the row length is passed on as the leading dimension.  ``bias`` is None or
+    a contiguous CUDA float32 tensor of N elements, added to every row;
+    ``activation`` is ACT_NONE or ACT_RELU.  ``stream`` is a torch.cuda.Stream
+    (default: the current stream).  Returns C.
     """
     import torch
 
@@ -146,9 +161,19 @@ def run(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
     a, lda = _matrix_args(A, "A")
     b, ldb = _matrix_args(B, "B")
     c, ldc = _matrix_args(C, "C")
+    bias_ptr = None
+    if bias is not None:
+        if not bias.is_cuda or str(bias.dtype) != "torch.float32" or bias.numel() != N or (
+                bias.dim() != 1 and not bias.is_contiguous()) or (bias.dim() == 1 and bias.stride(0) != 1):
+            raise ValueError("bias must be a contiguous CUDA float32 tensor of N elements")
+        bias_ptr = bias.data_ptr()
     s = (stream or torch.cuda.current_stream(C.device)).cuda_stream
     with torch.cuda.device(C.device):
-        _check(sgemm_run(M, N, K, alpha, a, lda, b, ldb, beta, c, ldc, s), "sgemm_run")
+        if bias_ptr is None and activation == ACT_NONE:
+            _check(sgemm_run(M, N, K, alpha, a, lda, b, ldb, beta, c, ldc, s), "sgemm_run")
+        else:
+            _check(sgemm_run_epilogue(M, N, K, alpha, a, lda, b, ldb, beta, c, ldc, bias_ptr,
+                                      activation, s), "sgemm_run_epilogue")
     return C
 
 

@@ -152,7 +152,7 @@ sgemm_status_t validate(int64_t M, int64_t N, int64_t K, float alpha, const floa
 
 sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                           int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-                          int64_t ldc, cudaStream_t stream, DeviceState &d) {
+                          int64_t ldc, const Epilogue &epi, cudaStream_t stream, DeviceState &d) {
     PlanInput in;
     in.M = M; in.N = N; in.K = K; in.lda = lda; in.ldb = ldb; in.ldc = ldc;
     in.a_addr = reinterpret_cast<uintptr_t>(A);
@@ -169,12 +169,13 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
         case kVarNone:
             return SGEMM_OK;
         case kVarScale:
-            return status_from(launch_scale((int)M, (int)N, beta, C, ldc, stream));
+            return status_from(launch_scale((int)M, (int)N, beta, C, ldc, epi, stream));
         case kVarGeneric: {
             GenericParams gp;
             gp.M = (int)M; gp.N = (int)N; gp.K = (int)K;
             gp.alpha = alpha; gp.beta = beta;
             gp.A = A; gp.lda = lda; gp.B = B; gp.ldb = ldb; gp.C = C; gp.ldc = ldc;
+            gp.epi = epi;
             return status_from(launch_generic(gp, stream));
         }
         case kVarTile:
@@ -196,6 +197,7 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             tp.dp_tiles = pl.dp_tiles; tp.sk_tiles = pl.sk_tiles; tp.sk_share = pl.sk_share;
             tp.group_m = pl.group_m;
             tp.alpha = alpha; tp.beta = beta; tp.C = C; tp.ldc = ldc; tp.c_vec4 = pl.c_vec4;
+            tp.epi = epi;
             tp.partials = nullptr; tp.counters = nullptr;
             tp.err = d.err;
             const unsigned long long to = g_timeout_ns.load();
@@ -228,6 +230,7 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             sp.slabs = pl.slabs; sp.kt_total = pl.kt_total; sp.share = pl.sk_share;
             sp.alpha = alpha; sp.beta = beta;
             sp.A = A; sp.lda = lda; sp.C = C; sp.ldc = ldc; sp.c_vec4 = 0;
+            sp.epi = epi;
             sp.err = d.err;
             const unsigned long long to = g_timeout_ns.load();
             sp.timeout_ns = to ? to : kDefaultTimeoutNs;
@@ -252,18 +255,30 @@ using namespace sgemm;
 
 extern "C" {
 
-sgemm_status_t sgemm_run(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
-                         int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-                         int64_t ldc, void *stream) {
+sgemm_status_t sgemm_run_epilogue(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                                  int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                                  int64_t ldc, const float *bias, int activation, void *stream) {
     const sgemm_status_t v = validate(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
     if (v != SGEMM_OK) return v;
+    if (activation != SGEMM_ACT_NONE && activation != SGEMM_ACT_RELU) return SGEMM_ERR_INVALID_ARG;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return SGEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return SGEMM_OK;
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState *d = nullptr;
     const sgemm_status_t s = device_state(&d);
     if (s != SGEMM_OK) return s;
-    return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+    Epilogue epi;
+    epi.bias = bias;
+    epi.act = activation == SGEMM_ACT_RELU ? kActRelu : kActNone;
+    return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi,
                       static_cast<cudaStream_t>(stream), *d);
+}
+
+sgemm_status_t sgemm_run(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                         int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                         int64_t ldc, void *stream) {
+    return sgemm_run_epilogue(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr,
+                              SGEMM_ACT_NONE, stream);
 }
 
 sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
@@ -308,7 +323,8 @@ sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha, cons
         cudaMemcpy2DAsync(hb.C, dldc * 4, C, ldc * 4, N * 4, M, cudaMemcpyHostToDevice, st) !=
             cudaSuccess)
         return SGEMM_ERR_LAUNCH;
-    s = run_locked(M, N, K, alpha, hb.A, dlda, hb.B, dldb, beta, hb.C, dldc, st, *d);
+    s = run_locked(M, N, K, alpha, hb.A, dlda, hb.B, dldb, beta, hb.C, dldc, Epilogue{nullptr, kActNone},
+                   st, *d);
     if (s != SGEMM_OK) return s;
     if (cudaMemcpy2DAsync(C, ldc * 4, hb.C, dldc * 4, N * 4, M, cudaMemcpyDeviceToHost, st) !=
         cudaSuccess)

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kernels.h"
+
 namespace sgemm {
 
 // Device error word bits (written with atomicOr, read and cleared by the host).
@@ -39,6 +41,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)
                  : "memory");
+}
+
+// Plain arrive (release at CTA scope): the caller's earlier shared-memory
+// accesses are ordered before the phase completes.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
@@ -98,6 +106,14 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 // following async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// The epilogue after alpha * acc + beta * c for column n: add the bias, then
+// the activation (ReLU as x < 0 ? 0 : x, which keeps NaN and -0).
+__device__ __forceinline__ float apply_epilogue(float v, const Epilogue &e, int n) {
+    if (e.bias) v += __ldg(e.bias + n);
+    if (e.act == kActRelu) v = (v < 0.0f) ? 0.0f : v;
+    return v;
 }
 
 __device__ __forceinline__ float4 ld_shared_f4(const float *p) {

@@ -1,6 +1,7 @@
 // Generic FP32 GEMM for operands the TMA path cannot map (pointers or leading
-// dimensions that break 16-byte alignment), and the C = beta * C kernel for
-// the alpha == 0 / K == 0 quick return.
+// dimensions that break 16-byte alignment, or products too small for the
+// tiled kernel), and the C = beta * C kernel for the alpha == 0 / K == 0
+// quick return.
 //
 // 64 x 64 block tile, K slice 16, 256 threads with a 4 x 4 micro-tile each
 // ("Optimizing Matrix Multiply on CUDA, Part 1", section "Stage 3: Register
@@ -87,18 +88,19 @@ __global__ void __launch_bounds__(GNT) sgemm_generic_kernel(const GenericParams 
             if (n >= p.N) continue;
             float o = p.alpha * acc[i][j];
             if (p.beta != 0.0f) o = __fmaf_rn(p.beta, crow[n], o);
-            crow[n] = o;
+            crow[n] = apply_epilogue(o, p.epi, n);
         }
     }
 }
 
-__global__ void sgemm_scale_kernel(int M, int N, float beta, float *C, long long ldc) {
+__global__ void sgemm_scale_kernel(int M, int N, float beta, float *C, long long ldc,
+                                   const Epilogue epi) {
     const long long total = (long long)M * N;
     for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
          e += (long long)gridDim.x * blockDim.x) {
         const long long m = e / N, n = e - m * N;
         float *c = C + m * ldc + n;
-        *c = (beta == 0.0f) ? 0.0f : beta * *c;
+        *c = apply_epilogue((beta == 0.0f) ? 0.0f : beta * *c, epi, (int)n);
     }
 }
 
@@ -111,12 +113,13 @@ cudaError_t launch_generic(const GenericParams &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, cudaStream_t stream) {
+cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, const Epilogue &epi,
+                         cudaStream_t stream) {
     const long long total = (long long)M * N;
     long long blocks = (total + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
-    sgemm_scale_kernel<<<(int)blocks, 256, 0, stream>>>(M, N, beta, C, ldc);
+    sgemm_scale_kernel<<<(int)blocks, 256, 0, stream>>>(M, N, beta, C, ldc, epi);
     return cudaGetLastError();
 }
 

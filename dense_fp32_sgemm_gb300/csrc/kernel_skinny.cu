@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
                             float *c = p.C + (long long)m * p.ldc + n;
                             float out = p.alpha * fin[m][o];
                             if (p.beta != 0.0f) out = __fmaf_rn(p.beta, *c, out);
-                            *c = out;
+                            *c = apply_epilogue(out, p.epi, n);
                         }
                     }
                 }

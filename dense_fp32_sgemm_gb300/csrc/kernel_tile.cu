@@ -373,6 +373,12 @@ __device__ __forceinline__ void store_tile(Acc<FM, TM> &acc, const TileParams &p
                         o.z = __fmaf_rn(beta, cv.z, o.z);
                         o.w = __fmaf_rn(beta, cv.w, o.w);
                     }
+                    if (p.epi.bias || p.epi.act) {
+                        o.x = apply_epilogue(o.x, p.epi, n + 0);
+                        o.y = apply_epilogue(o.y, p.epi, n + 1);
+                        o.z = apply_epilogue(o.z, p.epi, n + 2);
+                        o.w = apply_epilogue(o.w, p.epi, n + 3);
+                    }
                     *reinterpret_cast<float4 *>(crow + n) = o;
                 } else {
 #pragma unroll
@@ -380,7 +386,7 @@ __device__ __forceinline__ void store_tile(Acc<FM, TM> &acc, const TileParams &p
                         if (n + jj < p.N) {
                             float o = alpha * acc.at(ti, c * 4 + jj);
                             if (beta != 0.0f) o = __fmaf_rn(beta, crow[n + jj], o);
-                            crow[n + jj] = o;
+                            crow[n + jj] = apply_epilogue(o, p.epi, n + jj);
                         }
                     }
                 }

@@ -10,6 +10,17 @@
 namespace sgemm {
 
 // ---------------------------------------------------------------------------
+// Epilogue applied by every kernel after alpha * acc + beta * c: a bias per
+// column of C, then an activation.
+// ---------------------------------------------------------------------------
+enum : int { kActNone = 0, kActRelu = 1 };
+
+struct Epilogue {
+    const float *bias;  // N floats, or nullptr
+    int act;            // kActNone or kActRelu
+};
+
+// ---------------------------------------------------------------------------
 // Tiled FFMA kernel (TMA + mbarrier pipeline, in-CTA transposed A tile).
 // Block tile BM x BN = 128 x 256, K slice BK = 32; each thread a TM x 8
 // micro-tile.
@@ -38,6 +49,7 @@ struct TileParams {
     float *C;
     long long ldc;
     int c_vec4;         // C and ldc allow 16-byte accesses
+    Epilogue epi;
     float *partials;    // 2 * gridDim.x slots of BM*BN floats (stream-K)
     int *counters;      // one arrival counter per stream-K tile, zero at rest
     int *err;           // device error word
@@ -70,12 +82,13 @@ struct GenericParams {
     long long ldb;
     float *C;
     long long ldc;
+    Epilogue epi;
 };
 
 cudaError_t launch_generic(const GenericParams &p, cudaStream_t stream);
 
-// C = beta * C (beta == 0 writes zeros without reading C).
-cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc,
+// C = act(beta * C + bias) (beta == 0 does not read C).
+cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, const Epilogue &epi,
                          cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
@@ -109,6 +122,7 @@ struct SkinnyParams {
     float *C;
     long long ldc;
     int c_vec4;
+    Epilogue epi;
     float *partials;      // 2 * gridDim.x slots of kSkinnyMaxM * BN floats
     int *counters;        // one per slab
     int *err;

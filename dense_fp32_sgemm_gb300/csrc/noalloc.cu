@@ -142,8 +142,8 @@ extern "C" sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t
     if (s != SGEMM_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!product) {
-        return launch_scale((int)M, (int)N, beta, C, ldc, st) == cudaSuccess ? SGEMM_OK
-                                                                              : SGEMM_ERR_LAUNCH;
+        const cudaError_t e = launch_scale((int)M, (int)N, beta, C, ldc, Epilogue{nullptr, kActNone}, st);
+        return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
     }
 
     PlanInput in;
@@ -183,6 +183,7 @@ extern "C" sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t
     sp.slabs = pl.slabs; sp.kt_total = pl.kt_total; sp.share = pl.sk_share;
     sp.alpha = alpha; sp.beta = beta;
     sp.A = A; sp.lda = lda; sp.C = C; sp.ldc = ldc; sp.c_vec4 = 0;
+    sp.epi = Epilogue{nullptr, kActNone};
     sp.partials = reinterpret_cast<float *>(dev->scratch);
     sp.counters = counters;
     sp.err = err;

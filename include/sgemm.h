@@ -80,6 +80,34 @@ SGEMM_API sgemm_status_t sgemm_run(int64_t M, int64_t N, int64_t K, float alpha,
                          const float *A, int64_t lda, const float *B, int64_t ldb,
                          float beta, float *C, int64_t ldc, void *stream);
 
+/* Activation applied last by sgemm_run_epilogue. */
+enum {
+    SGEMM_ACT_NONE = 0, /* identity                                            */
+    SGEMM_ACT_RELU = 1  /* x < 0 ? 0 : x  (a NaN stays NaN, -0 stays -0)       */
+};
+
+/*
+ * sgemm_run_epilogue -- C = act(alpha * A * B + beta * C + bias) on the GPU,
+ * the bias and the activation applied in the GEMM's own epilogue, with no
+ * extra pass over C ("GEMM from Scratch", end of Module 08, "When to just
+ * call the library": fusing an epilogue or activation into the product is
+ * the reason given for writing one's own GEMM).
+ *
+ * bias: NULL, or a device pointer to N floats (4-byte aligned, owned by the
+ *   caller, only read); bias[j] is added to every element of column j, as a
+ *   linear layer's bias is added to each row of X * W.
+ * activation: one of SGEMM_ACT_*.  Other values return SGEMM_ERR_INVALID_ARG.
+ * Each element is rounded as fl(fl(alpha * acc + beta * c) + bias[j]) and the
+ * activation is exact.  Everything else (arguments, layout, workspace,
+ * asynchrony, errors) is as for sgemm_run, which is this call with
+ * bias = NULL and SGEMM_ACT_NONE.  When alpha == 0 or K == 0 the result is
+ * act(beta * C + bias); when M == 0 or N == 0 nothing is done.
+ */
+SGEMM_API sgemm_status_t sgemm_run_epilogue(int64_t M, int64_t N, int64_t K, float alpha,
+                                  const float *A, int64_t lda, const float *B, int64_t ldb,
+                                  float beta, float *C, int64_t ldc, const float *bias,
+                                  int activation, void *stream);
+
 /*
  * sgemm_run_host -- the same operation on HOST matrices.
  *

@@ -156,7 +156,7 @@ def sgemm_ref(A, B, C=None, alpha=1.0, beta=0.0, rows=None, threads=0,
                           rows=rows, threads=threads, want_absprod=want_absprod)
 
 
-def error_bound(absprod, C, alpha, beta, K):
+def error_bound(absprod, C, alpha, beta, K, bias=None):
     """Elementwise FP32 bound 2*K*2^-24*(|alpha|*(|A||B|)_ij + |beta|*|C_ij|).
 
     K is taken as max(K, 3).  A K-term FP32 dot product followed by the
@@ -164,10 +164,39 @@ def error_bound(absprod, C, alpha, beta, K):
     at most gamma_{K+2} = (K+2)u/(1-(K+2)u) relative to |alpha|(|A||B|)_ij,
     and the beta term through at most two.  2*K*u covers gamma_{K+2} for every
     K >= 3 (u = 2^-24), so smaller K use the K = 3 constant.
+
+    With a bias (a length-N vector added to every row) each term passes
+    through one more rounding, so |bias_j| joins the sum and K is taken as
+    max(K, 4) (2*K*u covers gamma_{K+3} for K >= 4).  ReLU is 1-Lipschitz and
+    exact, so the same bound holds after it.
     """
-    keff = max(int(K), 3)
+    keff = max(int(K), 4 if bias is not None else 3)
     u = 2.0 ** -24
     bound = np.abs(alpha) * absprod
     if beta != 0.0 and C is not None:
         bound = bound + np.abs(beta) * np.abs(np.asarray(C, dtype=np.float64))
+    if bias is not None:
+        bound = bound + np.abs(np.asarray(bias, dtype=np.float64))[None, :]
     return 2.0 * keff * u * bound
+
+
+ACT_NONE, ACT_RELU = 0, 1
+
+
+def apply_epilogue(ref, bias=None, activation=ACT_NONE):
+    """act(ref + bias) in double, on an oracle result ref (rows x N).
+
+    "GEMM from Scratch", end of Module 08 ("When to just call the library"):
+    fusing an epilogue or activation into the product is the reason given for
+    writing one's own GEMM.  The pages name no activation; ReLU is taken as
+    x < 0 ? 0 : x, so NaN passes through.  The bias is a vector of N values,
+    bias[j] added to every row's column j.
+    """
+    out = np.array(ref, dtype=np.float64, copy=True)
+    if bias is not None:
+        out = out + np.asarray(bias, dtype=np.float64)[None, :]
+    if activation == ACT_RELU:
+        out = np.where(out < 0.0, 0.0, out)
+    elif activation != ACT_NONE:
+        raise ValueError(f"unknown activation {activation}")
+    return out

@@ -56,16 +56,23 @@ class DeviceMatrix:
 
 
 def run_gemm(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, offsets=(0, 0, 0),
-             variant=-1, splits=0, c_fill=None):
-    """Run sgemm_run on device copies; returns (C result as M x N float32,
-    raw device C buffer on host, the DeviceMatrix for C)."""
+             variant=-1, splits=0, c_fill=None, bias=None, activation=0):
+    """Run sgemm_run (sgemm_run_epilogue when a bias or an activation is
+    given) on device copies; returns (C result as M x N float32, the
+    DeviceMatrix for C)."""
     dA = DeviceMatrix(A, M, lda, offsets[0])
     dB = DeviceMatrix(B, K, ldb, offsets[1])
     dC = DeviceMatrix(C, M, ldc, offsets[2], fill=c_fill)
+    dbias = DeviceMatrix(bias, 1, N) if bias is not None else None
     sg.set_plan_override(variant, splits)
     try:
-        st = sg.sgemm_run(M, N, K, alpha, dA.ptr, lda, dB.ptr, ldb, beta, dC.ptr, ldc,
-                          torch.cuda.current_stream().cuda_stream)
+        stream = torch.cuda.current_stream().cuda_stream
+        if bias is None and activation == 0:
+            st = sg.sgemm_run(M, N, K, alpha, dA.ptr, lda, dB.ptr, ldb, beta, dC.ptr, ldc, stream)
+        else:
+            st = sg.sgemm_run_epilogue(M, N, K, alpha, dA.ptr, lda, dB.ptr, ldb, beta, dC.ptr, ldc,
+                                       dbias.ptr if dbias is not None else None, activation,
+                                       stream)
     finally:
         sg.set_plan_override(-1, 0)
     assert st == 0, sg.status_string(st)
@@ -73,6 +80,9 @@ def run_gemm(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, offsets=(0, 0, 0),
     assert dev == 0, sg.status_string(dev)
     host = dC.to_host()
     assert dA.guards_intact() and dB.guards_intact(), "an operand buffer was written"
+    if dbias is not None:
+        assert dbias.guards_intact() and same_bits(dbias.region(), dbias.region(dbias.host_init)), \
+            "the bias buffer was written"
     assert dC.guards_intact(host), "C's guard band was written"
     region = dC.region(host)
     out = region[:M * ldc].reshape(M, ldc) if M * ldc else np.zeros((M, ldc), np.float32)

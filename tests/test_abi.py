@@ -72,6 +72,12 @@ def test_invalid_arguments_rejected_before_any_device_call(lib, args):
     assert st == 1, sg.status_string(st)
 
 
+@pytest.mark.parametrize("bias,activation", [(None, 2), (None, -1), (4098, 0), (4097, 1)])
+def test_epilogue_arguments_rejected_before_any_device_call(lib, bias, activation):
+    st = sg.sgemm_run_epilogue(4, 5, 6, 1.0, 4096, 6, 8192, 5, 0.0, 16384, 5, bias, activation)
+    assert st == 1, sg.status_string(st)
+
+
 def test_empty_output_is_a_no_op_without_device(lib):
     assert sg.sgemm_run(0, 5, 6, 1.0, None, 6, None, 5, 0.0, None, 5) == 0
     assert sg.sgemm_run(4, 0, 6, 1.0, None, 6, None, 1, 0.0, None, 1) == 0

@@ -86,6 +86,25 @@ def test_workload_full_size(name, sample):
     assert_within(got, ref, bound, name)
 
 
+def test_cublas_fp32_meets_the_same_bound():
+    # cuBLAS FP32 with TF32 off, on the 2048^3 workload: a second GPU product,
+    # independent of this library, must also sit within the bound against the
+    # oracle, which checks the oracle and the bound at a size the exact tests
+    # do not reach.
+    cfg, A, B, C = datagen.config_inputs("s2_2048")
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        out = torch.mm(torch.from_numpy(A).cuda().view(M, K),
+                       torch.from_numpy(B).cuda().view(K, N)).cpu().numpy()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    rows = sample_rows(M, 48, 11)
+    ref, bound = reference(M, N, K, 1.0, 0.0, A, K, B, N, None, N, rows=rows)
+    assert_within(out[np.asarray(rows)], ref, bound, "cuBLAS FP32")
+
+
 # ----- exact integer inputs: every variant must be bit-exact ---------------------
 
 @pytest.mark.parametrize("variant,splits", [(0, 0), (1, 0), (2, 2), (2, 3), (2, 4), (-1, 0)])
@@ -262,6 +281,74 @@ def test_probes_run():
     e1.record(stream)
     torch.cuda.synchronize()
     assert 1.9 <= e0.elapsed_time(e1) < 50.0
+
+
+# ----- fused epilogue: bias per column, then ReLU --------------------------------------
+
+EPI_CASES = [  # (M, N, K, variant, splits): every kernel and the alpha == 0 path
+    (130, 300, 96, 0, 0), (300, 520, 64, 1, 0), (300, 520, 256, 2, 3),
+    (257, 1030, 2048, -1, 0), (9, 1030, 1000, 3, 0), (16, 1024, 96, 3, 2),
+]
+
+
+@pytest.mark.parametrize("activation", [0, 1])
+@pytest.mark.parametrize("M,N,K,variant,splits", EPI_CASES)
+def test_epilogue_integers_bit_exact(M, N, K, variant, splits, activation):
+    Kp, Np = (K + 3) // 4 * 4, (N + 3) // 4 * 4
+    A, lda, B, ldb, C, ldc = inputs("ints", 31, M, N, K, lda=Kp, ldb=Np, ldc=Np)
+    bias = (np.arange(N) % 41 - 20).astype(np.float32)
+    out, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc, variant=variant, splits=splits,
+                      bias=bias, activation=activation)
+    want = (A.reshape(M, lda)[:, :K].astype(np.int64) @ B.reshape(K, ldb)[:, :N].astype(np.int64)
+            + C.reshape(M, ldc)[:, :N].astype(np.int64) + bias.astype(np.int64)[None, :])
+    if activation == 1:
+        want = np.maximum(want, 0)
+    assert np.array_equal(out.astype(np.int64), want)
+
+
+@pytest.mark.parametrize("M,N,K,variant,splits", EPI_CASES)
+def test_epilogue_floats_within_bound(M, N, K, variant, splits):
+    Kp, Np = (K + 3) // 4 * 4, (N + 3) // 4 * 4
+    A, lda, B, ldb, C, ldc = inputs("normal", 32, M, N, K, lda=Kp, ldb=Np, ldc=Np + 4)
+    bias = datagen.normal01(33, "C", N)
+    out, _ = run_gemm(M, N, K, 0.75, -0.5, A, lda, B, ldb, C, ldc, variant=variant, splits=splits,
+                      bias=bias, activation=1)
+    ref, absprod = oracle.sgemm_ref_flat(M, N, K, 0.75, A, lda, B, ldb, -0.5, C, ldc)
+    want = oracle.apply_epilogue(ref, bias, oracle.ACT_RELU)
+    bound = oracle.error_bound(absprod, C.reshape(M, ldc)[:, :N], 0.75, -0.5, K, bias=bias)
+    assert_within(out, want, bound, f"epilogue {M}x{N}x{K} variant={variant}")
+    assert (out >= 0).all()
+
+
+@pytest.mark.parametrize("K,alpha", [(0, 1.0), (64, 0.0)])
+def test_epilogue_on_the_scale_path(K, alpha):
+    # No product: C = relu(beta * C + bias), and a NaN in C stays NaN.
+    M, N = 33, 70
+    A, lda, B, ldb, C, ldc = inputs("normal", 34, M, N, max(K, 1), ldc=N)
+    C = C.copy()
+    C.reshape(M, ldc)[5, :] = np.nan
+    bias = datagen.normal01(35, "C", N)
+    out, _ = run_gemm(M, N, K, alpha, 2.0, A, lda, B, ldb, C, ldc, bias=bias, activation=1)
+    want = oracle.apply_epilogue(2.0 * C.reshape(M, ldc)[:, :N].astype(np.float64), bias,
+                                 oracle.ACT_RELU)
+    bound = oracle.error_bound(np.zeros((M, N)), C.reshape(M, ldc)[:, :N], 0.0, 2.0, 1, bias=bias)
+    assert np.isnan(out[5]).all() and np.isnan(want[5]).all()
+    keep = np.ones(M, bool)
+    keep[5] = False
+    assert_within(out[keep], want[keep], bound[keep], "scale path epilogue")
+
+
+def test_epilogue_torch_binding():
+    M, N, K = 70, 260, 130
+    A = torch.randn(M, K, device="cuda")
+    B = torch.randn(K, N, device="cuda")
+    C = torch.empty(M, N, device="cuda")
+    bias = torch.randn(N, device="cuda")
+    sg.run(A, B, C, 1.0, 0.0, bias=bias, activation=sg.ACT_RELU)
+    ref, absprod = oracle.sgemm_ref(A.cpu().numpy(), B.cpu().numpy())
+    want = oracle.apply_epilogue(ref, bias.cpu().numpy(), oracle.ACT_RELU)
+    bound = oracle.error_bound(absprod, None, 1.0, 0.0, K, bias=bias.cpu().numpy())
+    assert_within(C.cpu().numpy(), want, bound, "torch binding epilogue")
 
 
 # ----- skinny-M streaming kernel ---------------------------------------------------

@@ -191,3 +191,54 @@ def test_error_bound_k_floor():
     ab = np.ones((1, 1))
     assert oracle.error_bound(ab, None, 1.0, 0.0, 1)[0, 0] == 2 * 3 * 2.0 ** -24
     assert oracle.error_bound(ab, None, 1.0, 0.0, 100)[0, 0] == 2 * 100 * 2.0 ** -24
+
+
+# ----- the fused epilogue: bias per column, then ReLU -------------------------------
+
+def test_epilogue_all_ones_closed_form():
+    # All-ones operands give K everywhere; a bias b_j makes K + b_j, and ReLU
+    # clears exactly the columns whose bias is below -K.
+    M, N, K = 5, 8, 12
+    A = np.ones((M, K), np.float32)
+    B = np.ones((K, N), np.float32)
+    bias = np.array([-20, -13, -12, -11, 0, 1, 7, -100], np.float32)
+    out, _ = ref(A, B)
+    plain = oracle.apply_epilogue(out, bias, oracle.ACT_NONE)
+    relu = oracle.apply_epilogue(out, bias, oracle.ACT_RELU)
+    for j, b in enumerate(bias):
+        assert (plain[:, j] == K + b).all()
+        assert (relu[:, j] == max(K + b, 0.0)).all()
+
+
+def test_epilogue_integer_brute_force():
+    # Python integers give the exact act(A B + C + bias); the bias is indexed
+    # by column and the activation comes after it.
+    M, N, K = 7, 9, 16
+    A = datagen.small_ints(21, "A", M * K).reshape(M, K)
+    B = datagen.small_ints(21, "B", K * N).reshape(K, N)
+    C = datagen.small_ints(21, "C", M * N).reshape(M, N)
+    bias = (np.arange(N, dtype=np.float32) * 7 - 30).astype(np.float32)
+    out, _ = ref(A, B, C, alpha=1.0, beta=1.0)
+    got = oracle.apply_epilogue(out, bias, oracle.ACT_RELU)
+    for i in range(M):
+        for j in range(N):
+            s = sum(int(A[i, k]) * int(B[k, j]) for k in range(K)) + int(C[i, j]) + int(bias[j])
+            assert got[i, j] == (s if s > 0 else 0), (i, j)
+
+
+def test_relu_passes_nan_and_keeps_sign_of_zero():
+    x = np.array([[np.nan, -0.0, 0.0, -1.0, 2.5]])
+    y = oracle.apply_epilogue(x, None, oracle.ACT_RELU)
+    assert np.isnan(y[0, 0])
+    assert y[0, 1] == 0.0 and np.signbit(y[0, 1])
+    assert list(y[0, 2:]) == [0.0, 0.0, 2.5]
+    with pytest.raises(ValueError):
+        oracle.apply_epilogue(x, None, 7)
+
+
+def test_error_bound_with_bias_adds_its_magnitude():
+    ab = np.ones((2, 3))
+    bias = np.array([1.0, -2.0, 0.0])
+    b = oracle.error_bound(ab, None, 1.0, 0.0, 2, bias=bias)
+    u = 2.0 ** -24
+    assert np.array_equal(b, np.broadcast_to(2 * 4 * u * (1.0 + np.abs(bias)), (2, 3)))
