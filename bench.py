@@ -52,6 +52,7 @@ FP32_LANES_PER_SM = 128
 SM_MAX_MHZ = 2070.0
 L2_FLUSH_BYTES = 256 << 20
 HOLD_BATCH = 32
+REFERENCE_SECONDS = 120.0
 
 
 def nominal_fp32_tflops(sms=SMS_GB300, mhz=SM_MAX_MHZ):
@@ -63,6 +64,23 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def max_over_ranks(x, ws, device=None):
+    """The largest value of x over all ranks (the slowest rank's time)."""
+    if ws <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ws, steps, flops_per_step, slowest_total_s):
+    """Whole-job GFLOP/s: every rank ran `steps` steps; the job took as long
+    as its slowest rank's summed step time."""
+    return ws * steps * flops_per_step / slowest_total_s / 1e9
 
 
 def flops_of(cfg):
@@ -373,10 +391,7 @@ def gpu_arm(args, ws, rank, local):
     clocks = clk.summary()
     mean_s = sum(durs) / len(durs)
     # max over ranks of the summed GEMM time
-    total = torch.tensor([sum(durs)], device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(total, op=torch.distributed.ReduceOp.MAX)
-    value = ws * args.steps * flops / float(total.item()) / 1e9
+    value = job_throughput(ws, args.steps, flops, max_over_ranks(sum(durs), ws, dev))
 
     half = len(durs) // 2
     drift = {"first_half": round(half * flops / sum(durs[:half]) / 1e9, 2),
@@ -522,8 +537,11 @@ def reference_arm(args, ws, rank):
     cfg = datagen.CONFIGS[name]
     samples = []
     info = None
+    # The whole run stays within about REFERENCE_SECONDS of CPU work, however
+    # many steps are asked for: each step times a bounded row sample.
+    per_step = max(0.05, min(1.0, REFERENCE_SECONDS / (args.warmup + args.steps)))
     for i in range(args.warmup + args.steps):
-        info = time_oracle(name, budget_s=max(1.0, args.cpu_seconds / max(args.steps, 1)))
+        info = time_oracle(name, budget_s=per_step)
         if i >= args.warmup:
             samples.append(info["value"])
     value = statistics.mean(samples)
