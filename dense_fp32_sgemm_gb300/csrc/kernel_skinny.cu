@@ -12,17 +12,20 @@
 // a ring of shared-memory stages completed on mbarriers, several stages
 // ahead, so enough bytes are in flight to keep HBM busy.
 //
-// With 4 warps a CTA (two CTAs per SM, three stages each) the two CTAs of an
-// SM run out of step, so one computes while the other waits for its next
-// block; with 8 warps (one CTA, six stages) all warps of the SM meet at the
-// same stage.  Each lane owns 8 columns (two groups of four, so a
-// quarter-warp's 128-bit loads cover 32 consecutive banks) and a warp the
-// whole 256-column row; warp w takes rows w, w + W, w + 2W, ... of each
-// block.  A warp rewrites only the A columns it needs k-major into its own
-// corner of shared memory, so no CTA-wide barrier is needed inside a unit:
-// warps run through the stages independently, and the last warp to finish
-// with a stage (a counter in shared memory) refills it.  The update is the
-// packed FP32 fma (__ffma2_rn) on pairs along m: (a_m, a_m+1) * (b_n, b_n).
+// One CTA of 8 warps per SM holds a 6-stage ring (with the 4-warp build, two
+// CTAs of 4 warps share an SM, 3 stages each).  Each lane owns 8 columns (two
+// groups of four, so a quarter-warp's 128-bit loads cover 32 consecutive
+// banks) and a warp the whole 256-column row.  With 16 rows of A the warps
+// form two groups of four that take alternate positions, 8 rows of each
+// block per warp; with 8 rows all 8 warps share every position, 4 rows each.
+// Either way warp w of a group takes rows w, w + W, w + 2W, ... of a block
+// (W warps in the group).  A warp rewrites only the A columns it needs
+// k-major into its own corner of shared memory, so no CTA-wide barrier is
+// needed inside a unit: warps run through the stages independently, and the
+// last warp of the group to finish with a stage (a counter in shared memory)
+// refills it with the position SSTAGES further on, which belongs to the same
+// group.  The update is the packed FP32 fma (__ffma2_rn) on pairs along m:
+// (a_m, a_m+1) * (b_n, b_n).
 //
 // After a unit the warps' sums are added in warp order through shared
 // memory; a unit covering part of a slab writes them to a fixed slot and the
@@ -42,12 +45,23 @@ constexpr int WARPS = kSkinnyWarps;  // 4 or 8
 constexpr int SNT = kSkinnyThreads;
 constexpr int SSTAGES = kSkinnyStages;
 constexpr int CPL = 8;               // columns per lane: a warp covers the row
-constexpr int RPW = SBK / WARPS;     // rows of a block per warp
 constexpr int OWN = SBN / SNT;       // adjacent columns a thread owns after the reduction
-static_assert(32 * CPL == SBN && RPW * WARPS == SBK && (OWN == 1 || OWN == 2), "warp layout");
+static_assert(32 * CPL == SBN && (OWN == 1 || OWN == 2), "warp layout");
+
+// Warp groups: with 8 warps and 16 rows of A, two groups of four warps take
+// alternate positions (8 rows of each block per warp); otherwise all warps
+// share every position.
+template <int MT>
+struct WarpPlan {
+    static constexpr int groups = (WARPS == 8 && MT == 16) ? 2 : 1;
+    static constexpr int gwarps = WARPS / groups;  // warps per group
+    static constexpr int rpw = SBK / gwarps;       // rows of a block per warp
+    static_assert(rpw * gwarps == SBK, "rows per warp");
+};
 
 template <int MT>
 struct SkinnyLayout {
+    static constexpr int RPW = WarpPlan<MT>::rpw;
     static constexpr int a_floats = MT * SBK;  // M x 32, 128-byte rows, swizzled
     static constexpr int b_floats = SBK * SBN;
     static constexpr int stage_floats = a_floats + b_floats;
@@ -130,6 +144,9 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta = blockIdx.x;
     float *at_w = reinterpret_cast<float *>(smem + L::at_off) + warp * L::at_floats;
+    constexpr int GROUPS = WarpPlan<MT>::groups, GW = WarpPlan<MT>::gwarps;
+    constexpr int RPW = WarpPlan<MT>::rpw;
+    const int grp = warp / GW, wl = warp % GW;  // group, and warp within it
 
     const int total = p.slabs * p.kt_total;
     const int u0 = min(cta * p.share, total);
@@ -185,6 +202,7 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
             for (int j = 0; j < CPL; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
         for (int kt = k0; kt < k1; ++kt, ++q) {
+            if (GROUPS > 1 && q % GROUPS != grp) continue;  // the other group's position
             const int s = q % SSTAGES;
             // After a timeout anywhere in the CTA (flags[0], a hint) the
             // remaining waits are skipped; the garbage computed is discarded.
@@ -196,23 +214,23 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
             }
             const float *raw = stages + s * L::stage_floats;
             const float *bs = raw + L::a_floats;
-            // This warp's A columns k = warp + WARPS * kk, k-major: at_w[kk * MT + m].
+            // This warp's A columns k = wl + GW * kk, k-major: at_w[kk * MT + m].
 #pragma unroll
             for (int e = lane; e < RPW * MT; e += 32) {
                 const int m = e % MT, kk = e / MT;
-                at_w[kk * MT + m] = a_elem(raw, m, warp + WARPS * kk);
+                at_w[kk * MT + m] = a_elem(raw, m, wl + GW * kk);
             }
             __syncwarp();
 
             const float *bcol = bs + lane * 4;
             float4 bf[2][CPL / 4];
 #pragma unroll
-            for (int c = 0; c < CPL / 4; ++c) bf[0][c] = ld_shared_f4(bcol + warp * SBN + c * 128);
+            for (int c = 0; c < CPL / 4; ++c) bf[0][c] = ld_shared_f4(bcol + wl * SBN + c * 128);
 #pragma unroll
             for (int kk = 0; kk < RPW; ++kk) {
                 const int cur = kk & 1, nxt = cur ^ 1;
                 if (kk + 1 < RPW) {
-                    const float *brow = bcol + (warp + WARPS * (kk + 1)) * SBN;
+                    const float *brow = bcol + (wl + GW * (kk + 1)) * SBN;
 #pragma unroll
                     for (int c = 0; c < CPL / 4; ++c) bf[nxt][c] = ld_shared_f4(brow + c * 128);
                 }
@@ -240,11 +258,11 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
                 }
             }
             __syncwarp();
-            // Release the stage; the last warp to do so refills it.
+            // Release the stage; the last warp of the group to do so refills it.
             if (lane == 0) {
                 __threadfence_block();
                 const int old = atomicAdd(&release[s], 1);
-                if (old == WARPS - 1) {
+                if (old == GW - 1) {
                     release[s] = 0;
                     if (q + SSTAGES < q_total && !flags[0]) {
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

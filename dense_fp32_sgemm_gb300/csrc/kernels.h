@@ -100,10 +100,12 @@ cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, cons
 constexpr int kSkinnyBN = 256;   // columns per slab
 constexpr int kSkinnyBK = 32;    // B rows per TMA stage
 constexpr int kSkinnyMaxM = 16;  // rows of C the kernel covers (partial slots hold this many)
-// Warps per CTA: 4 (two CTAs per SM, 3 ring stages each) or 8 (one CTA per
-// SM, 6 stages).  A build constant so that both can be timed.
+// Warps per CTA: 8 (one CTA per SM, 6 ring stages) or 4 (two CTAs per SM, 3
+// stages each).  A build constant so that both can be timed; 8 measured
+// faster on GB300 (its warps share one ring, so no CTA of an SM falls behind
+// the other).
 #ifndef SGEMM_SKINNY_WARPS
-#define SGEMM_SKINNY_WARPS 4
+#define SGEMM_SKINNY_WARPS 8
 #endif
 constexpr int kSkinnyWarps = SGEMM_SKINNY_WARPS;
 static_assert(kSkinnyWarps == 4 || kSkinnyWarps == 8, "skinny kernel: 4 or 8 warps");

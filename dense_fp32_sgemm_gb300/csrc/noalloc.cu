@@ -36,7 +36,7 @@ constexpr size_t kSlotFloats = size_t(kSkinnyMaxM) * kSkinnyBN;
 constexpr size_t kPartialBytes = 2 * size_t(kMaxGrid) * kSlotFloats * sizeof(float);
 constexpr size_t kCounterBytes = size_t(kMaxSlabs) * sizeof(int);
 constexpr size_t kErrOffset = kPartialBytes + kCounterBytes;
-constexpr size_t kScratchBytes = kErrOffset + 256;  // 10 MiB + 16 KiB + 256 B (two CTAs per SM)
+constexpr size_t kScratchBytes = kErrOffset + 256;  // 5 MiB + 16 KiB + 256 B with one CTA per SM
 
 // The fixed scratch.  In host code this name is a host-side stand-in, not a
 // device address: the host only ever passes the address cudaGetSymbolAddress

@@ -131,13 +131,13 @@ SGEMM_API sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float a
  * start-up, or code that must not put a synchronising allocation between
  * queued work.  sgemm_run allocates its stream-K workspace on first use; this
  * entry point takes partial sums, tickets and its error word from one fixed
- * 10 MiB + 16 KiB buffer compiled into the library as a __device__ array,
+ * 5 MiB + 16 KiB buffer compiled into the library as a __device__ array,
  * which every GPU that loads the library holds until the process exits.
  *
  * Same arguments, layout and conventions as sgemm_run (device pointers owned
  * by the caller, queued on `stream`, no host synchronisation), with limits:
- * M <= 16; N <= 1,048,576 (4096 slabs of 256 columns); a grid of at most 320
- * CTAs (two per SM: GPUs of up to 160 SMs); A and B 16-byte aligned with lda
+ * M <= 16; N <= 1,048,576 (4096 slabs of 256 columns); a grid of at most 160
+ * CTAs (one per SM: GPUs of up to 160 SMs); A and B 16-byte aligned with lda
  * and ldb multiples of 4.
  * Requests beyond them return SGEMM_ERR_SCRATCH_LIMIT before any work is
  * queued.  The first call on each device looks up the buffer's device address

@@ -150,12 +150,12 @@ def test_skinny_plan(M, N, K):
     slabs, kt, share, grid, m_tile = ints(p, "tiles_n", "kt", "sk_share", "grid", "m_tile")
     assert slabs == math.ceil(N / 256) and kt == math.ceil(K / 32)
     assert m_tile == (8 if M <= 8 else 16)
-    # Two 4-warp CTAs per SM.
-    assert share == math.ceil(slabs * kt / (2 * SMS))
-    assert grid == math.ceil(slabs * kt / share) and grid <= 2 * SMS
+    # One 8-warp CTA per SM.
+    assert share == math.ceil(slabs * kt / SMS)
+    assert grid == math.ceil(slabs * kt / share) and grid <= SMS
 
 
 def test_skinny_16x8192x8192_split():
-    # 32 slabs x 256 k-steps over 2 x 152 CTAs: 27 k-steps each, about 10 pieces a slab.
+    # 32 slabs x 256 k-steps over 152 CTAs: 54 k-steps each, about 5 pieces a slab.
     p = plan(16, 8192, 8192)
-    assert ints(p, "tiles_n", "kt", "sk_share", "grid") == [32, 256, 27, 304]
+    assert ints(p, "tiles_n", "kt", "sk_share", "grid") == [32, 256, 54, 152]
