@@ -39,6 +39,8 @@ struct Workspace {
     size_t partial_bytes = 0;
     int *counters = nullptr;
     size_t counter_count = 0;
+    float *pack = nullptr;  // aligned copies of unaligned operands
+    size_t pack_bytes = 0;
 };
 
 struct HostBuffers {
@@ -118,6 +120,19 @@ sgemm_status_t ensure_workspace(DeviceState &d, cudaStream_t stream, size_t part
     return SGEMM_OK;
 }
 
+sgemm_status_t ensure_pack(DeviceState &d, cudaStream_t stream, size_t bytes, float **out) {
+    Workspace &w = d.ws[stream];
+    if (w.pack_bytes < bytes) {
+        if (w.pack) cudaFree(w.pack);
+        w.pack = nullptr;
+        w.pack_bytes = 0;
+        if (cudaMalloc(&w.pack, bytes) != cudaSuccess) return SGEMM_ERR_ALLOC;
+        w.pack_bytes = bytes;
+    }
+    *out = w.pack;
+    return SGEMM_OK;
+}
+
 // Row-major rows x cols FP32 matrix with leading dimension ld (elements),
 // box of box_rows x box_cols, zero fill outside the matrix.
 sgemm_status_t encode_2d(CUtensorMap *map, const float *base, int64_t rows, int64_t cols,
@@ -186,10 +201,34 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
                 if (tile_configure(fm, st, tm) != cudaSuccess) return SGEMM_ERR_LAUNCH;
                 d.configured_tiles.insert(key);
             }
+            const float *Ause = A, *Buse = B;
+            int64_t lda_use = lda, ldb_use = ldb;
+            if (pl.pack_a || pl.pack_b) {
+                // Copy the unaligned operand(s) to 16-byte-aligned rows first.
+                const size_t a_floats = pl.pack_a ? (size_t)M * pl.lda_packed : 0;
+                const size_t a_span = (a_floats + 63) / 64 * 64;  // keeps B's copy 256-byte aligned
+                const size_t b_floats = pl.pack_b ? (size_t)K * pl.ldb_packed : 0;
+                float *buf = nullptr;
+                sgemm_status_t s = ensure_pack(d, stream, (a_span + b_floats) * sizeof(float), &buf);
+                if (s != SGEMM_OK) return s;
+                PackJob jobs[2];
+                int n = 0;
+                if (pl.pack_a) {
+                    jobs[n++] = PackJob{A, lda, (int)M, (int)K, buf, pl.lda_packed};
+                    Ause = buf;
+                    lda_use = pl.lda_packed;
+                }
+                if (pl.pack_b) {
+                    jobs[n++] = PackJob{B, ldb, (int)K, (int)N, buf + a_span, pl.ldb_packed};
+                    Buse = buf + a_span;
+                    ldb_use = pl.ldb_packed;
+                }
+                if (launch_pack(jobs, n, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+            }
             CUtensorMap mapA, mapB;
-            sgemm_status_t s = encode_2d(&mapA, A, M, K, lda, kTileBK, kTileBM);
+            sgemm_status_t s = encode_2d(&mapA, Ause, M, K, lda_use, kTileBK, kTileBM);
             if (s != SGEMM_OK) return s;
-            s = encode_2d(&mapB, B, K, N, ldb, kTileBN, kTileBK);
+            s = encode_2d(&mapB, Buse, K, N, ldb_use, kTileBN, kTileBK);
             if (s != SGEMM_OK) return s;
             TileParams tp;
             tp.M = (int)M; tp.N = (int)N; tp.K = (int)K;
@@ -227,7 +266,8 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             if (s != SGEMM_OK) return s;
             SkinnyParams sp;
             sp.M = (int)M; sp.N = (int)N; sp.K = (int)K;
-            sp.slabs = pl.slabs; sp.kt_total = pl.kt_total; sp.share = pl.sk_share;
+            sp.slabs = pl.slabs; sp.kt_total = pl.kt_total;
+            for (int c = 0; c <= pl.grid; ++c) sp.starts[c] = pl.sk_starts[c];
             sp.alpha = alpha; sp.beta = beta;
             sp.A = A; sp.lda = lda; sp.C = C; sp.ldc = ldc; sp.c_vec4 = 0;
             sp.epi = epi;
@@ -428,6 +468,7 @@ sgemm_status_t sgemm_release_workspace(void) {
         for (auto &w : d.ws) {
             if (w.second.partials) cudaFree(w.second.partials);
             if (w.second.counters) cudaFree(w.second.counters);
+            if (w.second.pack) cudaFree(w.second.pack);
         }
         d.ws.clear();
         if (d.host.A) cudaFree(d.host.A);

@@ -102,6 +102,22 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// Load with acquire semantics at GPU scope (pairs with a writer's fence and
+// atomic): what the writer stored before its release is visible afterwards.
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Relaxed load at GPU scope: sees other CTAs' atomics without ordering the
+// loads and stores after it (follow with a fence to acquire).
+__device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 // Orders this thread's preceding (acquired) view of global memory before its
 // following async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {

@@ -1,7 +1,8 @@
 // Generic FP32 GEMM for operands the TMA path cannot map (pointers or leading
 // dimensions that break 16-byte alignment, or products too small for the
-// tiled kernel), and the C = beta * C kernel for the alpha == 0 / K == 0
-// quick return.
+// tiled kernel), the C = beta * C kernel for the alpha == 0 / K == 0 quick
+// return, and the copy of unaligned operands to aligned rows that lets larger
+// products take the tiled kernel.
 //
 // 64 x 64 block tile, K slice 16, 256 threads with a 4 x 4 micro-tile each
 // ("Optimizing Matrix Multiply on CUDA, Part 1", section "Stage 3: Register
@@ -104,7 +105,49 @@ __global__ void sgemm_scale_kernel(int M, int N, float beta, float *C, long long
     }
 }
 
+struct PackJobs {
+    PackJob job[2];
+};
+
+// Thread t of job blockIdx.y writes destination columns 4t..4t+3 of a row
+// with one 16-byte store (columns past `cols` get zeros); the source reads
+// are scalar, so any alignment works, and consecutive threads read
+// consecutive addresses.
+__global__ void sgemm_pack_kernel(const PackJobs jobs) {
+    const PackJob &j = jobs.job[blockIdx.y];
+    const long long quads = j.ldp / 4;
+    const long long total = (long long)j.rows * quads;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const long long r = e / quads;
+        const int c = (int)(e - r * quads) * 4;
+        const float *row = j.src + r * j.ld;
+        float4 v;
+        v.x = c + 0 < j.cols ? row[c + 0] : 0.0f;
+        v.y = c + 1 < j.cols ? row[c + 1] : 0.0f;
+        v.z = c + 2 < j.cols ? row[c + 2] : 0.0f;
+        v.w = c + 3 < j.cols ? row[c + 3] : 0.0f;
+        *reinterpret_cast<float4 *>(j.dst + r * j.ldp + c) = v;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_pack(const PackJob *jobs, int njobs, cudaStream_t stream) {
+    if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
+    PackJobs pj;
+    long long most = 0;
+    for (int i = 0; i < njobs; ++i) {
+        pj.job[i] = jobs[i];
+        const long long t = (long long)jobs[i].rows * (jobs[i].ldp / 4);
+        if (t > most) most = t;
+    }
+    long long blocks = (most + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (blocks < 1) blocks = 1;
+    sgemm_pack_kernel<<<dim3((unsigned)blocks, (unsigned)njobs), 256, 0, stream>>>(pj);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_generic(const GenericParams &p, cudaStream_t stream) {
     const dim3 grid((p.N + GBN - 1) / GBN, (p.M + GBM - 1) / GBM);

@@ -5,9 +5,11 @@
 // product re-reads all the weights and is memory-bound; Module 01: small or
 // skinny matrices are not compute-bound).
 //
-// Work: N is cut into slabs of 256 columns; the (slab, k) plane is shared
-// out in equal contiguous ranges of 32-row k-iterations to a persistent grid
-// (stream-K over the slabs).  For each k-iteration a TMA copy brings the
+// Work: N is cut into slabs of 256 columns; the (slab, k) plane of 32-row
+// k-iterations ("positions") is shared out in contiguous ranges to a
+// persistent grid (stream-K over the slabs), balanced in time by the planner:
+// a range that crosses a slab boundary is shorter by the cost of its extra
+// unit end.  For each k-iteration a TMA copy brings the
 // 32 x 256 block of B and the M x 32 block of A (128-byte swizzled rows) into
 // a ring of shared-memory stages completed on mbarriers, several stages
 // ahead, so enough bytes are in flight to keep HBM busy.
@@ -87,8 +89,21 @@ struct SkinnyLayout {
 
 __device__ __forceinline__ int skinny_slot(const SkinnyParams &p, int cta, int slab) {
     const int start = slab * p.kt_total;
-    const int k0 = max(cta * p.share, start) - start;
+    const int k0 = max(p.starts[cta], start) - start;
     return 2 * cta + (k0 == 0 ? 1 : 0);
+}
+
+// The CTA whose range holds position u (ranges are contiguous and ascending).
+__device__ __forceinline__ int skinny_owner(const SkinnyParams &p, int u) {
+    int lo = 0, hi = gridDim.x - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.starts[mid] <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
 }
 
 __device__ __forceinline__ const float *skinny_piece(const SkinnyParams &p, int cta, int slab) {
@@ -130,7 +145,8 @@ struct Vec<2> {
 template <int MT>
 __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
     sgemm_skinny_kernel(const __grid_constant__ CUtensorMap mapA,
-                        const __grid_constant__ CUtensorMap mapB, const SkinnyParams p) {
+                        const __grid_constant__ CUtensorMap mapB,
+                        const __grid_constant__ SkinnyParams p) {
     using L = SkinnyLayout<MT>;
     extern __shared__ __align__(1024) uint8_t smem[];
     float *stages = reinterpret_cast<float *>(smem);
@@ -148,9 +164,8 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
     constexpr int RPW = WarpPlan<MT>::rpw;
     const int grp = warp / GW, wl = warp % GW;  // group, and warp within it
 
-    const int total = p.slabs * p.kt_total;
-    const int u0 = min(cta * p.share, total);
-    const int q_total = min(u0 + p.share, total) - u0;
+    const int u0 = p.starts[cta];
+    const int q_total = p.starts[cta + 1] - u0;
     if (q_total <= 0) return;
 
     // Copy of position q (the CTA's q-th k-iteration) into stage q % SSTAGES.
@@ -321,8 +336,8 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
             for (int m = 0; m < MT; ++m) Vec<OWN>::store_cg(slot + m * SBN + col0, fin[m]);
             __threadfence();
             __syncthreads();
-            const int c_first = (slab * p.kt_total) / p.share;
-            const int c_last = (slab * p.kt_total + p.kt_total - 1) / p.share;
+            const int c_first = skinny_owner(p, slab * p.kt_total);
+            const int c_last = skinny_owner(p, slab * p.kt_total + p.kt_total - 1);
             if (tid == 0) {
                 const int old = atomicAdd(&p.counters[slab], 1);
                 flags[1] = (old == c_last - c_first) ? 1 : 0;

@@ -343,6 +343,80 @@ struct ProducerState {
     int pq, tm, tn, k, k1;  // next position to issue; its tile and k-range
 };
 
+// ---- the code after a unit's last slice ----
+// It runs once per unit, and on GB300 the first run of straight-line code
+// waits for its instructions: a fully unrolled 128 x 256 store measured about
+// 20 us the first time through and 3 us when repeated.  The stream-K fix-up
+// (whose unrolled form took 40 us at its first run) is therefore a few short
+// rolled loops.
+
+// One float4 of C: columns n .. n+3 of row m, from the raw sums a.
+__device__ __forceinline__ void store_c4(const TileParams &p, int m, int n, float4 a) {
+    if (m >= p.M) return;
+    float *crow = p.C + (long long)m * p.ldc;
+    float o[4] = {p.alpha * a.x, p.alpha * a.y, p.alpha * a.z, p.alpha * a.w};
+    if (p.c_vec4 && n + 3 < p.N) {
+        if (p.beta != 0.0f) {
+            const float4 cv = *reinterpret_cast<const float4 *>(crow + n);
+            o[0] = __fmaf_rn(p.beta, cv.x, o[0]);
+            o[1] = __fmaf_rn(p.beta, cv.y, o[1]);
+            o[2] = __fmaf_rn(p.beta, cv.z, o[2]);
+            o[3] = __fmaf_rn(p.beta, cv.w, o[3]);
+        }
+        if (p.epi.bias || p.epi.act) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) o[jj] = apply_epilogue(o[jj], p.epi, n + jj);
+        }
+        *reinterpret_cast<float4 *>(crow + n) = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            if (n + jj < p.N) {
+                float v = o[jj];
+                if (p.beta != 0.0f) v = __fmaf_rn(p.beta, crow[n + jj], v);
+                crow[n + jj] = apply_epilogue(v, p.epi, n + jj);
+            }
+        }
+    }
+}
+
+// Tile coordinates of accumulator element (ti, j) of thread t (TM = 16:
+// warps 2 x 4 of 64 x 64, lanes 4 x 8, rows in four groups of 4 at stride 16,
+// columns in two groups of 4 at stride 32).
+__device__ __forceinline__ int acc_row(int t, int ti) {
+    const int warp = t >> 5, wm = warp / 4, ty = (t & 31) >> 3;
+    return wm * 64 + (ti >> 2) * 16 + ty * 4 + (ti & 3);
+}
+__device__ __forceinline__ int acc_col(int t, int c) {
+    const int warp = t >> 5, wn = warp % 4, tx = t & 7;
+    return wn * 64 + c * 32 + tx * 4;
+}
+
+// Float4 number e4 of a thread's accumulators: row e4 / 2, columns
+// (e4 % 2) * 4 .. + 3.  A switch, so the accumulators stay in registers
+// while the caller's loop over e4 stays rolled.
+template <class AccT>
+__device__ __forceinline__ float4 acc_f4(AccT &acc, int e4) {
+    switch (e4) {
+#define SGEMM_E4(E)                                                                        \
+    case E:                                                                                \
+        return make_float4(acc.at((E) >> 1, ((E)&1) * 4 + 0), acc.at((E) >> 1, ((E)&1) * 4 + 1), \
+                           acc.at((E) >> 1, ((E)&1) * 4 + 2), acc.at((E) >> 1, ((E)&1) * 4 + 3));
+        SGEMM_E4(0) SGEMM_E4(1) SGEMM_E4(2) SGEMM_E4(3) SGEMM_E4(4) SGEMM_E4(5) SGEMM_E4(6)
+        SGEMM_E4(7) SGEMM_E4(8) SGEMM_E4(9) SGEMM_E4(10) SGEMM_E4(11) SGEMM_E4(12)
+        SGEMM_E4(13) SGEMM_E4(14) SGEMM_E4(15) SGEMM_E4(16) SGEMM_E4(17) SGEMM_E4(18)
+        SGEMM_E4(19) SGEMM_E4(20) SGEMM_E4(21) SGEMM_E4(22) SGEMM_E4(23) SGEMM_E4(24)
+        SGEMM_E4(25) SGEMM_E4(26) SGEMM_E4(27) SGEMM_E4(28) SGEMM_E4(29) SGEMM_E4(30)
+        SGEMM_E4(31)
+#undef SGEMM_E4
+    }
+    return make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// C = alpha * acc (+ beta C, epilogue) for a whole tile, unrolled: a rolled
+// version (one float4 per iteration through acc_f4) is compact but changes
+// the register allocation of the whole kernel, and measured 2.6 % slower on
+// the large products whose time is the main loop.
 template <int FM, int TM>
 __device__ __forceinline__ void store_tile(Acc<FM, TM> &acc, const TileParams &p, int tm, int tn,
                                            int wm, int wn, int ty, int tx) {
@@ -415,112 +489,84 @@ __device__ __forceinline__ int partial_slot(const TileParams &p, int cta, int t_
     return 2 * cta + (k0 == 0 ? 1 : 0);
 }
 
-// Sum the pieces of stream-K tile t_sk, CTAs c_first..c_last, in CTA order;
-// this CTA's own piece is taken from registers.
-template <int FM, int TM>
-__device__ __forceinline__ void reduce_pieces(Acc<FM, TM> &acc, const TileParams &p, int cta,
-                                              int t_sk, int c_first, int c_last, int tid) {
+// The stream-K fix-up: the pieces of tile t_sk (CTAs c_first .. c_last,
+// every one of them, this CTA's included, already in its partial slot) are
+// added in CTA order and C is written.  In a slot, float4 number e4 of thread
+// t sits at [(e4 * NT + t) * 4], so thread t sums and stores exactly the
+// elements it would have held in registers.
+
+// From L2, for a unit whose ring still holds copies in flight.
+template <int TM>
+__device__ __forceinline__ void fixup_from_l2(const TileParams &p, int tm, int tn, int t_sk,
+                                              int c_first, int c_last, int tid) {
     constexpr int NT = Cfg<TM>::NT;
-#pragma unroll
+#pragma unroll 1
     for (int e4 = 0; e4 < TILE_FLOATS / NT / 4; ++e4) {
-        const int ti = e4 >> 1, c = e4 & 1;
-        const float4 own = make_float4(acc.at(ti, c * 4 + 0), acc.at(ti, c * 4 + 1),
-                                       acc.at(ti, c * 4 + 2), acc.at(ti, c * 4 + 3));
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int cc = c_first; cc <= c_last; ++cc) {
-            float4 v;
-            if (cc == cta) {
-                v = own;
-            } else {
-                const float *slot =
-                    p.partials + (size_t)partial_slot(p, cc, t_sk) * TILE_FLOATS;
-                v = __ldcg(reinterpret_cast<const float4 *>(slot) + e4 * NT + tid);
-            }
-            if (cc == c_first) {
-                s = v;
-            } else {
-                s.x += v.x;
-                s.y += v.y;
-                s.z += v.z;
-                s.w += v.w;
-            }
+        const int f = e4 * NT + tid;
+        float4 s = __ldcg(reinterpret_cast<const float4 *>(
+                              p.partials + (size_t)partial_slot(p, c_first, t_sk) * TILE_FLOATS) + f);
+#pragma unroll 1
+        for (int c = c_first + 1; c <= c_last; ++c) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(
+                                        p.partials + (size_t)partial_slot(p, c, t_sk) * TILE_FLOATS) + f);
+            s.x += x.x;
+            s.y += x.y;
+            s.z += x.z;
+            s.w += x.w;
         }
-        acc.at(ti, c * 4 + 0) = s.x;
-        acc.at(ti, c * 4 + 1) = s.y;
-        acc.at(ti, c * 4 + 2) = s.z;
-        acc.at(ti, c * 4 + 3) = s.w;
+        store_c4(p, tm * BM + acc_row(tid, e4 >> 1), tn * BN + acc_col(tid, e4 & 1), s);
     }
 }
 
-// The same sum for a CTA's final unit, when its TMA ring is idle: the other
-// pieces' partial tiles are pulled into the ring with bulk asynchronous
-// copies (one L2 round trip per round, no registers), then added from
-// shared memory in CTA order.  ROUNDS splits the tile so that all other
-// pieces of a round fit the ring: 1 other piece -> 1 round, 2 -> 2, 3 or 4
-// -> 4.  Returns false if a copy did not arrive in time (the error word is
-// set; the caller still waits for the copies before exiting).
-template <int FM, int TM, int ROUNDS>
-__device__ __forceinline__ bool reduce_pieces_staged(Acc<FM, TM> &acc, const TileParams &p,
-                                                     int cta, int t_sk, int c_first, int c_last,
-                                                     int tid, float *ring, uint64_t *bar,
-                                                     uint32_t &phase) {
+// Through the idle ring of a CTA's final unit: band by band (four float4 per
+// thread, 16 KB per piece) the pieces come in with bulk copies, one L2 round
+// trip per band.  Takes up to ring capacity / 16 KB pieces.  Returns false
+// (uniformly) if a copy did not arrive in time; the caller then waits for the
+// copies before the CTA exits.
+template <int TM, int STAGES>
+__device__ __forceinline__ bool fixup_staged(const TileParams &p, int tm, int tn, int t_sk,
+                                             int c_first, int c_last, int tid, float *ring,
+                                             uint64_t *bar, uint32_t &phase) {
     constexpr int NT = Cfg<TM>::NT;
-    constexpr int E4 = TILE_FLOATS / NT / 4;
-    constexpr int E = E4 / ROUNDS;                    // float4 per thread per round
-    constexpr uint32_t CHUNK = uint32_t(E) * NT * 16;  // bytes per piece per round
-    const int others = c_last - c_first;
-    bool ok = true;
-#pragma unroll
-    for (int r = 0; r < ROUNDS; ++r) {
+    constexpr int BAND = 4 * NT * 4;  // floats of one band of one piece
+    const int n = c_last - c_first + 1;
+#pragma unroll 1
+    for (int band = 0; band < TILE_FLOATS / BAND; ++band) {
+        __syncthreads();  // the ring's previous contents are read
         if (tid == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             fence_proxy_async_global();
-            mbar_arrive_expect_tx(bar, CHUNK * others);
-            int j = 0;
-            for (int cc = c_first; cc <= c_last; ++cc) {
-                if (cc == cta) continue;
-                const char *slot = reinterpret_cast<const char *>(
-                    p.partials + (size_t)partial_slot(p, cc, t_sk) * TILE_FLOATS);
-                bulk_load(reinterpret_cast<char *>(ring) + j * CHUNK, slot + r * CHUNK, CHUNK, bar);
-                ++j;
-            }
+            mbar_arrive_expect_tx(bar, uint32_t(n) * BAND * 4);
+            for (int j = 0; j < n; ++j)
+                bulk_load(ring + j * BAND,
+                          p.partials + (size_t)partial_slot(p, c_first + j, t_sk) * TILE_FLOATS +
+                              band * BAND,
+                          BAND * 4, bar);
         }
-        if (!mbar_wait_bounded(bar, phase, p.timeout_ns)) {
-            atomicOr(p.err, kErrWaitTimeout);
-            ok = false;
-        }
+        const bool got = mbar_wait_bounded(bar, phase, p.timeout_ns);
         phase ^= 1u;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int e4 = r * E + e, ti = e4 >> 1, cg = e4 & 1;
-            const float4 own = make_float4(acc.at(ti, cg * 4 + 0), acc.at(ti, cg * 4 + 1),
-                                           acc.at(ti, cg * 4 + 2), acc.at(ti, cg * 4 + 3));
-            float4 sum = own;
-            int j = 0;
-            for (int cc = c_first; cc <= c_last; ++cc) {
-                float4 x;
-                if (cc == cta) {
-                    x = own;
-                } else {
-                    x = ld_shared_f4(ring + (size_t)j * (CHUNK / 4) + (e * NT + tid) * 4);
-                    ++j;
-                }
-                if (cc == c_first) {
-                    sum = x;
-                } else {
-                    sum.x += x.x;
-                    sum.y += x.y;
-                    sum.z += x.z;
-                    sum.w += x.w;
-                }
-            }
-            acc.at(ti, cg * 4 + 0) = sum.x;
-            acc.at(ti, cg * 4 + 1) = sum.y;
-            acc.at(ti, cg * 4 + 2) = sum.z;
-            acc.at(ti, cg * 4 + 3) = sum.w;
+        if (__syncthreads_or(!got)) {
+            if (tid == 0) atomicOr(p.err, kErrWaitTimeout);
+            return false;
         }
-        __syncthreads();  // the ring is read before the next round overwrites it
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+            const int f = k * NT + tid;
+            float4 s = ld_shared_f4(ring + f * 4);
+#pragma unroll 1
+            for (int j = 1; j < n; ++j) {
+                const float4 x = ld_shared_f4(ring + j * BAND + f * 4);
+                s.x += x.x;
+                s.y += x.y;
+                s.z += x.z;
+                s.w += x.w;
+            }
+            const int e4 = band * 4 + k;
+            store_c4(p, tm * BM + acc_row(tid, e4 >> 1), tn * BN + acc_col(tid, e4 & 1), s);
+        }
     }
-    return ok;
+    __syncthreads();
+    return true;
 }
 
 template <int FM, int STAGES, int TM>
@@ -645,11 +691,7 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
             }
             if (predict && kt == k1 - 1 && tid == 0) {
                 // Last slice: stage s is in use; the other two are idle.
-                int arrived;
-                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];"
-                             : "=r"(arrived)
-                             : "l"(p.counters + t_sk)
-                             : "memory");
+                const int arrived = ld_acquire_gpu(p.counters + t_sk);
                 flags[2] = arrived == 1;
                 if (arrived == 1) {
                     fence_proxy_async_global();
@@ -690,23 +732,23 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
             bool ok = mbar_wait_bounded(&pre_bar[0], 0, p.timeout_ns);
             ok = mbar_wait_bounded(&pre_bar[1], 0, p.timeout_ns) && ok;
             if (!ok) atomicOr(p.err, kErrWaitTimeout);
-            const float *part[3] = {stages + ((s_last + 1) % STAGES) * STAGE_FLOATS,
-                                    stages + ((s_last + 2) % STAGES) * STAGE_FLOATS,
-                                    stages + s_last * STAGE_FLOATS};
+            // The partner's partial tile now fills the ring in the order
+            // stages s_last + 1, s_last + 2, s_last; this CTA's piece is the
+            // first in CTA order.
             constexpr int NT = Cfg<TM>::NT;
             constexpr int PER_STAGE = STAGE_FLOATS / 4 / NT;  // float4 rows per stage
-#pragma unroll
+#pragma unroll 1
             for (int e4 = 0; e4 < TILE_FLOATS / NT / 4; ++e4) {
-                const int ti = e4 >> 1, cg = e4 & 1;
-                const float4 x =
-                    ld_shared_f4(part[e4 / PER_STAGE] + ((e4 % PER_STAGE) * NT + tid) * 4);
-                acc.at(ti, cg * 4 + 0) += x.x;
-                acc.at(ti, cg * 4 + 1) += x.y;
-                acc.at(ti, cg * 4 + 2) += x.z;
-                acc.at(ti, cg * 4 + 3) += x.w;
+                const float *part = stages + ((s_last + 1 + e4 / PER_STAGE) % STAGES) * STAGE_FLOATS;
+                const float4 x = ld_shared_f4(part + ((e4 % PER_STAGE) * NT + tid) * 4);
+                float4 v = acc_f4(acc, e4);
+                v.x += x.x;
+                v.y += x.y;
+                v.z += x.z;
+                v.w += x.w;
+                store_c4(p, tm * BM + acc_row(tid, e4 >> 1), tn * BN + acc_col(tid, e4 & 1), v);
             }
             if (tid == 0) p.counters[t_sk] = 0;
-            store_tile<FM, TM>(acc, p, tm, tn, wm, wn, ty, tx);
         } else if (whole) {
             store_tile<FM, TM>(acc, p, tm, tn, wm, wn, ty, tx);
         } else {
@@ -723,28 +765,19 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
             __syncthreads();
             if (flags[1]) {
                 __threadfence();
-                const int others = c_last - c_first;
-                // The final unit's ring is idle (every copy issued has been
-                // consumed): stage the other pieces there.
-                bool staged_ok = true;
-                if (q == q_total && others <= 4) {
-                    if (others == 1)
-                        staged_ok = reduce_pieces_staged<FM, TM, 1>(acc, p, cta, t_sk, c_first, c_last,
-                                                                    tid, stages, red_bar, red_phase);
-                    else if (others == 2)
-                        staged_ok = reduce_pieces_staged<FM, TM, 2>(acc, p, cta, t_sk, c_first, c_last,
-                                                                    tid, stages, red_bar, red_phase);
-                    else
-                        staged_ok = reduce_pieces_staged<FM, TM, 4>(acc, p, cta, t_sk, c_first, c_last,
-                                                                    tid, stages, red_bar, red_phase);
-                    if (!staged_ok && tid == 0 &&
-                        !mbar_wait_bounded(red_bar, red_phase ^ 1u, 1000000000ull))
+                // Every piece, this CTA's included, is in its slot.  The
+                // final unit's ring is idle (every copy issued has been
+                // consumed): stage the pieces there.
+                constexpr int kRingPieces = STAGES * STAGE_FLOATS / (4 * Cfg<TM>::NT * 4);
+                if (q == q_total && c_last - c_first + 1 <= kRingPieces) {
+                    if (!fixup_staged<TM, STAGES>(p, tm, tn, t_sk, c_first, c_last, tid, stages,
+                                                  red_bar, red_phase) &&
+                        tid == 0 && !mbar_wait_bounded(red_bar, red_phase ^ 1u, 1000000000ull))
                         atomicOr(p.err, kErrDrainTimeout);
                 } else {
-                    reduce_pieces<FM, TM>(acc, p, cta, t_sk, c_first, c_last, tid);
+                    fixup_from_l2<TM>(p, tm, tn, t_sk, c_first, c_last, tid);
                 }
                 if (tid == 0) p.counters[t_sk] = 0;
-                store_tile<FM, TM>(acc, p, tm, tn, wm, wn, ty, tx);
             }
         }
     }

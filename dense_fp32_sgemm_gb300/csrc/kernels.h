@@ -87,6 +87,19 @@ struct GenericParams {
 
 cudaError_t launch_generic(const GenericParams &p, cudaStream_t stream);
 
+// Copies of operands the TMA cannot map: rows x cols at src (leading
+// dimension ld, any 4-byte alignment) to dst with 16-byte-aligned rows of
+// ldp floats (ldp a multiple of 4, dst 16-byte aligned).  Up to two copies in
+// one launch.
+struct PackJob {
+    const float *src;
+    long long ld;
+    int rows, cols;
+    float *dst;
+    long long ldp;
+};
+cudaError_t launch_pack(const PackJob *jobs, int njobs, cudaStream_t stream);
+
 // C = act(beta * C + bias) (beta == 0 does not read C).
 cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, const Epilogue &epi,
                          cudaStream_t stream);
@@ -113,11 +126,21 @@ constexpr int kSkinnyThreads = 32 * kSkinnyWarps;
 constexpr int kSkinnyCtasPerSm = kSkinnyWarps == 4 ? 2 : 1;
 constexpr int kSkinnyStages = kSkinnyWarps == 4 ? 3 : 6;
 
+constexpr int kSkinnyMaxGrid = 160;  // CTAs a skinny launch may use
+// A unit end in the middle of a CTA's range (a reduction over the warps, a
+// partial written and a ticket taken while the ring keeps streaming) costs
+// about this many positions of streaming time on GB300; the planner shortens
+// such ranges by it.
+constexpr int kSkinnyUnitEndCost = 5;
+
 struct SkinnyParams {
     int M, N, K;
     int slabs;            // ceil(N / BN)
     int kt_total;         // ceil(K / BK)
-    int share;            // k-iterations per CTA over the (slab, k) space
+    // CTA c takes positions [starts[c], starts[c + 1]) of the (slab, k) plane
+    // (position u is slab u / kt_total, k-step u % kt_total); starts[grid] is
+    // slabs * kt_total.
+    int starts[kSkinnyMaxGrid + 1];
     float alpha, beta;
     const float *A;
     long long lda;

@@ -27,7 +27,7 @@
 namespace sgemm {
 namespace {
 
-constexpr int kMaxGrid = 160 * kSkinnyCtasPerSm;
+constexpr int kMaxGrid = kSkinnyMaxGrid;
 constexpr int kMaxSlabs = 4096;
 constexpr int kMaxDevices = 64;
 // The skinny kernel gives each CTA two partial slots of kSkinnyMaxM x 256
@@ -180,7 +180,8 @@ extern "C" sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t
 
     SkinnyParams sp;
     sp.M = (int)M; sp.N = (int)N; sp.K = (int)K;
-    sp.slabs = pl.slabs; sp.kt_total = pl.kt_total; sp.share = pl.sk_share;
+    sp.slabs = pl.slabs; sp.kt_total = pl.kt_total;
+            for (int c = 0; c <= pl.grid; ++c) sp.starts[c] = pl.sk_starts[c];
     sp.alpha = alpha; sp.beta = beta;
     sp.A = A; sp.lda = lda; sp.C = C; sp.ldc = ldc; sp.c_vec4 = 0;
     sp.epi = Epilogue{nullptr, kActNone};

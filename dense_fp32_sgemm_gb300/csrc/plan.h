@@ -34,8 +34,13 @@ struct Plan {
     int group_m;
     int grid;
     int c_vec4;
-    // skinny
+    // skinny: CTA c takes positions [sk_starts[c], sk_starts[c + 1])
     int m_tile, slabs;
+    int sk_starts[161];
+    int sk_two_units;  // CTAs whose range crosses a slab boundary
+    // operands copied to 16-byte-aligned rows first (leading dimensions after the copy)
+    bool pack_a, pack_b;
+    int64_t lda_packed, ldb_packed;
     double cost;  // estimated busiest-SM work, in k-iterations of one tile
     const char *reason;
 };

@@ -148,6 +148,33 @@ def test_misaligned_pointers(offsets):
     check(200, 300, 100, 1.0, 1.0, seed=6, offsets=offsets, lda=104, ldb=300, ldc=300)
 
 
+@pytest.mark.parametrize("offsets,lds,variant", [
+    ((1, 0, 0), (512, 1300, 1300), -1), ((0, 3, 0), (512, 1300, 1303), -1),
+    ((1, 2, 3), (513, 1301, 1302), -1), ((0, 0, 0), (513, 1300, 1300), 1),
+    ((2, 1, 0), (515, 1305, 1300), 2)])
+def test_unaligned_operands_copied_for_the_tiled_kernel(offsets, lds, variant):
+    # Large enough for the tiled kernel: the unaligned operand(s) are first
+    # copied to aligned rows; guard bands and leading-dimension gaps of the
+    # caller's buffers stay untouched.
+    M, N, K = 1400, 1300, 512
+    p = sg.plan_describe(M, N, K, lda=lds[0], ldb=lds[1], ldc=lds[2], a_addr=256 + 4 * offsets[0],
+                         b_addr=512 + 4 * offsets[1], c_addr=768 + 4 * offsets[2])
+    if variant < 0:
+        assert p["variant"] in ("tile", "streamk") and (p["pack_a"], p["pack_b"]) != ("0", "0")
+    check(M, N, K, 0.5, 2.0, dist="normal", seed=40 + sum(offsets), offsets=offsets,
+          lda=lds[0], ldb=lds[1], ldc=lds[2], variant=variant)
+
+
+def test_odd_workload_copies_both_operands_bit_exact():
+    # 1023 x 1025 x 513 with small integers: the copies change no value.
+    M, N, K = 1023, 1025, 513
+    A, lda, B, ldb, C, ldc = inputs("ints", 41, M, N, K)
+    out, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc)
+    want = (A.reshape(M, K).astype(np.int64) @ B.reshape(K, N).astype(np.int64)
+            + C.reshape(M, N).astype(np.int64))
+    assert np.array_equal(out.astype(np.int64), want)
+
+
 @pytest.mark.parametrize("splits", [2, 3, 4, 5])
 def test_stream_k_forced_splits(splits):
     check(640, 1024, 1000, 1.0, 0.5, seed=8, variant=2, splits=splits)
@@ -245,10 +272,11 @@ def test_wait_timeout_reports_and_recovers():
     dB = torch.from_numpy(B).cuda()
     dC = torch.zeros(M * N, device="cuda")
     stream = torch.cuda.current_stream()
-    # The producer stops issuing copies at k-iteration 5, so the consumers'
-    # wait for iteration 5 runs out after 2 ms; the kernel records the timeout
-    # and returns.
+    # The producer of the tiled kernel stops issuing copies at k-iteration 5,
+    # so the consumers' wait for iteration 5 runs out after 2 ms; the kernel
+    # records the timeout and returns.
     sg.set_wait_timeout_ns(2_000_000, 5)
+    sg.set_plan_override(sg.VARIANT_TILE, 0)
     try:
         st = sg.sgemm_run(M, N, K, 1.0, dA.data_ptr(), lda, dB.data_ptr(), ldb, 0.0,
                           dC.data_ptr(), N, stream.cuda_stream)
@@ -256,6 +284,7 @@ def test_wait_timeout_reports_and_recovers():
         assert sg.device_status(stream) == 5  # SGEMM_ERR_DEVICE_TIMEOUT
     finally:
         sg.set_wait_timeout_ns(0, -1)
+        sg.set_plan_override(-1, 0)
     assert sg.device_status(stream) == 0
     # The context and the library still work.
     out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
@@ -358,7 +387,8 @@ def ceil4(x):
 
 
 @pytest.mark.parametrize("M", [1, 5, 8, 9, 16])
-@pytest.mark.parametrize("N,K", [(256, 32), (300, 70), (1030, 1000), (4096, 513)])
+@pytest.mark.parametrize("N,K", [(256, 32), (300, 70), (1030, 1000), (4096, 513),
+                                 (10240, 320), (40000, 64)])
 def test_skinny_shapes(M, N, K):
     check(M, N, K, 0.5, 2.0, dist="normal", seed=M + N + K, lda=ceil4(K), ldb=ceil4(N),
           ldc=N + 1, label=f"skinny {M}x{N}x{K}")

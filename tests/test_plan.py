@@ -43,12 +43,30 @@ def test_quick_returns():
     assert plan(5, 6, 0)["variant"] == "scale"
 
 
-def test_misaligned_operands_take_generic_kernel():
-    # 1023 x 1025 x 513: lda = 513 and ldb = 1025 break 16-byte row alignment.
+def test_misaligned_operands():
+    # 1023^3: lda = ldb = 1023 break 16-byte row alignment.  The product is
+    # large enough for the tiled kernel to repay copying both operands to
+    # aligned rows first.
+    p = plan(1023, 1023, 1023, aligned_ld=False)
+    assert p["variant"] == "streamk" and ints(p, "pack_a", "pack_b") == [1, 1]
+    # 1023 x 1025 x 513 (4.5 slices per SM) does not repay the copies
     p = plan(1023, 1025, 513, aligned_ld=False)
-    assert p["variant"] == "generic"
-    p = plan(256, 256, 256, a_addr=(1 << 20) + 4)
-    assert p["variant"] == "generic"
+    assert p["variant"] == "generic" and ints(p, "pack_a", "pack_b") == [0, 0]
+    # only the unaligned operand is copied
+    p = plan(2048, 2048, 2048, a_addr=(1 << 20) + 4)
+    assert p["variant"] in ("tile", "streamk") and ints(p, "pack_a", "pack_b") == [1, 0]
+    # a small product, or M <= 16 (copying B would double the bytes moved),
+    # takes the bounds-checked 64 x 64 kernel instead
+    assert plan(256, 256, 256, a_addr=(1 << 20) + 4)["variant"] == "generic"
+    p = plan(16, 8192, 8191, aligned_ld=False)
+    assert p["variant"] == "generic" and ints(p, "pack_a", "pack_b") == [0, 0]
+    # forcing the tiled kernel on unaligned operands copies them
+    sg.set_plan_override(sg.VARIANT_TILE, 0)
+    try:
+        p = plan(300, 400, 500, b_addr=(2 << 20) + 8)
+        assert p["variant"] == "tile" and ints(p, "pack_a", "pack_b") == [0, 1]
+    finally:
+        sg.set_plan_override(-1, 0)
 
 
 def test_2048_cube_uses_stream_k_over_all_sms():
@@ -81,8 +99,8 @@ def test_exact_waves_stay_data_parallel():
     assert ints(p, "dp_tiles", "grid") == [304, SMS]
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128 * 39), (1000, 3000, 77), (8192, 6144, 2048),
-                                   (17, 8192, 8192), (4000, 300, 20000), (129, 257, 33 * 40),
+@pytest.mark.parametrize("M,N,K", [(128, 128, 32 * 700), (1000, 3000, 231), (8192, 6144, 2048),
+                                   (17, 8192, 8192), (4000, 300, 20000), (129, 257, 32 * 160),
                                    (40, 1, 100000), (5000, 5000, 1)])
 def test_plan_invariants(M, N, K):
     p = plan(M, N, K)
@@ -104,15 +122,20 @@ def test_plan_invariants(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (129, 257, 33), (1024, 1024, 64),
-                                   (2048, 2048, 16), (300, 520, 64)])
+                                   (2048, 2048, 16), (300, 520, 64), (768, 768, 768)])
 def test_small_products_take_the_64x64_kernel(M, N, K):
-    # No more 128 x 256 x 32 slices than SMs: the tiled kernel would idle
-    # most SMs, so the 64 x 64 kernel takes the product.
-    assert math.ceil(M / 128) * math.ceil(N / 256) * math.ceil(K / 32) <= SMS
+    # At most 4 tile slices (128 x 256 x 32) per SM: the tiled kernel would
+    # idle most SMs or split its few tiles too finely.
+    assert math.ceil(M / 128) * math.ceil(N / 256) * math.ceil(K / 32) <= 4 * SMS
     p = plan(M, N, K)
     assert p["variant"] == "generic" and p["reason"] == "small product"
-    # One more slice than SMs goes back to the tiled kernel.
-    assert plan(128 * 17, 256 * 9, 32)["variant"] in ("tile", "streamk")
+
+
+def test_the_tiled_kernel_takes_over_above_four_slices_per_sm():
+    assert 19 * 8 * 4 == 4 * SMS
+    assert plan(128 * 19, 256 * 8, 32 * 4)["variant"] == "generic"
+    assert plan(128 * 19, 256 * 8, 32 * 4 + 1)["variant"] in ("tile", "streamk")
+    assert plan(1024, 1024, 1024)["variant"] in ("tile", "streamk")
 
 
 def test_forced_split_count():
@@ -140,22 +163,34 @@ def test_forced_generic():
         sg.set_plan_override(-1, 0)
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 8192, 8192), (1, 4096, 4096), (9, 300, 70),
-                                   (8, 100000, 64)])
+UNIT_END = 5  # positions a range pays for each slab boundary it crosses
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 8192, 8192), (1, 4096, 4096), (9, 300, 72),
+                                   (8, 100000, 64), (16, 10240, 320)])
 def test_skinny_plan(M, N, K):
-    # M <= 16: the streaming kernel over 256-column slabs and 32-row k-steps,
-    # its (slab, k) plane shared evenly over the grid.
+    # M <= 16: the streaming kernel over 256-column slabs and 32-row positions,
+    # the (slab, k) plane cut into contiguous ranges, one per CTA of a
+    # one-CTA-per-SM grid, balanced in time: the budget is the smallest that
+    # fits the grid, at most one unit end above the even share.
     p = plan(M, N, K)
     assert p["variant"] == "skinny"
-    slabs, kt, share, grid, m_tile = ints(p, "tiles_n", "kt", "sk_share", "grid", "m_tile")
+    slabs, kt, budget, grid, m_tile, two = ints(p, "tiles_n", "kt", "sk_share", "grid", "m_tile",
+                                                "two_unit_ctas")
+    total = slabs * kt
     assert slabs == math.ceil(N / 256) and kt == math.ceil(K / 32)
     assert m_tile == (8 if M <= 8 else 16)
-    # One 8-warp CTA per SM.
-    assert share == math.ceil(slabs * kt / SMS)
-    assert grid == math.ceil(slabs * kt / share) and grid <= SMS
+    assert 1 <= grid <= SMS
+    assert budget >= math.ceil(total / SMS)
+    if kt >= 32:
+        # long slabs: a range crosses at most one boundary, so the budget is
+        # at most one unit end above the even share
+        assert budget <= math.ceil(total / SMS) + UNIT_END + 1
+        assert 0 <= two <= min(grid, slabs - 1)
 
 
 def test_skinny_16x8192x8192_split():
-    # 32 slabs x 256 k-steps over 152 CTAs: 54 k-steps each, about 5 pieces a slab.
+    # 32 slabs x 256 positions over 152 CTAs: budget 55; the 31 ranges that
+    # cross a slab boundary hold 50 positions and pay for one more unit end.
     p = plan(16, 8192, 8192)
-    assert ints(p, "tiles_n", "kt", "sk_share", "grid") == [32, 256, 54, 152]
+    assert ints(p, "tiles_n", "kt", "sk_share", "grid", "two_unit_ctas") == [32, 256, 55, 152, 31]
