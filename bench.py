@@ -45,6 +45,7 @@ WORKLOADS = {
     "s5_odd": "sgemm 1023x1025x513 fp32 row-major alpha=1 beta=0 A,B N(0,1)",
     "s6_skinny": "sgemm 16x8192x8192 fp32 row-major alpha=1 beta=0 A,B U[-1,1)",
     "s1_128": "sgemm 128x128x128 fp32 row-major alpha=1 beta=0 A,B U[-1,1)",
+    "s7_gemv": "sgemm 1x8192x8192 fp32 row-major alpha=1 beta=0 A,B U[-1,1) (GEMV)",
 }
 METRIC = "SGEMM GFLOP/s at 4092^3 and 2048^3 FP32; % of GB300 FP32 FFMA peak"
 SMS_GB300 = 152
@@ -459,7 +460,7 @@ def gpu_arm(args, ws, rank, local):
     # ---- the other workloads, timed the same way (fewer steps) ----
     if not args.no_secondary:
         others = []
-        for other in ("s3_4092", "s4_rect", "s5_odd", "s6_skinny", "s1_128"):
+        for other in ("s3_4092", "s4_rect", "s5_odd", "s6_skinny", "s7_gemv", "s1_128"):
             if other == name:
                 continue
             cfgo, _, _, _, dAo, dBo, dCo = device_inputs(other)
@@ -472,7 +473,7 @@ def gpu_arm(args, ws, rank, local):
                    "value": round(flops_of(cfgo) / mo / 1e9, 2), "unit": "GFLOP/s",
                    "ms_per_step": round(mo * 1e3, 4)}
             ao = flops_of(cfgo) / mo / 1e12
-            if other == "s6_skinny":
+            if other in ("s6_skinny", "s7_gemv"):
                 nbytes = algorithmic_bytes(cfgo)
                 ent["roofline"] = {"bound": "hbm", "achieved": round(nbytes / mo / 1e9, 1),
                                    "peak": hbm_peak, "unit": "GB/s",

@@ -182,6 +182,8 @@ CONFIGS = {
     "s4_rect": dict(M=8192, N=6144, K=2048, alpha=1.0, beta=0.0, dist="normal"),
     "s5_odd": dict(M=1023, N=1025, K=513, alpha=1.0, beta=0.0, dist="normal"),
     "s6_skinny": dict(M=16, N=8192, K=8192, alpha=1.0, beta=0.0, dist="uniform"),
+    # one row of A: the decode-step GEMV (matrix-vector) case of the skinny regime
+    "s7_gemv": dict(M=1, N=8192, K=8192, alpha=1.0, beta=0.0, dist="uniform"),
 }
 CONFIG_SEEDS = {name: 1000 + i for i, name in enumerate(CONFIGS)}
 

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -48,7 +49,17 @@ struct HostBuffers {
     size_t a_bytes = 0, b_bytes = 0, c_bytes = 0;
 };
 
+// Streams and events of the host entry point's copy / compute pipeline.
+constexpr int kHostMaxBlocks = 8;
+struct HostPipeline {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr;
+    cudaEvent_t in[kHostMaxBlocks] = {}, done[kHostMaxBlocks] = {};
+};
+
 struct DeviceState {
+    HostPipeline pipe;
     bool ready = false;
     bool supported = false;
     int num_sms = 0;
@@ -352,6 +363,60 @@ sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha, cons
     if (!grow(&hb.A, &hb.a_bytes, a_bytes ? a_bytes : 16) ||
         !grow(&hb.B, &hb.b_bytes, b_bytes ? b_bytes : 16) || !grow(&hb.C, &hb.c_bytes, c_bytes))
         return SGEMM_ERR_ALLOC;
+    // Row blocks: copies of block i + 1 in and of block i - 1 out overlap the
+    // product of block i (copy engines and SMs work at once).  B goes in
+    // first, whole; small products are one block.
+    int blocks = 1;
+    if (need_ab && M >= 1024) blocks = (int)std::min<int64_t>(4, M / 256);
+    const int64_t rows = ((M + blocks - 1) / blocks + 127) / 128 * 128;
+    blocks = (int)((M + rows - 1) / rows);
+    if (blocks > 1) {
+        HostPipeline &hp = d->pipe;
+        if (!hp.ready) {
+            bool ok = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+                      cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+                      cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
+                      cudaEventCreateWithFlags(&hp.end, cudaEventDisableTiming) == cudaSuccess;
+            for (int i = 0; ok && i < kHostMaxBlocks; ++i)
+                ok = cudaEventCreateWithFlags(&hp.in[i], cudaEventDisableTiming) == cudaSuccess &&
+                     cudaEventCreateWithFlags(&hp.done[i], cudaEventDisableTiming) == cudaSuccess;
+            if (!ok) return SGEMM_ERR_LAUNCH;
+            hp.ready = true;
+        }
+        // Everything already queued on `stream` comes first.
+        if (cudaEventRecord(hp.start, st) != cudaSuccess ||
+            cudaStreamWaitEvent(hp.h2d, hp.start, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(hp.d2h, hp.start, 0) != cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
+        if (cudaMemcpy2DAsync(hb.B, dldb * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice,
+                              hp.h2d) != cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
+        for (int i = 0; i < blocks; ++i) {
+            const int64_t r0 = i * rows, mi = std::min<int64_t>(rows, M - r0);
+            if (cudaMemcpy2DAsync(hb.A + r0 * dlda, dlda * 4, A + r0 * lda, lda * 4, K * 4, mi,
+                                  cudaMemcpyHostToDevice, hp.h2d) != cudaSuccess)
+                return SGEMM_ERR_LAUNCH;
+            if (beta != 0.0f &&
+                cudaMemcpy2DAsync(hb.C + r0 * dldc, dldc * 4, C + r0 * ldc, ldc * 4, N * 4, mi,
+                                  cudaMemcpyHostToDevice, hp.h2d) != cudaSuccess)
+                return SGEMM_ERR_LAUNCH;
+            if (cudaEventRecord(hp.in[i], hp.h2d) != cudaSuccess ||
+                cudaStreamWaitEvent(st, hp.in[i], 0) != cudaSuccess)
+                return SGEMM_ERR_LAUNCH;
+            s = run_locked(mi, N, K, alpha, hb.A + r0 * dlda, dlda, hb.B, dldb, beta,
+                           hb.C + r0 * dldc, dldc, Epilogue{nullptr, kActNone}, st, *d);
+            if (s != SGEMM_OK) return s;
+            if (cudaEventRecord(hp.done[i], st) != cudaSuccess ||
+                cudaStreamWaitEvent(hp.d2h, hp.done[i], 0) != cudaSuccess ||
+                cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, hb.C + r0 * dldc, dldc * 4, N * 4, mi,
+                                  cudaMemcpyDeviceToHost, hp.d2h) != cudaSuccess)
+                return SGEMM_ERR_LAUNCH;
+        }
+        if (cudaEventRecord(hp.end, hp.d2h) != cudaSuccess ||
+            cudaStreamWaitEvent(st, hp.end, 0) != cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
+        return status_from(cudaStreamSynchronize(st));
+    }
     if (need_ab) {
         if (cudaMemcpy2DAsync(hb.A, dlda * 4, A, lda * 4, K * 4, M, cudaMemcpyHostToDevice, st) !=
                 cudaSuccess ||

@@ -72,7 +72,7 @@ def sample_rows(M, count, seed):
 
 @pytest.mark.parametrize("name,sample", [
     ("s1_128", None), ("s2_2048", 192), ("s3_4092", 64), ("s4_rect", 48),
-    ("s5_odd", None), ("s6_skinny", None),
+    ("s5_odd", None), ("s6_skinny", None), ("s7_gemv", None),
 ])
 def test_workload_full_size(name, sample):
     cfg, A, B, C = datagen.config_inputs(name)
@@ -249,6 +249,19 @@ def test_host_entry_point():
     sg.run_host(Ah, Bh, Ch, alpha=0.5, beta=2.0)
     ref, bound = reference(M, N, K, 0.5, 2.0, A, lda, B, ldb, C, ldc)
     assert_within(Ch, ref, bound, "sgemm_run_host")
+
+
+@pytest.mark.parametrize("M,N,K,alpha,beta", [(1500, 1030, 700, 0.5, 2.0), (2048, 512, 384, 1.0, 0.0)])
+def test_host_entry_point_in_row_blocks(M, N, K, alpha, beta):
+    # From M = 1024 the host entry point copies and computes row blocks in a
+    # pipeline; pinned host buffers, a ragged last block, odd N.
+    A, lda, B, ldb, C, ldc = inputs("normal", 15, M, N, K)
+    Ah = torch.from_numpy(A.reshape(M, K)).pin_memory()
+    Bh = torch.from_numpy(B.reshape(K, N)).pin_memory()
+    Ch = torch.from_numpy(C.reshape(M, N).copy()).pin_memory()
+    sg.run_host(Ah, Bh, Ch, alpha=alpha, beta=beta)
+    ref, bound = reference(M, N, K, alpha, beta, A, lda, B, ldb, C if beta else None, ldc)
+    assert_within(Ch.numpy(), ref, bound, "sgemm_run_host in row blocks")
 
 
 def test_torch_binding_with_strided_rows():
@@ -433,3 +446,36 @@ def test_skinny_wait_timeout_reports_and_recovers():
     out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
     ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
     assert_within(out, ref, bound, "skinny after timeout")
+
+
+# ----- CUDA graphs -------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [(16, 4096, 2048), (1100, 1300, 512), (300, 520, 200)])
+def test_capture_in_a_cuda_graph_and_replay(M, N, K):
+    # After a first call has set up the stream's workspace, sgemm_run queues
+    # kernels only (no allocation, no host synchronisation), so it can be
+    # captured in a CUDA graph and replayed: the skinny, stream-K and 64 x 64
+    # paths each give the eager result, bit for bit, on every replay.
+    A, lda, B, ldb, C, ldc = inputs("uniform", 50 + M, M, N, K)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.zeros(M * N, device="cuda")
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        st = sg.sgemm_run(M, N, K, 1.0, dA.data_ptr(), lda, dB.data_ptr(), ldb, 0.0,
+                          dC.data_ptr(), N, side.cuda_stream)
+        assert st == 0
+    torch.cuda.synchronize()
+    eager = dC.clone()
+    dC.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        st = sg.sgemm_run(M, N, K, 1.0, dA.data_ptr(), lda, dB.data_ptr(), ldb, 0.0,
+                          dC.data_ptr(), N, side.cuda_stream)
+    assert st == 0
+    for _ in range(3):
+        dC.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(dC, eager)
+    assert sg.device_status() == 0
