@@ -332,6 +332,15 @@ sgemm_status_t sgemm_run(int64_t M, int64_t N, int64_t K, float alpha, const flo
                               SGEMM_ACT_NONE, stream);
 }
 
+// Host <-> device copy of `rows` rows of `width` floats; one contiguous copy
+// when both pitches equal the row length.
+cudaError_t copy_rows(float *dst, int64_t dpitch, const float *src, int64_t spitch, int64_t width,
+                      int64_t rows, cudaMemcpyKind kind, cudaStream_t st) {
+    if (dpitch == width && spitch == width)
+        return cudaMemcpyAsync(dst, src, (size_t)(rows * width) * 4, kind, st);
+    return cudaMemcpy2DAsync(dst, dpitch * 4, src, spitch * 4, width * 4, rows, kind, st);
+}
+
 sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                               int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                               int64_t ldc, void *stream) {
@@ -388,17 +397,16 @@ sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha, cons
             cudaStreamWaitEvent(hp.h2d, hp.start, 0) != cudaSuccess ||
             cudaStreamWaitEvent(hp.d2h, hp.start, 0) != cudaSuccess)
             return SGEMM_ERR_LAUNCH;
-        if (cudaMemcpy2DAsync(hb.B, dldb * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice,
-                              hp.h2d) != cudaSuccess)
+        if (copy_rows(hb.B, dldb, B, ldb, N, K, cudaMemcpyHostToDevice, hp.h2d) != cudaSuccess)
             return SGEMM_ERR_LAUNCH;
         for (int i = 0; i < blocks; ++i) {
             const int64_t r0 = i * rows, mi = std::min<int64_t>(rows, M - r0);
-            if (cudaMemcpy2DAsync(hb.A + r0 * dlda, dlda * 4, A + r0 * lda, lda * 4, K * 4, mi,
-                                  cudaMemcpyHostToDevice, hp.h2d) != cudaSuccess)
+            if (copy_rows(hb.A + r0 * dlda, dlda, A + r0 * lda, lda, K, mi, cudaMemcpyHostToDevice,
+                          hp.h2d) != cudaSuccess)
                 return SGEMM_ERR_LAUNCH;
             if (beta != 0.0f &&
-                cudaMemcpy2DAsync(hb.C + r0 * dldc, dldc * 4, C + r0 * ldc, ldc * 4, N * 4, mi,
-                                  cudaMemcpyHostToDevice, hp.h2d) != cudaSuccess)
+                copy_rows(hb.C + r0 * dldc, dldc, C + r0 * ldc, ldc, N, mi, cudaMemcpyHostToDevice,
+                          hp.h2d) != cudaSuccess)
                 return SGEMM_ERR_LAUNCH;
             if (cudaEventRecord(hp.in[i], hp.h2d) != cudaSuccess ||
                 cudaStreamWaitEvent(st, hp.in[i], 0) != cudaSuccess)
@@ -408,8 +416,8 @@ sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha, cons
             if (s != SGEMM_OK) return s;
             if (cudaEventRecord(hp.done[i], st) != cudaSuccess ||
                 cudaStreamWaitEvent(hp.d2h, hp.done[i], 0) != cudaSuccess ||
-                cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, hb.C + r0 * dldc, dldc * 4, N * 4, mi,
-                                  cudaMemcpyDeviceToHost, hp.d2h) != cudaSuccess)
+                copy_rows(C + r0 * ldc, ldc, hb.C + r0 * dldc, dldc, N, mi, cudaMemcpyDeviceToHost,
+                          hp.d2h) != cudaSuccess)
                 return SGEMM_ERR_LAUNCH;
         }
         if (cudaEventRecord(hp.end, hp.d2h) != cudaSuccess ||
@@ -418,20 +426,20 @@ sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha, cons
         return status_from(cudaStreamSynchronize(st));
     }
     if (need_ab) {
-        if (cudaMemcpy2DAsync(hb.A, dlda * 4, A, lda * 4, K * 4, M, cudaMemcpyHostToDevice, st) !=
+        if (copy_rows(hb.A, dlda, A, lda, K, M, cudaMemcpyHostToDevice, st) !=
                 cudaSuccess ||
-            cudaMemcpy2DAsync(hb.B, dldb * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice, st) !=
+            copy_rows(hb.B, dldb, B, ldb, N, K, cudaMemcpyHostToDevice, st) !=
                 cudaSuccess)
             return SGEMM_ERR_LAUNCH;
     }
     if (beta != 0.0f &&
-        cudaMemcpy2DAsync(hb.C, dldc * 4, C, ldc * 4, N * 4, M, cudaMemcpyHostToDevice, st) !=
+        copy_rows(hb.C, dldc, C, ldc, N, M, cudaMemcpyHostToDevice, st) !=
             cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     s = run_locked(M, N, K, alpha, hb.A, dlda, hb.B, dldb, beta, hb.C, dldc, Epilogue{nullptr, kActNone},
                    st, *d);
     if (s != SGEMM_OK) return s;
-    if (cudaMemcpy2DAsync(C, ldc * 4, hb.C, dldc * 4, N * 4, M, cudaMemcpyDeviceToHost, st) !=
+    if (copy_rows(C, ldc, hb.C, dldc, N, M, cudaMemcpyDeviceToHost, st) !=
         cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     return status_from(cudaStreamSynchronize(st));
