@@ -114,10 +114,11 @@ SGEMM_API sgemm_status_t sgemm_run_epilogue(int64_t M, int64_t N, int64_t K, flo
  * A, B, C are host pointers (pinned memory gives full copy bandwidth).  The
  * call copies A, B (and C when beta != 0) to device buffers it owns, runs
  * sgemm_run on `stream`, copies C back and synchronises `stream` before
- * returning, so C holds the result on return.  From M = 1024 on, the rows of
- * A and C are cut into up to four blocks: B goes in first, then block i + 1
- * is copied in and block i - 1 out (on two internal streams, after the work
- * already queued on `stream`) while block i is computed.  Device buffers are
+ * returning, so C holds the result on return.  From M = 1024 on, when each
+ * block keeps enough work for the tiled kernel, the rows of A and C are cut
+ * into two to four blocks: B goes in first, then block i + 1 is copied in and
+ * block i - 1 out (on two internal streams, after the work already queued on
+ * `stream`) while block i is computed.  Device buffers are
  * kept for reuse until sgemm_release_workspace().
  */
 SGEMM_API sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float alpha,

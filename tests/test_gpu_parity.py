@@ -251,17 +251,25 @@ def test_host_entry_point():
     assert_within(Ch, ref, bound, "sgemm_run_host")
 
 
-@pytest.mark.parametrize("M,N,K,alpha,beta", [(1500, 1030, 700, 0.5, 2.0), (2048, 512, 384, 1.0, 0.0)])
-def test_host_entry_point_in_row_blocks(M, N, K, alpha, beta):
-    # From M = 1024 the host entry point copies and computes row blocks in a
-    # pipeline; pinned host buffers, a ragged last block, odd N.
+@pytest.mark.parametrize("M,N,K,alpha,beta,blocks", [(3000, 1030, 4100, 0.5, 2.0, 4),
+                                                    (2048, 2056, 2048, 1.0, 0.0, 2)])
+def test_host_entry_point_in_row_blocks(M, N, K, alpha, beta, blocks):
+    # Large enough that the host entry point copies and computes row blocks in
+    # a pipeline (4 blocks with a ragged last one; 2 blocks); pinned host
+    # buffers; rows sampled on both sides of every block boundary.
     A, lda, B, ldb, C, ldc = inputs("normal", 15, M, N, K)
     Ah = torch.from_numpy(A.reshape(M, K)).pin_memory()
     Bh = torch.from_numpy(B.reshape(K, N)).pin_memory()
     Ch = torch.from_numpy(C.reshape(M, N).copy()).pin_memory()
     sg.run_host(Ah, Bh, Ch, alpha=alpha, beta=beta)
-    ref, bound = reference(M, N, K, alpha, beta, A, lda, B, ldb, C if beta else None, ldc)
-    assert_within(Ch.numpy(), ref, bound, "sgemm_run_host in row blocks")
+    rows_per = -(-(-(-M // blocks)) // 128) * 128
+    edges = {0, M - 1}
+    for b in range(1, blocks):
+        edges |= {b * rows_per - 1, b * rows_per}
+    rows = sorted(r for r in edges | set(sample_rows(M, 24, 3)) if 0 <= r < M)
+    ref, bound = reference(M, N, K, alpha, beta, A, lda, B, ldb, C if beta else None, ldc,
+                           rows=rows)
+    assert_within(Ch.numpy()[rows], ref, bound, "sgemm_run_host in row blocks")
 
 
 def test_torch_binding_with_strided_rows():
