@@ -110,6 +110,20 @@ __device__ __forceinline__ const float *skinny_piece(const SkinnyParams &p, int 
     return p.partials + (size_t)skinny_slot(p, cta, slab) * (kSkinnyMaxM * SBN);
 }
 
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                                 int c0, int c1, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "l"(pol)
+        : "memory");
+}
 // Element (m, k) of the TMA-loaded A block: rows of 32 floats whose 16-byte
 // chunks are XOR-swizzled with (row mod 8).
 __device__ __forceinline__ float a_elem(const float *raw, int m, int k) {
@@ -178,7 +192,7 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
         issued[s] = q;
         mbar_arrive_expect_tx(&full[s], L::tx_bytes);
         tma_load_2d(sa, &mapA, &full[s], k * SBK, 0);
-        tma_load_2d(sa + L::a_floats, &mapB, &full[s], slab * SBN, k * SBK);
+        tma_load_2d_hint(sa + L::a_floats, &mapB, &full[s], slab * SBN, k * SBK, policy_evict_first());
     };
 
     if (tid == 0) {
