@@ -44,6 +44,8 @@ _SIGNATURES = {
     "sgemm_run_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
     "sgemm_run_skinny_noalloc": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp,
                                         _i64, _vp]),
+    "sgemm_run_3xtf32": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
+    "sgemm_set_3xtf32_kslice": (_int, [_int]),
     "sgemm_status_string": (ctypes.c_char_p, [_int]),
     "sgemm_device_status": (_int, [_vp]),
     "sgemm_plan_describe": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_uint64,
@@ -121,6 +123,12 @@ def sgemm_run_epilogue(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias=None,
                                         int(activation), stream)
 
 
+def sgemm_run_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """Raw C-ABI call of the 3xTF32 tensor-core variant; returns the status."""
+    return library().sgemm_run_3xtf32(int(M), int(N), int(K), float(alpha), A, int(lda), B,
+                                      int(ldb), float(beta), C, int(ldc), stream)
+
+
 def sgemm_run_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
     """Raw C-ABI call with integer host addresses; returns the status."""
     return library().sgemm_run_host(int(M), int(N), int(K), float(alpha), A, int(lda), B,
@@ -175,6 +183,33 @@ def run(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, bias=None,
             _check(sgemm_run_epilogue(M, N, K, alpha, a, lda, b, ldb, beta, c, ldc, bias_ptr,
                                       activation, s), "sgemm_run_epilogue")
     return C
+
+
+def run_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha * A @ B + beta * C in place, on the tensor cores by the
+    3xTF32 split (hi*hi + hi*lo + lo*hi of TF32 parts, FP32 accumulation).
+    Same tensors and conventions as run(); no bias or activation."""
+    import torch
+
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch: A {tuple(A.shape)} B {tuple(B.shape)} C {tuple(C.shape)}")
+    for t, name in ((A, "A"), (B, "B"), (C, "C")):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    a, lda = _matrix_args(A, "A")
+    b, ldb = _matrix_args(B, "B")
+    c, ldc = _matrix_args(C, "C")
+    s = (stream or torch.cuda.current_stream(C.device)).cuda_stream
+    with torch.cuda.device(C.device):
+        _check(sgemm_run_3xtf32(M, N, K, alpha, a, lda, b, ldb, beta, c, ldc, s), "sgemm_run_3xtf32")
+    return C
+
+
+def set_3xtf32_kslice(bk: int = 32) -> None:
+    """K depth of one 3xTF32 pipeline stage: 32 (default) or 16."""
+    _check(library().sgemm_set_3xtf32_kslice(int(bk)), "sgemm_set_3xtf32_kslice")
 
 
 def run_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):

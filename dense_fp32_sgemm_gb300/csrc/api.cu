@@ -29,6 +29,7 @@ std::atomic<int> g_skip_loads_from{-1};
 std::atomic<int> g_fma_mode{kFmaPairMovB};
 std::atomic<int> g_stages{3};
 std::atomic<int> g_micro_m{16};
+std::atomic<int> g_x3_bk{32};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -42,6 +43,8 @@ struct Workspace {
     size_t counter_count = 0;
     float *pack = nullptr;  // aligned copies of unaligned operands
     size_t pack_bytes = 0;
+    float *split = nullptr;  // 3xTF32 hi / lo operand copies
+    size_t split_bytes = 0;
 };
 
 struct HostBuffers {
@@ -67,6 +70,7 @@ struct DeviceState {
     std::map<cudaStream_t, Workspace> ws;
     HostBuffers host;
     unsigned configured = 0;            // skinny configurations set up
+    unsigned x3_configured = 0;         // 3xTF32 K slices set up (bit bk / 16)
     std::set<int> configured_tiles;     // tile configurations set up
 };
 
@@ -332,6 +336,65 @@ sgemm_status_t sgemm_run(int64_t M, int64_t N, int64_t K, float alpha, const flo
                               SGEMM_ACT_NONE, stream);
 }
 
+sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                                int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                                int64_t ldc, void *stream) {
+    const sgemm_status_t v = validate(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    if (v != SGEMM_OK) return v;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState *d = nullptr;
+    sgemm_status_t s = device_state(&d);
+    if (s != SGEMM_OK) return s;
+    const Epilogue none{nullptr, kActNone};
+    if (K < kX3MinK || M <= 16 || alpha == 0.0f)
+        return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, none, st, *d);
+    if (M > (1 << 29) || N > (1 << 29) || K > (1 << 30) ||
+        ((M + kX3BM - 1) / kX3BM) * ((N + kX3BN - 1) / kX3BN) > INT32_MAX)
+        return SGEMM_ERR_INVALID_ARG;
+    const int bk = g_x3_bk.load();
+    const unsigned bit = 1u << (bk / 16);
+    if (!(d->x3_configured & bit)) {
+        if (x3_configure(bk) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        d->x3_configured |= bit;
+    }
+    const int64_t Mp = (M + kX3BM - 1) / kX3BM * kX3BM;
+    const int64_t Np = (N + kX3BN - 1) / kX3BN * kX3BN;
+    const int64_t Kp = (K + 3) / 4 * 4;
+    const size_t a_floats = (size_t)(2 * Mp * Kp), b_floats = (size_t)(2 * Np * Kp);
+    Workspace &w = d->ws[st];
+    const size_t bytes = (a_floats + b_floats) * sizeof(float);
+    if (w.split_bytes < bytes) {
+        if (w.split) cudaFree(w.split);
+        w.split = nullptr;
+        w.split_bytes = 0;
+        if (cudaMalloc(&w.split, bytes) != cudaSuccess) return SGEMM_ERR_ALLOC;
+        w.split_bytes = bytes;
+    }
+    float *sa = w.split, *sb = w.split + a_floats;  // a_floats is a multiple of 256
+    if (launch_x3_split(A, lda, (int)M, B, ldb, (int)N, (int)K, sa, (int)Mp, sb, (int)Np,
+                        (int)Kp, d->num_sms, st) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    const CUtensorMapSwizzle sw = bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUtensorMap mapA, mapB;
+    s = encode_2d(&mapA, sa, 2 * Mp, Kp, Kp, bk, kX3BM, sw);
+    if (s != SGEMM_OK) return s;
+    s = encode_2d(&mapB, sb, 2 * Np, Kp, Kp, bk, kX3BN, sw);
+    if (s != SGEMM_OK) return s;
+    X3Params p;
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.tiles_m = (int)(Mp / kX3BM); p.tiles_n = (int)(Np / kX3BN);
+    p.kt_total = (int)((K + bk - 1) / bk);
+    p.a_lo_row = (int)Mp; p.b_lo_row = (int)Np;
+    p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
+    p.err = d->err;
+    const unsigned long long to = g_timeout_ns.load();
+    p.timeout_ns = to ? to : kDefaultTimeoutNs;
+    p.skip_loads_from = g_skip_loads_from.load();
+    return status_from(launch_x3(bk, mapA, mapB, p, st));
+}
+
 // Host <-> device copy of `rows` rows of `width` floats; one contiguous copy
 // when both pitches equal the row length.
 cudaError_t copy_rows(float *dst, int64_t dpitch, const float *src, int64_t spitch, int64_t width,
@@ -543,6 +606,12 @@ sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages, int micro_m) {
     return SGEMM_OK;
 }
 
+sgemm_status_t sgemm_set_3xtf32_kslice(int bk) {
+    if (bk != 16 && bk != 32) return SGEMM_ERR_INVALID_ARG;
+    g_x3_bk.store(bk);
+    return SGEMM_OK;
+}
+
 sgemm_status_t sgemm_release_workspace(void) {
     std::lock_guard<std::mutex> lock(g_mu);
     int prev = 0;
@@ -556,6 +625,7 @@ sgemm_status_t sgemm_release_workspace(void) {
             if (w.second.partials) cudaFree(w.second.partials);
             if (w.second.counters) cudaFree(w.second.counters);
             if (w.second.pack) cudaFree(w.second.pack);
+            if (w.second.split) cudaFree(w.second.split);
         }
         d.ws.clear();
         if (d.host.A) cudaFree(d.host.A);

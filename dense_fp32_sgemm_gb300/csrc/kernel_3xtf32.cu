@@ -1,0 +1,439 @@
+// 3xTF32 SGEMM on the fifth-generation tensor cores (tcgen05, sm_103a).
+//
+// Why a tensor-core variant at all: "GEMM from Scratch", Module 07 ("Tensor
+// Cores -- Why They Dominate Peak") puts the tensor units on a separate,
+// much higher throughput ceiling than the FP32 cores, and "Optimizing Matrix
+// Multiply on CUDA, Part 2", section "Looking Back", names lower-precision
+// inputs on tensor cores as the route past FP32-core parity.  The same module
+// warns that TF32 drops mantissa bits, which FP32 work cannot accept, and
+// "Optimizing CUDA matmul, steps 4 to 6", section "The honest target", keeps
+// the FP32 contract free of TF32.  So this variant is a separate entry point
+// that must meet the FP32 error bound of the FFMA kernels, and gets there by
+// split-precision emulation (the published 3xTF32 method: Markidis et al.
+// 2018; Ootomo and Yokota 2022):
+//
+//   x = hi + lo + e,   hi = tf32(x),  lo = tf32(x - hi)   (round to nearest)
+//   |x - hi| <= 2^-11 |x|,  |e| <= 2^-22 |x|
+//   a * b ~= hi_a*hi_b + hi_a*lo_b + lo_a*hi_b      (lo_a*lo_b <= 2^-22 |ab| dropped)
+//
+// Each TF32 x TF32 product (11 x 11 significant bits) is exact in the FP32
+// accumulator, so the result differs from the FP32 one only by the dropped
+// terms and the accumulation order.
+//
+// Structure (one 128 x 256 tile of C per CTA, 128 threads):
+//   split pass   A -> [A_hi; A_lo] (K-major rows), B -> [B_hi^T; B_lo^T]
+//                (transposed to K-major), zero padded; an HBM-bound pass.
+//   warp 0       one thread issues the TMA loads of the four operand tiles
+//                of each K slice into a ring of swizzled shared-memory stages.
+//   warp 1       one thread issues tcgen05.mma (M 128, N 256, K 8) three
+//                times per K step, accumulating in tensor memory, and
+//                releases each stage with tcgen05.commit.
+//   warp 2       allocates and frees the 256 tensor-memory columns.
+//   all 4 warps  epilogue: tcgen05.ld of their 32 accumulator lanes, through
+//                shared memory to coalesced rows, alpha / beta, store.
+// Every wait is bounded; on a timeout the kernel flags the error word, waits
+// (bounded) for its copies and MMAs in flight, frees tensor memory and exits.
+#include <algorithm>
+
+#include "device_common.cuh"
+
+namespace sgemm {
+namespace {
+
+constexpr int BM = kX3BM;
+constexpr int BN = kX3BN;
+constexpr int THREADS = 128;
+constexpr int TMEM_COLS = BN;  // FP32 accumulator: 128 lanes x 256 columns
+
+template <int BK>
+struct X3Cfg {
+    static_assert(BK == 32 || BK == 16, "K slice of 32 (128-byte rows) or 16 (64-byte rows)");
+    static constexpr int kRowBytes = BK * 4;                  // one swizzled row of K
+    static constexpr uint32_t kA = BM * BK * 4;               // one A part (hi or lo)
+    static constexpr uint32_t kB = BN * BK * 4;               // one B part
+    static constexpr uint32_t kStage = 2 * kA + 2 * kB;
+    static constexpr int kStages = BK == 32 ? 2 : 4;
+    static constexpr uint32_t kAlign = 8 * kRowBytes;         // one swizzle atom
+    static constexpr size_t kSmem = (size_t)kStages * kStage + 1024;
+    // shared-memory descriptor layout type: 2 = 128-byte swizzle, 4 = 64-byte
+    static constexpr uint64_t kLayout = BK == 32 ? 2 : 4;
+};
+
+// tcgen05 shared-memory matrix descriptor for a K-major operand stored as
+// rows of BK FP32 values with the TMA's matching swizzle: start address,
+// stride between 8-row groups (one swizzle atom), fixed version bits 46-47 =
+// 1, layout type in bits 61-63.  The leading offset is unused for swizzled
+// K-major operands.
+template <int BK>
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    using L = X3Cfg<BK>;
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;                       // leading byte offset 16 (unused)
+    d |= (uint64_t)(L::kAlign >> 4) << 32;        // stride byte offset: 8 rows
+    d |= (uint64_t)1 << 46;
+    d |= L::kLayout << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::tf32: FP32 accumulator (bits 4-5 = 1), A and
+// B TF32 (bits 7-9, 10-12 = 2), both K-major (bits 15, 16 = 0), N >> 3 in
+// bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on `bar` once every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
+                     "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Whole-warp tensor-memory allocation; the column base is written to *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(TMEM_COLS)
+                 : "memory");
+}
+
+// 32 consecutive accumulator columns of this warp's 32 lanes: thread i gets
+// lane (base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    // The registers are valid only after the wait; tying them to it keeps
+    // every use below it.
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Round to TF32 (10 explicit mantissa bits), nearest with ties away from
+// zero; the low 13 bits of the FP32 pattern are cleared.
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r & 0xFFFFE000u);
+}
+
+__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
+    hi = to_tf32(x);
+    lo = to_tf32(x - hi);  // x - hi is exact in FP32
+}
+
+// ---------------------------------------------------------------------------
+// Split pass.
+// ---------------------------------------------------------------------------
+
+// A (rows x cols, leading dimension ldx, any 4-byte alignment) -> out, rows
+// [0, rows_p) the hi parts and [rows_p, 2 rows_p) the lo parts, each row
+// cols_p floats (a multiple of 4), zero outside A.
+__global__ void __launch_bounds__(256) x3_split_rows_kernel(const float *__restrict__ X,
+                                                            long long ldx, int rows, int cols,
+                                                            float *__restrict__ out, int rows_p,
+                                                            int cols_p) {
+    const int q_row = cols_p / 4;
+    const long long total = (long long)rows_p * q_row;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(i / q_row), c = (int)(i % q_row) * 4;
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[j] = (r < rows && c + j < cols) ? __ldg(X + (long long)r * ldx + c + j) : 0.0f;
+        float4 h, l;
+        split_tf32(v[0], h.x, l.x);
+        split_tf32(v[1], h.y, l.y);
+        split_tf32(v[2], h.z, l.z);
+        split_tf32(v[3], h.w, l.w);
+        *reinterpret_cast<float4 *>(out + (size_t)r * cols_p + c) = h;
+        *reinterpret_cast<float4 *>(out + ((size_t)rows_p + r) * cols_p + c) = l;
+    }
+}
+
+// B (k_rows x n_cols, leading dimension ldb) -> out transposed: row n of the
+// hi part holds column n of B's hi values over k; lo rows start at n_p.  Row
+// length k_p (a multiple of 4); zero outside B.  32 x 32 tiles through
+// shared memory so that reads and writes both run along rows; the grid
+// strides over the tiles (k fastest).
+__global__ void __launch_bounds__(256) x3_split_cols_kernel(const float *__restrict__ B,
+                                                            long long ldb, int k_rows,
+                                                            int n_cols, float *__restrict__ out,
+                                                            int n_p, int k_p) {
+    __shared__ float t[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    const long long k_tiles = (k_p + 31) / 32, tiles = k_tiles * ((n_p + 31) / 32);
+    for (long long b = blockIdx.x; b < tiles; b += gridDim.x) {
+        const int k0 = (int)(b % k_tiles) * 32, n0 = (int)(b / k_tiles) * 32;
+#pragma unroll
+        for (int r = ty; r < 32; r += 8) {
+            const int k = k0 + r, n = n0 + tx;
+            t[r][tx] = (k < k_rows && n < n_cols) ? __ldg(B + (long long)k * ldb + n) : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = ty; r < 32; r += 8) {
+            const int n = n0 + r, k = k0 + tx;
+            if (n < n_p && k < k_p) {
+                float h, l;
+                split_tf32(t[tx][r], h, l);
+                out[(size_t)n * k_p + k] = h;
+                out[((size_t)n_p + n) * k_p + k] = l;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MMA kernel.
+// ---------------------------------------------------------------------------
+template <int BK>
+__global__ void __launch_bounds__(THREADS, 1)
+    sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap mapA,
+                        const __grid_constant__ CUtensorMap mapB, const X3Params p) {
+    using L = X3Cfg<BK>;
+    constexpr int S = L::kStages;
+    extern __shared__ unsigned char x3_smem_raw[];
+    __shared__ uint64_t full[S], empty[S], accum_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int s_abort;
+    __shared__ int s_issued, s_consumed, s_accum_ok;
+
+    // Stages start on a 1024-byte boundary of the shared window (the
+    // swizzle pattern is taken from address bits).
+    const uint32_t raw = smem_addr(x3_smem_raw);
+    unsigned char *smem = x3_smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tm = blockIdx.x % p.tiles_m, tn = blockIdx.x / p.tiles_m;
+    const int m0 = tm * BM, n0 = tn * BN;
+
+    if (tid == 0) {
+        prefetch_tensormap(&mapA);
+        prefetch_tensormap(&mapB);
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&accum_bar, 1);
+        s_abort = 0;
+        s_issued = 0;
+        s_consumed = 0;
+        s_accum_ok = 0;
+        fence_barrier_init();
+    }
+    if (warp == 2) tmem_alloc(&tmem_slot);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // Producer: the four operand tiles of K slice kt into stage kt % S.
+            int kt = 0;
+            for (; kt < p.kt_total; ++kt) {
+                if (p.skip_loads_from >= 0 && kt >= p.skip_loads_from) break;
+                const int s = kt % S;
+                if (kt >= S && !mbar_wait_bounded(&empty[s], ((kt / S) - 1) & 1, p.timeout_ns)) {
+                    atomicOr(p.err, kErrWaitTimeout);
+                    s_abort = 1;
+                    break;
+                }
+                unsigned char *st = smem + (size_t)s * L::kStage;
+                mbar_arrive_expect_tx(&full[s], L::kStage);
+                const int k = kt * BK;
+                tma_load_2d(st, &mapA, &full[s], k, m0);
+                tma_load_2d(st + L::kA, &mapA, &full[s], k, p.a_lo_row + m0);
+                tma_load_2d(st + 2 * L::kA, &mapB, &full[s], k, n0);
+                tma_load_2d(st + 2 * L::kA + L::kB, &mapB, &full[s], k, p.b_lo_row + n0);
+            }
+            s_issued = kt;
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // MMA issuer: per K step of 8, the two correction products first,
+            // then hi*hi; the first product of the tile overwrites D.
+            int kt = 0;
+            for (; kt < p.kt_total; ++kt) {
+                const int s = kt % S;
+                if (!mbar_wait_bounded(&full[s], (kt / S) & 1, p.timeout_ns)) {
+                    atomicOr(p.err, kErrWaitTimeout);
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_hi = sbase + s * L::kStage, a_lo = a_hi + L::kA;
+                const uint32_t b_hi = a_hi + 2 * L::kA, b_lo = b_hi + L::kB;
+#pragma unroll
+                for (int kk = 0; kk < BK / 8; ++kk) {
+                    const uint32_t off = kk * 32;  // 8 TF32 values along K
+                    mma_tf32(tmem, smem_desc<BK>(a_lo + off), smem_desc<BK>(b_hi + off),
+                             (kt | kk) != 0);
+                    mma_tf32(tmem, smem_desc<BK>(a_hi + off), smem_desc<BK>(b_lo + off), 1);
+                    mma_tf32(tmem, smem_desc<BK>(a_hi + off), smem_desc<BK>(b_hi + off), 1);
+                }
+                mma_commit(&empty[s]);  // stage s is free once these MMAs are done
+            }
+            s_consumed = kt;
+            mma_commit(&accum_bar);
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+
+    if (tid == 0) {
+        // The accumulator is final (and every MMA finished) once the last
+        // commit arrives.
+        s_accum_ok = mbar_wait_bounded(&accum_bar, 0, p.timeout_ns) ? 1 : 0;
+        if (!s_accum_ok) atomicOr(p.err, kErrDrainTimeout);
+    }
+    __syncthreads();
+
+    if (!s_abort && s_accum_ok) {
+        tc_fence_after();
+        // Epilogue: warp w owns accumulator lanes (rows) 32w .. 32w + 31.
+        // Each 32-column block goes register -> shared (row per thread) ->
+        // global (one row of 32 consecutive floats per warp store).
+        float *stage = reinterpret_cast<float *>(smem) + warp * (32 * 33);
+        const uint32_t t_warp = tmem + ((uint32_t)(warp * 32) << 16);
+        const int row0 = m0 + warp * 32;
+        for (int c = 0; c < BN / 32; ++c) {
+            if (n0 + c * 32 >= p.N) break;  // uniform over the warp
+            uint32_t r[32];
+            tmem_ld32(t_warp + c * 32, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = __uint_as_float(r[j]);
+            __syncwarp();
+            const int n = n0 + c * 32 + lane;
+            if (n < p.N) {
+#pragma unroll 4
+                for (int i = 0; i < 32; ++i) {
+                    const int m = row0 + i;
+                    if (m >= p.M) break;
+                    float *cp = p.C + (long long)m * p.ldc + n;
+                    float v = p.alpha * stage[i * 33 + lane];
+                    if (p.beta != 0.0f) v = __fmaf_rn(p.beta, *cp, v);
+                    *cp = v;
+                }
+            }
+            __syncwarp();
+        }
+    }
+
+    if (tid == 0) {
+        // Nothing may land in this CTA's shared memory after it exits: the
+        // stage-release arrivals of the last commits, and (after a timeout)
+        // loads that were issued but never consumed.
+        const int consumed = s_consumed, issued = s_issued;
+        for (int s = 0; s < S && s < consumed; ++s) {
+            const int uses = (consumed - s + S - 1) / S;  // commits made to empty[s]
+            if (!mbar_wait_bounded(&empty[s], (uses - 1) & 1, 1000000000ull)) {
+                atomicOr(p.err, kErrDrainTimeout);
+                break;
+            }
+        }
+        for (int j = consumed; j < issued; ++j) {
+            if (!mbar_wait_bounded(&full[j % S], (j / S) & 1, 1000000000ull)) {
+                atomicOr(p.err, kErrDrainTimeout);
+                break;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem);
+    }
+}
+
+}  // namespace
+
+int x3_stages(int bk) { return bk == 16 ? X3Cfg<16>::kStages : X3Cfg<32>::kStages; }
+
+size_t x3_smem_bytes(int bk) { return bk == 16 ? X3Cfg<16>::kSmem : X3Cfg<32>::kSmem; }
+
+cudaError_t x3_configure(int bk) {
+    if (bk == 16)
+        return cudaFuncSetAttribute(sgemm_3xtf32_kernel<16>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)X3Cfg<16>::kSmem);
+    if (bk == 32)
+        return cudaFuncSetAttribute(sgemm_3xtf32_kernel<32>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)X3Cfg<32>::kSmem);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_x3(int bk, const CUtensorMap &mapA, const CUtensorMap &mapB,
+                      const X3Params &p, cudaStream_t stream) {
+    const int grid = p.tiles_m * p.tiles_n;
+    if (bk == 16)
+        sgemm_3xtf32_kernel<16><<<grid, THREADS, X3Cfg<16>::kSmem, stream>>>(mapA, mapB, p);
+    else if (bk == 32)
+        sgemm_3xtf32_kernel<32><<<grid, THREADS, X3Cfg<32>::kSmem, stream>>>(mapA, mapB, p);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_x3_split(const float *A, long long lda, int M, const float *B, long long ldb,
+                            int N, int K, float *splitA, int Mp, float *splitB, int Np, int Kp,
+                            int num_sms, cudaStream_t stream) {
+    const long long quads = (long long)Mp * (Kp / 4);
+    const long long blocks = std::min<long long>((quads + 255) / 256, (long long)num_sms * 8);
+    x3_split_rows_kernel<<<(int)std::max<long long>(blocks, 1), 256, 0, stream>>>(
+        A, lda, M, K, splitA, Mp, Kp);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long tiles = (long long)((Kp + 31) / 32) * ((Np + 31) / 32);
+    const int g = (int)std::min<long long>(tiles, (long long)num_sms * 16);
+    x3_split_cols_kernel<<<g, 256, 0, stream>>>(B, ldb, K, N, splitB, Np, Kp);
+    return cudaGetLastError();
+}
+
+}  // namespace sgemm

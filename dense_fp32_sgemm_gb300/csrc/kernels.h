@@ -161,6 +161,43 @@ size_t skinny_smem_bytes(int m_tile, int share);
 cudaError_t skinny_configure(int m_tile);
 
 // ---------------------------------------------------------------------------
+// 3xTF32 variant on the tensor cores (tcgen05, accumulator in tensor memory).
+// A split pass writes each operand as TF32 hi and lo parts, K-major, zero
+// padded: A as (2 * Mp) x Kp rows (hi rows [0, Mp), lo rows [Mp, 2 Mp)), B
+// transposed as (2 * Np) x Kp rows.  The MMA kernel takes one 128 x 256 tile
+// of C per CTA and sums hi*hi + hi*lo + lo*hi over K.
+// ---------------------------------------------------------------------------
+constexpr int kX3BM = 128;
+constexpr int kX3BN = 256;
+constexpr int kX3MinK = 64;  // shorter products run the FFMA kernels
+
+struct X3Params {
+    int M, N, K;
+    int tiles_m, tiles_n;
+    int kt_total;          // ceil(K / BK)
+    int a_lo_row;          // Mp: first row of A's lo part in the split buffer
+    int b_lo_row;          // Np: first row of B's lo part
+    float alpha, beta;
+    float *C;
+    long long ldc;
+    int *err;
+    unsigned long long timeout_ns;
+    int skip_loads_from;   // testing hook, -1 = off
+};
+
+// bk: 32 (128-byte swizzled rows) or 16 (64-byte swizzled rows).
+int x3_stages(int bk);
+size_t x3_smem_bytes(int bk);
+cudaError_t x3_configure(int bk);
+cudaError_t launch_x3(int bk, const CUtensorMap &mapA, const CUtensorMap &mapB, const X3Params &p,
+                      cudaStream_t stream);
+// Split A (M x K, lda) and B (K x N, ldb) into the buffers above.  Kp is a
+// multiple of 4; Mp and Np multiples of the tile sizes.
+cudaError_t launch_x3_split(const float *A, long long lda, int M, const float *B, long long ldb,
+                            int N, int K, float *splitA, int Mp, float *splitB, int Np, int Kp,
+                            int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
 // Measurement probes (same library, used by the benchmark).
 // ---------------------------------------------------------------------------
 cudaError_t launch_ffma_probe(int paired, long long iters, int blocks, float *sink,

@@ -225,6 +225,47 @@ SGEMM_API sgemm_status_t sgemm_set_wait_timeout_ns(uint64_t timeout_ns, int skip
  */
 SGEMM_API sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages, int micro_m);
 
+/*
+ * sgemm_run_3xtf32 -- the same operation, C = alpha * A * B + beta * C, on
+ * the tensor cores by split-precision emulation ("3xTF32"): each FP32 operand
+ * x is split into TF32 parts hi = tf32(x) and lo = tf32(x - hi) (round to
+ * nearest), and a * b is taken as hi_a*hi_b + hi_a*lo_b + lo_a*hi_b,
+ * accumulated in FP32.  A separate entry point: sgemm_run never takes it,
+ * because the FP32 contract excludes TF32 arithmetic
+ * ("Optimizing CUDA matmul, steps 4 to 6", section "The honest target");
+ * tensor cores are the route the pages name past FP32-core parity ("GEMM from
+ * Scratch", Module 07; "Optimizing Matrix Multiply on CUDA, Part 2", section
+ * "Looking Back").
+ *
+ * Arguments, layout, ownership and errors are those of sgemm_run; pointers
+ * need only 4-byte alignment.  A split pass writes hi and lo copies of A and
+ * of B (transposed) into a per-(device, stream) workspace of
+ * 8 * K' * (ceil(M/128)*128 + ceil(N/256)*256) bytes, K' = ceil(K/4)*4,
+ * kept until sgemm_release_workspace().
+ * Accuracy: measured within the FFMA path's bound
+ * 2 * K * 2^-24 * (|alpha| (|A||B|)ij + |beta| |Cij|) on the test
+ * distributions; no worst-case proof (the tensor core's accumulation rounding
+ * is not documented).  Products with K < 64 or M <= 16 run the FFMA kernels
+ * (the split's own error, up to about 3 * 2^-22 |a b| per product, would use
+ * up the bound of a short sum, and such shapes gain nothing from the tensor
+ * cores).  Non-finite values in A or B give NaN in the outputs they reach
+ * (hi - x is not finite); |x| at or above (2 - 2^-11) * 2^127 rounds to Inf
+ * in the split.
+ * Results are bitwise reproducible for a given shape.
+ */
+SGEMM_API sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha,
+                                          const float *A, int64_t lda, const float *B,
+                                          int64_t ldb, float beta, float *C, int64_t ldc,
+                                          void *stream);
+
+/*
+ * sgemm_set_3xtf32_kslice -- tuning hook, process-wide: the K depth of one
+ * pipeline stage of the 3xTF32 kernel, 32 (two stages of 128-byte swizzled
+ * rows, the default) or 16 (four stages of 64-byte rows).  Both compute the
+ * same products in the same order.  SGEMM_ERR_INVALID_ARG otherwise.
+ */
+SGEMM_API sgemm_status_t sgemm_set_3xtf32_kslice(int bk);
+
 /* Free every workspace and host-path buffer the library holds on all devices. */
 SGEMM_API sgemm_status_t sgemm_release_workspace(void);
 

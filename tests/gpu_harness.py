@@ -56,10 +56,10 @@ class DeviceMatrix:
 
 
 def run_gemm(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, offsets=(0, 0, 0),
-             variant=-1, splits=0, c_fill=None, bias=None, activation=0):
+             variant=-1, splits=0, c_fill=None, bias=None, activation=0, entry="sgemm_run"):
     """Run sgemm_run (sgemm_run_epilogue when a bias or an activation is
-    given) on device copies; returns (C result as M x N float32, the
-    DeviceMatrix for C)."""
+    given; sgemm_run_3xtf32 with entry="sgemm_run_3xtf32") on device copies;
+    returns (C result as M x N float32, the DeviceMatrix for C)."""
     dA = DeviceMatrix(A, M, lda, offsets[0])
     dB = DeviceMatrix(B, K, ldb, offsets[1])
     dC = DeviceMatrix(C, M, ldc, offsets[2], fill=c_fill)
@@ -67,7 +67,10 @@ def run_gemm(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, offsets=(0, 0, 0),
     sg.set_plan_override(variant, splits)
     try:
         stream = torch.cuda.current_stream().cuda_stream
-        if bias is None and activation == 0:
+        if entry == "sgemm_run_3xtf32":
+            st = sg.sgemm_run_3xtf32(M, N, K, alpha, dA.ptr, lda, dB.ptr, ldb, beta, dC.ptr, ldc,
+                                     stream)
+        elif bias is None and activation == 0:
             st = sg.sgemm_run(M, N, K, alpha, dA.ptr, lda, dB.ptr, ldb, beta, dC.ptr, ldc, stream)
         else:
             st = sg.sgemm_run_epilogue(M, N, K, alpha, dA.ptr, lda, dB.ptr, ldb, beta, dC.ptr, ldc,

@@ -72,6 +72,18 @@ def test_invalid_arguments_rejected_before_any_device_call(lib, args):
     assert st == 1, sg.status_string(st)
 
 
+@pytest.mark.parametrize("args", [dict(M=-1), dict(lda=3), dict(A=None), dict(B=4098), dict(C=None)])
+def test_3xtf32_arguments_rejected_before_any_device_call(lib, args):
+    call = dict(M=4, N=5, K=6, alpha=1.0, A=4096, lda=6, B=8192, ldb=5, beta=0.0,
+                C=16384, ldc=5)
+    call.update(args)
+    st = sg.sgemm_run_3xtf32(call["M"], call["N"], call["K"], call["alpha"], call["A"],
+                             call["lda"], call["B"], call["ldb"], call["beta"], call["C"],
+                             call["ldc"])
+    assert st == 1, sg.status_string(st)
+    assert sg.sgemm_run_3xtf32(0, 5, 6, 1.0, None, 6, None, 5, 0.0, None, 5) == 0
+
+
 @pytest.mark.parametrize("bias,activation", [(None, 2), (None, -1), (4098, 0), (4097, 1)])
 def test_epilogue_arguments_rejected_before_any_device_call(lib, bias, activation):
     st = sg.sgemm_run_epilogue(4, 5, 6, 1.0, 4096, 6, 8192, 5, 0.0, 16384, 5, bias, activation)
@@ -109,6 +121,11 @@ def test_hooks_validate(lib):
         sg.set_tile_config(3, 3, 8)
     with pytest.raises(sg.SgemmError):
         sg.set_wait_timeout_ns(0, -5)
+    for bk in (0, 8, 24, 64):
+        with pytest.raises(sg.SgemmError):
+            sg.set_3xtf32_kslice(bk)
+    sg.set_3xtf32_kslice(16)
+    sg.set_3xtf32_kslice(32)
     sg.set_plan_override(-1, 0)
     sg.set_tile_config(3, 3, 16)
     sg.set_wait_timeout_ns(0, -1)

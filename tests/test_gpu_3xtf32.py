@@ -1,0 +1,178 @@
+"""GPU parity of the 3xTF32 tensor-core entry point (sgemm_run_3xtf32) against
+the CPU oracle, through the C ABI.
+
+The variant must meet the bound of the FFMA path,
+|C_gpu - C_ref| <= 2*K*2^-24*(|alpha|(|A||B|)_ij + |beta||C_ij|), and be
+bit-exact on small-integer inputs (every TF32 split of an integer below 2^11
+has lo = 0, and the products and partial sums are exact).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import datagen
+import dense_fp32_sgemm_gb300 as sg
+import oracle
+from tests.checks import assert_within
+from tests.gpu_harness import run_gemm
+
+pytestmark = pytest.mark.gpu
+
+X3 = "sgemm_run_3xtf32"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sg.build()
+    sg.set_plan_override(-1, 0)
+    sg.set_wait_timeout_ns(0, -1)
+    sg.set_3xtf32_kslice(32)
+    yield
+    sg.set_plan_override(-1, 0)
+    sg.set_wait_timeout_ns(0, -1)
+    sg.set_3xtf32_kslice(32)
+
+
+def inputs(dist, seed, M, N, K, lda=None, ldb=None, ldc=None):
+    lda, ldb, ldc = lda or K, ldb or N, ldc or N
+    A = datagen.matrix(dist, seed, "A", M, K, ld=lda)
+    B = datagen.matrix(dist, seed, "B", K, N, ld=ldb)
+    C = datagen.matrix(dist, seed, "C", M, N, ld=ldc)
+    return A, lda, B, ldb, C, ldc
+
+
+def reference(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, rows=None):
+    ref, absprod = oracle.sgemm_ref_flat(M, N, K, alpha, A, lda, B, ldb, beta,
+                                         C if beta != 0 else None, ldc, rows=rows)
+    rows_idx = np.arange(M) if rows is None else np.asarray(rows)
+    Cm = C.reshape(M, ldc)[rows_idx, :N] if (C is not None and beta != 0) else None
+    return ref, oracle.error_bound(absprod, Cm, alpha, beta, K)
+
+
+def check(M, N, K, alpha=1.0, beta=0.0, dist="uniform", seed=3, lda=None, ldb=None, ldc=None,
+          offsets=(0, 0, 0), rows=None, exact=False):
+    A, lda, B, ldb, C, ldc = inputs(dist, seed, M, N, K, lda, ldb, ldc)
+    out, _ = run_gemm(M, N, K, alpha, beta, A, lda, B, ldb, C if beta != 0 else None, ldc,
+                      offsets=offsets, c_fill=None if beta != 0 else float("nan"), entry=X3)
+    ref, bound = reference(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, rows=rows)
+    got = out if rows is None else out[np.asarray(rows)]
+    label = f"3xTF32 {M}x{N}x{K} {dist} alpha={alpha} beta={beta}"
+    if exact:
+        np.testing.assert_array_equal(got, ref.astype(np.float32), err_msg=label)
+    else:
+        assert_within(got, ref, bound, label)
+    return out, got, ref, bound
+
+
+# Shapes above the FFMA hand-over (M > 16, K >= 64) spanning several 128 x 256
+# tiles, with ragged edges in M, N and K (K not a multiple of the 32-deep slice).
+SHAPES = [(128, 256, 64), (257, 513, 100), (1000, 1030, 333), (17, 300, 64), (640, 2304, 1000),
+          (300, 520, 200)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_small_integers_bit_exact(M, N, K):
+    check(M, N, K, 1.0, 0.0, dist="ints", exact=True)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (0.5, 2.0)])
+def test_floats_within_bound(M, N, K, alpha, beta):
+    check(M, N, K, alpha, beta, dist="uniform")
+
+
+def test_normal_inputs_within_bound():
+    check(700, 900, 1500, 1.0, 0.0, dist="normal")
+
+
+@pytest.mark.parametrize("bk", [16, 32])
+def test_k_slices_bitwise_identical(bk):
+    M, N, K = 520, 770, 700
+    A, lda, B, ldb, C, ldc = inputs("uniform", 5, M, N, K)
+    sg.set_3xtf32_kslice(32)
+    ref_out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
+    sg.set_3xtf32_kslice(bk)
+    try:
+        out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
+    finally:
+        sg.set_3xtf32_kslice(32)
+    assert np.array_equal(out.view(np.uint32), ref_out.view(np.uint32))
+    ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc)
+    assert_within(out, ref, bound, f"3xTF32 bk={bk}")
+
+
+@pytest.mark.parametrize("offsets,pad", [((1, 2, 3), (1, 3, 5)), ((0, 0, 0), (7, 1, 2))])
+def test_unaligned_pointers_and_leading_dimensions(offsets, pad):
+    M, N, K = 300, 333, 257
+    check(M, N, K, 1.5, -0.5, lda=K + pad[0], ldb=N + pad[1], ldc=N + pad[2], offsets=offsets)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 4096, 512), (300, 500, 63), (5, 7, 3)])
+def test_short_products_take_the_ffma_kernels(M, N, K):
+    # K < 64 or M <= 16: the same kernels and results as sgemm_run.
+    A, lda, B, ldb, C, ldc = inputs("uniform", 9, M, N, K)
+    out3, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc, entry=X3)
+    out1, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc)
+    assert np.array_equal(out3.view(np.uint32), out1.view(np.uint32))
+
+
+def test_bitwise_deterministic():
+    M, N, K = 600, 700, 800
+    A, lda, B, ldb, C, ldc = inputs("uniform", 4, M, N, K)
+    o1, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
+    o2, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
+    assert np.array_equal(o1.view(np.uint32), o2.view(np.uint32))
+
+
+@pytest.mark.parametrize("name,sample", [("s2_2048", 96), ("s3_4092", 40)])
+def test_workload_full_size_sampled(name, sample):
+    cfg, A, B, C = datagen.config_inputs(name)
+    M, N, K, alpha, beta = cfg["M"], cfg["N"], cfg["K"], cfg["alpha"], cfg["beta"]
+    out, _ = run_gemm(M, N, K, alpha, beta, A, K, B, N, C, N,
+                      c_fill=None if beta != 0 else float("nan"), entry=X3)
+    rng = np.random.default_rng(17)
+    rows = sorted({0, 127, 128, M - 1} | set(rng.choice(M, size=sample, replace=False).tolist()))
+    ref, bound = reference(M, N, K, alpha, beta, A, K, B, N, C, N, rows=rows)
+    assert np.isfinite(out).all()
+    assert_within(out[np.asarray(rows)], ref, bound, f"3xTF32 {name}")
+    ratio = float(np.max(np.abs(out[np.asarray(rows)] - ref) / bound))
+    print(f"3xTF32 {name}: max |err|/bound = {ratio:.3g}")
+
+
+def test_torch_binding():
+    M, N, K = 384, 512, 320
+    A = torch.from_numpy(datagen.matrix("uniform", 8, "A", M, K)).cuda().view(M, K)
+    B = torch.from_numpy(datagen.matrix("uniform", 8, "B", K, N)).cuda().view(K, N)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    sg.run_3xtf32(A, B, C)
+    torch.cuda.synchronize()
+    ref, absprod = oracle.sgemm_ref_flat(M, N, K, 1.0, A.cpu().numpy().ravel(), K,
+                                         B.cpu().numpy().ravel(), N, 0.0, None, N)
+    assert_within(C.cpu().numpy(), ref, oracle.error_bound(absprod, None, 1.0, 0.0, K), "binding")
+
+
+def test_wait_timeout_reports_and_recovers():
+    M, N, K = 512, 1024, 1024
+    A, lda, B, ldb, _, _ = inputs("uniform", 16, M, N, K)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.zeros(M * N, device="cuda")
+    stream = torch.cuda.current_stream()
+    # The load issuer stops at K slice 3, so the MMA issuer's wait for slice 3
+    # runs out after 2 ms; the kernel records the timeout, lets its MMAs
+    # finish, frees its tensor memory and returns.
+    sg.set_wait_timeout_ns(2_000_000, 3)
+    try:
+        st = sg.sgemm_run_3xtf32(M, N, K, 1.0, dA.data_ptr(), lda, dB.data_ptr(), ldb, 0.0,
+                                 dC.data_ptr(), N, stream.cuda_stream)
+        assert st == 0
+        assert sg.device_status(stream) == 5  # SGEMM_ERR_DEVICE_TIMEOUT
+    finally:
+        sg.set_wait_timeout_ns(0, -1)
+    assert sg.device_status(stream) == 0
+    out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, entry=X3)
+    ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, rows=[0, 255, 511])
+    assert_within(out[[0, 255, 511]], ref, bound, "3xTF32 after timeout")
