@@ -15,6 +15,10 @@ also carries:
                 of the same workload;
   secondary     the 4092^3 (alpha=0.5, beta=2) workload, timed the same way;
   cublas_context  the same products through cuBLAS FP32 with TF32 off (context);
+  tensor_core_3xtf32  the separate 3xTF32 entry point (sgemm_run_3xtf32) on
+                the 2048^3 and 4092^3 workloads: FP32 GFLOP/s, and its MMA
+                kernel against the TF32 tensor peak (3 TF32 products per FP32
+                product); reported apart from the FP32 metric;
   sets          the value over the first and the second half of the timed steps;
   clocks        SM clocks sampled with nvidia-smi during the timed region.
 
@@ -92,6 +96,24 @@ def algorithmic_bytes(cfg):
     """Read A and B once, read C if beta != 0, write C once (FP32)."""
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     return 4 * (M * K + K * N + M * N * (2 if cfg["beta"] != 0 else 1))
+
+
+# Nominal dense tensor rates (PFLOP/s) on GB300: TF32 1.1, BF16 2.25.  The
+# TF32 denominator is the measured BF16 rate scaled by their ratio.
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def measured_tf32_peak():
+    """TF32 tensor peak (TFLOP/s): measured BF16 x nominal TF32/BF16, else the
+    fallback BF16 figure x the same ratio."""
+    try:
+        pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return (round(float(pk["bf16_tflops"]) * TF32_PER_BF16, 1),
+                round(float(pk["bf16_tflops_sustained"]) * TF32_PER_BF16, 1),
+                "MEASURED_PEAKS.json bf16_tflops x 1.1/2.25 (nominal TF32/BF16), of measured")
+    except (OSError, KeyError, ValueError):
+        return (round(1900.0 * TF32_PER_BF16, 1), round(1700.0 * TF32_PER_BF16, 1),
+                "fallback 1.9 PFLOP/s bf16 x 1.1/2.25, of fallback")
 
 
 def measured_hbm_peak():
@@ -263,16 +285,16 @@ def gpu_arm(args, ws, rank, local):
         flush.fill_(1.0)
         torch.sum(flush, dim=0, keepdim=True, out=flush_sink)
 
-    def step(cfg, dA, dB, dC):
-        st = sg.sgemm_run(cfg["M"], cfg["N"], cfg["K"], cfg["alpha"], dA.data_ptr(), cfg["K"],
-                          dB.data_ptr(), cfg["N"], cfg["beta"], dC.data_ptr(), cfg["N"],
-                          stream.cuda_stream)
+    def step(cfg, dA, dB, dC, entry=None):
+        fn = getattr(sg, entry or args.entry)
+        st = fn(cfg["M"], cfg["N"], cfg["K"], cfg["alpha"], dA.data_ptr(), cfg["K"],
+                dB.data_ptr(), cfg["N"], cfg["beta"], dC.data_ptr(), cfg["N"], stream.cuda_stream)
         if st != 0:
-            raise RuntimeError("sgemm_run: " + sg.status_string(st))
+            raise RuntimeError(f"{entry or args.entry}: " + sg.status_string(st))
 
-    def timed(cfg, dA, dB, dC, steps, warmup, C0=None):
+    def timed(cfg, dA, dB, dC, steps, warmup, entry=None):
         for _ in range(warmup):
-            step(cfg, dA, dB, dC)
+            step(cfg, dA, dB, dC, entry)
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(steps)]
@@ -290,7 +312,7 @@ def gpu_arm(args, ws, rank, local):
             for e0, e1 in evs[b:b + HOLD_BATCH]:
                 flush_l2()
                 e0.record(stream)
-                step(cfg, dA, dB, dC)
+                step(cfg, dA, dB, dC, entry)
                 e1.record(stream)
             host_ns = (time.perf_counter() - h0) * 1e9
             hold_ns = int(min(1e9, max(hold_ns, 2 * host_ns)))
@@ -402,6 +424,9 @@ def gpu_arm(args, ws, rank, local):
     plan = sg.plan_describe(cfg["M"], cfg["N"], cfg["K"], a_addr=dA.data_ptr(),
                             b_addr=dB.data_ptr(), c_addr=dC.data_ptr(), beta=cfg["beta"])
 
+    # sgemm_run: one kernel per step; sgemm_run_3xtf32: two split kernels and
+    # the MMA kernel
+    per_step = 3 if args.entry == "sgemm_run_3xtf32" else 1
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
@@ -414,10 +439,12 @@ def gpu_arm(args, ws, rank, local):
                          "with CUDA events; steps queued in batches of 32 behind a hold kernel "
                          "so the device never waits for the host",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
-                   "plan": plan.get("variant"), "grid": int(plan.get("grid", 0))},
+                   "plan": plan.get("variant") if args.entry == "sgemm_run" else "3xtf32",
+                   "grid": int(plan.get("grid", 0)) if args.entry == "sgemm_run" else None,
+                   "entry": args.entry},
         "sets": drift,
-        "gpu_launches": args.steps + -(-args.steps // HOLD_BATCH),
-        "gpu_launches_detail": {"sgemm (inside the event pairs)": args.steps,
+        "gpu_launches": per_step * args.steps + -(-args.steps // HOLD_BATCH),
+        "gpu_launches_detail": {"sgemm (inside the event pairs)": per_step * args.steps,
                                 "hold (between batches)": -(-args.steps // HOLD_BATCH)},
         "clocks": clocks,
     }
@@ -506,6 +533,31 @@ def gpu_arm(args, ws, rank, local):
             del dAc, dBc, dCc
         result["cublas_context"] = ctx
 
+    # ---- the 3xTF32 tensor-core entry point (reported apart) ----
+    if not args.no_secondary and args.entry == "sgemm_run":
+        tf32_burst, tf32_sust, tf32_src = measured_tf32_peak()
+        x3 = []
+        for xname in ("s2_2048", "s3_4092"):
+            cfgx, _, _, _, dAx, dBx, dCx = device_inputs(xname)
+            steps_x = max(5, min(200, args.steps // 10))
+            dx = statistics.median(timed(cfgx, dAx, dBx, dCx, steps_x, args.warmup,
+                                         entry="sgemm_run_3xtf32")[0])
+            fl = flops_of(cfgx)
+            x3.append({"workload": WORKLOADS[xname], "api": "sgemm_run_3xtf32",
+                       "value": round(fl / dx / 1e9, 2), "unit": "GFLOP/s (FP32 products)",
+                       "ms_per_step": round(dx * 1e3, 4), "steps": steps_x,
+                       "vs_ffma_path": round(fl / dx / 1e12 / achieved, 3)
+                       if xname == name else None,
+                       "roofline": {"bound": "tensor",
+                                    "achieved": round(3 * fl / dx / 1e12, 1),
+                                    "peak": tf32_burst, "unit": "TFLOP/s",
+                                    "frac": round(3 * fl / dx / 1e12 / tf32_burst, 4),
+                                    "note": "3 TF32 products per FP32 product; step time "
+                                            "includes the split pass",
+                                    "peak_source": tf32_src, "sustained_peak": tf32_sust}})
+            del dAx, dBx, dCx
+        result["tensor_core_3xtf32"] = x3
+
     # ---- end to end through the host entry point ----
     pA = torch.from_numpy(A.reshape(cfg["M"], cfg["K"])).pin_memory()
     pB = torch.from_numpy(B.reshape(cfg["K"], cfg["N"])).pin_memory()
@@ -575,6 +627,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     ap.add_argument("--no-secondary", action="store_true", help="skip the 4092^3 line")
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS context timings")
+    ap.add_argument("--entry", choices=["sgemm_run", "sgemm_run_3xtf32"], default="sgemm_run",
+                    help="entry point of the timed steps (the metric is sgemm_run's; "
+                         "sgemm_run_3xtf32 is for profiler runs of that variant)")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed GEMM steps (for profiler runs)")
     args = ap.parse_args()

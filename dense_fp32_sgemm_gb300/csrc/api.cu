@@ -29,7 +29,8 @@ std::atomic<int> g_skip_loads_from{-1};
 std::atomic<int> g_fma_mode{kFmaPairMovB};
 std::atomic<int> g_stages{3};
 std::atomic<int> g_micro_m{16};
-std::atomic<int> g_x3_bk{32};
+std::atomic<int> g_x3_bk{16};
+std::atomic<int> g_x3_a_in_kernel{-1};  // -1: chosen per call
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -70,7 +71,7 @@ struct DeviceState {
     std::map<cudaStream_t, Workspace> ws;
     HostBuffers host;
     unsigned configured = 0;            // skinny configurations set up
-    unsigned x3_configured = 0;         // 3xTF32 K slices set up (bit bk / 16)
+    unsigned x3_configured = 0;         // 3xTF32 kernels set up (bit bk / 16 + 4 * a_raw)
     std::set<int> configured_tiles;     // tile configurations set up
 };
 
@@ -351,20 +352,34 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
     if (K < kX3MinK || M <= 16 || alpha == 0.0f)
         return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, none, st, *d);
     if (M > (1 << 29) || N > (1 << 29) || K > (1 << 30) ||
-        ((M + kX3BM - 1) / kX3BM) * ((N + kX3BN - 1) / kX3BN) > INT32_MAX)
+        ((M + kX3BM - 1) / kX3BM) * ((N + 127) / 128) > INT32_MAX)
         return SGEMM_ERR_INVALID_ARG;
     const int bk = g_x3_bk.load();
-    const unsigned bit = 1u << (bk / 16);
+    // A split inside the kernel pays off on large products whose A rows start
+    // on 128-byte lines (measured on GB300: 8192^3 281 against 270 TFLOP/s,
+    // 2048^3 190 against 194, 4092^3 with 16368-byte rows 233 against 246).
+    const int a_mode = g_x3_a_in_kernel.load();
+    const bool a_raw = a_mode >= 0 ? a_mode != 0
+                                   : ((lda % 32) == 0 && !(reinterpret_cast<uintptr_t>(A) & 127u) &&
+                                      (double)M * (double)N * (double)K >= 68719476736.0);
+    const unsigned bit = 1u << (bk / 16 + (a_raw ? 4 : 0));
     if (!(d->x3_configured & bit)) {
-        if (x3_configure(bk) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        if (x3_configure(bk, a_raw) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         d->x3_configured |= bit;
     }
+    const int bn = x3_tile_width(M, N, d->num_sms);
     const int64_t Mp = (M + kX3BM - 1) / kX3BM * kX3BM;
-    const int64_t Np = (N + kX3BN - 1) / kX3BN * kX3BN;
-    const int64_t Kp = (K + 3) / 4 * 4;
-    const size_t a_floats = (size_t)(2 * Mp * Kp), b_floats = (size_t)(2 * Np * Kp);
+    const int64_t Np = (N + bn - 1) / bn * bn;
+    const int64_t Kp = (K + 31) / 32 * 32;  // rows of whole 128-byte lines
+    // Workspace: [A hi; A lo] (split pass only) | [B hi^T; B lo^T] | A copied
+    // to 16-byte-aligned rows (A split in the kernel, when the TMA cannot
+    // map A itself).
+    const bool a_pack = a_raw && ((reinterpret_cast<uintptr_t>(A) & 15u) || (lda & 3));
+    const int64_t ld_pack = (K + 3) / 4 * 4;
+    const size_t a_floats = a_raw ? 0 : (size_t)(2 * Mp * Kp), b_floats = (size_t)(2 * Np * Kp);
+    const size_t p_floats = a_pack ? (size_t)(M * ld_pack) : 0;
     Workspace &w = d->ws[st];
-    const size_t bytes = (a_floats + b_floats) * sizeof(float);
+    const size_t bytes = (a_floats + b_floats + p_floats) * sizeof(float);
     if (w.split_bytes < bytes) {
         if (w.split) cudaFree(w.split);
         w.split = nullptr;
@@ -372,19 +387,30 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
         if (cudaMalloc(&w.split, bytes) != cudaSuccess) return SGEMM_ERR_ALLOC;
         w.split_bytes = bytes;
     }
-    float *sa = w.split, *sb = w.split + a_floats;  // a_floats is a multiple of 256
-    if (launch_x3_split(A, lda, (int)M, B, ldb, (int)N, (int)K, sa, (int)Mp, sb, (int)Np,
-                        (int)Kp, d->num_sms, st) != cudaSuccess)
+    // a_floats and b_floats are multiples of 64 floats (256 bytes)
+    float *sa = w.split, *sb = w.split + a_floats, *pa = sb + b_floats;
+    const float *a_map = A;
+    int64_t lda_map = lda;
+    if (a_pack) {
+        const PackJob job{A, lda, (int)M, (int)K, pa, ld_pack};
+        if (launch_pack(&job, 1, st) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        a_map = pa;
+        lda_map = ld_pack;
+    }
+    if (launch_x3_split(a_raw ? nullptr : A, lda, (int)M, B, ldb, (int)N, (int)K, sa, (int)Mp, sb,
+                        (int)Np, (int)Kp, d->num_sms, st) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     const CUtensorMapSwizzle sw = bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUtensorMap mapA, mapB;
-    s = encode_2d(&mapA, sa, 2 * Mp, Kp, Kp, bk, kX3BM, sw);
+    s = a_raw ? encode_2d(&mapA, a_map, M, K, lda_map, bk, kX3BM, sw)
+              : encode_2d(&mapA, sa, 2 * Mp, Kp, Kp, bk, kX3BM, sw);
     if (s != SGEMM_OK) return s;
-    s = encode_2d(&mapB, sb, 2 * Np, Kp, Kp, bk, kX3BN, sw);
+    s = encode_2d(&mapB, sb, 2 * Np, Kp, Kp, bk, bn, sw);
     if (s != SGEMM_OK) return s;
     X3Params p;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
-    p.tiles_m = (int)(Mp / kX3BM); p.tiles_n = (int)(Np / kX3BN);
+    p.bn = bn;
+    p.tiles_m = (int)(Mp / kX3BM); p.tiles_n = (int)(Np / bn);
     p.kt_total = (int)((K + bk - 1) / bk);
     p.a_lo_row = (int)Mp; p.b_lo_row = (int)Np;
     p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
@@ -392,7 +418,7 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
     const unsigned long long to = g_timeout_ns.load();
     p.timeout_ns = to ? to : kDefaultTimeoutNs;
     p.skip_loads_from = g_skip_loads_from.load();
-    return status_from(launch_x3(bk, mapA, mapB, p, st));
+    return status_from(launch_x3(bk, a_raw, mapA, mapB, p, st));
 }
 
 // Host <-> device copy of `rows` rows of `width` floats; one contiguous copy
@@ -606,9 +632,11 @@ sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages, int micro_m) {
     return SGEMM_OK;
 }
 
-sgemm_status_t sgemm_set_3xtf32_kslice(int bk) {
-    if (bk != 16 && bk != 32) return SGEMM_ERR_INVALID_ARG;
+sgemm_status_t sgemm_set_3xtf32_config(int bk, int a_in_kernel) {
+    if ((bk != 16 && bk != 32) || a_in_kernel < -1 || a_in_kernel > 1)
+        return SGEMM_ERR_INVALID_ARG;
     g_x3_bk.store(bk);
+    g_x3_a_in_kernel.store(a_in_kernel);
     return SGEMM_OK;
 }
 

@@ -20,12 +20,12 @@
 // accumulator, so the result differs from the FP32 one only by the dropped
 // terms and the accumulation order.
 //
-// Structure (one 128 x 256 tile of C per CTA, 128 threads):
+// Structure (one 128 x bn tile of C per CTA, bn <= 256, 128 threads):
 //   split pass   A -> [A_hi; A_lo] (K-major rows), B -> [B_hi^T; B_lo^T]
 //                (transposed to K-major), zero padded; an HBM-bound pass.
 //   warp 0       one thread issues the TMA loads of the four operand tiles
 //                of each K slice into a ring of swizzled shared-memory stages.
-//   warp 1       one thread issues tcgen05.mma (M 128, N 256, K 8) three
+//   warp 1       one thread issues tcgen05.mma (M 128, N bn, K 8) three
 //                times per K step, accumulating in tensor memory, and
 //                releases each stage with tcgen05.commit.
 //   warp 2       allocates and frees the 256 tensor-memory columns.
@@ -50,7 +50,7 @@ struct X3Cfg {
     static_assert(BK == 32 || BK == 16, "K slice of 32 (128-byte rows) or 16 (64-byte rows)");
     static constexpr int kRowBytes = BK * 4;                  // one swizzled row of K
     static constexpr uint32_t kA = BM * BK * 4;               // one A part (hi or lo)
-    static constexpr uint32_t kB = BN * BK * 4;               // one B part
+    static constexpr uint32_t kB = BN * BK * 4;               // one B part (room for N 256)
     static constexpr uint32_t kStage = 2 * kA + 2 * kB;
     static constexpr int kStages = BK == 32 ? 2 : 4;
     static constexpr uint32_t kAlign = 8 * kRowBytes;         // one swizzle atom
@@ -77,17 +77,19 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
 
 // Instruction descriptor, kind::tf32: FP32 accumulator (bits 4-5 = 1), A and
 // B TF32 (bits 7-9, 10-12 = 2), both K-major (bits 15, 16 = 0), N >> 3 in
-// bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+// bits 17-22, M >> 4 in bits 24-28.  N is a multiple of 16 in [16, 256].
+__host__ __device__ constexpr uint32_t make_idesc(int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(BM >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b,
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -227,17 +229,27 @@ __global__ void __launch_bounds__(256) x3_split_cols_kernel(const float *__restr
 // ---------------------------------------------------------------------------
 // MMA kernel.
 // ---------------------------------------------------------------------------
-template <int BK>
+// Makes this thread's shared-memory writes visible to the tensor cores'
+// (async proxy) reads that a later barrier orders after them.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ARAW: the TMA brings A's FP32 tile into the hi slot and warps 2 and 3 split
+// it in place (hi there, lo into the lo slot) before the MMAs of that stage;
+// otherwise both parts come from the split pass.
+template <int BK, bool ARAW>
 __global__ void __launch_bounds__(THREADS, 1)
     sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap mapA,
                         const __grid_constant__ CUtensorMap mapB, const X3Params p) {
     using L = X3Cfg<BK>;
     constexpr int S = L::kStages;
+    constexpr int kConvThreads = 64;  // warps 2 and 3
     extern __shared__ unsigned char x3_smem_raw[];
-    __shared__ uint64_t full[S], empty[S], accum_bar;
+    __shared__ uint64_t full[S], empty[S], conv[S], accum_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_abort;
-    __shared__ int s_issued, s_consumed, s_accum_ok;
+    __shared__ int s_issued, s_consumed, s_accum_ok, s_converted;
 
     // Stages start on a 1024-byte boundary of the shared window (the
     // swizzle pattern is taken from address bits).
@@ -247,7 +259,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tm = blockIdx.x % p.tiles_m, tn = blockIdx.x / p.tiles_m;
-    const int m0 = tm * BM, n0 = tn * BN;
+    const int bn = p.bn;
+    const int m0 = tm * BM, n0 = tn * bn;
 
     if (tid == 0) {
         prefetch_tensormap(&mapA);
@@ -256,12 +269,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&conv[s], kConvThreads);
         }
         mbar_init(&accum_bar, 1);
         s_abort = 0;
         s_issued = 0;
         s_consumed = 0;
         s_accum_ok = 0;
+        s_converted = 0;
         fence_barrier_init();
     }
     if (warp == 2) tmem_alloc(&tmem_slot);
@@ -283,10 +298,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 unsigned char *st = smem + (size_t)s * L::kStage;
-                mbar_arrive_expect_tx(&full[s], L::kStage);
+                mbar_arrive_expect_tx(&full[s],
+                                      (ARAW ? 1 : 2) * L::kA + 2 * (uint32_t)bn * BK * 4);
                 const int k = kt * BK;
                 tma_load_2d(st, &mapA, &full[s], k, m0);
-                tma_load_2d(st + L::kA, &mapA, &full[s], k, p.a_lo_row + m0);
+                if (!ARAW) tma_load_2d(st + L::kA, &mapA, &full[s], k, p.a_lo_row + m0);
                 tma_load_2d(st + 2 * L::kA, &mapB, &full[s], k, n0);
                 tma_load_2d(st + 2 * L::kA + L::kB, &mapB, &full[s], k, p.b_lo_row + n0);
             }
@@ -300,7 +316,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             int kt = 0;
             for (; kt < p.kt_total; ++kt) {
                 const int s = kt % S;
-                if (!mbar_wait_bounded(&full[s], (kt / S) & 1, p.timeout_ns)) {
+                if (!mbar_wait_bounded(ARAW ? &conv[s] : &full[s], (kt / S) & 1, p.timeout_ns)) {
                     atomicOr(p.err, kErrWaitTimeout);
                     s_abort = 1;
                     break;
@@ -308,19 +324,51 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t a_hi = sbase + s * L::kStage, a_lo = a_hi + L::kA;
                 const uint32_t b_hi = a_hi + 2 * L::kA, b_lo = b_hi + L::kB;
+                const uint32_t idesc = make_idesc(bn);
 #pragma unroll
                 for (int kk = 0; kk < BK / 8; ++kk) {
                     const uint32_t off = kk * 32;  // 8 TF32 values along K
-                    mma_tf32(tmem, smem_desc<BK>(a_lo + off), smem_desc<BK>(b_hi + off),
+                    mma_tf32(tmem, smem_desc<BK>(a_lo + off), smem_desc<BK>(b_hi + off), idesc,
                              (kt | kk) != 0);
-                    mma_tf32(tmem, smem_desc<BK>(a_hi + off), smem_desc<BK>(b_lo + off), 1);
-                    mma_tf32(tmem, smem_desc<BK>(a_hi + off), smem_desc<BK>(b_hi + off), 1);
+                    mma_tf32(tmem, smem_desc<BK>(a_hi + off), smem_desc<BK>(b_lo + off), idesc, 1);
+                    mma_tf32(tmem, smem_desc<BK>(a_hi + off), smem_desc<BK>(b_hi + off), idesc, 1);
                 }
                 mma_commit(&empty[s]);  // stage s is free once these MMAs are done
             }
             s_consumed = kt;
             mma_commit(&accum_bar);
         }
+        __syncwarp();
+    } else if (ARAW) {
+        // Warps 2 and 3: split each landed A tile in place.  The conversion
+        // is elementwise, so the swizzled positions the TMA chose are kept.
+        const int c = tid - 64;
+        int kt = 0;
+        for (; kt < p.kt_total; ++kt) {
+            const int s = kt % S;
+            if (!mbar_wait_bounded(&full[s], (kt / S) & 1, p.timeout_ns)) {
+                atomicOr(p.err, kErrWaitTimeout);
+                s_abort = 1;
+                break;
+            }
+            float *a_hi = reinterpret_cast<float *>(smem + (size_t)s * L::kStage);
+            float *a_lo = a_hi + L::kA / 4;
+#pragma unroll
+            for (int i = 0; i < (int)(L::kA / 16) / kConvThreads; ++i) {
+                const int off = (i * kConvThreads + c) * 4;
+                const float4 x = ld_shared_f4(a_hi + off);
+                float4 h, l;
+                split_tf32(x.x, h.x, l.x);
+                split_tf32(x.y, h.y, l.y);
+                split_tf32(x.z, h.z, l.z);
+                split_tf32(x.w, h.w, l.w);
+                st_shared_f4(a_hi + off, h);
+                st_shared_f4(a_lo + off, l);
+            }
+            fence_proxy_async_shared();
+            mbar_arrive(&conv[s]);
+        }
+        if (lane == 0) atomicMax(&s_converted, kt);
         __syncwarp();
     }
     __syncthreads();
@@ -341,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         float *stage = reinterpret_cast<float *>(smem) + warp * (32 * 33);
         const uint32_t t_warp = tmem + ((uint32_t)(warp * 32) << 16);
         const int row0 = m0 + warp * 32;
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c * 32 < bn; ++c) {
             if (n0 + c * 32 >= p.N) break;  // uniform over the warp
             uint32_t r[32];
             tmem_ld32(t_warp + c * 32, r);
@@ -349,7 +397,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = __uint_as_float(r[j]);
             __syncwarp();
             const int n = n0 + c * 32 + lane;
-            if (n < p.N) {
+            if (n < p.N && c * 32 + lane < bn) {
 #pragma unroll 4
                 for (int i = 0; i < 32; ++i) {
                     const int m = row0 + i;
@@ -369,6 +417,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // stage-release arrivals of the last commits, and (after a timeout)
         // loads that were issued but never consumed.
         const int consumed = s_consumed, issued = s_issued;
+        // loads whose arrival someone waited for: by the converters (ARAW)
+        // or by the MMA issuer
+        const int landed = ARAW ? s_converted : consumed;
         for (int s = 0; s < S && s < consumed; ++s) {
             const int uses = (consumed - s + S - 1) / S;  // commits made to empty[s]
             if (!mbar_wait_bounded(&empty[s], (uses - 1) & 1, 1000000000ull)) {
@@ -376,7 +427,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
         }
-        for (int j = consumed; j < issued; ++j) {
+        for (int j = landed; j < issued; ++j) {
             if (!mbar_wait_bounded(&full[j % S], (j / S) & 1, 1000000000ull)) {
                 atomicOr(p.err, kErrDrainTimeout);
                 break;
@@ -397,39 +448,50 @@ int x3_stages(int bk) { return bk == 16 ? X3Cfg<16>::kStages : X3Cfg<32>::kStage
 
 size_t x3_smem_bytes(int bk) { return bk == 16 ? X3Cfg<16>::kSmem : X3Cfg<32>::kSmem; }
 
-cudaError_t x3_configure(int bk) {
-    if (bk == 16)
-        return cudaFuncSetAttribute(sgemm_3xtf32_kernel<16>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)X3Cfg<16>::kSmem);
-    if (bk == 32)
-        return cudaFuncSetAttribute(sgemm_3xtf32_kernel<32>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)X3Cfg<32>::kSmem);
+namespace {
+template <int BK, bool ARAW>
+cudaError_t x3_configure_one() {
+    return cudaFuncSetAttribute(sgemm_3xtf32_kernel<BK, ARAW>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)X3Cfg<BK>::kSmem);
+}
+template <int BK, bool ARAW>
+cudaError_t x3_launch_one(const CUtensorMap &mapA, const CUtensorMap &mapB, const X3Params &p,
+                          cudaStream_t stream) {
+    sgemm_3xtf32_kernel<BK, ARAW><<<p.tiles_m * p.tiles_n, THREADS, X3Cfg<BK>::kSmem, stream>>>(
+        mapA, mapB, p);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t x3_configure(int bk, bool a_raw) {
+    if (bk == 16) return a_raw ? x3_configure_one<16, true>() : x3_configure_one<16, false>();
+    if (bk == 32) return a_raw ? x3_configure_one<32, true>() : x3_configure_one<32, false>();
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_x3(int bk, const CUtensorMap &mapA, const CUtensorMap &mapB,
+cudaError_t launch_x3(int bk, bool a_raw, const CUtensorMap &mapA, const CUtensorMap &mapB,
                       const X3Params &p, cudaStream_t stream) {
-    const int grid = p.tiles_m * p.tiles_n;
     if (bk == 16)
-        sgemm_3xtf32_kernel<16><<<grid, THREADS, X3Cfg<16>::kSmem, stream>>>(mapA, mapB, p);
-    else if (bk == 32)
-        sgemm_3xtf32_kernel<32><<<grid, THREADS, X3Cfg<32>::kSmem, stream>>>(mapA, mapB, p);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+        return a_raw ? x3_launch_one<16, true>(mapA, mapB, p, stream)
+                     : x3_launch_one<16, false>(mapA, mapB, p, stream);
+    if (bk == 32)
+        return a_raw ? x3_launch_one<32, true>(mapA, mapB, p, stream)
+                     : x3_launch_one<32, false>(mapA, mapB, p, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_x3_split(const float *A, long long lda, int M, const float *B, long long ldb,
                             int N, int K, float *splitA, int Mp, float *splitB, int Np, int Kp,
                             int num_sms, cudaStream_t stream) {
-    const long long quads = (long long)Mp * (Kp / 4);
-    const long long blocks = std::min<long long>((quads + 255) / 256, (long long)num_sms * 8);
-    x3_split_rows_kernel<<<(int)std::max<long long>(blocks, 1), 256, 0, stream>>>(
-        A, lda, M, K, splitA, Mp, Kp);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (A) {
+        const long long quads = (long long)Mp * (Kp / 4);
+        const long long blocks = std::min<long long>((quads + 255) / 256, (long long)num_sms * 8);
+        x3_split_rows_kernel<<<(int)std::max<long long>(blocks, 1), 256, 0, stream>>>(
+            A, lda, M, K, splitA, Mp, Kp);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const long long tiles = (long long)((Kp + 31) / 32) * ((Np + 31) / 32);
     const int g = (int)std::min<long long>(tiles, (long long)num_sms * 16);
     x3_split_cols_kernel<<<g, 256, 0, stream>>>(B, ldb, K, N, splitB, Np, Kp);

@@ -238,10 +238,13 @@ SGEMM_API sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages, int mic
  * "Looking Back").
  *
  * Arguments, layout, ownership and errors are those of sgemm_run; pointers
- * need only 4-byte alignment.  A split pass writes hi and lo copies of A and
- * of B (transposed) into a per-(device, stream) workspace of
- * 8 * K' * (ceil(M/128)*128 + ceil(N/256)*256) bytes, K' = ceil(K/4)*4,
- * kept until sgemm_release_workspace().
+ * need only 4-byte alignment.  A split pass writes hi and lo copies of B
+ * (transposed to K-major) into a per-(device, stream) workspace of
+ * 8 * K' * ceil(N/w)*w bytes, K' = ceil(K/32)*32 and w the tile width (128 to
+ * 256) chosen for the shape; A is split tile by tile inside the kernel (A not
+ * 16-byte aligned, or lda not a multiple of 4, is first copied to aligned
+ * rows in the same workspace: 4 * M * ceil(K/4)*4 more bytes).  The
+ * workspace is kept until sgemm_release_workspace().
  * Accuracy: measured within the FFMA path's bound
  * 2 * K * 2^-24 * (|alpha| (|A||B|)ij + |beta| |Cij|) on the test
  * distributions; no worst-case proof (the tensor core's accumulation rounding
@@ -259,12 +262,17 @@ SGEMM_API sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float
                                           void *stream);
 
 /*
- * sgemm_set_3xtf32_kslice -- tuning hook, process-wide: the K depth of one
- * pipeline stage of the 3xTF32 kernel, 32 (two stages of 128-byte swizzled
- * rows, the default) or 16 (four stages of 64-byte rows).  Both compute the
- * same products in the same order.  SGEMM_ERR_INVALID_ARG otherwise.
+ * sgemm_set_3xtf32_config -- tuning hook, process-wide, for the 3xTF32 kernel.
+ * bk: the K depth of one pipeline stage, 16 (four stages of 64-byte swizzled
+ *   rows, the default) or 32 (two stages of 128-byte rows).
+ * a_in_kernel: 1 = the kernel loads A itself and splits each A tile in
+ *   shared memory; 0 = a split pass writes A's hi and lo parts first;
+ *   -1 (default) = 1 when M*N*K >= 2^36 and A's rows start on 128-byte
+ *   lines (A 128-byte aligned, lda a multiple of 32), else 0.
+ * All four forms compute the same products in the same order (bitwise equal
+ * results).  SGEMM_ERR_INVALID_ARG for other values.
  */
-SGEMM_API sgemm_status_t sgemm_set_3xtf32_kslice(int bk);
+SGEMM_API sgemm_status_t sgemm_set_3xtf32_config(int bk, int a_in_kernel);
 
 /* Free every workspace and host-path buffer the library holds on all devices. */
 SGEMM_API sgemm_status_t sgemm_release_workspace(void);

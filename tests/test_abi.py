@@ -123,9 +123,11 @@ def test_hooks_validate(lib):
         sg.set_wait_timeout_ns(0, -5)
     for bk in (0, 8, 24, 64):
         with pytest.raises(sg.SgemmError):
-            sg.set_3xtf32_kslice(bk)
-    sg.set_3xtf32_kslice(16)
-    sg.set_3xtf32_kslice(32)
+            sg.set_3xtf32_config(bk, True)
+    assert lib.sgemm_set_3xtf32_config(16, 2) == 1
+    assert lib.sgemm_set_3xtf32_config(16, -2) == 1
+    sg.set_3xtf32_config(32, False)
+    sg.set_3xtf32_config(16, None)
     sg.set_plan_override(-1, 0)
     sg.set_tile_config(3, 3, 16)
     sg.set_wait_timeout_ns(0, -1)

@@ -29,11 +29,11 @@ def gpu():
     sg.build()
     sg.set_plan_override(-1, 0)
     sg.set_wait_timeout_ns(0, -1)
-    sg.set_3xtf32_kslice(32)
+    sg.set_3xtf32_config(16, None)
     yield
     sg.set_plan_override(-1, 0)
     sg.set_wait_timeout_ns(0, -1)
-    sg.set_3xtf32_kslice(32)
+    sg.set_3xtf32_config(16, None)
 
 
 def inputs(dist, seed, M, N, K, lda=None, ldb=None, ldc=None):
@@ -88,26 +88,45 @@ def test_normal_inputs_within_bound():
     check(700, 900, 1500, 1.0, 0.0, dist="normal")
 
 
-@pytest.mark.parametrize("bk", [16, 32])
-def test_k_slices_bitwise_identical(bk):
+@pytest.mark.parametrize("bk,a_in_kernel", [(16, False), (32, True), (32, False), (16, None)])
+def test_kernel_forms_bitwise_identical(bk, a_in_kernel):
+    # Same split, same products, same order: the K depth of a stage and where
+    # A is split do not change a bit of the result.
     M, N, K = 520, 770, 700
     A, lda, B, ldb, C, ldc = inputs("uniform", 5, M, N, K)
-    sg.set_3xtf32_kslice(32)
+    sg.set_3xtf32_config(16, True)
     ref_out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
-    sg.set_3xtf32_kslice(bk)
+    sg.set_3xtf32_config(bk, a_in_kernel)
     try:
         out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
     finally:
-        sg.set_3xtf32_kslice(32)
+        sg.set_3xtf32_config(16, None)
     assert np.array_equal(out.view(np.uint32), ref_out.view(np.uint32))
     ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc)
-    assert_within(out, ref, bound, f"3xTF32 bk={bk}")
+    assert_within(out, ref, bound, f"3xTF32 bk={bk} a_in_kernel={a_in_kernel}")
 
 
-@pytest.mark.parametrize("offsets,pad", [((1, 2, 3), (1, 3, 5)), ((0, 0, 0), (7, 1, 2))])
-def test_unaligned_pointers_and_leading_dimensions(offsets, pad):
+@pytest.mark.parametrize("bk,a_in_kernel", [(16, False), (16, True), (32, True)])
+def test_timeout_in_other_forms(bk, a_in_kernel):
+    sg.set_3xtf32_config(bk, a_in_kernel)
+    try:
+        test_wait_timeout_reports_and_recovers()
+    finally:
+        sg.set_3xtf32_config(16, None)
+
+
+@pytest.mark.parametrize("a_in_kernel", [True, False])
+@pytest.mark.parametrize("offsets,pad", [((1, 2, 3), (1, 3, 5)), ((0, 0, 0), (7, 1, 2)),
+                                         ((4, 0, 0), (3, 0, 0))])
+def test_unaligned_pointers_and_leading_dimensions(offsets, pad, a_in_kernel):
+    # A that the TMA cannot map is copied to aligned rows when the kernel
+    # splits it; the split pass reads any alignment.
     M, N, K = 300, 333, 257
-    check(M, N, K, 1.5, -0.5, lda=K + pad[0], ldb=N + pad[1], ldc=N + pad[2], offsets=offsets)
+    sg.set_3xtf32_config(16, a_in_kernel)
+    try:
+        check(M, N, K, 1.5, -0.5, lda=K + pad[0], ldb=N + pad[1], ldc=N + pad[2], offsets=offsets)
+    finally:
+        sg.set_3xtf32_config(16, None)
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 512), (300, 500, 63), (5, 7, 3)])
