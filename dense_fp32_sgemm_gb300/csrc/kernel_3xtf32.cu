@@ -166,64 +166,97 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
 // Split pass.
 // ---------------------------------------------------------------------------
 
-// A (rows x cols, leading dimension ldx, any 4-byte alignment) -> out, rows
-// [0, rows_p) the hi parts and [rows_p, 2 rows_p) the lo parts, each row
-// cols_p floats (a multiple of 4), zero outside A.
-__global__ void __launch_bounds__(256) x3_split_rows_kernel(const float *__restrict__ X,
-                                                            long long ldx, int rows, int cols,
-                                                            float *__restrict__ out, int rows_p,
-                                                            int cols_p) {
-    const int q_row = cols_p / 4;
-    const long long total = (long long)rows_p * q_row;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
+struct SplitJob {
+    const float *A;   // M x K, lda (null: A is split inside the MMA kernel)
+    long long lda;
+    int M, Mp;
+    int a_vec4;       // A 16-byte aligned and lda a multiple of 4
+    const float *B;   // K x N, ldb
+    long long ldb;
+    int N, Np;
+    int K, Kp;
+    float *outA, *outB;
+    int a_blocks;     // blocks [0, a_blocks) split A; the rest split B
+};
+
+// A -> outA: rows [0, Mp) the hi parts and [Mp, 2 Mp) the lo parts, each row
+// Kp floats (a multiple of 32), zero outside A.
+__device__ __forceinline__ void split_a(const SplitJob &j, int block, int nblocks) {
+    const int q_row = j.Kp / 4;
+    const long long total = (long long)j.Mp * q_row;
+    for (long long i = block * 256LL + threadIdx.x; i < total; i += nblocks * 256LL) {
         const int r = (int)(i / q_row), c = (int)(i % q_row) * 4;
-        float v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            v[j] = (r < rows && c + j < cols) ? __ldg(X + (long long)r * ldx + c + j) : 0.0f;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < j.M) {
+            const float *row = j.A + (long long)r * j.lda;
+            if (j.a_vec4 && c + 3 < j.K) {
+                x = __ldg(reinterpret_cast<const float4 *>(row + c));
+            } else {
+                if (c < j.K) x.x = __ldg(row + c);
+                if (c + 1 < j.K) x.y = __ldg(row + c + 1);
+                if (c + 2 < j.K) x.z = __ldg(row + c + 2);
+                if (c + 3 < j.K) x.w = __ldg(row + c + 3);
+            }
+        }
         float4 h, l;
-        split_tf32(v[0], h.x, l.x);
-        split_tf32(v[1], h.y, l.y);
-        split_tf32(v[2], h.z, l.z);
-        split_tf32(v[3], h.w, l.w);
-        *reinterpret_cast<float4 *>(out + (size_t)r * cols_p + c) = h;
-        *reinterpret_cast<float4 *>(out + ((size_t)rows_p + r) * cols_p + c) = l;
+        split_tf32(x.x, h.x, l.x);
+        split_tf32(x.y, h.y, l.y);
+        split_tf32(x.z, h.z, l.z);
+        split_tf32(x.w, h.w, l.w);
+        *reinterpret_cast<float4 *>(j.outA + (size_t)r * j.Kp + c) = h;
+        *reinterpret_cast<float4 *>(j.outA + ((size_t)j.Mp + r) * j.Kp + c) = l;
     }
 }
 
-// B (k_rows x n_cols, leading dimension ldb) -> out transposed: row n of the
-// hi part holds column n of B's hi values over k; lo rows start at n_p.  Row
-// length k_p (a multiple of 4); zero outside B.  32 x 32 tiles through
-// shared memory so that reads and writes both run along rows; the grid
-// strides over the tiles (k fastest).
-__global__ void __launch_bounds__(256) x3_split_cols_kernel(const float *__restrict__ B,
-                                                            long long ldb, int k_rows,
-                                                            int n_cols, float *__restrict__ out,
-                                                            int n_p, int k_p) {
-    __shared__ float t[32][33];
+// B -> outB transposed: row n of the hi part holds column n of B's hi values
+// over k; lo rows start at Np.  Rows of Kp floats, zero outside B.  64 x 64
+// tiles through shared memory (k fastest over the grid), so that reads run
+// along B's rows and writes along the output's.
+__device__ __forceinline__ void split_b(const SplitJob &j, int block, int nblocks,
+                                        float (*t)[65]) {
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-    const long long k_tiles = (k_p + 31) / 32, tiles = k_tiles * ((n_p + 31) / 32);
-    for (long long b = blockIdx.x; b < tiles; b += gridDim.x) {
-        const int k0 = (int)(b % k_tiles) * 32, n0 = (int)(b / k_tiles) * 32;
+    const long long k_tiles = (j.Kp + 63) / 64, tiles = k_tiles * ((j.Np + 63) / 64);
+    for (long long b = block; b < tiles; b += nblocks) {
+        const int k0 = (int)(b % k_tiles) * 64, n0 = (int)(b / k_tiles) * 64;
 #pragma unroll
-        for (int r = ty; r < 32; r += 8) {
-            const int k = k0 + r, n = n0 + tx;
-            t[r][tx] = (k < k_rows && n < n_cols) ? __ldg(B + (long long)k * ldb + n) : 0.0f;
+        for (int r = ty; r < 64; r += 8) {
+            const int k = k0 + r;
+            const float *row = j.B + (long long)k * j.ldb;
+            const bool kin = k < j.K;
+            t[r][tx] = (kin && n0 + tx < j.N) ? __ldg(row + n0 + tx) : 0.0f;
+            t[r][tx + 32] = (kin && n0 + tx + 32 < j.N) ? __ldg(row + n0 + tx + 32) : 0.0f;
         }
         __syncthreads();
 #pragma unroll
-        for (int r = ty; r < 32; r += 8) {
-            const int n = n0 + r, k = k0 + tx;
-            if (n < n_p && k < k_p) {
+        for (int r = ty; r < 64; r += 8) {
+            const int n = n0 + r;
+            if (n < j.Np) {
+                float *hi = j.outB + (size_t)n * j.Kp, *lo = j.outB + ((size_t)j.Np + n) * j.Kp;
                 float h, l;
-                split_tf32(t[tx][r], h, l);
-                out[(size_t)n * k_p + k] = h;
-                out[((size_t)n_p + n) * k_p + k] = l;
+                if (k0 + tx < j.Kp) {
+                    split_tf32(t[tx][r], h, l);
+                    hi[k0 + tx] = h;
+                    lo[k0 + tx] = l;
+                }
+                if (k0 + tx + 32 < j.Kp) {
+                    split_tf32(t[tx + 32][r], h, l);
+                    hi[k0 + tx + 32] = h;
+                    lo[k0 + tx + 32] = l;
+                }
             }
         }
         __syncthreads();
     }
+}
+
+// One launch for both operands: the A blocks and the B blocks run side by
+// side.
+__global__ void __launch_bounds__(256) x3_split_kernel(const SplitJob j) {
+    __shared__ float t[64][65];
+    if ((int)blockIdx.x < j.a_blocks)
+        split_a(j, blockIdx.x, j.a_blocks);
+    else
+        split_b(j, blockIdx.x - j.a_blocks, gridDim.x - j.a_blocks, t);
 }
 
 // ---------------------------------------------------------------------------
@@ -484,17 +517,21 @@ cudaError_t launch_x3(int bk, bool a_raw, const CUtensorMap &mapA, const CUtenso
 cudaError_t launch_x3_split(const float *A, long long lda, int M, const float *B, long long ldb,
                             int N, int K, float *splitA, int Mp, float *splitB, int Np, int Kp,
                             int num_sms, cudaStream_t stream) {
-    if (A) {
-        const long long quads = (long long)Mp * (Kp / 4);
-        const long long blocks = std::min<long long>((quads + 255) / 256, (long long)num_sms * 8);
-        x3_split_rows_kernel<<<(int)std::max<long long>(blocks, 1), 256, 0, stream>>>(
-            A, lda, M, K, splitA, Mp, Kp);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    const long long tiles = (long long)((Kp + 31) / 32) * ((Np + 31) / 32);
-    const int g = (int)std::min<long long>(tiles, (long long)num_sms * 16);
-    x3_split_cols_kernel<<<g, 256, 0, stream>>>(B, ldb, K, N, splitB, Np, Kp);
+    SplitJob j;
+    j.A = A; j.lda = lda; j.M = M; j.Mp = Mp;
+    j.a_vec4 = A && !(reinterpret_cast<uintptr_t>(A) & 15u) && !(lda & 3);
+    j.B = B; j.ldb = ldb; j.N = N; j.Np = Np; j.K = K; j.Kp = Kp;
+    j.outA = splitA; j.outB = splitB;
+    // Blocks in proportion to the bytes each side moves (the same per
+    // element), 16 per SM in all.
+    const long long a_elems = A ? (long long)Mp * Kp : 0, b_elems = (long long)Np * Kp;
+    const long long total_blocks = (long long)num_sms * 16;
+    long long a_blocks = A ? std::max<long long>(1, total_blocks * a_elems / (a_elems + b_elems)) : 0;
+    a_blocks = std::min<long long>(a_blocks, (a_elems / 4 + 255) / 256);
+    const long long b_tiles = (long long)((Kp + 63) / 64) * ((Np + 63) / 64);
+    const long long b_blocks = std::max<long long>(1, std::min(total_blocks - a_blocks, b_tiles));
+    j.a_blocks = (int)a_blocks;
+    x3_split_kernel<<<(int)(a_blocks + b_blocks), 256, 0, stream>>>(j);
     return cudaGetLastError();
 }
 
