@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
 SOURCES = ["api.cu", "plan.cpp", "kernel_tile.cu", "kernel_skinny.cu", "kernel_generic.cu",
            "probes.cu", "noalloc.cu", "kernel_3xtf32.cu"]
-HEADERS = ["device_common.cuh", "kernels.h", "plan.h"]
+HEADERS = ["device_common.cuh", "kernels.h", "kernels_3xtf32.h", "plan.h"]
 PUBLIC_HEADERS = ["sgemm.h", "sgemm_probe.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

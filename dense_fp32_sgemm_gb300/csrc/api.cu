@@ -15,6 +15,7 @@
 #include "../../include/sgemm.h"
 #include "../../include/sgemm_probe.h"
 #include "kernels.h"
+#include "kernels_3xtf32.h"
 #include "plan.h"
 
 namespace sgemm {
@@ -418,7 +419,14 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
     const unsigned long long to = g_timeout_ns.load();
     p.timeout_ns = to ? to : kDefaultTimeoutNs;
     p.skip_loads_from = g_skip_loads_from.load();
-    return status_from(launch_x3(bk, a_raw, mapA, mapB, p, st));
+    CUtensorMap mapC = mapB;  // unused unless C is read through the TMA
+    p.c_tma = 0;
+    if (beta != 0.0f && !(reinterpret_cast<uintptr_t>(C) & 15u) && !(ldc & 3)) {
+        s = encode_2d(&mapC, C, M, N, ldc, 32, 32);
+        if (s != SGEMM_OK) return s;
+        p.c_tma = 1;
+    }
+    return status_from(launch_x3(bk, a_raw, mapA, mapB, mapC, p, st));
 }
 
 // Host <-> device copy of `rows` rows of `width` floats; one contiguous copy

@@ -30,12 +30,15 @@
 //                releases each stage with tcgen05.commit.
 //   warp 2       allocates and frees the 256 tensor-memory columns.
 //   all 4 warps  epilogue: tcgen05.ld of their 32 accumulator lanes, through
-//                shared memory to coalesced rows, alpha / beta, store.
+//                shared memory to coalesced rows, alpha / beta, store; with
+//                beta != 0 the tile of C is first brought into the idle
+//                stages by the TMA.
 // Every wait is bounded; on a timeout the kernel flags the error word, waits
 // (bounded) for its copies and MMAs in flight, frees tensor memory and exits.
 #include <algorithm>
 
 #include "device_common.cuh"
+#include "kernels_3xtf32.h"
 
 namespace sgemm {
 namespace {
@@ -274,15 +277,16 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
 template <int BK, bool ARAW>
 __global__ void __launch_bounds__(THREADS, 1)
     sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap mapA,
-                        const __grid_constant__ CUtensorMap mapB, const X3Params p) {
+                        const __grid_constant__ CUtensorMap mapB,
+                        const __grid_constant__ CUtensorMap mapC, const X3Params p) {
     using L = X3Cfg<BK>;
     constexpr int S = L::kStages;
     constexpr int kConvThreads = 64;  // warps 2 and 3
     extern __shared__ unsigned char x3_smem_raw[];
-    __shared__ uint64_t full[S], empty[S], conv[S], accum_bar;
+    __shared__ uint64_t full[S], empty[S], conv[S], accum_bar, c_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_abort;
-    __shared__ int s_issued, s_consumed, s_accum_ok, s_converted;
+    __shared__ int s_issued, s_consumed, s_accum_ok, s_converted, s_c_issued;
 
     // Stages start on a 1024-byte boundary of the shared window (the
     // swizzle pattern is taken from address bits).
@@ -305,11 +309,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&conv[s], kConvThreads);
         }
         mbar_init(&accum_bar, 1);
+        mbar_init(&c_bar, 1);
         s_abort = 0;
         s_issued = 0;
         s_consumed = 0;
         s_accum_ok = 0;
         s_converted = 0;
+        s_c_issued = 0;
         fence_barrier_init();
     }
     if (warp == 2) tmem_alloc(&tmem_slot);
@@ -411,6 +417,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         // commit arrives.
         s_accum_ok = mbar_wait_bounded(&accum_bar, 0, p.timeout_ns) ? 1 : 0;
         if (!s_accum_ok) atomicOr(p.err, kErrDrainTimeout);
+        // beta != 0: the stages are idle now; bring this tile's C in with the
+        // TMA, 32 x 32 blocks, block (w, c) at floats (w * 8 + c) * 1024.
+        if (s_accum_ok && !s_abort && p.beta != 0.0f && p.c_tma) {
+            const int chunks = (bn + 31) / 32;
+            mbar_arrive_expect_tx(&c_bar, 4u * chunks * 32 * 32 * 4);
+            for (int w = 0; w < 4; ++w)
+                for (int c = 0; c < chunks; ++c)
+                    tma_load_2d(smem + (size_t)(w * 8 + c) * 4096, &mapC, &c_bar, n0 + c * 32,
+                                m0 + w * 32);
+            s_c_issued = 1;
+        }
     }
     __syncthreads();
 
@@ -419,26 +436,55 @@ __global__ void __launch_bounds__(THREADS, 1)
         // Epilogue: warp w owns accumulator lanes (rows) 32w .. 32w + 31.
         // Each 32-column block goes register -> shared (row per thread) ->
         // global (one row of 32 consecutive floats per warp store).
-        float *stage = reinterpret_cast<float *>(smem) + warp * (32 * 33);
+        // C (beta != 0) comes from shared memory when the TMA brought it,
+        // else from global memory, 32 independent loads per thread first.
+        const float *c_tile = reinterpret_cast<const float *>(smem);  // 128 KB
+        float *stage = reinterpret_cast<float *>(smem + 128 * 1024) + warp * (32 * 33);
         const uint32_t t_warp = tmem + ((uint32_t)(warp * 32) << 16);
         const int row0 = m0 + warp * 32;
-        for (int c = 0; c * 32 < bn; ++c) {
+        bool c_ok = true;
+        if (s_c_issued) {
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait_bounded(&c_bar, 0, p.timeout_ns) ? 1 : 0;
+            c_ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+            if (!c_ok && lane == 0) atomicOr(p.err, kErrWaitTimeout);
+        }
+        for (int c = 0; c_ok && c * 32 < bn; ++c) {
             if (n0 + c * 32 >= p.N) break;  // uniform over the warp
+            const int n = n0 + c * 32 + lane;
+            const bool col_ok = n < p.N && c * 32 + lane < bn;
+            float cv[32];
+            if (p.beta != 0.0f) {
+                if (s_c_issued) {
+                    const float *blk = c_tile + (warp * 8 + c) * 1024;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) cv[i] = blk[i * 32 + lane];
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        cv[i] = (col_ok && row0 + i < p.M) ? p.C[(long long)(row0 + i) * p.ldc + n]
+                                                           : 0.0f;
+                }
+            }
             uint32_t r[32];
             tmem_ld32(t_warp + c * 32, r);
 #pragma unroll
             for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = __uint_as_float(r[j]);
             __syncwarp();
-            const int n = n0 + c * 32 + lane;
-            if (n < p.N && c * 32 + lane < bn) {
+            if (col_ok && p.beta != 0.0f) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int m = row0 + i;
+                    if (m < p.M)
+                        p.C[(long long)m * p.ldc + n] =
+                            __fmaf_rn(p.beta, cv[i], p.alpha * stage[i * 33 + lane]);
+                }
+            } else if (col_ok) {
 #pragma unroll 4
                 for (int i = 0; i < 32; ++i) {
                     const int m = row0 + i;
                     if (m >= p.M) break;
-                    float *cp = p.C + (long long)m * p.ldc + n;
-                    float v = p.alpha * stage[i * 33 + lane];
-                    if (p.beta != 0.0f) v = __fmaf_rn(p.beta, *cp, v);
-                    *cp = v;
+                    p.C[(long long)m * p.ldc + n] = p.alpha * stage[i * 33 + lane];
                 }
             }
             __syncwarp();
@@ -460,6 +506,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
         }
+        if (s_c_issued && !mbar_wait_bounded(&c_bar, 0, 1000000000ull))
+            atomicOr(p.err, kErrDrainTimeout);
         for (int j = landed; j < issued; ++j) {
             if (!mbar_wait_bounded(&full[j % S], (j / S) & 1, 1000000000ull)) {
                 atomicOr(p.err, kErrDrainTimeout);
@@ -489,10 +537,10 @@ cudaError_t x3_configure_one() {
                                 (int)X3Cfg<BK>::kSmem);
 }
 template <int BK, bool ARAW>
-cudaError_t x3_launch_one(const CUtensorMap &mapA, const CUtensorMap &mapB, const X3Params &p,
-                          cudaStream_t stream) {
+cudaError_t x3_launch_one(const CUtensorMap &mapA, const CUtensorMap &mapB,
+                          const CUtensorMap &mapC, const X3Params &p, cudaStream_t stream) {
     sgemm_3xtf32_kernel<BK, ARAW><<<p.tiles_m * p.tiles_n, THREADS, X3Cfg<BK>::kSmem, stream>>>(
-        mapA, mapB, p);
+        mapA, mapB, mapC, p);
     return cudaGetLastError();
 }
 }  // namespace
@@ -504,13 +552,13 @@ cudaError_t x3_configure(int bk, bool a_raw) {
 }
 
 cudaError_t launch_x3(int bk, bool a_raw, const CUtensorMap &mapA, const CUtensorMap &mapB,
-                      const X3Params &p, cudaStream_t stream) {
+                      const CUtensorMap &mapC, const X3Params &p, cudaStream_t stream) {
     if (bk == 16)
-        return a_raw ? x3_launch_one<16, true>(mapA, mapB, p, stream)
-                     : x3_launch_one<16, false>(mapA, mapB, p, stream);
+        return a_raw ? x3_launch_one<16, true>(mapA, mapB, mapC, p, stream)
+                     : x3_launch_one<16, false>(mapA, mapB, mapC, p, stream);
     if (bk == 32)
-        return a_raw ? x3_launch_one<32, true>(mapA, mapB, p, stream)
-                     : x3_launch_one<32, false>(mapA, mapB, p, stream);
+        return a_raw ? x3_launch_one<32, true>(mapA, mapB, mapC, p, stream)
+                     : x3_launch_one<32, false>(mapA, mapB, mapC, p, stream);
     return cudaErrorInvalidValue;
 }
 
