@@ -554,7 +554,9 @@ def gpu_arm(args, ws, rank, local):
                                     "frac": round(3 * fl / dx / 1e12 / tf32_burst, 4),
                                     "note": "3 TF32 products per FP32 product; step time "
                                             "includes the split pass",
-                                    "peak_source": tf32_src, "sustained_peak": tf32_sust}})
+                                    "peak_source": tf32_src, "sustained_peak": tf32_sust,
+                                    "traffic": recorded_traffic("sgemm_3xtf32_kernel", xname),
+                                    "kernel": "sgemm_3xtf32_kernel"}})
             del dAx, dBx, dCx
         result["tensor_core_3xtf32"] = x3
 
