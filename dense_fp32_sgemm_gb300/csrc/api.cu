@@ -356,13 +356,15 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
         ((M + kX3BM - 1) / kX3BM) * ((N + 127) / 128) > INT32_MAX)
         return SGEMM_ERR_INVALID_ARG;
     const int bk = g_x3_bk.load();
-    // A split inside the kernel pays off on large products whose A rows start
-    // on 128-byte lines (measured on GB300: 8192^3 281 against 270 TFLOP/s,
-    // 2048^3 190 against 194, 4092^3 with 16368-byte rows 233 against 246).
+    // A split inside the kernel pays off only for large outputs whose A rows
+    // start on 128-byte lines.  Measured on GB300 (TFLOP/s, split pass
+    // against in-kernel split): 8192^3 270 / 281, 8192x6144x2048 227 / 238,
+    // 6144x6144x2048 243 / 242, 4096x4096x8192 265 / 242, 4096^3 249 / 232,
+    // 2048x8192x4096 254 / 221, 2048^3 194 / 190.
     const int a_mode = g_x3_a_in_kernel.load();
     const bool a_raw = a_mode >= 0 ? a_mode != 0
                                    : ((lda % 32) == 0 && !(reinterpret_cast<uintptr_t>(A) & 127u) &&
-                                      (double)M * (double)N * (double)K >= 68719476736.0);
+                                      M * N >= (int64_t)48 << 20);
     const unsigned bit = 1u << (bk / 16 + (a_raw ? 4 : 0));
     if (!(d->x3_configured & bit)) {
         if (x3_configure(bk, a_raw) != cudaSuccess) return SGEMM_ERR_LAUNCH;

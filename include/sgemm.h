@@ -267,7 +267,7 @@ SGEMM_API sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float
  *   rows, the default) or 32 (two stages of 128-byte rows).
  * a_in_kernel: 1 = the kernel loads A itself and splits each A tile in
  *   shared memory; 0 = a split pass writes A's hi and lo parts first;
- *   -1 (default) = 1 when M*N*K >= 2^36 and A's rows start on 128-byte
+ *   -1 (default) = 1 when M*N >= 48 * 2^20 and A's rows start on 128-byte
  *   lines (A 128-byte aligned, lda a multiple of 32), else 0.
  * All four forms compute the same products in the same order (bitwise equal
  * results).  SGEMM_ERR_INVALID_ARG for other values.

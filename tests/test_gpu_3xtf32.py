@@ -195,3 +195,61 @@ def test_wait_timeout_reports_and_recovers():
     out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, entry=X3)
     ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, rows=[0, 255, 511])
     assert_within(out[[0, 255, 511]], ref, bound, "3xTF32 after timeout")
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 100, 64), (200, 7, 64), (129, 129, 65), (300, 1000, 8192)])
+def test_edges_of_the_tensor_core_path(M, N, K):
+    # K at the hand-over (64), N far below the narrowest tile (128), odd
+    # sizes one past a tile, and a long K (error growth of the FP32
+    # accumulation in the tensor core): all within the bound.
+    check(M, N, K, 1.0, 0.0, dist="uniform", seed=21)
+    check(M, N, K, -0.75, 0.5, dist="normal", seed=22)
+
+
+def test_nan_in_a_reaches_only_its_row():
+    # IEEE semantics the FFMA path also has: a NaN in row i of A makes row i
+    # of C NaN and leaves every other row finite and within the bound.
+    M, N, K = 384, 512, 256
+    A, lda, B, ldb, C, ldc = inputs("uniform", 23, M, N, K)
+    A = A.copy()
+    A[5 * lda + 17] = np.nan
+    out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
+    assert np.isnan(out[5]).all()
+    rows = [r for r in range(M) if r != 5]
+    assert np.isfinite(out[rows]).all()
+    ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, rows=rows)
+    assert_within(out[rows], ref, bound, "3xTF32 NaN row")
+
+
+@pytest.mark.parametrize("a_in_kernel", [True, False])
+def test_capture_in_a_cuda_graph_and_replay(a_in_kernel):
+    # After a first call has sized the stream's workspace, the split pass and
+    # the MMA kernel are queued without allocation or host synchronisation:
+    # the call can be captured in a CUDA graph and replayed bit for bit.
+    M, N, K = 640, 700, 512
+    A, lda, B, ldb, C, ldc = inputs("uniform", 24, M, N, K)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC0 = torch.from_numpy(C).cuda()
+    dC = dC0.clone()
+    sg.set_3xtf32_config(16, a_in_kernel)
+    try:
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            assert sg.sgemm_run_3xtf32(M, N, K, 0.5, dA.data_ptr(), lda, dB.data_ptr(), ldb, 2.0,
+                                       dC.data_ptr(), ldc, side.cuda_stream) == 0
+        torch.cuda.synchronize()
+        eager = dC.clone()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            st = sg.sgemm_run_3xtf32(M, N, K, 0.5, dA.data_ptr(), lda, dB.data_ptr(), ldb, 2.0,
+                                     dC.data_ptr(), ldc, side.cuda_stream)
+        assert st == 0
+        for _ in range(3):
+            dC.copy_(dC0)
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(dC, eager)
+        assert sg.device_status() == 0
+    finally:
+        sg.set_3xtf32_config(16, None)
