@@ -23,6 +23,9 @@
 // Structure (one 128 x bn tile of C per CTA, bn <= 256, 128 threads):
 //   split pass   A -> [A_hi; A_lo] (K-major rows), B -> [B_hi^T; B_lo^T]
 //                (transposed to K-major), zero padded; an HBM-bound pass.
+//                The MMA kernel is launched as its programmatic dependent:
+//                its CTAs set up while the pass finishes, and the load
+//                issuer waits for the pass's results before its first copy.
 //   warp 0       one thread issues the TMA loads of the four operand tiles
 //                of each K slice into a ring of swizzled shared-memory stages.
 //   warp 1       one thread issues tcgen05.mma (M 128, N bn, K 8) three
@@ -256,6 +259,9 @@ __device__ __forceinline__ void split_b(const SplitJob &j, int block, int nblock
 // side.
 __global__ void __launch_bounds__(256) x3_split_kernel(const SplitJob j) {
     __shared__ float t[64][65];
+    // The MMA kernel may start its set-up now; it waits for this grid's
+    // results before its first load.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if ((int)blockIdx.x < j.a_blocks)
         split_a(j, blockIdx.x, j.a_blocks);
     else
@@ -295,7 +301,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t sbase = smem_addr(smem);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tm = blockIdx.x % p.tiles_m, tn = blockIdx.x / p.tiles_m;
+    // Tiles in groups of 16 tile rows, column by column inside a group: a
+    // wave of CTAs shares about as many A rows as B columns, so fewer operand
+    // bytes fall out of L2 between the CTAs that read them (measured 3-5 %
+    // faster than walking whole columns at 4092^3 and above).
+    constexpr int kGroupM = 16;
+    const int per_group = kGroupM * p.tiles_n;
+    const int first_m = ((int)blockIdx.x / per_group) * kGroupM;
+    const int gsz = min(p.tiles_m - first_m, kGroupM);
+    const int in_group = (int)blockIdx.x % per_group;
+    const int tm = first_m + in_group % gsz, tn = in_group / gsz;
     const int bn = p.bn;
     const int m0 = tm * BM, n0 = tn * bn;
 
@@ -327,6 +342,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // Producer: the four operand tiles of K slice kt into stage kt % S.
+            // The split pass's output is complete and visible after this.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             int kt = 0;
             for (; kt < p.kt_total; ++kt) {
                 if (p.skip_loads_from >= 0 && kt >= p.skip_loads_from) break;
@@ -539,9 +556,17 @@ cudaError_t x3_configure_one() {
 template <int BK, bool ARAW>
 cudaError_t x3_launch_one(const CUtensorMap &mapA, const CUtensorMap &mapB,
                           const CUtensorMap &mapC, const X3Params &p, cudaStream_t stream) {
-    sgemm_3xtf32_kernel<BK, ARAW><<<p.tiles_m * p.tiles_n, THREADS, X3Cfg<BK>::kSmem, stream>>>(
-        mapA, mapB, mapC, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.tiles_m * p.tiles_n);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = X3Cfg<BK>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel<BK, ARAW>, mapA, mapB, mapC, p);
 }
 }  // namespace
 
@@ -573,7 +598,7 @@ cudaError_t launch_x3_split(const float *A, long long lda, int M, const float *B
     // Blocks in proportion to the bytes each side moves (the same per
     // element), 16 per SM in all.
     const long long a_elems = A ? (long long)Mp * Kp : 0, b_elems = (long long)Np * Kp;
-    const long long total_blocks = (long long)num_sms * 16;
+    const long long total_blocks = (long long)num_sms * 8;  // all resident at once
     long long a_blocks = A ? std::max<long long>(1, total_blocks * a_elems / (a_elems + b_elems)) : 0;
     a_blocks = std::min<long long>(a_blocks, (a_elems / 4 + 255) / 256);
     const long long b_tiles = (long long)((Kp + 63) / 64) * ((Np + 63) / 64);
