@@ -353,7 +353,7 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
     if (K < kX3MinK || M <= 16 || alpha == 0.0f)
         return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, none, st, *d);
     if (M > (1 << 29) || N > (1 << 29) || K > (1 << 30) ||
-        ((M + kX3BM - 1) / kX3BM) * ((N + 127) / 128) > INT32_MAX)
+        ((M + kX3BM - 1) / kX3BM) * ((N + kX3MinBN - 1) / kX3MinBN) > INT32_MAX)
         return SGEMM_ERR_INVALID_ARG;
     const int bk = g_x3_bk.load();
     // A split inside the kernel pays off only for large outputs whose A rows

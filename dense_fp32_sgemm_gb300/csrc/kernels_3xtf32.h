@@ -19,15 +19,16 @@ namespace sgemm {
 constexpr int kX3BM = 128;
 constexpr int kX3BN = 256;
 constexpr int kX3MinK = 64;  // shorter products run the FFMA kernels
+constexpr int kX3MinBN = 64;  // narrowest tile (small products fill more SMs)
 
 // Tile width for an M x N product on num_sms SMs (one tile per CTA, one CTA
-// per SM): the multiple of 16 in [128, 256] whose whole number of waves
+// per SM): the multiple of 16 in [64, 256] whose whole number of waves
 // costs least, a wave costing its width plus 32 (the A tile every CTA loads
 // whatever its width); ties go to the wider tile.
 inline int x3_tile_width(long long M, long long N, int num_sms) {
     int best = kX3BN;
     long long best_cost = -1;
-    for (int bn = kX3BN; bn >= 128; bn -= 16) {
+    for (int bn = kX3BN; bn >= kX3MinBN; bn -= 16) {
         const long long tiles = ((M + kX3BM - 1) / kX3BM) * ((N + bn - 1) / bn);
         const long long cost = ((tiles + num_sms - 1) / num_sms) * (bn + 32);
         if (best_cost < 0 || cost < best_cost) {
@@ -40,7 +41,7 @@ inline int x3_tile_width(long long M, long long N, int num_sms) {
 
 struct X3Params {
     int M, N, K;
-    int bn;                // tile width: a multiple of 16 in [128, 256]
+    int bn;                // tile width: a multiple of 16 in [64, 256]
     int tiles_m, tiles_n;
     int kt_total;          // ceil(K / BK)
     int a_lo_row;          // Mp: first row of A's lo part in the split buffer

@@ -240,7 +240,7 @@ SGEMM_API sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages, int mic
  * Arguments, layout, ownership and errors are those of sgemm_run; pointers
  * need only 4-byte alignment.  A split pass writes hi and lo copies of B
  * (transposed to K-major) into a per-(device, stream) workspace of
- * 8 * K' * ceil(N/w)*w bytes, K' = ceil(K/32)*32 and w the tile width (128 to
+ * 8 * K' * ceil(N/w)*w bytes, K' = ceil(K/32)*32 and w the tile width (64 to
  * 256) chosen for the shape; A is split tile by tile inside the kernel (A not
  * 16-byte aligned, or lda not a multiple of 4, is first copied to aligned
  * rows in the same workspace: 4 * M * ceil(K/4)*4 more bytes).  The
