@@ -32,6 +32,7 @@ std::atomic<int> g_stages{3};
 std::atomic<int> g_micro_m{16};
 std::atomic<int> g_x3_bk{16};
 std::atomic<int> g_x3_a_in_kernel{-1};  // -1: chosen per call
+std::atomic<int> g_x3_splits{0};         // 0: chosen per call
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -353,7 +354,7 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
     if (K < kX3MinK || M <= 16 || alpha == 0.0f)
         return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, none, st, *d);
     if (M > (1 << 29) || N > (1 << 29) || K > (1 << 30) ||
-        ((M + kX3BM - 1) / kX3BM) * ((N + kX3MinBN - 1) / kX3MinBN) > INT32_MAX)
+        ((M + kX3BM - 1) / kX3BM) * ((N + kX3MinBN - 1) / kX3MinBN) * kX3MaxSplits > INT32_MAX)
         return SGEMM_ERR_INVALID_ARG;
     const int bk = g_x3_bk.load();
     // A split inside the kernel pays off only for large outputs whose A rows
@@ -370,19 +371,22 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
         if (x3_configure(bk, a_raw) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         d->x3_configured |= bit;
     }
-    const int bn = x3_tile_width(M, N, d->num_sms);
+    const int kt_total = (int)((K + bk - 1) / bk);
+    int bn = kX3BN, splits = 1;
+    x3_plan(M, N, kt_total, d->num_sms, g_x3_splits.load(), &bn, &splits);
     const int64_t Mp = (M + kX3BM - 1) / kX3BM * kX3BM;
     const int64_t Np = (N + bn - 1) / bn * bn;
     const int64_t Kp = (K + 31) / 32 * 32;  // rows of whole 128-byte lines
     // Workspace: [A hi; A lo] (split pass only) | [B hi^T; B lo^T] | A copied
     // to 16-byte-aligned rows (A split in the kernel, when the TMA cannot
-    // map A itself).
+    // map A itself) | the K ranges' raw tiles (K split).
     const bool a_pack = a_raw && ((reinterpret_cast<uintptr_t>(A) & 15u) || (lda & 3));
     const int64_t ld_pack = (K + 3) / 4 * 4;
     const size_t a_floats = a_raw ? 0 : (size_t)(2 * Mp * Kp), b_floats = (size_t)(2 * Np * Kp);
-    const size_t p_floats = a_pack ? (size_t)(M * ld_pack) : 0;
+    const size_t p_floats = a_pack ? (size_t)((M * ld_pack + 63) / 64 * 64) : 0;
+    const size_t r_floats = splits > 1 ? (size_t)(splits * Mp * Np) : 0;
     Workspace &w = d->ws[st];
-    const size_t bytes = (a_floats + b_floats + p_floats) * sizeof(float);
+    const size_t bytes = (a_floats + b_floats + p_floats + r_floats) * sizeof(float);
     if (w.split_bytes < bytes) {
         if (w.split) cudaFree(w.split);
         w.split = nullptr;
@@ -391,7 +395,7 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
         w.split_bytes = bytes;
     }
     // a_floats and b_floats are multiples of 64 floats (256 bytes)
-    float *sa = w.split, *sb = w.split + a_floats, *pa = sb + b_floats;
+    float *sa = w.split, *sb = w.split + a_floats, *pa = sb + b_floats, *pr = pa + p_floats;
     const float *a_map = A;
     int64_t lda_map = lda;
     if (a_pack) {
@@ -414,21 +418,31 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
     p.bn = bn;
     p.tiles_m = (int)(Mp / kX3BM); p.tiles_n = (int)(Np / bn);
-    p.kt_total = (int)((K + bk - 1) / bk);
+    p.kt_total = kt_total;
+    p.splits = splits;
+    p.kt_per_split = (kt_total + splits - 1) / splits;
+    p.part = pr; p.part_stride = Mp * Np; p.part_ld = Np;
     p.a_lo_row = (int)Mp; p.b_lo_row = (int)Np;
-    p.alpha = alpha; p.beta = beta; p.C = C; p.ldc = ldc;
+    // A K split writes raw sums; the reduction applies alpha and beta.
+    p.alpha = splits > 1 ? 1.0f : alpha;
+    p.beta = splits > 1 ? 0.0f : beta;
+    p.C = C; p.ldc = ldc;
     p.err = d->err;
     const unsigned long long to = g_timeout_ns.load();
     p.timeout_ns = to ? to : kDefaultTimeoutNs;
     p.skip_loads_from = g_skip_loads_from.load();
     CUtensorMap mapC = mapB;  // unused unless C is read through the TMA
     p.c_tma = 0;
-    if (beta != 0.0f && !(reinterpret_cast<uintptr_t>(C) & 15u) && !(ldc & 3)) {
+    if (p.beta != 0.0f && !(reinterpret_cast<uintptr_t>(C) & 15u) && !(ldc & 3)) {
         s = encode_2d(&mapC, C, M, N, ldc, 32, 32);
         if (s != SGEMM_OK) return s;
         p.c_tma = 1;
     }
-    return status_from(launch_x3(bk, a_raw, mapA, mapB, mapC, p, st));
+    if (launch_x3(bk, a_raw, mapA, mapB, mapC, p, st) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (splits > 1 && launch_x3_reduce(pr, splits, Mp * Np, Np, (int)M, (int)N, alpha, beta, C,
+                                       ldc, d->num_sms, st) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    return SGEMM_OK;
 }
 
 // Host <-> device copy of `rows` rows of `width` floats; one contiguous copy
@@ -642,11 +656,13 @@ sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages, int micro_m) {
     return SGEMM_OK;
 }
 
-sgemm_status_t sgemm_set_3xtf32_config(int bk, int a_in_kernel) {
-    if ((bk != 16 && bk != 32) || a_in_kernel < -1 || a_in_kernel > 1)
+sgemm_status_t sgemm_set_3xtf32_config(int bk, int a_in_kernel, int splits) {
+    if ((bk != 16 && bk != 32) || a_in_kernel < -1 || a_in_kernel > 1 || splits < 0 ||
+        splits > kX3MaxSplits)
         return SGEMM_ERR_INVALID_ARG;
     g_x3_bk.store(bk);
     g_x3_a_in_kernel.store(a_in_kernel);
+    g_x3_splits.store(splits);
     return SGEMM_OK;
 }
 

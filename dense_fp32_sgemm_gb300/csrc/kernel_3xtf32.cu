@@ -20,7 +20,9 @@
 // accumulator, so the result differs from the FP32 one only by the dropped
 // terms and the accumulation order.
 //
-// Structure (one 128 x bn tile of C per CTA, bn <= 256, 128 threads):
+// Structure (one 128 x bn tile of C per CTA, bn <= 256, 128 threads; deep
+// products with few tiles give each CTA one K range of a tile instead, and a
+// reduction kernel adds the ranges' raw tiles in order):
 //   split pass   A -> [A_hi; A_lo] (K-major rows), B -> [B_hi^T; B_lo^T]
 //                (transposed to K-major), zero padded; an HBM-bound pass.
 //                The MMA kernel is launched as its programmatic dependent:
@@ -268,6 +270,25 @@ __global__ void __launch_bounds__(256) x3_split_kernel(const SplitJob j) {
         split_b(j, blockIdx.x - j.a_blocks, gridDim.x - j.a_blocks, t);
 }
 
+// C = alpha * (sum of the K ranges' raw tiles, in range order) + beta * C.
+__global__ void __launch_bounds__(256) x3_reduce_kernel(const float *__restrict__ part,
+                                                        int splits, long long stride,
+                                                        long long ld_part, int M, int N,
+                                                        float alpha, float beta, float *C,
+                                                        long long ldc) {
+    const long long total = (long long)M * N;
+    for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += gridDim.x * 256LL) {
+        const int m = (int)(i / N), n = (int)(i % N);
+        const float *q = part + (long long)m * ld_part + n;
+        float sum = q[0];
+        for (int j = 1; j < splits; ++j) sum += q[(long long)j * stride];
+        float *c = C + (long long)m * ldc + n;
+        float v = alpha * sum;
+        if (beta != 0.0f) v = __fmaf_rn(beta, *c, v);
+        *c = v;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // MMA kernel.
 // ---------------------------------------------------------------------------
@@ -305,12 +326,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     // wave of CTAs shares about as many A rows as B columns, so fewer operand
     // bytes fall out of L2 between the CTAs that read them (measured 3-5 %
     // faster than walking whole columns at 4092^3 and above).
+    // With a K split, CTA blockIdx takes K range blockIdx / tiles of tile
+    // blockIdx % tiles.
+    const int n_tiles = p.tiles_m * p.tiles_n;
+    const int split = (int)blockIdx.x / n_tiles, tile = (int)blockIdx.x % n_tiles;
     constexpr int kGroupM = 16;
     const int per_group = kGroupM * p.tiles_n;
-    const int first_m = ((int)blockIdx.x / per_group) * kGroupM;
+    const int first_m = (tile / per_group) * kGroupM;
     const int gsz = min(p.tiles_m - first_m, kGroupM);
-    const int in_group = (int)blockIdx.x % per_group;
+    const int in_group = tile % per_group;
     const int tm = first_m + in_group % gsz, tn = in_group / gsz;
+    const int kt0 = split * p.kt_per_split;
+    const int nkt = min(p.kt_total - kt0, p.kt_per_split);  // >= 1
+    // Output: C, or (K split) this range's slice of the partial sums, raw.
+    float *const out = p.splits > 1 ? p.part + (size_t)split * p.part_stride : p.C;
+    const long long ldo = p.splits > 1 ? p.part_ld : p.ldc;
     const int bn = p.bn;
     const int m0 = tm * BM, n0 = tn * bn;
 
@@ -345,7 +375,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // The split pass's output is complete and visible after this.
             asm volatile("griddepcontrol.wait;" ::: "memory");
             int kt = 0;
-            for (; kt < p.kt_total; ++kt) {
+            for (; kt < nkt; ++kt) {
                 if (p.skip_loads_from >= 0 && kt >= p.skip_loads_from) break;
                 const int s = kt % S;
                 if (kt >= S && !mbar_wait_bounded(&empty[s], ((kt / S) - 1) & 1, p.timeout_ns)) {
@@ -356,7 +386,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 unsigned char *st = smem + (size_t)s * L::kStage;
                 mbar_arrive_expect_tx(&full[s],
                                       (ARAW ? 1 : 2) * L::kA + 2 * (uint32_t)bn * BK * 4);
-                const int k = kt * BK;
+                const int k = (kt0 + kt) * BK;
                 tma_load_2d(st, &mapA, &full[s], k, m0);
                 if (!ARAW) tma_load_2d(st + L::kA, &mapA, &full[s], k, p.a_lo_row + m0);
                 tma_load_2d(st + 2 * L::kA, &mapB, &full[s], k, n0);
@@ -370,7 +400,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // MMA issuer: per K step of 8, the two correction products first,
             // then hi*hi; the first product of the tile overwrites D.
             int kt = 0;
-            for (; kt < p.kt_total; ++kt) {
+            for (; kt < nkt; ++kt) {
                 const int s = kt % S;
                 if (!mbar_wait_bounded(ARAW ? &conv[s] : &full[s], (kt / S) & 1, p.timeout_ns)) {
                     atomicOr(p.err, kErrWaitTimeout);
@@ -400,7 +430,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // is elementwise, so the swizzled positions the TMA chose are kept.
         const int c = tid - 64;
         int kt = 0;
-        for (; kt < p.kt_total; ++kt) {
+        for (; kt < nkt; ++kt) {
             const int s = kt % S;
             if (!mbar_wait_bounded(&full[s], (kt / S) & 1, p.timeout_ns)) {
                 atomicOr(p.err, kErrWaitTimeout);
@@ -479,7 +509,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        cv[i] = (col_ok && row0 + i < p.M) ? p.C[(long long)(row0 + i) * p.ldc + n]
+                        cv[i] = (col_ok && row0 + i < p.M) ? out[(long long)(row0 + i) * ldo + n]
                                                            : 0.0f;
                 }
             }
@@ -493,7 +523,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int i = 0; i < 32; ++i) {
                     const int m = row0 + i;
                     if (m < p.M)
-                        p.C[(long long)m * p.ldc + n] =
+                        out[(long long)m * ldo + n] =
                             __fmaf_rn(p.beta, cv[i], p.alpha * stage[i * 33 + lane]);
                 }
             } else if (col_ok) {
@@ -501,7 +531,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int i = 0; i < 32; ++i) {
                     const int m = row0 + i;
                     if (m >= p.M) break;
-                    p.C[(long long)m * p.ldc + n] = p.alpha * stage[i * 33 + lane];
+                    out[(long long)m * ldo + n] = p.alpha * stage[i * 33 + lane];
                 }
             }
             __syncwarp();
@@ -557,7 +587,7 @@ template <int BK, bool ARAW>
 cudaError_t x3_launch_one(const CUtensorMap &mapA, const CUtensorMap &mapB,
                           const CUtensorMap &mapC, const X3Params &p, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.tiles_m * p.tiles_n);
+    cfg.gridDim = dim3(p.tiles_m * p.tiles_n * p.splits);
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = X3Cfg<BK>::kSmem;
     cfg.stream = stream;
@@ -585,6 +615,16 @@ cudaError_t launch_x3(int bk, bool a_raw, const CUtensorMap &mapA, const CUtenso
         return a_raw ? x3_launch_one<32, true>(mapA, mapB, mapC, p, stream)
                      : x3_launch_one<32, false>(mapA, mapB, mapC, p, stream);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_x3_reduce(const float *part, int splits, long long stride, long long ld_part,
+                             int M, int N, float alpha, float beta, float *C, long long ldc,
+                             int num_sms, cudaStream_t stream) {
+    const long long total = (long long)M * N;
+    const long long blocks = std::min<long long>((total + 255) / 256, (long long)num_sms * 8);
+    x3_reduce_kernel<<<(int)std::max<long long>(blocks, 1), 256, 0, stream>>>(
+        part, splits, stride, ld_part, M, N, alpha, beta, C, ldc);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_x3_split(const float *A, long long lda, int M, const float *B, long long ldb,

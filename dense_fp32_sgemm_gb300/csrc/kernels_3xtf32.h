@@ -20,23 +20,44 @@ constexpr int kX3BM = 128;
 constexpr int kX3BN = 256;
 constexpr int kX3MinK = 64;  // shorter products run the FFMA kernels
 constexpr int kX3MinBN = 64;  // narrowest tile (small products fill more SMs)
+constexpr int kX3MaxSplits = 8;  // K ranges per tile (deep products with few tiles)
 
-// Tile width for an M x N product on num_sms SMs (one tile per CTA, one CTA
-// per SM): the multiple of 16 in [64, 256] whose whole number of waves
-// costs least, a wave costing its width plus 32 (the A tile every CTA loads
-// whatever its width); ties go to the wider tile.
-inline int x3_tile_width(long long M, long long N, int num_sms) {
-    int best = kX3BN;
-    long long best_cost = -1;
+// Tile width and K split for an M x N x (kt_total K slices) product on
+// num_sms SMs (one tile and K range per CTA, one CTA per SM).  Cost of a
+// choice, in units of one K slice of one tile column (about 1.75 ns on
+// GB300): whole waves x (width + 32, the A tile every CTA loads whatever its
+// width) x (slices per split + 8, a tile's fill and epilogue), plus for a
+// split the extra launch and the bytes its reduction moves.  Widths are the
+// multiples of 16 in [64, 256]; a split keeps at least 16 slices per range.
+// Ties go to the wider tile, then to fewer splits.  forced_splits > 0 fixes
+// the split count (the nearest feasible one).
+inline void x3_plan(long long M, long long N, int kt_total, int num_sms, int forced_splits,
+                    int *bn_out, int *splits_out) {
+    int best_bn = kX3BN, best_s = 1;
+    double best = -1.0;
     for (int bn = kX3BN; bn >= kX3MinBN; bn -= 16) {
         const long long tiles = ((M + kX3BM - 1) / kX3BM) * ((N + bn - 1) / bn);
-        const long long cost = ((tiles + num_sms - 1) / num_sms) * (bn + 32);
-        if (best_cost < 0 || cost < best_cost) {
-            best = bn;
-            best_cost = cost;
+        for (int sp = 1; sp <= kX3MaxSplits; ++sp) {
+            const int kps = (kt_total + sp - 1) / sp;
+            if (sp > 1 && (kps < 16 || (long long)(sp - 1) * kps >= kt_total)) continue;
+            if (forced_splits > 0 && sp != forced_splits && !(sp == 1 && forced_splits == 1))
+                continue;
+            const long long rounds = (tiles * sp + num_sms - 1) / num_sms;
+            double cost = (double)rounds * (bn + 32) * (kps + 8);
+            if (sp > 1) cost += 1700.0 + (double)(sp + 2) * (double)M * (double)N / 2625.0;
+            if (best < 0 || cost < best) {
+                best = cost;
+                best_bn = bn;
+                best_s = sp;
+            }
         }
     }
-    return best;
+    if (best < 0) {  // the forced split count is not feasible for this K
+        x3_plan(M, N, kt_total, num_sms, 0, bn_out, splits_out);
+        return;
+    }
+    *bn_out = best_bn;
+    *splits_out = best_s;
 }
 
 struct X3Params {
@@ -44,6 +65,11 @@ struct X3Params {
     int bn;                // tile width: a multiple of 16 in [64, 256]
     int tiles_m, tiles_n;
     int kt_total;          // ceil(K / BK)
+    int splits;            // K ranges per tile; CTA blockIdx / tiles takes range
+    int kt_per_split;      //   [split * kt_per_split, + kt_per_split) of the slices
+    float *part;           // splits > 1: raw sums, slice s at part + s * part_stride
+    long long part_stride; //   (floats), row m of a slice at m * part_ld
+    long long part_ld;
     int a_lo_row;          // Mp: first row of A's lo part in the split buffer
     int b_lo_row;          // Np: first row of B's lo part
     float alpha, beta;
@@ -64,6 +90,11 @@ cudaError_t x3_configure(int bk, bool a_raw);
 // mapC: C as M x N FP32, 32 x 32 boxes, used when beta != 0 and p.c_tma.
 cudaError_t launch_x3(int bk, bool a_raw, const CUtensorMap &mapA, const CUtensorMap &mapB,
                       const CUtensorMap &mapC, const X3Params &p, cudaStream_t stream);
+// C = alpha * (part[0] + ... + part[splits - 1]) + beta * C, the slices added
+// in order (deterministic).
+cudaError_t launch_x3_reduce(const float *part, int splits, long long stride, long long ld_part,
+                             int M, int N, float alpha, float beta, float *C, long long ldc,
+                             int num_sms, cudaStream_t stream);
 // Split A (M x K, lda; skipped when A is null) and B (K x N, ldb) into the
 // buffers above.  Kp is a multiple of 4; Mp and Np multiples of the tile
 // sizes.

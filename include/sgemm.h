@@ -243,7 +243,9 @@ SGEMM_API sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages, int mic
  * 8 * K' * ceil(N/w)*w bytes, K' = ceil(K/32)*32 and w the tile width (64 to
  * 256) chosen for the shape; A is split tile by tile inside the kernel (A not
  * 16-byte aligned, or lda not a multiple of 4, is first copied to aligned
- * rows in the same workspace: 4 * M * ceil(K/4)*4 more bytes).  The
+ * rows in the same workspace: 4 * M * ceil(K/4)*4 more bytes).  A product
+ * cut into s K ranges (see sgemm_set_3xtf32_config) adds 4 * s * M' * N'
+ * bytes for the ranges' raw tiles (M', N' rounded up to the tile).  The
  * workspace is kept until sgemm_release_workspace().
  * Accuracy: measured within the FFMA path's bound
  * 2 * K * 2^-24 * (|alpha| (|A||B|)ij + |beta| |Cij|) on the test
@@ -269,10 +271,15 @@ SGEMM_API sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float
  *   shared memory; 0 = a split pass writes A's hi and lo parts first;
  *   -1 (default) = 1 when M*N >= 48 * 2^20 and A's rows start on 128-byte
  *   lines (A 128-byte aligned, lda a multiple of 32), else 0.
- * All four forms compute the same products in the same order (bitwise equal
- * results).  SGEMM_ERR_INVALID_ARG for other values.
+ * splits: the number of K ranges each output tile is cut into, 1 to 8, or
+ *   0 (default) = chosen per call from a cost model of whole waves: deep
+ *   products with few tiles are cut so that more SMs work, and a reduction
+ *   kernel adds the ranges' raw tiles in range order, then applies alpha and
+ *   beta.  A count that leaves a range under 16 K slices is not taken.
+ * For a given split count all forms compute the same products in the same
+ * order (bitwise equal results).  SGEMM_ERR_INVALID_ARG for other values.
  */
-SGEMM_API sgemm_status_t sgemm_set_3xtf32_config(int bk, int a_in_kernel);
+SGEMM_API sgemm_status_t sgemm_set_3xtf32_config(int bk, int a_in_kernel, int splits);
 
 /* Free every workspace and host-path buffer the library holds on all devices. */
 SGEMM_API sgemm_status_t sgemm_release_workspace(void);

@@ -253,3 +253,36 @@ def test_capture_in_a_cuda_graph_and_replay(a_in_kernel):
         assert sg.device_status() == 0
     finally:
         sg.set_3xtf32_config(16, None)
+
+
+@pytest.mark.parametrize("splits", [2, 3, 5])
+def test_forced_k_split(splits):
+    # Each K range writes its raw tile; the reduction adds the ranges in
+    # order and applies alpha and beta.  Integers stay bit-exact (every
+    # partial sum is exact), floats stay within the bound.
+    M, N, K = 300, 520, 2000
+    sg.set_3xtf32_config(16, None, splits)
+    try:
+        check(M, N, K, 1.0, 0.0, dist="ints", seed=31, exact=True)
+        check(M, N, K, 0.5, 2.0, dist="uniform", seed=32)
+        A, lda, B, ldb, C, ldc = inputs("uniform", 33, M, N, K)
+        o1, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
+        o2, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
+        assert np.array_equal(o1.view(np.uint32), o2.view(np.uint32))
+    finally:
+        sg.set_3xtf32_config(16, None, 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 8192), (768, 768, 4096), (130, 1000, 3000)])
+def test_deep_products_with_few_tiles(M, N, K):
+    # The planner cuts these into K ranges (few tiles, long K).
+    check(M, N, K, 1.0, 0.0, dist="uniform", seed=34)
+    check(M, N, K, -1.5, 0.25, dist="normal", seed=35)
+
+
+def test_timeout_with_a_k_split():
+    sg.set_3xtf32_config(16, None, 2)
+    try:
+        test_wait_timeout_reports_and_recovers()
+    finally:
+        sg.set_3xtf32_config(16, None, 0)
