@@ -10,9 +10,12 @@
 //   - stream-K: keep d full waves of whole tiles (d = floor(T/G) or one
 //     fewer) and share the k-iterations of the other tiles evenly, with an
 //     allowance per extra piece for combining partial sums.  Pieces are kept
-//     to at most about five per tile (shares of at least a quarter of K):
-//     finer splits cost more than they balance ("Part 2": up to 16 pieces
-//     lost to cuBLAS; two to four worked).
+//     to at most nine per tile (shares of at least an eighth of K), the most
+//     the last CTA of a tile combines through its idle TMA ring; beyond that
+//     the combination runs from L2 and costs more than it balances ("Part 2"
+//     found two to four pieces best on a 48-SM part; measured on GB300,
+//     640 x 640 x 8192: 5 pieces 320 us, 9 pieces 180 us, 11 pieces 217 us;
+//     768 x 768 x 4096: 5 pieces 172 us, 9 pieces 105 us).
 #include "plan.h"
 
 #include <stdio.h>
@@ -26,7 +29,10 @@ static_assert(sizeof(Plan::sk_starts) / sizeof(int) == kSkinnyMaxGrid + 1,
 
 namespace {
 
-constexpr double kFixupCost = 0.5;  // per extra piece, in k-iterations of a tile
+// Per extra piece of a stream-K tile, in k-iterations of a tile: measured on
+// GB300, 1024^3 with 6 pieces per tile (share 7) took 63.5 us against 61.4
+// with 5 (share 8), one iteration less work for one piece more.
+constexpr double kFixupCost = 1.5;
 constexpr int64_t kSmallSlicesPerSm = 4;
 // With the copy of an unaligned operand to pay for, the tiled kernel needs
 // more work: measured, 1023 x 1025 x 513 (4.5 slices per SM) is faster on the
@@ -83,32 +89,42 @@ static void plan_tile(const PlanInput &in, Plan *pl, bool allow_sk) {
             if (sk_tiles <= 0) continue;
             const int64_t total = sk_tiles * KT;
             int64_t share = ceil_div(total, G);
-            const int64_t min_share = ceil_div(KT, 4);
+            const int64_t min_share = ceil_div(KT, 8);
+            // Shares from the smallest the grid and the piece limit allow, a
+            // little upward: a larger share can save a piece.
+            int64_t last = share;
             if (in.force_splits > 0) {
                 // As close to the requested split as the grid allows.
                 const int64_t want = ceil_div(KT, in.force_splits);
                 share = want > share ? want : share;
-            } else if (share < min_share) {
-                share = min_share;
+                last = share;
+            } else {
+                if (share < min_share) share = min_share;
+                last = share + share / 2 + 2;
+                if (last > KT) last = KT > share ? KT : share;
             }
             if (share < 1) share = 1;
-            const int64_t ctas = ceil_div(total, share);
-            if (ctas > G) continue;
-            // Most pieces any tile is cut into.
-            const int64_t pieces = (KT + share - 2) / share + 1;
-            const int64_t max_pieces = pieces < ctas ? pieces : ctas;
-            const double cost = (double)d * KT + (double)share +
-                                kFixupCost * (double)(max_pieces > 1 ? max_pieces - 1 : 0);
-            if (cost < best.cost || in.force_variant == kVarStreamK) {
-                best.variant = kVarStreamK;
-                best.dp_tiles = (int)dp;
-                best.sk_tiles = (int)sk_tiles;
-                best.sk_share = (int)share;
-                best.grid = (int)(dp > 0 ? G : ctas);
-                best.cost = cost;
-                best.reason = "stream-K tail";
-                if (in.force_variant == kVarStreamK) break;
+            bool taken = false;
+            for (int64_t sh = share; sh <= last; ++sh) {
+                const int64_t ctas = ceil_div(total, sh);
+                if (ctas > G) continue;
+                // Most pieces any tile is cut into.
+                const int64_t pieces = (KT + sh - 2) / sh + 1;
+                const int64_t max_pieces = pieces < ctas ? pieces : ctas;
+                const double cost = (double)d * KT + (double)sh +
+                                    kFixupCost * (double)(max_pieces > 1 ? max_pieces - 1 : 0);
+                if (cost < best.cost || (in.force_variant == kVarStreamK && !taken)) {
+                    best.variant = kVarStreamK;
+                    best.dp_tiles = (int)dp;
+                    best.sk_tiles = (int)sk_tiles;
+                    best.sk_share = (int)sh;
+                    best.grid = (int)(dp > 0 ? G : ctas);
+                    best.cost = cost;
+                    best.reason = "stream-K tail";
+                    taken = true;
+                }
             }
+            if (taken && in.force_variant == kVarStreamK) break;
         }
     }
     *pl = best;

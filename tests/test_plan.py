@@ -115,8 +115,9 @@ def test_plan_invariants(M, N, K):
         assert dp % SMS == 0
         # every stream-K iteration is owned by some CTA of the grid
         assert share * grid >= sk * kt
-        # pieces per tile stay small
-        assert share >= math.ceil(kt / 4)
+        # pieces per tile stay within what the idle ring combines (nine)
+        assert share >= math.ceil(kt / 8)
+        assert (kt + share - 2) // share + 1 <= 9
     # the chosen cost never exceeds the data-parallel cost
     assert float(p["cost"]) <= math.ceil(T / SMS) * kt + 1e-9
 
@@ -194,3 +195,12 @@ def test_skinny_16x8192x8192_split():
     # cross a slab boundary hold 50 positions and pay for one more unit end.
     p = plan(16, 8192, 8192)
     assert ints(p, "tiles_n", "kt", "sk_share", "grid", "two_unit_ctas") == [32, 256, 55, 152, 31]
+
+
+@pytest.mark.parametrize("M,N,K,share,grid", [(768, 768, 4096, 16, 144), (640, 640, 8192, 32, 120)])
+def test_deep_products_with_few_tiles_split_finer(M, N, K, share, grid):
+    # 18 and 15 tiles: shares of an eighth of K keep most SMs busy while each
+    # tile stays within nine pieces.
+    p = plan(M, N, K)
+    assert p["variant"] == "streamk"
+    assert ints(p, "sk_share", "grid") == [share, grid]
