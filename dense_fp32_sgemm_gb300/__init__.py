@@ -45,7 +45,7 @@ _SIGNATURES = {
     "sgemm_run_skinny_noalloc": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp,
                                         _i64, _vp]),
     "sgemm_run_3xtf32": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
-    "sgemm_set_3xtf32_config": (_int, [_int, _int, _int]),
+    "sgemm_set_3xtf32_config": (_int, [_int, _int, _int, _int]),
     "sgemm_status_string": (ctypes.c_char_p, [_int]),
     "sgemm_device_status": (_int, [_vp]),
     "sgemm_plan_describe": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_uint64,
@@ -207,13 +207,15 @@ def run_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
     return C
 
 
-def set_3xtf32_config(bk: int = 16, a_in_kernel=None, splits: int = 0) -> None:
+def set_3xtf32_config(bk: int = 16, a_in_kernel=None, splits: int = 0,
+                      ctas_per_sm: int = 0) -> None:
     """3xTF32 kernel form: K depth of one pipeline stage (16, default, or 32);
     whether A is split inside the kernel (True), by a split pass (False) or as
     the library chooses per call (None, default); K ranges per output tile
-    (1 to 8, or 0 = chosen per call)."""
+    (1 to 8, or 0 = chosen per call); CTAs per SM (1, 2, or 0 = chosen per
+    call)."""
     mode = -1 if a_in_kernel is None else int(bool(a_in_kernel))
-    _check(library().sgemm_set_3xtf32_config(int(bk), mode, int(splits)),
+    _check(library().sgemm_set_3xtf32_config(int(bk), mode, int(splits), int(ctas_per_sm)),
            "sgemm_set_3xtf32_config")
 
 

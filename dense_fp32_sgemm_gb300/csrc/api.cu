@@ -33,6 +33,7 @@ std::atomic<int> g_micro_m{16};
 std::atomic<int> g_x3_bk{16};
 std::atomic<int> g_x3_a_in_kernel{-1};  // -1: chosen per call
 std::atomic<int> g_x3_splits{0};         // 0: chosen per call
+std::atomic<int> g_x3_ctas_per_sm{0};    // 0: chosen per call
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -73,7 +74,7 @@ struct DeviceState {
     std::map<cudaStream_t, Workspace> ws;
     HostBuffers host;
     unsigned configured = 0;            // skinny configurations set up
-    unsigned x3_configured = 0;         // 3xTF32 kernels set up (bit bk / 16 + 4 * a_raw)
+    std::set<int> x3_configured;        // 3xTF32 kernel forms set up
     std::set<int> configured_tiles;     // tile configurations set up
 };
 
@@ -366,14 +367,23 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
     const bool a_raw = a_mode >= 0 ? a_mode != 0
                                    : ((lda % 32) == 0 && !(reinterpret_cast<uintptr_t>(A) & 127u) &&
                                       M * N >= (int64_t)48 << 20);
-    const unsigned bit = 1u << (bk / 16 + (a_raw ? 4 : 0));
-    if (!(d->x3_configured & bit)) {
-        if (x3_configure(bk, a_raw) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-        d->x3_configured |= bit;
-    }
     const int kt_total = (int)((K + bk - 1) / bk);
     int bn = kX3BN, splits = 1;
     x3_plan(M, N, kt_total, d->num_sms, g_x3_splits.load(), &bn, &splits);
+    // Two CTAs per SM (K slice 16 only) overlap one tile's epilogue and
+    // start-up with another's MMAs; they pay off once there are at least two
+    // CTAs per SM to run (measured on GB300: 4092^3 520 -> 500 us, 8192^3
+    // 293 -> 308 TFLOP/s), while a single wave would crowd onto half the SMs
+    // (2048^3: 80 -> 128 us).
+    const int64_t ctas = ((M + kX3BM - 1) / kX3BM) * ((N + bn - 1) / bn) * splits;
+    const int cps = g_x3_ctas_per_sm.load();
+    const int stages = bk == 32 ? 2
+                       : (cps == 2 || (cps == 0 && ctas >= 2 * (int64_t)d->num_sms)) ? 2 : 4;
+    const int form = bk * 100 + stages * 10 + (a_raw ? 1 : 0);
+    if (!d->x3_configured.count(form)) {
+        if (x3_configure(bk, stages, a_raw) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        d->x3_configured.insert(form);
+    }
     const int64_t Mp = (M + kX3BM - 1) / kX3BM * kX3BM;
     const int64_t Np = (N + bn - 1) / bn * bn;
     const int64_t Kp = (K + 31) / 32 * 32;  // rows of whole 128-byte lines
@@ -438,7 +448,8 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
         if (s != SGEMM_OK) return s;
         p.c_tma = 1;
     }
-    if (launch_x3(bk, a_raw, mapA, mapB, mapC, p, st) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (launch_x3(bk, stages, a_raw, mapA, mapB, mapC, p, st) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
     if (splits > 1 && launch_x3_reduce(pr, splits, Mp * Np, Np, (int)M, (int)N, alpha, beta, C,
                                        ldc, d->num_sms, st) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
@@ -656,13 +667,15 @@ sgemm_status_t sgemm_set_tile_config(int fma_mode, int stages, int micro_m) {
     return SGEMM_OK;
 }
 
-sgemm_status_t sgemm_set_3xtf32_config(int bk, int a_in_kernel, int splits) {
+sgemm_status_t sgemm_set_3xtf32_config(int bk, int a_in_kernel, int splits, int ctas_per_sm) {
     if ((bk != 16 && bk != 32) || a_in_kernel < -1 || a_in_kernel > 1 || splits < 0 ||
-        splits > kX3MaxSplits)
+        splits > kX3MaxSplits || ctas_per_sm < 0 || ctas_per_sm > 2 ||
+        (bk == 32 && ctas_per_sm == 2))
         return SGEMM_ERR_INVALID_ARG;
     g_x3_bk.store(bk);
     g_x3_a_in_kernel.store(a_in_kernel);
     g_x3_splits.store(splits);
+    g_x3_ctas_per_sm.store(ctas_per_sm);
     return SGEMM_OK;
 }
 

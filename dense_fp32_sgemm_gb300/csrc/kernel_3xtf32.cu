@@ -53,16 +53,23 @@ constexpr int BN = kX3BN;
 constexpr int THREADS = 128;
 constexpr int TMEM_COLS = BN;  // FP32 accumulator: 128 lanes x 256 columns
 
-template <int BK>
+// Kernel forms: K slice BK (16 or 32) and ring stages S.  16 x 4 and 32 x 2
+// take about 193 KB of shared memory (one CTA per SM); 16 x 2 takes 97 KB, so
+// two CTAs share an SM and one's epilogue and start-up overlap the other's
+// MMAs (each holds 256 of the SM's 512 tensor-memory columns).
+template <int BK, int S>
 struct X3Cfg {
     static_assert(BK == 32 || BK == 16, "K slice of 32 (128-byte rows) or 16 (64-byte rows)");
     static constexpr int kRowBytes = BK * 4;                  // one swizzled row of K
     static constexpr uint32_t kA = BM * BK * 4;               // one A part (hi or lo)
     static constexpr uint32_t kB = BN * BK * 4;               // one B part (room for N 256)
     static constexpr uint32_t kStage = 2 * kA + 2 * kB;
-    static constexpr int kStages = BK == 32 ? 2 : 4;
+    static constexpr int kStages = S;
     static constexpr uint32_t kAlign = 8 * kRowBytes;         // one swizzle atom
     static constexpr size_t kSmem = (size_t)kStages * kStage + 1024;
+    static constexpr int kCtasPerSm = kSmem <= 112 * 1024 ? 2 : 1;
+    // The epilogue's C tile (128 KB) and staging (17 KB) fit in the idle ring.
+    static constexpr bool kCTile = (size_t)kStages * kStage >= 145 * 1024;
     // shared-memory descriptor layout type: 2 = 128-byte swizzle, 4 = 64-byte
     static constexpr uint64_t kLayout = BK == 32 ? 2 : 4;
 };
@@ -74,7 +81,7 @@ struct X3Cfg {
 // K-major operands.
 template <int BK>
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
-    using L = X3Cfg<BK>;
+    using L = X3Cfg<BK, 2>;
     uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
     d |= (uint64_t)1 << 16;                       // leading byte offset 16 (unused)
     d |= (uint64_t)(L::kAlign >> 4) << 32;        // stride byte offset: 8 rows
@@ -301,12 +308,12 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
 // ARAW: the TMA brings A's FP32 tile into the hi slot and warps 2 and 3 split
 // it in place (hi there, lo into the lo slot) before the MMAs of that stage;
 // otherwise both parts come from the split pass.
-template <int BK, bool ARAW>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int BK, int STAGES, bool ARAW>
+__global__ void __launch_bounds__(THREADS, (X3Cfg<BK, STAGES>::kCtasPerSm))
     sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap mapA,
                         const __grid_constant__ CUtensorMap mapB,
                         const __grid_constant__ CUtensorMap mapC, const X3Params p) {
-    using L = X3Cfg<BK>;
+    using L = X3Cfg<BK, STAGES>;
     constexpr int S = L::kStages;
     constexpr int kConvThreads = 64;  // warps 2 and 3
     extern __shared__ unsigned char x3_smem_raw[];
@@ -466,7 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!s_accum_ok) atomicOr(p.err, kErrDrainTimeout);
         // beta != 0: the stages are idle now; bring this tile's C in with the
         // TMA, 32 x 32 blocks, block (w, c) at floats (w * 8 + c) * 1024.
-        if (s_accum_ok && !s_abort && p.beta != 0.0f && p.c_tma) {
+        if (L::kCTile && s_accum_ok && !s_abort && p.beta != 0.0f && p.c_tma) {
             const int chunks = (bn + 31) / 32;
             mbar_arrive_expect_tx(&c_bar, 4u * chunks * 32 * 32 * 4);
             for (int w = 0; w < 4; ++w)
@@ -486,7 +493,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // C (beta != 0) comes from shared memory when the TMA brought it,
         // else from global memory, 32 independent loads per thread first.
         const float *c_tile = reinterpret_cast<const float *>(smem);  // 128 KB
-        float *stage = reinterpret_cast<float *>(smem + 128 * 1024) + warp * (32 * 33);
+        float *stage = reinterpret_cast<float *>(smem + (L::kCTile ? 128 * 1024 : 0)) +
+                       warp * (32 * 33);
         const uint32_t t_warp = tmem + ((uint32_t)(warp * 32) << 16);
         const int row0 = m0 + warp * 32;
         bool c_ok = true;
@@ -572,48 +580,60 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-int x3_stages(int bk) { return bk == 16 ? X3Cfg<16>::kStages : X3Cfg<32>::kStages; }
-
-size_t x3_smem_bytes(int bk) { return bk == 16 ? X3Cfg<16>::kSmem : X3Cfg<32>::kSmem; }
-
 namespace {
-template <int BK, bool ARAW>
+template <int BK, int S, bool ARAW>
 cudaError_t x3_configure_one() {
-    return cudaFuncSetAttribute(sgemm_3xtf32_kernel<BK, ARAW>,
+    const cudaError_t e = cudaFuncSetAttribute(sgemm_3xtf32_kernel<BK, S, ARAW>,
+                                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               100);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(sgemm_3xtf32_kernel<BK, S, ARAW>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)X3Cfg<BK>::kSmem);
+                                (int)X3Cfg<BK, S>::kSmem);
 }
-template <int BK, bool ARAW>
+template <int BK, int S, bool ARAW>
 cudaError_t x3_launch_one(const CUtensorMap &mapA, const CUtensorMap &mapB,
                           const CUtensorMap &mapC, const X3Params &p, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.tiles_m * p.tiles_n * p.splits);
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = X3Cfg<BK>::kSmem;
+    cfg.dynamicSmemBytes = X3Cfg<BK, S>::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel<BK, ARAW>, mapA, mapB, mapC, p);
+    return cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel<BK, S, ARAW>, mapA, mapB, mapC, p);
 }
 }  // namespace
 
-cudaError_t x3_configure(int bk, bool a_raw) {
-    if (bk == 16) return a_raw ? x3_configure_one<16, true>() : x3_configure_one<16, false>();
-    if (bk == 32) return a_raw ? x3_configure_one<32, true>() : x3_configure_one<32, false>();
+bool x3_form_valid(int bk, int stages) {
+    return (bk == 16 && (stages == 4 || stages == 2)) || (bk == 32 && stages == 2);
+}
+
+cudaError_t x3_configure(int bk, int stages, bool a_raw) {
+    if (bk == 16 && stages == 4)
+        return a_raw ? x3_configure_one<16, 4, true>() : x3_configure_one<16, 4, false>();
+    if (bk == 16 && stages == 2)
+        return a_raw ? x3_configure_one<16, 2, true>() : x3_configure_one<16, 2, false>();
+    if (bk == 32 && stages == 2)
+        return a_raw ? x3_configure_one<32, 2, true>() : x3_configure_one<32, 2, false>();
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_x3(int bk, bool a_raw, const CUtensorMap &mapA, const CUtensorMap &mapB,
-                      const CUtensorMap &mapC, const X3Params &p, cudaStream_t stream) {
-    if (bk == 16)
-        return a_raw ? x3_launch_one<16, true>(mapA, mapB, mapC, p, stream)
-                     : x3_launch_one<16, false>(mapA, mapB, mapC, p, stream);
-    if (bk == 32)
-        return a_raw ? x3_launch_one<32, true>(mapA, mapB, mapC, p, stream)
-                     : x3_launch_one<32, false>(mapA, mapB, mapC, p, stream);
+cudaError_t launch_x3(int bk, int stages, bool a_raw, const CUtensorMap &mapA,
+                      const CUtensorMap &mapB, const CUtensorMap &mapC, const X3Params &p,
+                      cudaStream_t stream) {
+    if (bk == 16 && stages == 4)
+        return a_raw ? x3_launch_one<16, 4, true>(mapA, mapB, mapC, p, stream)
+                     : x3_launch_one<16, 4, false>(mapA, mapB, mapC, p, stream);
+    if (bk == 16 && stages == 2)
+        return a_raw ? x3_launch_one<16, 2, true>(mapA, mapB, mapC, p, stream)
+                     : x3_launch_one<16, 2, false>(mapA, mapB, mapC, p, stream);
+    if (bk == 32 && stages == 2)
+        return a_raw ? x3_launch_one<32, 2, true>(mapA, mapB, mapC, p, stream)
+                     : x3_launch_one<32, 2, false>(mapA, mapB, mapC, p, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -81,15 +81,17 @@ struct X3Params {
     int skip_loads_from;   // testing hook, -1 = off
 };
 
-// bk: 32 (128-byte swizzled rows) or 16 (64-byte swizzled rows).
+// Kernel forms (bk = K slice, stages = ring depth): 16 x 4 and 32 x 2 run
+// one CTA per SM; 16 x 2 runs two CTAs per SM.
 // a_raw: mapA covers A itself (FP32, M x K) and the kernel splits each A
 // tile in shared memory; otherwise mapA covers the split pass's A buffer.
-int x3_stages(int bk);
-size_t x3_smem_bytes(int bk);
-cudaError_t x3_configure(int bk, bool a_raw);
-// mapC: C as M x N FP32, 32 x 32 boxes, used when beta != 0 and p.c_tma.
-cudaError_t launch_x3(int bk, bool a_raw, const CUtensorMap &mapA, const CUtensorMap &mapB,
-                      const CUtensorMap &mapC, const X3Params &p, cudaStream_t stream);
+// mapC: C as M x N FP32, 32 x 32 boxes, used when beta != 0 and p.c_tma (one
+// CTA per SM forms only; the two-CTA form reads C directly).
+bool x3_form_valid(int bk, int stages);
+cudaError_t x3_configure(int bk, int stages, bool a_raw);
+cudaError_t launch_x3(int bk, int stages, bool a_raw, const CUtensorMap &mapA,
+                      const CUtensorMap &mapB, const CUtensorMap &mapC, const X3Params &p,
+                      cudaStream_t stream);
 // C = alpha * (part[0] + ... + part[splits - 1]) + beta * C, the slices added
 // in order (deterministic).
 cudaError_t launch_x3_reduce(const float *part, int splits, long long stride, long long ld_part,

@@ -265,8 +265,8 @@ SGEMM_API sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float
 
 /*
  * sgemm_set_3xtf32_config -- tuning hook, process-wide, for the 3xTF32 kernel.
- * bk: the K depth of one pipeline stage, 16 (four stages of 64-byte swizzled
- *   rows, the default) or 32 (two stages of 128-byte rows).
+ * bk: the K depth of one pipeline stage, 16 (64-byte swizzled rows, the
+ *   default) or 32 (two stages of 128-byte rows, one CTA per SM).
  * a_in_kernel: 1 = the kernel loads A itself and splits each A tile in
  *   shared memory; 0 = a split pass writes A's hi and lo parts first;
  *   -1 (default) = 1 when M*N >= 48 * 2^20 and A's rows start on 128-byte
@@ -276,10 +276,15 @@ SGEMM_API sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float
  *   products with few tiles are cut so that more SMs work, and a reduction
  *   kernel adds the ranges' raw tiles in range order, then applies alpha and
  *   beta.  A count that leaves a range under 16 K slices is not taken.
+ * ctas_per_sm: 1 = one CTA per SM with a 4-stage ring; 2 = two CTAs per SM
+ *   with 2 stages each (bk 16 only), so that one CTA's epilogue and start-up
+ *   overlap the other's MMAs; 0 (default) = 2 when the launch has at least
+ *   two CTAs per SM to run, else 1.
  * For a given split count all forms compute the same products in the same
  * order (bitwise equal results).  SGEMM_ERR_INVALID_ARG for other values.
  */
-SGEMM_API sgemm_status_t sgemm_set_3xtf32_config(int bk, int a_in_kernel, int splits);
+SGEMM_API sgemm_status_t sgemm_set_3xtf32_config(int bk, int a_in_kernel, int splits,
+                                                 int ctas_per_sm);
 
 /* Free every workspace and host-path buffer the library holds on all devices. */
 SGEMM_API sgemm_status_t sgemm_release_workspace(void);

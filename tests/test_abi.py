@@ -124,10 +124,12 @@ def test_hooks_validate(lib):
     for bk in (0, 8, 24, 64):
         with pytest.raises(sg.SgemmError):
             sg.set_3xtf32_config(bk, True)
-    assert lib.sgemm_set_3xtf32_config(16, 2, 0) == 1
-    assert lib.sgemm_set_3xtf32_config(16, -2, 0) == 1
-    assert lib.sgemm_set_3xtf32_config(16, -1, -1) == 1
-    assert lib.sgemm_set_3xtf32_config(16, -1, 9) == 1
+    assert lib.sgemm_set_3xtf32_config(16, 2, 0, 0) == 1
+    assert lib.sgemm_set_3xtf32_config(16, -2, 0, 0) == 1
+    assert lib.sgemm_set_3xtf32_config(16, -1, -1, 0) == 1
+    assert lib.sgemm_set_3xtf32_config(16, -1, 9, 0) == 1
+    assert lib.sgemm_set_3xtf32_config(16, -1, 0, 3) == 1
+    assert lib.sgemm_set_3xtf32_config(32, -1, 0, 2) == 1
     sg.set_3xtf32_config(32, False)
     sg.set_3xtf32_config(16, None)
     sg.set_plan_override(-1, 0)

@@ -88,27 +88,30 @@ def test_normal_inputs_within_bound():
     check(700, 900, 1500, 1.0, 0.0, dist="normal")
 
 
-@pytest.mark.parametrize("bk,a_in_kernel", [(16, False), (32, True), (32, False), (16, None)])
-def test_kernel_forms_bitwise_identical(bk, a_in_kernel):
+@pytest.mark.parametrize("bk,a_in_kernel,cps", [(16, False, 0), (32, True, 0), (32, False, 0),
+                                                (16, None, 0), (16, True, 2), (16, False, 2),
+                                                (16, None, 1)])
+def test_kernel_forms_bitwise_identical(bk, a_in_kernel, cps):
     # Same split, same products, same order: the K depth of a stage and where
     # A is split do not change a bit of the result.
     M, N, K = 520, 770, 700
     A, lda, B, ldb, C, ldc = inputs("uniform", 5, M, N, K)
     sg.set_3xtf32_config(16, True)
     ref_out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
-    sg.set_3xtf32_config(bk, a_in_kernel)
+    sg.set_3xtf32_config(bk, a_in_kernel, 0, cps)
     try:
         out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc, entry=X3)
     finally:
         sg.set_3xtf32_config(16, None)
     assert np.array_equal(out.view(np.uint32), ref_out.view(np.uint32))
     ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, ldc)
-    assert_within(out, ref, bound, f"3xTF32 bk={bk} a_in_kernel={a_in_kernel}")
+    assert_within(out, ref, bound, f"3xTF32 bk={bk} a_in_kernel={a_in_kernel} cps={cps}")
 
 
-@pytest.mark.parametrize("bk,a_in_kernel", [(16, False), (16, True), (32, True)])
-def test_timeout_in_other_forms(bk, a_in_kernel):
-    sg.set_3xtf32_config(bk, a_in_kernel)
+@pytest.mark.parametrize("bk,a_in_kernel,cps", [(16, False, 0), (16, True, 0), (32, True, 0),
+                                                (16, True, 2), (16, False, 2)])
+def test_timeout_in_other_forms(bk, a_in_kernel, cps):
+    sg.set_3xtf32_config(bk, a_in_kernel, 0, cps)
     try:
         test_wait_timeout_reports_and_recovers()
     finally:
@@ -286,3 +289,14 @@ def test_timeout_with_a_k_split():
         test_wait_timeout_reports_and_recovers()
     finally:
         sg.set_3xtf32_config(16, None, 0)
+
+
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (0.5, 2.0)])
+def test_two_ctas_per_sm_with_beta(alpha, beta):
+    # The two-CTA form reads C directly (no room for the TMA C tile).
+    sg.set_3xtf32_config(16, None, 0, 2)
+    try:
+        check(1000, 1030, 333, alpha, beta, dist="uniform", seed=41)
+        check(257, 513, 100, alpha, beta, dist="ints", seed=42, exact=(beta == 0.0))
+    finally:
+        sg.set_3xtf32_config(16, None)
