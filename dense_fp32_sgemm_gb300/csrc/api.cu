@@ -371,14 +371,14 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
     int bn = kX3BN, splits = 1;
     x3_plan(M, N, kt_total, d->num_sms, g_x3_splits.load(), &bn, &splits);
     // Two CTAs per SM (K slice 16 only) overlap one tile's epilogue and
-    // start-up with another's MMAs; they pay off once there are at least two
-    // CTAs per SM to run (measured on GB300: 4092^3 520 -> 500 us, 8192^3
-    // 293 -> 308 TFLOP/s), while a single wave would crowd onto half the SMs
-    // (2048^3: 80 -> 128 us).
+    // start-up with another's MMAs; they pay off once the launch has more
+    // than one wave (measured on GB300: 3072^3 with 288 CTAs 230 -> 217 us,
+    // 4092^3 520 -> 500 us, 8192^3 293 -> 308 TFLOP/s), while a single wave
+    // would crowd onto half the SMs (2048^3: 80 -> 128 us).
     const int64_t ctas = ((M + kX3BM - 1) / kX3BM) * ((N + bn - 1) / bn) * splits;
     const int cps = g_x3_ctas_per_sm.load();
     const int stages = bk == 32 ? 2
-                       : (cps == 2 || (cps == 0 && ctas >= 2 * (int64_t)d->num_sms)) ? 2 : 4;
+                       : (cps == 2 || (cps == 0 && ctas > (int64_t)d->num_sms)) ? 2 : 4;
     const int form = bk * 100 + stages * 10 + (a_raw ? 1 : 0);
     if (!d->x3_configured.count(form)) {
         if (x3_configure(bk, stages, a_raw) != cudaSuccess) return SGEMM_ERR_LAUNCH;

@@ -278,8 +278,8 @@ SGEMM_API sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float
  *   beta.  A count that leaves a range under 16 K slices is not taken.
  * ctas_per_sm: 1 = one CTA per SM with a 4-stage ring; 2 = two CTAs per SM
  *   with 2 stages each (bk 16 only), so that one CTA's epilogue and start-up
- *   overlap the other's MMAs; 0 (default) = 2 when the launch has at least
- *   two CTAs per SM to run, else 1.
+ *   overlap the other's MMAs; 0 (default) = 2 when the launch has more CTAs
+ *   than the GPU has SMs, else 1.
  * For a given split count all forms compute the same products in the same
  * order (bitwise equal results).  SGEMM_ERR_INVALID_ARG for other values.
  */
