@@ -300,3 +300,31 @@ def test_two_ctas_per_sm_with_beta(alpha, beta):
         check(257, 513, 100, alpha, beta, dist="ints", seed=42, exact=(beta == 0.0))
     finally:
         sg.set_3xtf32_config(16, None)
+
+
+def _random_cases(seed, count):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(count):
+        M = int(rng.integers(17, 1500))
+        N = int(rng.integers(1, 1500))
+        K = int(rng.integers(64, 3000))
+        alpha = float(rng.choice([1.0, 0.5, -2.0]))
+        beta = float(rng.choice([0.0, 1.0, -0.5]))
+        bk = int(rng.choice([16, 32]))
+        a_mode = [None, True, False][int(rng.integers(0, 3))]
+        splits = int(rng.choice([0, 0, 2, 3, 8]))
+        cps = 0 if bk == 32 else int(rng.choice([0, 1, 2]))
+        cases.append((M, N, K, alpha, beta, bk, a_mode, splits, cps))
+    return cases
+
+
+@pytest.mark.parametrize("M,N,K,alpha,beta,bk,a_mode,splits,cps", _random_cases(2026, 24))
+def test_random_shapes_and_forms(M, N, K, alpha, beta, bk, a_mode, splits, cps):
+    # Seeded random shapes (ragged in every dimension) crossed with random
+    # kernel forms, K splits and CTAs per SM: all within the bound.
+    sg.set_3xtf32_config(bk, a_mode, splits, cps)
+    try:
+        check(M, N, K, alpha, beta, dist="uniform", seed=M + N + K)
+    finally:
+        sg.set_3xtf32_config(16, None)

@@ -487,3 +487,23 @@ def test_capture_in_a_cuda_graph_and_replay(M, N, K):
         torch.cuda.synchronize()
         assert torch.equal(dC, eager)
     assert sg.device_status() == 0
+
+
+def _random_ffma_cases(seed, count):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        M = int(rng.integers(1, 1400))
+        N = int(rng.integers(1, 1400))
+        K = int(rng.integers(1, 2500))
+        pad = [int(rng.choice([0, 0, 1, 3])) for _ in range(3)]
+        out.append((M, N, K, float(rng.choice([1.0, -0.5])), float(rng.choice([0.0, 2.0])), pad))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,alpha,beta,pad", _random_ffma_cases(7, 24))
+def test_random_shapes_planned(M, N, K, alpha, beta, pad):
+    # Seeded random shapes and leading-dimension padding through whatever
+    # plan the planner picks (skinny, 64 x 64, tiled, stream-K, copies).
+    check(M, N, K, alpha, beta, lda=K + pad[0], ldb=N + pad[1], ldc=N + pad[2], seed=M ^ N ^ K,
+          label=f"random {M}x{N}x{K} pad={pad}")
