@@ -45,6 +45,8 @@ _SIGNATURES = {
     "sgemm_run_skinny_noalloc": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp,
                                         _i64, _vp]),
     "sgemm_run_3xtf32": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
+    "sgemm_run_3xtf32_epilogue": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp,
+                                         _i64, _vp, _int, _vp]),
     "sgemm_set_3xtf32_config": (_int, [_int, _int, _int, _int]),
     "sgemm_status_string": (ctypes.c_char_p, [_int]),
     "sgemm_device_status": (_int, [_vp]),
@@ -129,6 +131,14 @@ def sgemm_run_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) 
                                       int(ldb), float(beta), C, int(ldc), stream)
 
 
+def sgemm_run_3xtf32_epilogue(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias=None,
+                              activation=ACT_NONE, stream=None) -> int:
+    """Raw C-ABI call of the 3xTF32 variant with bias / activation."""
+    return library().sgemm_run_3xtf32_epilogue(int(M), int(N), int(K), float(alpha), A, int(lda),
+                                               B, int(ldb), float(beta), C, int(ldc), bias,
+                                               int(activation), stream)
+
+
 def sgemm_run_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
     """Raw C-ABI call with integer host addresses; returns the status."""
     return library().sgemm_run_host(int(M), int(N), int(K), float(alpha), A, int(lda), B,
@@ -185,10 +195,11 @@ def run(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, bias=None,
     return C
 
 
-def run_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
-    """C = alpha * A @ B + beta * C in place, on the tensor cores by the
-    3xTF32 split (hi*hi + hi*lo + lo*hi of TF32 parts, FP32 accumulation).
-    Same tensors and conventions as run(); no bias or activation."""
+def run_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, bias=None,
+               activation: int = ACT_NONE):
+    """C = act(alpha * A @ B + beta * C + bias) in place, on the tensor cores
+    by the 3xTF32 split (hi*hi + hi*lo + lo*hi of TF32 parts, FP32
+    accumulation).  Same tensors and conventions as run()."""
     import torch
 
     M, K = A.shape
@@ -202,8 +213,19 @@ def run_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
     b, ldb = _matrix_args(B, "B")
     c, ldc = _matrix_args(C, "C")
     s = (stream or torch.cuda.current_stream(C.device)).cuda_stream
+    bias_ptr = None
+    if bias is not None:
+        if not bias.is_cuda or str(bias.dtype) != "torch.float32" or bias.numel() != N or (
+                bias.dim() != 1 and not bias.is_contiguous()) or (bias.dim() == 1 and bias.stride(0) != 1):
+            raise ValueError("bias must be a contiguous CUDA float32 tensor of N elements")
+        bias_ptr = bias.data_ptr()
     with torch.cuda.device(C.device):
-        _check(sgemm_run_3xtf32(M, N, K, alpha, a, lda, b, ldb, beta, c, ldc, s), "sgemm_run_3xtf32")
+        if bias_ptr is None and activation == ACT_NONE:
+            _check(sgemm_run_3xtf32(M, N, K, alpha, a, lda, b, ldb, beta, c, ldc, s),
+                   "sgemm_run_3xtf32")
+        else:
+            _check(sgemm_run_3xtf32_epilogue(M, N, K, alpha, a, lda, b, ldb, beta, c, ldc, bias_ptr,
+                                             activation, s), "sgemm_run_3xtf32_epilogue")
     return C
 
 

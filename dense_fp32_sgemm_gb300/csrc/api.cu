@@ -340,20 +340,25 @@ sgemm_status_t sgemm_run(int64_t M, int64_t N, int64_t K, float alpha, const flo
                               SGEMM_ACT_NONE, stream);
 }
 
-sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
-                                int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-                                int64_t ldc, void *stream) {
+sgemm_status_t sgemm_run_3xtf32_epilogue(int64_t M, int64_t N, int64_t K, float alpha,
+                                         const float *A, int64_t lda, const float *B, int64_t ldb,
+                                         float beta, float *C, int64_t ldc, const float *bias,
+                                         int activation, void *stream) {
     const sgemm_status_t v = validate(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
     if (v != SGEMM_OK) return v;
+    if (activation != SGEMM_ACT_NONE && activation != SGEMM_ACT_RELU) return SGEMM_ERR_INVALID_ARG;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return SGEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return SGEMM_OK;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState *d = nullptr;
     sgemm_status_t s = device_state(&d);
     if (s != SGEMM_OK) return s;
-    const Epilogue none{nullptr, kActNone};
+    Epilogue epi;
+    epi.bias = bias;
+    epi.act = activation == SGEMM_ACT_RELU ? kActRelu : kActNone;
     if (K < kX3MinK || M <= 16 || alpha == 0.0f)
-        return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, none, st, *d);
+        return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, st, *d);
     if (M > (1 << 29) || N > (1 << 29) || K > (1 << 30) ||
         ((M + kX3BM - 1) / kX3BM) * ((N + kX3MinBN - 1) / kX3MinBN) * kX3MaxSplits > INT32_MAX)
         return SGEMM_ERR_INVALID_ARG;
@@ -437,6 +442,7 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
     p.alpha = splits > 1 ? 1.0f : alpha;
     p.beta = splits > 1 ? 0.0f : beta;
     p.C = C; p.ldc = ldc;
+    p.epi = splits > 1 ? Epilogue{nullptr, kActNone} : epi;
     p.err = d->err;
     const unsigned long long to = g_timeout_ns.load();
     p.timeout_ns = to ? to : kDefaultTimeoutNs;
@@ -451,9 +457,16 @@ sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, co
     if (launch_x3(bk, stages, a_raw, mapA, mapB, mapC, p, st) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     if (splits > 1 && launch_x3_reduce(pr, splits, Mp * Np, Np, (int)M, (int)N, alpha, beta, C,
-                                       ldc, d->num_sms, st) != cudaSuccess)
+                                       ldc, epi, d->num_sms, st) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                                int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                                int64_t ldc, void *stream) {
+    return sgemm_run_3xtf32_epilogue(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, nullptr,
+                                     SGEMM_ACT_NONE, stream);
 }
 
 // Host <-> device copy of `rows` rows of `width` floats; one contiguous copy

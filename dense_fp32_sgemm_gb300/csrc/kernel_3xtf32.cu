@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(256) x3_reduce_kernel(const float *__restrict_
                                                         int splits, long long stride,
                                                         long long ld_part, int M, int N,
                                                         float alpha, float beta, float *C,
-                                                        long long ldc) {
+                                                        long long ldc, const Epilogue epi) {
     const long long total = (long long)M * N;
     for (long long i = blockIdx.x * 256LL + threadIdx.x; i < total; i += gridDim.x * 256LL) {
         const int m = (int)(i / N), n = (int)(i % N);
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(256) x3_reduce_kernel(const float *__restrict_
         float *c = C + (long long)m * ldc + n;
         float v = alpha * sum;
         if (beta != 0.0f) v = __fmaf_rn(beta, *c, v);
-        *c = v;
+        *c = apply_epilogue(v, epi, n);
     }
 }
 
@@ -531,15 +531,16 @@ __global__ void __launch_bounds__(THREADS, (X3Cfg<BK, STAGES>::kCtasPerSm))
                 for (int i = 0; i < 32; ++i) {
                     const int m = row0 + i;
                     if (m < p.M)
-                        out[(long long)m * ldo + n] =
-                            __fmaf_rn(p.beta, cv[i], p.alpha * stage[i * 33 + lane]);
+                        out[(long long)m * ldo + n] = apply_epilogue(
+                            __fmaf_rn(p.beta, cv[i], p.alpha * stage[i * 33 + lane]), p.epi, n);
                 }
             } else if (col_ok) {
 #pragma unroll 4
                 for (int i = 0; i < 32; ++i) {
                     const int m = row0 + i;
                     if (m >= p.M) break;
-                    out[(long long)m * ldo + n] = p.alpha * stage[i * 33 + lane];
+                    out[(long long)m * ldo + n] =
+                        apply_epilogue(p.alpha * stage[i * 33 + lane], p.epi, n);
                 }
             }
             __syncwarp();
@@ -639,11 +640,11 @@ cudaError_t launch_x3(int bk, int stages, bool a_raw, const CUtensorMap &mapA,
 
 cudaError_t launch_x3_reduce(const float *part, int splits, long long stride, long long ld_part,
                              int M, int N, float alpha, float beta, float *C, long long ldc,
-                             int num_sms, cudaStream_t stream) {
+                             const Epilogue &epi, int num_sms, cudaStream_t stream) {
     const long long total = (long long)M * N;
     const long long blocks = std::min<long long>((total + 255) / 256, (long long)num_sms * 8);
     x3_reduce_kernel<<<(int)std::max<long long>(blocks, 1), 256, 0, stream>>>(
-        part, splits, stride, ld_part, M, N, alpha, beta, C, ldc);
+        part, splits, stride, ld_part, M, N, alpha, beta, C, ldc, epi);
     return cudaGetLastError();
 }
 

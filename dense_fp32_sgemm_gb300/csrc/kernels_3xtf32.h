@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kernels.h"  // Epilogue
+
 namespace sgemm {
 
 // ---------------------------------------------------------------------------
@@ -76,6 +78,7 @@ struct X3Params {
     float *C;
     long long ldc;
     int c_tma;             // mapC covers C (16-byte aligned, ldc a multiple of 4)
+    Epilogue epi;          // bias / activation after alpha and beta (none for K splits)
     int *err;
     unsigned long long timeout_ns;
     int skip_loads_from;   // testing hook, -1 = off
@@ -92,11 +95,11 @@ cudaError_t x3_configure(int bk, int stages, bool a_raw);
 cudaError_t launch_x3(int bk, int stages, bool a_raw, const CUtensorMap &mapA,
                       const CUtensorMap &mapB, const CUtensorMap &mapC, const X3Params &p,
                       cudaStream_t stream);
-// C = alpha * (part[0] + ... + part[splits - 1]) + beta * C, the slices added
-// in order (deterministic).
+// C = act(alpha * (part[0] + ... + part[splits - 1]) + beta * C + bias), the
+// slices added in order (deterministic).
 cudaError_t launch_x3_reduce(const float *part, int splits, long long stride, long long ld_part,
                              int M, int N, float alpha, float beta, float *C, long long ldc,
-                             int num_sms, cudaStream_t stream);
+                             const Epilogue &epi, int num_sms, cudaStream_t stream);
 // Split A (M x K, lda; skipped when A is null) and B (K x N, ldb) into the
 // buffers above.  Kp is a multiple of 4; Mp and Np multiples of the tile
 // sizes.

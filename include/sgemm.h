@@ -264,6 +264,19 @@ SGEMM_API sgemm_status_t sgemm_run_3xtf32(int64_t M, int64_t N, int64_t K, float
                                           void *stream);
 
 /*
+ * sgemm_run_3xtf32_epilogue -- sgemm_run_3xtf32 with the epilogue of
+ * sgemm_run_epilogue: C = act(alpha * A * B + beta * C + bias), bias a
+ * device vector of N floats (or NULL), activation SGEMM_ACT_NONE or
+ * SGEMM_ACT_RELU, each element rounded as fl(fl(alpha*acc + beta*c) + bias_j)
+ * before the activation.  Argument checks and errors are those of
+ * sgemm_run_epilogue; accuracy that of sgemm_run_3xtf32.
+ */
+SGEMM_API sgemm_status_t sgemm_run_3xtf32_epilogue(int64_t M, int64_t N, int64_t K, float alpha,
+                                                   const float *A, int64_t lda, const float *B,
+                                                   int64_t ldb, float beta, float *C, int64_t ldc,
+                                                   const float *bias, int activation, void *stream);
+
+/*
  * sgemm_set_3xtf32_config -- tuning hook, process-wide, for the 3xTF32 kernel.
  * bk: the K depth of one pipeline stage, 16 (64-byte swizzled rows, the
  *   default) or 32 (two stages of 128-byte rows, one CTA per SM).

@@ -67,7 +67,12 @@ def run_gemm(M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, offsets=(0, 0, 0),
     sg.set_plan_override(variant, splits)
     try:
         stream = torch.cuda.current_stream().cuda_stream
-        if entry == "sgemm_run_3xtf32":
+        if entry == "sgemm_run_3xtf32" and (bias is not None or activation != 0):
+            st = sg.sgemm_run_3xtf32_epilogue(M, N, K, alpha, dA.ptr, lda, dB.ptr, ldb, beta,
+                                              dC.ptr, ldc,
+                                              dbias.ptr if dbias is not None else None,
+                                              activation, stream)
+        elif entry == "sgemm_run_3xtf32":
             st = sg.sgemm_run_3xtf32(M, N, K, alpha, dA.ptr, lda, dB.ptr, ldb, beta, dC.ptr, ldc,
                                      stream)
         elif bias is None and activation == 0:

@@ -88,6 +88,9 @@ def test_3xtf32_arguments_rejected_before_any_device_call(lib, args):
 def test_epilogue_arguments_rejected_before_any_device_call(lib, bias, activation):
     st = sg.sgemm_run_epilogue(4, 5, 6, 1.0, 4096, 6, 8192, 5, 0.0, 16384, 5, bias, activation)
     assert st == 1, sg.status_string(st)
+    st = sg.sgemm_run_3xtf32_epilogue(4, 5, 6, 1.0, 4096, 6, 8192, 5, 0.0, 16384, 5, bias,
+                                      activation)
+    assert st == 1, sg.status_string(st)
 
 
 def test_empty_output_is_a_no_op_without_device(lib):

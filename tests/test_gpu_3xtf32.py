@@ -328,3 +328,56 @@ def test_random_shapes_and_forms(M, N, K, alpha, beta, bk, a_mode, splits, cps):
         check(M, N, K, alpha, beta, dist="uniform", seed=M + N + K)
     finally:
         sg.set_3xtf32_config(16, None)
+
+
+# (M, N, K, splits, ctas per SM): the MMA kernel's store in both forms, the
+# reduction of a K split, and the FFMA hand-over (M <= 16).
+X3_EPI_CASES = [(300, 520, 256, 0, 0), (640, 1030, 1024, 0, 2), (300, 520, 2000, 3, 0),
+                (16, 1024, 300, 0, 0)]
+
+
+@pytest.mark.parametrize("activation", [0, 1])
+@pytest.mark.parametrize("M,N,K,splits,cps", X3_EPI_CASES)
+def test_epilogue_integers_bit_exact(M, N, K, splits, cps, activation):
+    A, lda, B, ldb, C, ldc = inputs("ints", 51, M, N, K)
+    bias = (np.arange(N) % 41 - 20).astype(np.float32)
+    sg.set_3xtf32_config(16, None, splits, cps)
+    try:
+        out, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc, bias=bias,
+                          activation=activation, entry=X3)
+    finally:
+        sg.set_3xtf32_config(16, None)
+    want = (A.reshape(M, lda)[:, :K].astype(np.int64) @ B.reshape(K, ldb)[:, :N].astype(np.int64)
+            + C.reshape(M, ldc)[:, :N].astype(np.int64) + bias.astype(np.int64)[None, :])
+    if activation == 1:
+        want = np.maximum(want, 0)
+    assert np.array_equal(out.astype(np.int64), want)
+
+
+@pytest.mark.parametrize("M,N,K,splits,cps", X3_EPI_CASES)
+def test_epilogue_floats_within_bound(M, N, K, splits, cps):
+    A, lda, B, ldb, C, ldc = inputs("normal", 52, M, N, K, ldc=N + 4)
+    bias = datagen.normal01(53, "C", N)
+    sg.set_3xtf32_config(16, None, splits, cps)
+    try:
+        out, _ = run_gemm(M, N, K, 0.75, -0.5, A, lda, B, ldb, C, ldc, bias=bias, activation=1,
+                          entry=X3)
+    finally:
+        sg.set_3xtf32_config(16, None)
+    ref, absprod = oracle.sgemm_ref_flat(M, N, K, 0.75, A, lda, B, ldb, -0.5, C, ldc)
+    want = oracle.apply_epilogue(ref, bias, oracle.ACT_RELU)
+    bound = oracle.error_bound(absprod, C.reshape(M, ldc)[:, :N], 0.75, -0.5, K, bias=bias)
+    assert_within(out, want, bound, f"3xTF32 epilogue {M}x{N}x{K} splits={splits} cps={cps}")
+    assert (out >= 0).all()
+
+
+def test_epilogue_torch_binding():
+    M, N, K = 384, 512, 320
+    A = torch.from_numpy(datagen.matrix("ints", 54, "A", M, K)).cuda().view(M, K)
+    B = torch.from_numpy(datagen.matrix("ints", 54, "B", K, N)).cuda().view(K, N)
+    C = torch.zeros(M, N, device="cuda")
+    bias = torch.arange(N, dtype=torch.float32, device="cuda") - 256.0
+    sg.run_3xtf32(A, B, C, bias=bias, activation=sg.ACT_RELU)
+    torch.cuda.synchronize()
+    want = torch.clamp(A.cpu().double() @ B.cpu().double() + bias.cpu().double(), min=0)
+    assert torch.equal(C.cpu().double(), want)
