@@ -526,21 +526,36 @@ __global__ void __launch_bounds__(THREADS, (X3Cfg<BK, STAGES>::kCtasPerSm))
 #pragma unroll
             for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = __uint_as_float(r[j]);
             __syncwarp();
-            if (col_ok && p.beta != 0.0f) {
+            // The bias / activation test is made once per column block: the
+            // plain loops are what calls without an epilogue run.
+            const bool has_bias = p.epi.bias != nullptr, relu = p.epi.act == kActRelu;
+            if (col_ok && (has_bias || relu)) {
+                const float bias_n = has_bias ? __ldg(p.epi.bias + n) : 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int m = row0 + i;
+                    if (m < p.M) {
+                        float v = p.alpha * stage[i * 33 + lane];
+                        if (p.beta != 0.0f) v = __fmaf_rn(p.beta, cv[i], v);
+                        if (has_bias) v += bias_n;  // as apply_epilogue: no add without a bias
+                        if (relu) v = (v < 0.0f) ? 0.0f : v;
+                        out[(long long)m * ldo + n] = v;
+                    }
+                }
+            } else if (col_ok && p.beta != 0.0f) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int m = row0 + i;
                     if (m < p.M)
-                        out[(long long)m * ldo + n] = apply_epilogue(
-                            __fmaf_rn(p.beta, cv[i], p.alpha * stage[i * 33 + lane]), p.epi, n);
+                        out[(long long)m * ldo + n] =
+                            __fmaf_rn(p.beta, cv[i], p.alpha * stage[i * 33 + lane]);
                 }
             } else if (col_ok) {
 #pragma unroll 4
                 for (int i = 0; i < 32; ++i) {
                     const int m = row0 + i;
                     if (m >= p.M) break;
-                    out[(long long)m * ldo + n] =
-                        apply_epilogue(p.alpha * stage[i * 33 + lane], p.epi, n);
+                    out[(long long)m * ldo + n] = p.alpha * stage[i * 33 + lane];
                 }
             }
             __syncwarp();
