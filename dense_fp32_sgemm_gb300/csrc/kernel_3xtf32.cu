@@ -20,24 +20,27 @@
 // accumulator, so the result differs from the FP32 one only by the dropped
 // terms and the accumulation order.
 //
-// Structure (one 128 x bn tile of C per CTA, bn <= 256, 128 threads; deep
-// products with few tiles give each CTA one K range of a tile instead, and a
-// reduction kernel adds the ranges' raw tiles in order):
+// Structure (one 128 x bn tile of C per CTA, 64 <= bn <= 256, 128 threads,
+// one or two CTAs per SM; deep products with few tiles give each CTA one K
+// range of a tile instead, and a reduction kernel adds the ranges' raw tiles
+// in order):
 //   split pass   A -> [A_hi; A_lo] (K-major rows), B -> [B_hi^T; B_lo^T]
 //                (transposed to K-major), zero padded; an HBM-bound pass.
 //                The MMA kernel is launched as its programmatic dependent:
 //                its CTAs set up while the pass finishes, and the load
 //                issuer waits for the pass's results before its first copy.
-//   warp 0       one thread issues the TMA loads of the four operand tiles
-//                of each K slice into a ring of swizzled shared-memory stages.
+//   warp 0       one thread issues the TMA loads of the operand tiles of each
+//                K slice into a ring of swizzled shared-memory stages.
 //   warp 1       one thread issues tcgen05.mma (M 128, N bn, K 8) three
 //                times per K step, accumulating in tensor memory, and
 //                releases each stage with tcgen05.commit.
 //   warp 2       allocates and frees the 256 tensor-memory columns.
+//   warps 2, 3   (large outputs) split each FP32 A tile in shared memory
+//                instead of the pass.
 //   all 4 warps  epilogue: tcgen05.ld of their 32 accumulator lanes, through
-//                shared memory to coalesced rows, alpha / beta, store; with
-//                beta != 0 the tile of C is first brought into the idle
-//                stages by the TMA.
+//                shared memory to coalesced rows, alpha / beta, bias and
+//                ReLU, store; with beta != 0 the one-CTA forms bring the
+//                tile of C into the idle stages with the TMA first.
 // Every wait is bounded; on a timeout the kernel flags the error word, waits
 // (bounded) for its copies and MMAs in flight, frees tensor memory and exits.
 #include <algorithm>
