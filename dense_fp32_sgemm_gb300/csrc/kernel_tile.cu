@@ -431,6 +431,15 @@ __device__ __forceinline__ void store_tile(Acc<FM, TM> &acc, const TileParams &p
             if (m >= p.M) continue;
             float *crow = p.C + (long long)m * p.ldc;
             const int ti = r * 4 + i;
+            float4 cvr[2];
+            if (beta != 0.0f && p.c_vec4) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int n = n_base + c * 32;
+                    cvr[c] = n + 3 < p.N ? *reinterpret_cast<const float4 *>(crow + n)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int n = n_base + c * 32;
@@ -441,7 +450,7 @@ __device__ __forceinline__ void store_tile(Acc<FM, TM> &acc, const TileParams &p
                     o.z = alpha * acc.at(ti, c * 4 + 2);
                     o.w = alpha * acc.at(ti, c * 4 + 3);
                     if (beta != 0.0f) {
-                        const float4 cv = *reinterpret_cast<const float4 *>(crow + n);
+                        const float4 cv = cvr[c];
                         o.x = __fmaf_rn(beta, cv.x, o.x);
                         o.y = __fmaf_rn(beta, cv.y, o.y);
                         o.z = __fmaf_rn(beta, cv.z, o.z);
@@ -519,53 +528,83 @@ __device__ __forceinline__ void fixup_from_l2(const TileParams &p, int tm, int t
 }
 
 // Through the idle ring of a CTA's final unit: band by band (four float4 per
-// thread, 16 KB per piece) the pieces come in with bulk copies, one L2 round
-// trip per band.  Takes up to ring capacity / 16 KB pieces.  Returns false
-// (uniformly) if a copy did not arrive in time; the caller then waits for the
-// copies before the CTA exits.
+// thread, 16 KB per piece) the pieces come in with bulk copies.  Up to three
+// bands are in flight at once, each on its own barrier (bars[0..2]: the
+// fix-up barrier and the two partner-prefetch barriers, idle in a unit that
+// takes this path), so the L2 round trips overlap the sums.  Takes up to
+// ring capacity / 16 KB pieces.  Returns false (uniformly) if a copy did not
+// arrive in time, after waiting (bounded) for every copy still in flight.
 template <int TM, int STAGES>
 __device__ __forceinline__ bool fixup_staged(const TileParams &p, int tm, int tn, int t_sk,
                                              int c_first, int c_last, int tid, float *ring,
-                                             uint64_t *bar, uint32_t &phase) {
+                                             uint64_t *bars, uint32_t &phase) {
     constexpr int NT = Cfg<TM>::NT;
     constexpr int BAND = 4 * NT * 4;  // floats of one band of one piece
+    constexpr int NBANDS = TILE_FLOATS / BAND;
+    constexpr int RING_BANDS = STAGES * STAGE_FLOATS / BAND;
     const int n = c_last - c_first + 1;
+    const int nslots = min(3, RING_BANDS / n);  // >= 1: the caller checks n <= RING_BANDS
+    const uint32_t ph0 = phase;                // bars[1] and bars[2] are at phase 0
+    // Parity of the wait for band b: slot b % nslots, its (b / nslots)-th use.
+    auto parity = [&](int b) -> uint32_t {
+        return ((b % nslots == 0 ? ph0 : 0u) + (uint32_t)(b / nslots)) & 1u;
+    };
+    auto issue = [&](int b) {  // thread 0
+        const int s = b % nslots;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        fence_proxy_async_global();
+        mbar_arrive_expect_tx(&bars[s], uint32_t(n) * BAND * 4);
+        for (int j = 0; j < n; ++j)
+            bulk_load(ring + (s * n + j) * BAND,
+                      p.partials + (size_t)partial_slot(p, c_first + j, t_sk) * TILE_FLOATS +
+                          b * BAND,
+                      BAND * 4, &bars[s]);
+    };
+    __syncthreads();  // the ring's previous contents are read
+    const int first = min(nslots, NBANDS);
+    if (tid == 0)
+        for (int b = 0; b < first; ++b) issue(b);
+    int issued = first;
 #pragma unroll 1
-    for (int band = 0; band < TILE_FLOATS / BAND; ++band) {
-        __syncthreads();  // the ring's previous contents are read
-        if (tid == 0) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            fence_proxy_async_global();
-            mbar_arrive_expect_tx(bar, uint32_t(n) * BAND * 4);
-            for (int j = 0; j < n; ++j)
-                bulk_load(ring + j * BAND,
-                          p.partials + (size_t)partial_slot(p, c_first + j, t_sk) * TILE_FLOATS +
-                              band * BAND,
-                          BAND * 4, bar);
-        }
-        const bool got = mbar_wait_bounded(bar, phase, p.timeout_ns);
-        phase ^= 1u;
+    for (int band = 0; band < NBANDS; ++band) {
+        const int s = band % nslots;
+        const bool got = mbar_wait_bounded(&bars[s], parity(band), p.timeout_ns);
         if (__syncthreads_or(!got)) {
-            if (tid == 0) atomicOr(p.err, kErrWaitTimeout);
+            if (tid == 0) {
+                atomicOr(p.err, kErrWaitTimeout);
+                for (int b = band; b < issued; ++b) {
+                    if (!mbar_wait_bounded(&bars[b % nslots], parity(b), 1000000000ull)) {
+                        atomicOr(p.err, kErrDrainTimeout);
+                        break;
+                    }
+                }
+            }
+            __syncthreads();
             return false;
         }
+        const float *slot = ring + s * n * BAND;
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
             const int f = k * NT + tid;
-            float4 s = ld_shared_f4(ring + f * 4);
+            float4 sum = ld_shared_f4(slot + f * 4);
 #pragma unroll 1
             for (int j = 1; j < n; ++j) {
-                const float4 x = ld_shared_f4(ring + j * BAND + f * 4);
-                s.x += x.x;
-                s.y += x.y;
-                s.z += x.z;
-                s.w += x.w;
+                const float4 x = ld_shared_f4(slot + j * BAND + f * 4);
+                sum.x += x.x;
+                sum.y += x.y;
+                sum.z += x.z;
+                sum.w += x.w;
             }
             const int e4 = band * 4 + k;
-            store_c4(p, tm * BM + acc_row(tid, e4 >> 1), tn * BN + acc_col(tid, e4 & 1), s);
+            store_c4(p, tm * BM + acc_row(tid, e4 >> 1), tn * BN + acc_col(tid, e4 & 1), sum);
+        }
+        __syncthreads();  // slot s is read by every thread
+        if (band + nslots < NBANDS) {
+            if (tid == 0) issue(band + nslots);
+            ++issued;
         }
     }
-    __syncthreads();
+    phase = ph0 ^ (uint32_t)(((NBANDS + nslots - 1) / nslots) & 1);  // bars[0]'s uses
     return true;
 }
 
@@ -770,10 +809,10 @@ __global__ void __launch_bounds__(Cfg<TM>::NT, 1)
                 // consumed): stage the pieces there.
                 constexpr int kRingPieces = STAGES * STAGE_FLOATS / (4 * Cfg<TM>::NT * 4);
                 if (q == q_total && c_last - c_first + 1 <= kRingPieces) {
-                    if (!fixup_staged<TM, STAGES>(p, tm, tn, t_sk, c_first, c_last, tid, stages,
-                                                  red_bar, red_phase) &&
-                        tid == 0 && !mbar_wait_bounded(red_bar, red_phase ^ 1u, 1000000000ull))
-                        atomicOr(p.err, kErrDrainTimeout);
+                    // red_bar and the two pre_bar barriers follow each other
+                    // (waits on them are bounded; a timeout drains inside).
+                    fixup_staged<TM, STAGES>(p, tm, tn, t_sk, c_first, c_last, tid, stages, red_bar,
+                                             red_phase);
                 } else {
                     fixup_from_l2<TM>(p, tm, tn, t_sk, c_first, c_last, tid);
                 }
