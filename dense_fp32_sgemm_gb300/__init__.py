@@ -53,6 +53,8 @@ _SIGNATURES = {
     "sgemm_plan_describe": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_uint64,
                                    ctypes.c_uint64, ctypes.c_uint64, _f32, _int,
                                    ctypes.c_char_p, ctypes.c_size_t]),
+    "sgemm_plan_describe_3xtf32": (_int, [_i64, _i64, _i64, _i64, ctypes.c_uint64, _int,
+                                          ctypes.c_char_p, ctypes.c_size_t]),
     "sgemm_set_plan_override": (_int, [_int, _int]),
     "sgemm_set_wait_timeout_ns": (_int, [ctypes.c_uint64, _int]),
     "sgemm_set_tile_config": (_int, [_int, _int, _int]),
@@ -296,6 +298,18 @@ def plan_describe(M, N, K, lda=None, ldb=None, ldc=None, a_addr=0, b_addr=0, c_a
     if sep:
         out["reason"] = reason
     return out
+
+
+def plan_describe_3xtf32(M, N, K, lda=None, a_addr=0, num_sms=0) -> dict:
+    """What sgemm_run_3xtf32 would do for these sizes (host only), as a dict of
+    strings: path (ffma or tensor) and, for the tensor path, bk, stages,
+    ctas_per_sm, a_in_kernel, tile_n, splits, kt and ctas."""
+    lda = K if lda is None else lda
+    buf = ctypes.create_string_buffer(256)
+    _check(library().sgemm_plan_describe_3xtf32(int(M), int(N), int(K), int(max(lda, 1)),
+                                                int(a_addr), int(num_sms), buf, len(buf)),
+           "sgemm_plan_describe_3xtf32")
+    return dict(kv.partition("=")[::2] for kv in buf.value.decode().split())
 
 
 def set_plan_override(variant: int = VARIANT_AUTO, splits: int = 0) -> None:

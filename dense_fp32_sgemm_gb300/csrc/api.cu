@@ -307,6 +307,44 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
     }
 }
 
+// The 3xTF32 entry point's choices for one call: whether the FFMA kernels
+// take it, where A is split, the tile width, the K split and the kernel form.
+struct X3Decision {
+    bool ffma = false;  // K < 64, M <= 16 or alpha == 0: the FFMA kernels
+    bool a_raw = false;
+    int bk = 16, stages = 4, bn = kX3BN, splits = 1, kt_total = 0;
+    int64_t ctas = 0;
+};
+
+X3Decision x3_decide(int64_t M, int64_t N, int64_t K, float alpha, uint64_t a_addr, int64_t lda,
+                     int num_sms) {
+    X3Decision x;
+    if (K < kX3MinK || M <= 16 || alpha == 0.0f) {
+        x.ffma = true;
+        return x;
+    }
+    x.bk = g_x3_bk.load();
+    // A split inside the kernel pays off only for large outputs whose A rows
+    // start on 128-byte lines.  Measured on GB300 (TFLOP/s, split pass
+    // against in-kernel split): 8192^3 270 / 281, 8192x6144x2048 227 / 238,
+    // 6144x6144x2048 243 / 242, 4096x4096x8192 265 / 242, 4096^3 249 / 232,
+    // 2048x8192x4096 254 / 221, 2048^3 194 / 190.
+    const int a_mode = g_x3_a_in_kernel.load();
+    x.a_raw = a_mode >= 0 ? a_mode != 0
+                          : ((lda % 32) == 0 && !(a_addr & 127u) && M * N >= (int64_t)48 << 20);
+    x.kt_total = (int)((K + x.bk - 1) / x.bk);
+    x3_plan(M, N, x.kt_total, num_sms, g_x3_splits.load(), &x.bn, &x.splits);
+    // Two CTAs per SM (K slice 16 only) overlap one tile's epilogue and
+    // start-up with another's MMAs; they pay off once the launch has more
+    // than one wave (measured on GB300: 3072^3 with 288 CTAs 230 -> 217 us,
+    // 4092^3 520 -> 500 us, 8192^3 293 -> 308 TFLOP/s), while a single wave
+    // would crowd onto half the SMs (2048^3: 80 -> 128 us).
+    x.ctas = ((M + kX3BM - 1) / kX3BM) * ((N + x.bn - 1) / x.bn) * x.splits;
+    const int cps = g_x3_ctas_per_sm.load();
+    x.stages = x.bk == 32 ? 2 : (cps == 2 || (cps == 0 && x.ctas > (int64_t)num_sms)) ? 2 : 4;
+    return x;
+}
+
 }  // namespace
 }  // namespace sgemm
 
@@ -357,33 +395,14 @@ sgemm_status_t sgemm_run_3xtf32_epilogue(int64_t M, int64_t N, int64_t K, float 
     Epilogue epi;
     epi.bias = bias;
     epi.act = activation == SGEMM_ACT_RELU ? kActRelu : kActNone;
-    if (K < kX3MinK || M <= 16 || alpha == 0.0f)
-        return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, st, *d);
+    const X3Decision x = x3_decide(M, N, K, alpha, reinterpret_cast<uintptr_t>(A), lda,
+                                   d->num_sms);
+    if (x.ffma) return run_locked(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, st, *d);
     if (M > (1 << 29) || N > (1 << 29) || K > (1 << 30) ||
         ((M + kX3BM - 1) / kX3BM) * ((N + kX3MinBN - 1) / kX3MinBN) * kX3MaxSplits > INT32_MAX)
         return SGEMM_ERR_INVALID_ARG;
-    const int bk = g_x3_bk.load();
-    // A split inside the kernel pays off only for large outputs whose A rows
-    // start on 128-byte lines.  Measured on GB300 (TFLOP/s, split pass
-    // against in-kernel split): 8192^3 270 / 281, 8192x6144x2048 227 / 238,
-    // 6144x6144x2048 243 / 242, 4096x4096x8192 265 / 242, 4096^3 249 / 232,
-    // 2048x8192x4096 254 / 221, 2048^3 194 / 190.
-    const int a_mode = g_x3_a_in_kernel.load();
-    const bool a_raw = a_mode >= 0 ? a_mode != 0
-                                   : ((lda % 32) == 0 && !(reinterpret_cast<uintptr_t>(A) & 127u) &&
-                                      M * N >= (int64_t)48 << 20);
-    const int kt_total = (int)((K + bk - 1) / bk);
-    int bn = kX3BN, splits = 1;
-    x3_plan(M, N, kt_total, d->num_sms, g_x3_splits.load(), &bn, &splits);
-    // Two CTAs per SM (K slice 16 only) overlap one tile's epilogue and
-    // start-up with another's MMAs; they pay off once the launch has more
-    // than one wave (measured on GB300: 3072^3 with 288 CTAs 230 -> 217 us,
-    // 4092^3 520 -> 500 us, 8192^3 293 -> 308 TFLOP/s), while a single wave
-    // would crowd onto half the SMs (2048^3: 80 -> 128 us).
-    const int64_t ctas = ((M + kX3BM - 1) / kX3BM) * ((N + bn - 1) / bn) * splits;
-    const int cps = g_x3_ctas_per_sm.load();
-    const int stages = bk == 32 ? 2
-                       : (cps == 2 || (cps == 0 && ctas > (int64_t)d->num_sms)) ? 2 : 4;
+    const int bk = x.bk, bn = x.bn, splits = x.splits, stages = x.stages, kt_total = x.kt_total;
+    const bool a_raw = x.a_raw;
     const int form = bk * 100 + stages * 10 + (a_raw ? 1 : 0);
     if (!d->x3_configured.count(form)) {
         if (x3_configure(bk, stages, a_raw) != cudaSuccess) return SGEMM_ERR_LAUNCH;
@@ -655,6 +674,28 @@ sgemm_status_t sgemm_plan_describe(int64_t M, int64_t N, int64_t K, int64_t lda,
     Plan pl;
     if (make_plan(in, &pl) != 0) return SGEMM_ERR_INVALID_ARG;
     describe_plan(pl, buf, len);
+    return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_plan_describe_3xtf32(int64_t M, int64_t N, int64_t K, int64_t lda,
+                                          uint64_t a_addr, int num_sms, char *buf, size_t len) {
+    if (M < 0 || N < 0 || K < 0 || lda < (K > 1 ? K : 1) || !buf || len == 0)
+        return SGEMM_ERR_INVALID_ARG;
+    if (num_sms <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SGEMM_ERR_NO_DEVICE;
+    }
+    const X3Decision x = x3_decide(M, N, K, 1.0f, a_addr, lda, num_sms);
+    if (x.ffma)
+        snprintf(buf, len, "path=ffma");
+    else
+        snprintf(buf, len,
+                 "path=tensor bk=%d stages=%d ctas_per_sm=%d a_in_kernel=%d tile_n=%d splits=%d "
+                 "kt=%d ctas=%lld",
+                 x.bk, x.stages, x.bk == 16 && x.stages == 2 ? 2 : 1, x.a_raw ? 1 : 0, x.bn,
+                 x.splits, x.kt_total, (long long)x.ctas);
     return SGEMM_OK;
 }
 

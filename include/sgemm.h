@@ -277,6 +277,21 @@ SGEMM_API sgemm_status_t sgemm_run_3xtf32_epilogue(int64_t M, int64_t N, int64_t
                                                    const float *bias, int activation, void *stream);
 
 /*
+ * sgemm_plan_describe_3xtf32 -- host-only: write into buf (NUL-terminated, at
+ * most len bytes) what sgemm_run_3xtf32 would do for these sizes, A's leading
+ * dimension and address on a GPU with `num_sms` SMs (0 = query the current
+ * device), under the current sgemm_set_3xtf32_config settings: "path=ffma"
+ * (the FFMA kernels take the call), or "path=tensor" followed by the K slice,
+ * ring stages, CTAs per SM, whether A is split in the kernel, the tile width,
+ * the K split, the K slices and the CTA count.  Touches no device memory.
+ * Returns SGEMM_ERR_INVALID_ARG on bad sizes, SGEMM_ERR_NO_DEVICE if
+ * num_sms == 0 and no device is present.
+ */
+SGEMM_API sgemm_status_t sgemm_plan_describe_3xtf32(int64_t M, int64_t N, int64_t K, int64_t lda,
+                                                    uint64_t a_addr, int num_sms, char *buf,
+                                                    size_t len);
+
+/*
  * sgemm_set_3xtf32_config -- tuning hook, process-wide, for the 3xTF32 kernel.
  * bk: the K depth of one pipeline stage, 16 (64-byte swizzled rows, the
  *   default) or 32 (two stages of 128-byte rows, one CTA per SM).

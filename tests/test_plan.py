@@ -204,3 +204,65 @@ def test_deep_products_with_few_tiles_split_finer(M, N, K, share, grid):
     p = plan(M, N, K)
     assert p["variant"] == "streamk"
     assert ints(p, "sk_share", "grid") == [share, grid]
+
+
+# ----- the 3xTF32 entry point's choices (sgemm_plan_describe_3xtf32) --------
+
+def x3(M, N, K, **kw):
+    kw.setdefault("lda", K)
+    kw.setdefault("a_addr", 1 << 20)
+    kw.setdefault("num_sms", SMS)
+    return sg.plan_describe_3xtf32(M, N, K, **kw)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 8192, 8192), (1000, 1000, 63), (1, 5, 7)])
+def test_3xtf32_short_or_skinny_products_take_the_ffma_kernels(M, N, K):
+    assert x3(M, N, K) == {"path": "ffma"}
+
+
+@pytest.mark.parametrize("M,N,K,tile_n,splits,cps,a_in", [
+    # one wave of 240-wide tiles (144 CTAs), one CTA per SM
+    (2048, 2048, 2048, 240, 1, 1, 0),
+    # 608 tiles of 224: exactly four waves; two CTAs per SM
+    (4092, 4092, 4092, 224, 1, 2, 0),
+    # large output with A rows on 128-byte lines: A split in the kernel
+    (8192, 8192, 8192, 256, 1, 2, 1),
+    # deep products with few tiles: cut into K ranges
+    (768, 768, 4096, 128, 4, 1, 0),
+    (1024, 1024, 8192, 176, 3, 1, 0),
+])
+def test_3xtf32_plans(M, N, K, tile_n, splits, cps, a_in):
+    p = x3(M, N, K)
+    assert p["path"] == "tensor"
+    assert [int(p[k]) for k in ("tile_n", "splits", "ctas_per_sm", "a_in_kernel")] == \
+        [tile_n, splits, cps, a_in]
+    tiles = math.ceil(M / 128) * math.ceil(N / tile_n)
+    assert int(p["ctas"]) == tiles * splits
+    # at least 16 K slices per range
+    assert math.ceil(int(p["kt"]) / splits) >= 16 or splits == 1
+
+
+@pytest.mark.parametrize("M,N", [(300, 520), (2048, 2048), (4092, 4092), (777, 6000), (130, 100)])
+def test_3xtf32_tile_width_costs_no_more_waves_than_the_widest(M, N):
+    # The chosen width never needs more waves x (width + 32) than 256.
+    p = x3(M, N, 1024)
+    bn = int(p["tile_n"])
+    assert 64 <= bn <= 256 and bn % 16 == 0
+    def cost(w):
+        return math.ceil(math.ceil(M / 128) * math.ceil(N / w) / SMS) * (w + 32)
+    assert cost(bn) <= cost(256)
+
+
+def test_3xtf32_a_split_needs_aligned_rows():
+    assert x3(8192, 8192, 8192, a_addr=(1 << 20) + 64)["a_in_kernel"] == "0"
+    assert x3(8192, 8192, 8190, lda=8190)["a_in_kernel"] == "0"
+
+
+def test_3xtf32_config_forces_forms():
+    sg.set_3xtf32_config(32, True, 4, 0)
+    try:
+        p = x3(2048, 2048, 4096)
+        assert (p["bk"], p["stages"], p["ctas_per_sm"], p["a_in_kernel"], p["splits"]) == \
+            ("32", "2", "1", "1", "4")
+    finally:
+        sg.set_3xtf32_config(16, None)
