@@ -2,6 +2,7 @@
 stream-K split, on a GPU described by its SM count (152 on GB300)."""
 import math
 
+import numpy as np
 import pytest
 
 import dense_fp32_sgemm_gb300 as sg
@@ -266,3 +267,53 @@ def test_3xtf32_config_forces_forms():
             ("32", "2", "1", "1", "4")
     finally:
         sg.set_3xtf32_config(16, None)
+
+
+def _random_shapes(seed, count):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(1, 20000)), int(rng.integers(1, 20000)), int(rng.integers(1, 40000)))
+            for _ in range(count)]
+
+
+def test_random_plans_cover_the_work():
+    # Over many seeded shapes the FFMA plan covers every k-iteration of every
+    # tile exactly, keeps stream-K tiles within nine pieces, and never costs
+    # more than whole tiles; skinny ranges cover every (slab, k) position.
+    for M, N, K in _random_shapes(11, 300):
+        p = plan(M, N, K)
+        v = p["variant"]
+        assert v in ("tile", "streamk", "generic", "skinny", "scale", "none"), (M, N, K, v)
+        if v in ("tile", "streamk"):
+            tm, tn, kt, dp, sk, share, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles",
+                                                   "sk_tiles", "sk_share", "grid")
+            T = tm * tn
+            assert dp + sk == T and 1 <= grid <= SMS
+            if sk:
+                assert dp % SMS == 0
+                assert share * grid >= sk * kt, (M, N, K)
+                assert (kt + share - 2) // share + 1 <= 9, (M, N, K, share)
+            assert float(p["cost"]) <= math.ceil(T / SMS) * kt + 1e-9
+        elif v == "skinny":
+            assert M <= 16
+            slabs, kt, grid = ints(p, "tiles_n", "kt", "grid")
+            assert 1 <= grid <= SMS and slabs == math.ceil(N / 256)
+
+
+def test_random_3xtf32_plans():
+    # The tensor-core plan: widths in [64, 256] in steps of 16, K ranges of at
+    # least 16 slices, CTA count = tiles x ranges, two CTAs per SM only past
+    # one wave.
+    for M, N, K in _random_shapes(12, 300):
+        p = x3(M, N, K)
+        if K < 64 or M <= 16:
+            assert p == {"path": "ffma"}
+            continue
+        bn, splits, kt, ctas, cps = (int(p[k]) for k in ("tile_n", "splits", "kt", "ctas",
+                                                         "ctas_per_sm"))
+        assert 64 <= bn <= 256 and bn % 16 == 0
+        assert 1 <= splits <= 8
+        if splits > 1:
+            kps = math.ceil(kt / splits)
+            assert kps >= 16 and (splits - 1) * kps < kt
+        assert ctas == math.ceil(M / 128) * math.ceil(N / bn) * splits
+        assert cps == (2 if ctas > SMS else 1)
