@@ -543,7 +543,9 @@ def gpu_arm(args, ws, rank, local):
             dx = statistics.median(timed(cfgx, dAx, dBx, dCx, steps_x, args.warmup,
                                          entry="sgemm_run_3xtf32")[0])
             fl = flops_of(cfgx)
-            x3.append({"workload": WORKLOADS[xname], "api": "sgemm_run_3xtf32",
+            xplan = sg.plan_describe_3xtf32(cfgx["M"], cfgx["N"], cfgx["K"], lda=cfgx["K"],
+                                            a_addr=dAx.data_ptr())
+            x3.append({"workload": WORKLOADS[xname], "api": "sgemm_run_3xtf32", "plan": xplan,
                        "value": round(fl / dx / 1e9, 2), "unit": "GFLOP/s (FP32 products)",
                        "ms_per_step": round(dx * 1e3, 4), "steps": steps_x,
                        "vs_ffma_path": round(fl / dx / 1e12 / achieved, 3)
