@@ -52,16 +52,25 @@ WORKLOADS = {
     "s7_gemv": "sgemm 1x8192x8192 fp32 row-major alpha=1 beta=0 A,B U[-1,1) (GEMV)",
 }
 METRIC = "SGEMM GFLOP/s at 4092^3 and 2048^3 FP32; % of GB300 FP32 FFMA peak"
-SMS_GB300 = 152
 FP32_LANES_PER_SM = 128
-SM_MAX_MHZ = 2070.0
+SM_MAX_MHZ = 2070.0  # GB300's maximum SM clock, used when nvidia-smi reports none
 L2_FLUSH_BYTES = 256 << 20
 HOLD_BATCH = 32
 REFERENCE_SECONDS = 120.0
 
 
-def nominal_fp32_tflops(sms=SMS_GB300, mhz=SM_MAX_MHZ):
+def nominal_fp32_tflops(sms, mhz=SM_MAX_MHZ):
     return sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def workload_config(name):
+    """The `config` object of a bench line: the workload alone (the same for
+    the GPU arm and the reference arm), plus how L2 is handled."""
+    cfg = datagen.CONFIGS[name]
+    return {"workload": WORKLOADS[name], "M": cfg["M"], "N": cfg["N"], "K": cfg["K"],
+            "alpha": cfg["alpha"], "beta": cfg["beta"], "seed": datagen.CONFIG_SEEDS[name],
+            "l2": "GPU arm: L2 flushed before every timed step (256 MiB write, then a read "
+                  "of it so no dirty lines remain); CPU reference arm: not applicable"}
 
 
 def dist_env():
@@ -265,6 +274,7 @@ def gpu_arm(args, ws, rank, local):
     dev = torch.device("cuda", local)
     sg.build()
     sg.library()
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     def device_inputs(name):
         cfg, A, B, C = datagen.config_inputs(name)
@@ -359,7 +369,7 @@ def gpu_arm(args, ws, rank, local):
 
     def ffma_probe(seconds_target, paired):
         sink = torch.zeros(4096, device=dev)
-        blocks = SMS_GB300 * 4
+        blocks = num_sms * 4
         iters = 200
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         # calibrate
@@ -393,7 +403,7 @@ def gpu_arm(args, ws, rank, local):
         for _ in range(5):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            nb = sg.probe_read(buf.data_ptr(), buf.numel(), sink.data_ptr(), SMS_GB300 * 4, stream)
+            nb = sg.probe_read(buf.data_ptr(), buf.numel(), sink.data_ptr(), num_sms * 4, stream)
             e1.record(stream)
             torch.cuda.synchronize()
             best = max(best, nb / (e0.elapsed_time(e1) / 1e3) / 1e9)
@@ -432,16 +442,14 @@ def gpu_arm(args, ws, rank, local):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(mean_s * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOADS[name], "M": cfg["M"], "N": cfg["N"], "K": cfg["K"],
-                   "alpha": cfg["alpha"], "beta": cfg["beta"], "seed": datagen.CONFIG_SEEDS[name],
-                   "l2": "flushed before every step (256 MiB write, then a read of it so no "
-                         "dirty lines remain); GEMM timed per step "
-                         "with CUDA events; steps queued in batches of 32 behind a hold kernel "
-                         "so the device never waits for the host",
+        "config": workload_config(name),
+        "method": {"timing": "GEMM timed per step with CUDA events on its stream; steps "
+                             "queued in batches of 32 behind a hold kernel so the device "
+                             "never waits for the host",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "plan": plan.get("variant") if args.entry == "sgemm_run" else "3xtf32",
                    "grid": int(plan.get("grid", 0)) if args.entry == "sgemm_run" else None,
-                   "entry": args.entry},
+                   "entry": args.entry, "sms": num_sms},
         "sets": drift,
         "gpu_launches": per_step * args.steps + -(-args.steps // HOLD_BATCH),
         "gpu_launches_detail": {"sgemm (inside the event pairs)": per_step * args.steps,
@@ -458,7 +466,8 @@ def gpu_arm(args, ws, rank, local):
     ffma2 = ffma_probe(probe_s, True)
     probe_peak = max(ffma["sustained"], ffma2["sustained"])
     achieved = flops / mean_s / 1e12
-    peak = nominal_fp32_tflops()
+    sm_mhz_max = clocks.get("sm_max_mhz") or SM_MAX_MHZ
+    peak = nominal_fp32_tflops(num_sms, sm_mhz_max)
     hbm_peak, hbm_src = measured_hbm_peak()
     kernel = {"tile": "sgemm_tile_kernel", "streamk": "sgemm_tile_kernel",
               "skinny": "sgemm_skinny_kernel", "generic": "sgemm_generic_kernel"}.get(
@@ -478,7 +487,8 @@ def gpu_arm(args, ws, rank, local):
             "bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
             "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
             "traffic": recorded_traffic(kernel, name),
-            "peak_source": "152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz (max SM clock)",
+            "peak_source": f"{num_sms} SMs x 128 FP32 lanes x 2 flop x {sm_mhz_max:.0f} MHz "
+                           "(max SM clock)",
             "probe": {"ffma_tflops": ffma, "ffma2_tflops": ffma2,
                       "frac_of_probe": round(achieved / probe_peak, 4)},
             "kernel": kernel,
@@ -584,7 +594,46 @@ def gpu_arm(args, ws, rank, local):
         result["cpu_baseline"] = time_oracle(name, budget_s=args.cpu_seconds)
         result["cpu_baseline"]["s1_128_one_thread_gflops"] = time_oracle("s1_128", budget_s=1.0,
                                                                  threads=1)["value"]
-    return result, rank
+    return with_summary_last(result, name), rank
+
+
+def with_summary_last(result, name):
+    """The line with its long per-workload sections moved to the end and a
+    compact summary of every workload after them, so that a reader who keeps
+    only the tail of the line still sees each workload's rate and fraction."""
+    short = {"s1_128": "s1 128^3", "s2_2048": "s2 2048^3", "s3_4092": "s3 4092^3",
+             "s4_rect": "s4 8192x6144x2048", "s5_odd": "s5 1023x1025x513",
+             "s6_skinny": "s6 16x8192x8192", "s7_gemv": "gemv 1x8192x8192"}
+    by_text = {v: k for k, v in WORKLOADS.items()}
+    summary = {}
+
+    def put(key, ent, frac, of):
+        summary[key] = {"GFLOP/s": ent.get("value"), "us": round(ent["ms_per_step"] * 1e3, 1),
+                        "frac": frac, "of": of}
+
+    rl = result.get("roofline", {})
+    if rl.get("bound") == "hbm":
+        put(short[name], result, rl.get("frac"), "HBM copy peak")
+    elif rl:
+        put(short[name], result, rl.get("frac"), "FP32 nominal")
+    for ent in ([result["secondary"]] if "secondary" in result else []) + \
+            result.get("other_workloads", []):
+        key = short.get(by_text.get(ent["workload"], ""), ent["workload"])
+        if "roofline" in ent:
+            put(key, ent, ent["roofline"]["frac"], "HBM copy peak")
+        else:
+            put(key, ent, ent.get("frac_of_peak"), "FP32 nominal")
+    for ent in result.get("tensor_core_3xtf32", []):
+        key = "3xTF32 " + short.get(by_text.get(ent["workload"], ""), ent["workload"])
+        put(key, ent, ent["roofline"]["frac"], "TF32 tensor peak")
+    out = {k: v for k, v in result.items()
+           if k not in ("cublas_context", "tensor_core_3xtf32", "other_workloads", "secondary")}
+    for k in ("cublas_context", "tensor_core_3xtf32", "other_workloads", "secondary"):
+        if k in result:
+            out[k] = result[k]
+    if summary:
+        out["summary"] = summary
+    return out
 
 
 def reference_arm(args, ws, rank):
@@ -608,10 +657,9 @@ def reference_arm(args, ws, rank):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(flops / (value * 1e9) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOADS[name], "M": cfg["M"], "N": cfg["N"], "K": cfg["K"],
-                   "alpha": cfg["alpha"], "beta": cfg["beta"],
-                   "note": "each step times a bounded row sample of the workload; "
-                           "ms_per_step is extrapolated to the whole product"},
+        "config": workload_config(name),
+        "method": {"timing": "each step times a bounded row sample of the workload on the "
+                             "host cores; ms_per_step is extrapolated to the whole product"},
         "cpu_baseline": {"value": round(value, 3), "unit": "GFLOP/s", "cores": info["cores"],
                          "kind": "oracle", "sample": info["sample"]},
         "e2e": {"value": round(value, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,

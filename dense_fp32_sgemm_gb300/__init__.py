@@ -50,6 +50,7 @@ _SIGNATURES = {
     "sgemm_set_3xtf32_config": (_int, [_int, _int, _int, _int]),
     "sgemm_status_string": (ctypes.c_char_p, [_int]),
     "sgemm_device_status": (_int, [_vp]),
+    "sgemm_skinny_noalloc_status": (_int, [_vp]),
     "sgemm_plan_describe": (_int, [_i64, _i64, _i64, _i64, _i64, _i64, ctypes.c_uint64,
                                    ctypes.c_uint64, ctypes.c_uint64, _f32, _int,
                                    ctypes.c_char_p, ctypes.c_size_t]),

@@ -203,7 +203,7 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
         case kVarNone:
             return SGEMM_OK;
         case kVarScale:
-            return status_from(launch_scale((int)M, (int)N, beta, C, ldc, epi, stream));
+            return status_from(launch_scale((int)M, (int)N, beta, C, ldc, epi, d.num_sms, stream));
         case kVarGeneric: {
             GenericParams gp;
             gp.M = (int)M; gp.N = (int)N; gp.K = (int)K;
@@ -242,7 +242,7 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
                     Buse = buf + a_span;
                     ldb_use = pl.ldb_packed;
                 }
-                if (launch_pack(jobs, n, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+                if (launch_pack(jobs, n, d.num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
             }
             CUtensorMap mapA, mapB;
             sgemm_status_t s = encode_2d(&mapA, Ause, M, K, lda_use, kTileBK, kTileBM);
@@ -346,6 +346,13 @@ X3Decision x3_decide(int64_t M, int64_t N, int64_t K, float alpha, uint64_t a_ad
 }
 
 }  // namespace
+
+void wait_hooks(unsigned long long *timeout_ns, int *skip_loads_from) {
+    const unsigned long long to = g_timeout_ns.load();
+    *timeout_ns = to ? to : kDefaultTimeoutNs;
+    *skip_loads_from = g_skip_loads_from.load();
+}
+
 }  // namespace sgemm
 
 using namespace sgemm;
@@ -434,7 +441,7 @@ sgemm_status_t sgemm_run_3xtf32_epilogue(int64_t M, int64_t N, int64_t K, float 
     int64_t lda_map = lda;
     if (a_pack) {
         const PackJob job{A, lda, (int)M, (int)K, pa, ld_pack};
-        if (launch_pack(&job, 1, st) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        if (launch_pack(&job, 1, d->num_sms, st) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         a_map = pa;
         lda_map = ld_pack;
     }

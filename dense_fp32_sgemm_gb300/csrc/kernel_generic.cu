@@ -133,7 +133,7 @@ __global__ void sgemm_pack_kernel(const PackJobs jobs) {
 
 }  // namespace
 
-cudaError_t launch_pack(const PackJob *jobs, int njobs, cudaStream_t stream) {
+cudaError_t launch_pack(const PackJob *jobs, int njobs, int num_sms, cudaStream_t stream) {
     if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
     PackJobs pj;
     long long most = 0;
@@ -143,7 +143,7 @@ cudaError_t launch_pack(const PackJob *jobs, int njobs, cudaStream_t stream) {
         if (t > most) most = t;
     }
     long long blocks = (most + 255) / 256;
-    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (blocks > (long long)num_sms * 8) blocks = (long long)num_sms * 8;
     if (blocks < 1) blocks = 1;
     sgemm_pack_kernel<<<dim3((unsigned)blocks, (unsigned)njobs), 256, 0, stream>>>(pj);
     return cudaGetLastError();
@@ -157,10 +157,10 @@ cudaError_t launch_generic(const GenericParams &p, cudaStream_t stream) {
 }
 
 cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, const Epilogue &epi,
-                         cudaStream_t stream) {
+                         int num_sms, cudaStream_t stream) {
     const long long total = (long long)M * N;
     long long blocks = (total + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks > (long long)num_sms * 16) blocks = (long long)num_sms * 16;
     if (blocks < 1) blocks = 1;
     sgemm_scale_kernel<<<(int)blocks, 256, 0, stream>>>(M, N, beta, C, ldc, epi);
     return cudaGetLastError();

@@ -98,11 +98,12 @@ struct PackJob {
     float *dst;
     long long ldp;
 };
-cudaError_t launch_pack(const PackJob *jobs, int njobs, cudaStream_t stream);
+// Grids are capped at a few CTAs per SM of the device (num_sms).
+cudaError_t launch_pack(const PackJob *jobs, int njobs, int num_sms, cudaStream_t stream);
 
 // C = act(beta * C + bias) (beta == 0 does not read C).
 cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, const Epilogue &epi,
-                         cudaStream_t stream);
+                         int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Skinny-M kernel (M <= 16): streams B once through a TMA ring together with
@@ -159,6 +160,14 @@ cudaError_t launch_skinny(int m_tile, const CUtensorMap &mapA, const CUtensorMap
                           const SkinnyParams &p, int grid, cudaStream_t stream);
 size_t skinny_smem_bytes(int m_tile, int share);
 cudaError_t skinny_configure(int m_tile);
+
+// ---------------------------------------------------------------------------
+// Testing hooks set through sgemm_set_wait_timeout_ns (api.cu): the limit of
+// every bounded device wait (the default, one second, when none is set) and
+// the k-iteration of each CTA from which copy producers stop issuing loads
+// (-1 = never).
+// ---------------------------------------------------------------------------
+void wait_hooks(unsigned long long *timeout_ns, int *skip_loads_from);
 
 // ---------------------------------------------------------------------------
 // Measurement probes (same library, used by the benchmark).

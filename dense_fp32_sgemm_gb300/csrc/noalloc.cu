@@ -12,11 +12,17 @@
 // file-scope __device__ array, created by the CUDA runtime on each GPU that
 // loads the library and held there until the process exits.
 //
-// Limits: M <= 16, at most kMaxGrid CTAs (the plan fills every SM with
-// kSkinnyCtasPerSm CTAs: any GPU with up to 160 SMs), at most kMaxSlabs slabs of 256 columns
-// (N <= 1,048,576), A and B 16-byte aligned with leading dimensions that are
-// multiples of 4.  Anything else is rejected with SGEMM_ERR_SCRATCH_LIMIT
-// before any work is queued.
+// Limits: M <= 16, at most kMaxSlabs slabs of 256 columns (N <= 1,048,576),
+// A and B 16-byte aligned with leading dimensions that are multiples of 4.
+// Anything else is rejected with SGEMM_ERR_SCRATCH_LIMIT before any work is
+// queued.  The plan uses at most kMaxGrid = 160 CTAs in total
+// (kSkinnyCtasPerSm per SM, so 160 / kSkinnyCtasPerSm SMs): a GPU with more
+// SMs than that leaves the rest idle rather than outgrowing the buffer.
+//
+// A bounded device wait that gives up (a TMA copy that never lands) sets the
+// buffer's own error word; sgemm_skinny_noalloc_status() reads and clears it.
+// The calls themselves never clear it, so a timeout stays visible until it
+// has been read.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -99,6 +105,14 @@ sgemm_status_t setup_current_device(DeviceSetup **out) {
         s.done = true;
     }
     if (!s.ok) return SGEMM_ERR_NO_DEVICE;
+    *out = &s;
+    return SGEMM_OK;
+}
+
+sgemm_status_t setup_with_encoder(DeviceSetup **out) {
+    DeviceSetup *s = nullptr;
+    const sgemm_status_t st = setup_current_device(&s);
+    if (st != SGEMM_OK) return st;
     if (!g_encode_fn) {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -108,7 +122,7 @@ sgemm_status_t setup_current_device(DeviceSetup **out) {
             return SGEMM_ERR_TMA;
         g_encode_fn = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    *out = &s;
+    *out = s;
     return SGEMM_OK;
 }
 
@@ -136,13 +150,16 @@ extern "C" sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t
     if (product && ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
                     lda % 4 != 0 || ldb % 4 != 0))
         return SGEMM_ERR_SCRATCH_LIMIT;
+    // Sizes no kernel of the library takes (the same answer sgemm_run gives).
+    if (K > INT32_MAX / 2 || N > INT32_MAX / 2) return SGEMM_ERR_INVALID_ARG;
 
     DeviceSetup *dev = nullptr;
-    sgemm_status_t s = setup_current_device(&dev);
+    sgemm_status_t s = setup_with_encoder(&dev);
     if (s != SGEMM_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!product) {
-        const cudaError_t e = launch_scale((int)M, (int)N, beta, C, ldc, Epilogue{nullptr, kActNone}, st);
+        const cudaError_t e = launch_scale((int)M, (int)N, beta, C, ldc, Epilogue{nullptr, kActNone},
+                                           dev->num_sms, st);
         return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
     }
 
@@ -156,7 +173,10 @@ extern "C" sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t
     in.force_variant = kVarSkinny;
     in.force_splits = 0;
     Plan pl;
-    if (make_plan(in, &pl) != 0 || pl.variant != kVarSkinny) return SGEMM_ERR_SCRATCH_LIMIT;
+    // The checks above leave only a (slab, k) plane too large for the
+    // kernel's int positions (K of about 2^18 rows per slab and more), which
+    // the skinny plan declines: no kernel here takes it.
+    if (make_plan(in, &pl) != 0 || pl.variant != kVarSkinny) return SGEMM_ERR_UNSUPPORTED;
     if (pl.grid > kMaxGrid || pl.slabs > kMaxSlabs) return SGEMM_ERR_SCRATCH_LIMIT;
 
     bool &configured = pl.m_tile == 8 ? dev->configured8 : dev->configured16;
@@ -172,24 +192,41 @@ extern "C" sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t
 
     int *counters = reinterpret_cast<int *>(dev->scratch + kPartialBytes);
     int *err = reinterpret_cast<int *>(dev->scratch + kErrOffset);
-    // The buffer keeps the previous call's contents: the tickets and the
-    // error word must start at zero.
-    if (cudaMemsetAsync(counters, 0, (size_t)pl.slabs * sizeof(int), st) != cudaSuccess ||
-        cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess)
+    // The buffer keeps the previous call's contents: the tickets must start
+    // at zero (a call that gave up a wait may have left some taken).  The
+    // error word is left alone, so an earlier timeout stays visible to
+    // sgemm_skinny_noalloc_status().
+    if (cudaMemsetAsync(counters, 0, (size_t)pl.slabs * sizeof(int), st) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
 
     SkinnyParams sp;
     sp.M = (int)M; sp.N = (int)N; sp.K = (int)K;
     sp.slabs = pl.slabs; sp.kt_total = pl.kt_total;
-            for (int c = 0; c <= pl.grid; ++c) sp.starts[c] = pl.sk_starts[c];
+    for (int c = 0; c <= pl.grid; ++c) sp.starts[c] = pl.sk_starts[c];
     sp.alpha = alpha; sp.beta = beta;
     sp.A = A; sp.lda = lda; sp.C = C; sp.ldc = ldc; sp.c_vec4 = 0;
     sp.epi = Epilogue{nullptr, kActNone};
     sp.partials = reinterpret_cast<float *>(dev->scratch);
     sp.counters = counters;
     sp.err = err;
-    sp.timeout_ns = 1000000000ull;
-    sp.skip_loads_from = -1;
+    wait_hooks(&sp.timeout_ns, &sp.skip_loads_from);
     return launch_skinny(pl.m_tile, mapA, mapB, sp, pl.grid, st) == cudaSuccess ? SGEMM_OK
                                                                                  : SGEMM_ERR_LAUNCH;
+}
+
+extern "C" sgemm_status_t sgemm_skinny_noalloc_status(void *stream) {
+    DeviceSetup *dev = nullptr;
+    const sgemm_status_t s = setup_current_device(&dev);
+    if (s != SGEMM_OK) return s;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    int *err = reinterpret_cast<int *>(dev->scratch + kErrOffset);
+    int word = 0;
+    if (cudaMemcpy(&word, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    if (word == 0) return SGEMM_OK;
+    // Clear the word; the tickets are cleared by the next call itself.
+    if (cudaMemset(err, 0, sizeof(int)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+    return SGEMM_ERR_DEVICE_TIMEOUT;
 }

@@ -140,22 +140,38 @@ SGEMM_API sgemm_status_t sgemm_run_host(int64_t M, int64_t N, int64_t K, float a
  *
  * Same arguments, layout and conventions as sgemm_run (device pointers owned
  * by the caller, queued on `stream`, no host synchronisation), with limits:
- * M <= 16; N <= 1,048,576 (4096 slabs of 256 columns); a grid of at most 160
- * CTAs (one per SM: GPUs of up to 160 SMs); A and B 16-byte aligned with lda
- * and ldb multiples of 4.
- * Requests beyond them return SGEMM_ERR_SCRATCH_LIMIT before any work is
- * queued.  The first call on each device looks up the buffer's device address
- * (no work is queued by that set-up, but make the first call before any stream
- * capture).  Every call shares the one buffer: calls that overlap on the GPU
- * (different streams, or concurrent host threads) race and must be ordered by
- * the caller.  Each call clears the tickets and error word it uses.  A bounded
- * device wait that gives up is recorded in the buffer's own error word, not
- * in the word sgemm_device_status() reads.
+ * M <= 16; N <= 1,048,576 (4096 slabs of 256 columns); A and B 16-byte
+ * aligned with lda and ldb multiples of 4.  Requests beyond them return
+ * SGEMM_ERR_SCRATCH_LIMIT before any work is queued.  Sizes no kernel of the
+ * library takes (K or N above 2^30) return SGEMM_ERR_INVALID_ARG, as from
+ * sgemm_run; a K so deep that the kernel's position counter would overflow
+ * (about 2^18 * 32 rows per 256-column slab) returns SGEMM_ERR_UNSUPPORTED.
+ * The plan uses at most 160 CTAs in total (one per SM), so a GPU with more
+ * than 160 SMs leaves the others idle.  The first call on each device looks
+ * up the buffer's device address (no work is queued by that set-up, but make
+ * the first call before any stream capture).  Every call shares the one
+ * buffer: calls that overlap on the GPU (different streams, or concurrent
+ * host threads) race and must be ordered by the caller.  Each call clears
+ * the tickets it uses before its kernel runs.  A bounded device wait that
+ * gives up is recorded in the buffer's own error word, which no call clears:
+ * read it with sgemm_skinny_noalloc_status(), not sgemm_device_status().
  */
 SGEMM_API sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                                                   const float *A, int64_t lda, const float *B,
                                                   int64_t ldb, float beta, float *C, int64_t ldc,
                                                   void *stream);
+
+/*
+ * sgemm_skinny_noalloc_status -- synchronise `stream`, then read and clear
+ * the error word of sgemm_run_skinny_noalloc's fixed buffer on the current
+ * device.  Returns SGEMM_ERR_DEVICE_TIMEOUT if a call since the last read
+ * gave up a bounded device wait (the C it wrote is then undefined; the next
+ * call is valid, since each call clears its tickets first),
+ * SGEMM_ERR_LAUNCH if the stream reports a CUDA error, SGEMM_ERR_NO_DEVICE
+ * without an sm_103 device, else SGEMM_OK.  Allocates nothing.  (A library
+ * convenience; the pages have no counterpart.)
+ */
+SGEMM_API sgemm_status_t sgemm_skinny_noalloc_status(void *stream);
 
 /* Human-readable name of a status code (a static string). */
 SGEMM_API const char *sgemm_status_string(sgemm_status_t status);

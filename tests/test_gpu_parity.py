@@ -14,6 +14,7 @@ import dense_fp32_sgemm_gb300 as sg
 import oracle
 from tests.checks import assert_within
 from tests.gpu_harness import run_gemm
+from tests.oracle_cache import workload_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -58,40 +59,27 @@ def check(M, N, K, alpha, beta, dist="uniform", seed=1, lda=None, ldb=None, ldc=
     return out
 
 
-def sample_rows(M, count, seed):
-    """Rows spread over the matrix, always including both ends and the rows
-    on either side of 128-row tile boundaries near them."""
-    rng = np.random.default_rng(seed)
-    fixed = {0, 1, 127, 128, 129, M // 2, M - 129, M - 128, M - 2, M - 1}
-    fixed = {r for r in fixed if 0 <= r < M}
-    extra = rng.choice(M, size=min(M, count), replace=False).tolist()
-    return sorted(fixed | set(extra))
-
-
 # ----- the six workloads at full size, launched as the benchmark launches them ---
 
-@pytest.mark.parametrize("name,sample", [
-    ("s1_128", None), ("s2_2048", 192), ("s3_4092", 64), ("s4_rect", 48),
-    ("s5_odd", None), ("s6_skinny", None), ("s7_gemv", None),
+@pytest.mark.parametrize("name", [
+    "s1_128", "s2_2048", "s3_4092", "s4_rect", "s5_odd", "s6_skinny", "s7_gemv",
 ])
-def test_workload_full_size(name, sample):
-    cfg, A, B, C = datagen.config_inputs(name)
+def test_workload_full_size(name):
+    # Every element of every workload, launched as the benchmark launches it.
+    cfg, A, B, C, ref, bound = workload_reference(name)
     M, N, K, alpha, beta = cfg["M"], cfg["N"], cfg["K"], cfg["alpha"], cfg["beta"]
     out, _ = run_gemm(M, N, K, alpha, beta, A, K, B, N, C, N,
                       c_fill=None if beta != 0 else float("nan"))
-    rows = None if sample is None else sample_rows(M, sample, 7)
-    ref, bound = reference(M, N, K, alpha, beta, A, K, B, N, C, N, rows=rows)
-    got = out if rows is None else out[np.asarray(rows)]
     assert np.isfinite(out).all()
-    assert_within(got, ref, bound, name)
+    assert_within(out, ref, bound, name)
 
 
 def test_cublas_fp32_meets_the_same_bound():
     # cuBLAS FP32 with TF32 off, on the 2048^3 workload: a second GPU product,
     # independent of this library, must also sit within the bound against the
-    # oracle, which checks the oracle and the bound at a size the exact tests
-    # do not reach.
-    cfg, A, B, C = datagen.config_inputs("s2_2048")
+    # oracle at every element, which checks the oracle and the bound at a
+    # size the exact tests do not reach.
+    cfg, A, B, C, ref, bound = workload_reference("s2_2048")
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     prev = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = False
@@ -100,9 +88,7 @@ def test_cublas_fp32_meets_the_same_bound():
                        torch.from_numpy(B).cuda().view(K, N)).cpu().numpy()
     finally:
         torch.backends.cuda.matmul.allow_tf32 = prev
-    rows = sample_rows(M, 48, 11)
-    ref, bound = reference(M, N, K, 1.0, 0.0, A, K, B, N, None, N, rows=rows)
-    assert_within(out[np.asarray(rows)], ref, bound, "cuBLAS FP32")
+    assert_within(out, ref, bound, "cuBLAS FP32")
 
 
 # ----- exact integer inputs: every variant must be bit-exact ---------------------
@@ -256,20 +242,14 @@ def test_host_entry_point():
 def test_host_entry_point_in_row_blocks(M, N, K, alpha, beta, blocks):
     # Large enough that the host entry point copies and computes row blocks in
     # a pipeline (4 blocks with a ragged last one; 2 blocks); pinned host
-    # buffers; rows sampled on both sides of every block boundary.
+    # buffers; every element checked.
     A, lda, B, ldb, C, ldc = inputs("normal", 15, M, N, K)
     Ah = torch.from_numpy(A.reshape(M, K)).pin_memory()
     Bh = torch.from_numpy(B.reshape(K, N)).pin_memory()
     Ch = torch.from_numpy(C.reshape(M, N).copy()).pin_memory()
     sg.run_host(Ah, Bh, Ch, alpha=alpha, beta=beta)
-    rows_per = -(-(-(-M // blocks)) // 128) * 128
-    edges = {0, M - 1}
-    for b in range(1, blocks):
-        edges |= {b * rows_per - 1, b * rows_per}
-    rows = sorted(r for r in edges | set(sample_rows(M, 24, 3)) if 0 <= r < M)
-    ref, bound = reference(M, N, K, alpha, beta, A, lda, B, ldb, C if beta else None, ldc,
-                           rows=rows)
-    assert_within(Ch.numpy()[rows], ref, bound, "sgemm_run_host in row blocks")
+    ref, bound = reference(M, N, K, alpha, beta, A, lda, B, ldb, C if beta else None, ldc)
+    assert_within(Ch.numpy(), ref, bound, "sgemm_run_host in row blocks")
 
 
 def test_torch_binding_with_strided_rows():
@@ -309,8 +289,8 @@ def test_wait_timeout_reports_and_recovers():
     assert sg.device_status(stream) == 0
     # The context and the library still work.
     out, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
-    ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, rows=[0, 255, 511])
-    assert_within(out[[0, 255, 511]], ref, bound, "after timeout")
+    ref, bound = reference(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
+    assert_within(out, ref, bound, "after timeout")
 
 
 # ----- probes ----------------------------------------------------------------------

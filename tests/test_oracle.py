@@ -193,6 +193,39 @@ def test_error_bound_k_floor():
     assert oracle.error_bound(ab, None, 1.0, 0.0, 100)[0, 0] == 2 * 100 * 2.0 ** -24
 
 
+def check_bound_pins(error_bound):
+    """Values of the stated bound 2*K*2^-24*(|alpha|(|A||B|)_ij + |beta||C_ij|)
+    worked out by hand (K at least 3, at least 4 with a bias, whose magnitude
+    joins the sum), so that a dropped or mis-scaled term, a signed scalar, a
+    transposed C or a wrong constant in ``error_bound`` fails here."""
+    u = 2.0 ** -24
+    one = lambda v: np.array([[float(v)]])
+    # alpha 0.5, beta 2, |C| 3, (|A||B|) 10, K 10: 2*10*u*(0.5*10 + 2*3) = 220 u
+    assert error_bound(one(10), one(-3), 0.5, 2.0, 10)[0, 0] == 220 * u
+    # the scalars enter by magnitude
+    assert error_bound(one(10), one(3), -0.5, -2.0, 10)[0, 0] == 220 * u
+    # K = 1 takes the K = 3 constant: 2*3*u*(1*4 + 0.25*8) = 36 u
+    assert error_bound(one(4), one(8), 1.0, 0.25, 1)[0, 0] == 36 * u
+    # K = 7 with only the beta term: 2*7*u*(0 + 3*5) = 210 u
+    assert error_bound(one(0), one(5), 1.0, 3.0, 7)[0, 0] == 210 * u
+    # beta = 0: C takes no part, even when it holds a NaN: 2*5*u*4 = 40 u
+    assert error_bound(one(4), one(np.nan), 1.0, 0.0, 5)[0, 0] == 40 * u
+    # a bias: K = 2 takes the K = 4 constant: 2*4*u*(2*1 + 1*1 + 5) = 64 u
+    assert error_bound(one(1), one(1), 2.0, -1.0, 2, bias=np.array([-5.0]))[0, 0] == 64 * u
+    # elementwise, row-major: element (i, j) uses C[i][j] and bias[j]
+    C = np.array([[1.0, 2.0, 3.0], [4.0, 5.0, 6.0]])
+    ab = np.array([[0.0, 1.0, 2.0], [3.0, 4.0, 5.0]])
+    got = error_bound(ab, C, 1.0, 0.5, 8)
+    assert np.array_equal(got, 2 * 8 * u * (ab + 0.5 * C))
+    bias = np.array([10.0, -20.0, 30.0])
+    got = error_bound(ab, C, 1.0, 0.5, 8, bias=bias)
+    assert np.array_equal(got, 2 * 8 * u * (ab + 0.5 * C + np.abs(bias)[None, :]))
+
+
+def test_error_bound_hand_computed_values():
+    check_bound_pins(oracle.error_bound)
+
+
 # ----- the fused epilogue: bias per column, then ReLU -------------------------------
 
 def test_epilogue_all_ones_closed_form():
