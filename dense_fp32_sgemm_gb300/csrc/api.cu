@@ -271,6 +271,33 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             }
             return status_from(launch_tile(fm, st, tm, mapA, mapB, tp, pl.grid, stream));
         }
+        case kVarMid:
+        case kVarMid64: {
+            const int key = 1000 + pl.mid_bm * 10 + pl.b_vec;
+            if (!d.configured_tiles.count(key)) {
+                if (mid_configure(pl.mid_bm, pl.b_vec) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+                d.configured_tiles.insert(key);
+            }
+            MidParams mp;
+            mp.M = (int)M; mp.N = (int)N; mp.K = (int)K;
+            mp.tiles_m = pl.tiles_m; mp.tiles_n = pl.tiles_n; mp.kt_total = pl.kt_total;
+            mp.dp_tiles = pl.dp_tiles; mp.sk_tiles = pl.sk_tiles; mp.sk_share = pl.sk_share;
+            mp.group_m = pl.group_m;
+            mp.alpha = alpha; mp.beta = beta;
+            mp.A = A; mp.lda = lda; mp.B = B; mp.ldb = ldb; mp.C = C; mp.ldc = ldc;
+            mp.c_vec4 = pl.c_vec4;
+            mp.epi = epi;
+            mp.partials = nullptr; mp.counters = nullptr;
+            if (pl.sk_tiles > 0) {
+                Workspace *w = nullptr;
+                const size_t pbytes = (size_t)2 * pl.grid * pl.mid_bm * kMidBN * sizeof(float);
+                const sgemm_status_t s = ensure_workspace(d, stream, pbytes, (size_t)pl.sk_tiles, &w);
+                if (s != SGEMM_OK) return s;
+                mp.partials = w->partials;
+                mp.counters = w->counters;
+            }
+            return status_from(launch_mid(pl.mid_bm, pl.b_vec, mp, pl.grid, stream));
+        }
         case kVarSkinny: {
             const unsigned bit = 1u << (24 + pl.m_tile / 8);
             if (!(d.configured & bit)) {
@@ -707,7 +734,7 @@ sgemm_status_t sgemm_plan_describe_3xtf32(int64_t M, int64_t N, int64_t K, int64
 }
 
 sgemm_status_t sgemm_set_plan_override(int variant, int splits) {
-    if (variant < -1 || variant > SGEMM_VARIANT_SKINNY || splits < 0) return SGEMM_ERR_INVALID_ARG;
+    if (variant < -1 || variant > SGEMM_VARIANT_MID64 || splits < 0) return SGEMM_ERR_INVALID_ARG;
     g_force_variant.store(variant);
     g_force_splits.store(splits);
     return SGEMM_OK;

@@ -87,6 +87,42 @@ struct GenericParams {
 
 cudaError_t launch_generic(const GenericParams &p, cudaStream_t stream);
 
+// ---------------------------------------------------------------------------
+// Mid-size kernel: BM x 128 tiles (BM = 128 or 64) fed by cp.async copies of
+// 4 bytes (A, and B when it is not 16-byte aligned) or 16 bytes (aligned B),
+// so any alignment and leading dimension works without a copy pass; A lands
+// k-major with an XOR swizzle; 8 x 8 micro-tiles on packed FFMA2; 2 * BM
+// threads, several CTAs per SM; data-parallel tiles, then a stream-K tail
+// with the same deterministic fix-up as the tiled kernel.
+// ---------------------------------------------------------------------------
+constexpr int kMidBN = 128;
+constexpr int kMidBK = 16;
+constexpr int kMidStages = 4;
+
+struct MidParams {
+    int M, N, K;
+    int tiles_m, tiles_n;
+    int kt_total;       // ceil(K / kMidBK)
+    int dp_tiles, sk_tiles, sk_share;
+    int group_m;
+    float alpha, beta;
+    const float *A;
+    long long lda;
+    const float *B;
+    long long ldb;
+    float *C;
+    long long ldc;
+    int c_vec4;
+    Epilogue epi;
+    float *partials;    // 2 * gridDim.x slots of BM * 128 floats (stream-K)
+    int *counters;      // one per stream-K tile, zero at rest
+};
+
+// bm: 128 or 64; b_vec: 4 (B 16-byte aligned, ldb % 4 == 0) or 1.
+cudaError_t launch_mid(int bm, int b_vec, const MidParams &p, int grid, cudaStream_t stream);
+cudaError_t mid_configure(int bm, int b_vec);
+constexpr int mid_ctas_per_sm(int bm) { return bm == 64 ? 4 : 2; }
+
 // Copies of operands the TMA cannot map: rows x cols at src (leading
 // dimension ld, any 4-byte alignment) to dst with 16-byte-aligned rows of
 // ldp floats (ldp a multiple of 4, dst 16-byte aligned).  Up to two copies in

@@ -29,15 +29,49 @@ static_assert(sizeof(Plan::sk_starts) / sizeof(int) == kSkinnyMaxGrid + 1,
 
 namespace {
 
-// Per extra piece of a stream-K tile, in k-iterations of a tile: measured on
-// GB300, 1024^3 with 6 pieces per tile (share 7) took 63.5 us against 61.4
-// with 5 (share 8), one iteration less work for one piece more.
+// Per extra piece of a stream-K tile of the tiled kernel, in k-iterations of
+// a tile: measured on GB300, 1024^3 with 6 pieces per tile (share 7) took
+// 63.5 us against 61.4 with 5 (share 8), one iteration less work for one
+// piece more.
 constexpr double kFixupCost = 1.5;
-constexpr int64_t kSmallSlicesPerSm = 4;
-// With the copy of an unaligned operand to pay for, the tiled kernel needs
-// more work: measured, 1023 x 1025 x 513 (4.5 slices per SM) is faster on the
-// 64 x 64 kernel and 1023^3 (6.7) through the copy.
-constexpr int64_t kPackSlicesPerSm = 6;
+
+// Time model of each kernel on GB300 (2070 MHz), fitted to CUDA-event times
+// of single launches after an L2 flush (the planner sweep):
+//   t = launch + slices of the busiest CTA x time of one slice at the SM's
+//       CTA occupancy + (split tiles) fix-up + per extra piece,
+// plus, for the tiled kernel on unaligned operands, the copy to aligned rows.
+// launch: a 1 x 1 x 1 product takes 6.1 us from event to event.
+struct KernelModel {
+    int64_t bm, bn, bk;
+    int ctas_per_sm;
+    double slice_us[5];  // [c]: one CTA's slice with c CTAs resident per SM
+    double fixup_us;     // once, when some tile is split
+    double piece_us;     // per extra piece of the most-split tile
+};
+constexpr double kLaunchUs = 6.1;
+// Tiled kernel: 2^20 multiply-adds per 128 x 256 x 32 slice, one CTA per SM
+// (2048^3: cost 57 slices, 273 us); extra pieces at kFixupCost slices.
+constexpr KernelModel kTileModel = {kTileBM, kTileBN, kTileBK, 1, {0, 4.7, 0, 0, 0}, 0.0,
+                                    kFixupCost * 4.7};
+// Mid-size kernel, 128 x 128 x 16 slices: 1.55 us alone on an SM (1024 x
+// 1024 x 512 with 128 CTAs), 2.77 us per CTA with two per SM (2048^3 with 304
+// CTAs of 108 slices: 305 us); fix-up through the ring 4 us plus 2.5 us per
+// extra piece (1024 x 1024 x 512 with 2 and 4 pieces: 37.3 and 39.4 us).
+constexpr KernelModel kMidModel = {128, kMidBN, kMidBK, 2, {0, 1.55, 2.77, 0, 0}, 4.0, 2.5};
+// 64 x 128 x 16 slices, up to four CTAs per SM (64 x 8192 x 8192 with 512
+// CTAs of 64 slices: 191 us).
+constexpr KernelModel kMid64Model = {64, kMidBN, kMidBK, 4, {0, 1.0, 1.5, 2.2, 2.8}, 3.0, 1.5};
+// B in 4-byte copies (rows off 16 bytes) makes a mid-size slice slower
+// (2049^3: 2.93 us per slice against 2.77 at 2048^3).
+constexpr double kMidUnalignedB = 1.06;
+// 64 x 64 kernel, one tile per CTA and 16-k slices: 0.78 us per slice at up to
+// one CTA per SM (128^3: 12.3 us; 512^3: 30.9 us), growing with the CTAs an
+// SM holds (1024^3, 1.7 per SM: 80 us).
+constexpr double kGenericSliceUs = 0.78;
+// Copy of unaligned operands for the tiled kernel: read and write at about
+// 3 TB/s, plus its own launch.
+constexpr double kPackBytesPerUs = 3.0e6;
+constexpr double kPackFixedUs = 3.0;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -55,15 +89,33 @@ const char *variant_name(int v) {
         case kVarTile: return "tile";
         case kVarStreamK: return "streamk";
         case kVarSkinny: return "skinny";
+        case kVarMid: return "mid";
+        case kVarMid64: return "mid64";
         default: return "?";
     }
 }
 
-static void plan_tile(const PlanInput &in, Plan *pl, bool allow_sk) {
-    const int64_t G = in.num_sms > 0 ? in.num_sms : 1;
-    const int64_t tm = ceil_div(in.M, kTileBM), tn = ceil_div(in.N, kTileBN);
+// Time of one CTA slice when `ctas` CTAs share `sms` SMs (at most the
+// model's CTAs per SM).
+static double slice_us(const KernelModel &m, int64_t ctas, int64_t sms) {
+    int64_t c = ceil_div(ctas, sms);
+    if (c < 1) c = 1;
+    if (c > m.ctas_per_sm) c = m.ctas_per_sm;
+    return m.slice_us[c];
+}
+
+// Tiles of the model's shape on a persistent grid of at most
+// sms * ctas_per_sm CTAs: whole tiles round-robin, or full waves whole and a
+// stream-K tail; the candidate with the least estimated time.  `cost` is the
+// busiest CTA's slices plus the fix-up allowance in slices; `est_us` the
+// model's time (launch included).
+static void plan_grid(const PlanInput &in, Plan *pl, bool allow_sk, bool force_sk,
+                      const KernelModel &m, double slice_scale) {
+    const int64_t sms = in.num_sms > 0 ? in.num_sms : 1;
+    const int64_t G = sms * m.ctas_per_sm;
+    const int64_t tm = ceil_div(in.M, m.bm), tn = ceil_div(in.N, m.bn);
     const int64_t T = tm * tn;
-    const int64_t KT = ceil_div(in.K, kTileBK);
+    const int64_t KT = ceil_div(in.K, m.bk);
     pl->tiles_m = (int)tm;
     pl->tiles_n = (int)tn;
     pl->kt_total = (int)KT;
@@ -78,11 +130,13 @@ static void plan_tile(const PlanInput &in, Plan *pl, bool allow_sk) {
     best.sk_share = 1;
     best.grid = (int)(T < G ? T : G);
     best.cost = (double)ceil_div(T, G) * (double)KT;
+    best.est_us = kLaunchUs + best.cost * slice_us(m, best.grid, sms) * slice_scale;
     best.reason = "whole tiles";
 
     const bool sk_fits = T * KT < (int64_t(1) << 30);
-    if (allow_sk && sk_fits && (T % G != 0 || in.force_variant == kVarStreamK)) {
+    if (allow_sk && sk_fits && (T % G != 0 || force_sk)) {
         const int64_t full = T / G;
+        const double piece_slices = m.piece_us / (m.slice_us[m.ctas_per_sm] * slice_scale);
         for (int64_t d = full; d >= 0 && d >= full - 1; --d) {
             const int64_t dp = d * G;
             const int64_t sk_tiles = T - dp;
@@ -90,8 +144,9 @@ static void plan_tile(const PlanInput &in, Plan *pl, bool allow_sk) {
             const int64_t total = sk_tiles * KT;
             int64_t share = ceil_div(total, G);
             const int64_t min_share = ceil_div(KT, 8);
-            // Shares from the smallest the grid and the piece limit allow, a
-            // little upward: a larger share can save a piece.
+            // Shares from the smallest the grid and the piece limit allow,
+            // upward: a larger share can save a piece or leave the SMs fewer
+            // CTAs each.
             int64_t last = share;
             if (in.force_splits > 0) {
                 // As close to the requested split as the grid allows.
@@ -100,7 +155,7 @@ static void plan_tile(const PlanInput &in, Plan *pl, bool allow_sk) {
                 last = share;
             } else {
                 if (share < min_share) share = min_share;
-                last = share + share / 2 + 2;
+                last = m.ctas_per_sm > 1 ? 2 * share + 2 : share + share / 2 + 2;
                 if (last > KT) last = KT > share ? KT : share;
             }
             if (share < 1) share = 1;
@@ -111,23 +166,60 @@ static void plan_tile(const PlanInput &in, Plan *pl, bool allow_sk) {
                 // Most pieces any tile is cut into.
                 const int64_t pieces = (KT + sh - 2) / sh + 1;
                 const int64_t max_pieces = pieces < ctas ? pieces : ctas;
-                const double cost = (double)d * KT + (double)sh +
-                                    kFixupCost * (double)(max_pieces > 1 ? max_pieces - 1 : 0);
-                if (cost < best.cost || (in.force_variant == kVarStreamK && !taken)) {
+                const int64_t extra = max_pieces > 1 ? max_pieces - 1 : 0;
+                const int64_t grid = dp > 0 ? G : ctas;
+                const double cost = (double)d * KT + (double)sh + piece_slices * (double)extra;
+                const double est =
+                    kLaunchUs + ((double)d * KT + (double)sh) * slice_us(m, grid, sms) * slice_scale +
+                    (extra > 0 ? m.fixup_us + m.piece_us * (double)extra : 0.0);
+                if (est < best.est_us || (force_sk && !taken)) {
                     best.variant = kVarStreamK;
                     best.dp_tiles = (int)dp;
                     best.sk_tiles = (int)sk_tiles;
                     best.sk_share = (int)sh;
-                    best.grid = (int)(dp > 0 ? G : ctas);
+                    best.grid = (int)grid;
                     best.cost = cost;
+                    best.est_us = est;
                     best.reason = "stream-K tail";
                     taken = true;
                 }
             }
-            if (taken && in.force_variant == kVarStreamK) break;
+            if (taken && force_sk) break;
         }
     }
     *pl = best;
+}
+
+static void plan_tile(const PlanInput &in, Plan *pl, bool allow_sk, int64_t pack_floats) {
+    plan_grid(in, pl, allow_sk, in.force_variant == kVarStreamK, kTileModel, 1.0);
+    if (pl->pack_a || pl->pack_b)
+        pl->est_us += 2.0 * 4.0 * (double)pack_floats / kPackBytesPerUs + kPackFixedUs;
+}
+
+// The mid-size kernel (any alignment): bm x 128 tiles, K slices of 16,
+// mid_ctas_per_sm(bm) CTAs per SM.
+static void plan_mid(const PlanInput &in, Plan *pl, int bm) {
+    const bool b_ok = aligned16(in.b_addr) && in.ldb % 4 == 0;
+    plan_grid(in, pl, true, in.force_splits > 0, bm == 64 ? kMid64Model : kMidModel,
+              b_ok ? 1.0 : kMidUnalignedB);
+    pl->variant = kVarMid;
+    pl->mid_bm = bm;
+    pl->b_vec = b_ok ? 4 : 1;
+    pl->reason = pl->sk_tiles > 0 ? "mid tiles, stream-K tail" : "mid tiles";
+}
+
+// The 64 x 64 kernel: one tile per CTA over the whole K.
+static void plan_generic(const PlanInput &in, Plan *pl) {
+    const int64_t sms = in.num_sms > 0 ? in.num_sms : 1;
+    pl->variant = kVarGeneric;
+    pl->tiles_m = (int)ceil_div(in.M, kGenBM);
+    pl->tiles_n = (int)ceil_div(in.N, kGenBN);
+    pl->kt_total = (int)ceil_div(in.K, kGenBK);
+    pl->grid = pl->tiles_m * pl->tiles_n;
+    const double per_sm = (double)pl->grid / (double)sms;
+    const double scale = per_sm <= 1.0 ? 1.0 : 0.4 + 0.6 * per_sm;
+    pl->cost = (double)pl->kt_total;
+    pl->est_us = kLaunchUs + (double)pl->kt_total * kGenericSliceUs * scale;
 }
 
 // Contiguous ranges of the skinny kernel's positions, one per CTA, balanced
@@ -233,50 +325,66 @@ int make_plan(const PlanInput &in, Plan *pl) {
         }
     }
 
-    // A product with at most kSmallSlicesPerSm 128 x 256 x 32 tile slices per
-    // SM leaves most SMs idle under the tiled kernel, or splits its few tiles
-    // into pieces whose combination costs more than they balance; 64 x 64
-    // tiles spread it over more SMs.  (Measured on GB300 over square sizes:
-    // the 64 x 64 kernel wins up to 768^3, 2.8 slices per SM; the tiled
-    // kernel from 1024^3, 6.7.)
-    bool small = false, small_unaligned = false;
-    if (want < 0) {
-        const int64_t G = in.num_sms > 0 ? in.num_sms : 1;
-        const int64_t slices = ceil_div(in.M, kTileBM) * ceil_div(in.N, kTileBN) *
-                               ceil_div(in.K, kTileBK);
-        small = slices <= kSmallSlicesPerSm * G;
-        small_unaligned = slices <= kPackSlicesPerSm * G;
-    }
-    // Operands the TMA cannot map (a pointer or leading dimension off 16
-    // bytes) are first copied to 16-byte-aligned rows when the product is
-    // large enough for the tiled kernel to repay the copy; smaller products
-    // (and the M <= 16 regime, where copying B would double the bytes moved)
-    // take the bounds-checked 64 x 64 kernel.
-    const int64_t pack_floats = (a_ok ? 0 : in.M * round_up4(in.K)) +
-                                (b_ok ? 0 : in.K * round_up4(in.N));
-    const bool packable = pack_floats < (int64_t(1) << 31);
-    const bool pack = !tma_ok && packable &&
-                      (want == kVarTile || want == kVarStreamK ||
-                       (want < 0 && !small_unaligned && in.M > kSkinnyMaxM));
-    if ((want == kVarTile || want == kVarStreamK) && !tma_ok && !pack) return -2;
-    if (want == kVarGeneric || (want < 0 && ((!tma_ok && !pack) || small))) {
-        p.variant = kVarGeneric;
-        p.tiles_m = (int)ceil_div(in.M, kGenBM);
-        p.tiles_n = (int)ceil_div(in.N, kGenBN);
-        p.kt_total = (int)ceil_div(in.K, kGenBK);
-        p.grid = p.tiles_m * p.tiles_n;
-        p.cost = 0;
-        p.reason = !tma_ok ? "operands not 16-byte aligned" : small ? "small product" : "forced";
+    // Forced kernels (tests and the planner sweep).
+    if (want == kVarGeneric) {
+        plan_generic(in, &p);
+        p.reason = "forced";
         *pl = p;
         return 0;
     }
-    p.pack_a = pack && !a_ok;
-    p.pack_b = pack && !b_ok;
-    p.lda_packed = p.pack_a ? round_up4(in.K) : in.lda;
-    p.ldb_packed = p.pack_b ? round_up4(in.N) : in.ldb;
-    plan_tile(in, &p, want != kVarTile);
-    if (pack) p.reason = "operands copied to aligned rows";
-    *pl = p;
+    if (want == kVarMid || want == kVarMid64) {
+        plan_mid(in, &p, want == kVarMid64 ? 64 : 128);
+        *pl = p;
+        return 0;
+    }
+    // Operands the TMA cannot map (a pointer or leading dimension off 16
+    // bytes) can be copied to 16-byte-aligned rows for the tiled kernel.
+    const int64_t pack_floats = (a_ok ? 0 : in.M * round_up4(in.K)) +
+                                (b_ok ? 0 : in.K * round_up4(in.N));
+    const bool packable = pack_floats < (int64_t(1) << 31);
+    auto tile_plan = [&](Plan *t, bool allow_sk) {
+        t->pack_a = !a_ok;
+        t->pack_b = !b_ok;
+        t->lda_packed = t->pack_a ? round_up4(in.K) : in.lda;
+        t->ldb_packed = t->pack_b ? round_up4(in.N) : in.ldb;
+        plan_tile(in, t, allow_sk, pack_floats);
+        if (!tma_ok) t->reason = "operands copied to aligned rows";
+    };
+    if (want == kVarTile || want == kVarStreamK) {
+        if (!tma_ok && !packable) return -2;
+        tile_plan(&p, want != kVarTile);
+        *pl = p;
+        return 0;
+    }
+
+    // Automatic ("Part 2", section "Selecting Among Three Kernels"): the
+    // least estimated time among the tiled kernel (aligned operands, or
+    // copies of them unless M <= 16, where copying B would double the bytes
+    // moved), the mid-size kernel with 128-row tiles and, for M <= 64, with
+    // 64-row tiles, and the 64 x 64 kernel.
+    Plan cand[4];
+    int n = 0;
+    cand[n] = p;
+    plan_mid(in, &cand[n++], 128);
+    if (in.M <= 64) {
+        cand[n] = p;
+        plan_mid(in, &cand[n++], 64);
+    }
+    if (tma_ok || (packable && in.M > kSkinnyMaxM)) {
+        cand[n] = p;
+        tile_plan(&cand[n++], true);
+    }
+    cand[n] = p;
+    plan_generic(in, &cand[n]);
+    cand[n++].reason = "64 x 64 tiles";
+    int bi = 0;
+    for (int i = 1; i < n; ++i)
+        if (cand[i].est_us < cand[bi].est_us) bi = i;
+    double alt = 0;
+    for (int i = 0; i < n; ++i)
+        if (i != bi && (alt == 0 || cand[i].est_us < alt)) alt = cand[i].est_us;
+    cand[bi].alt_us = alt;
+    *pl = cand[bi];
     return 0;
 }
 
@@ -284,11 +392,12 @@ int describe_plan(const Plan &p, char *buf, size_t len) {
     return snprintf(buf, len,
                     "variant=%s tiles_m=%d tiles_n=%d kt=%d dp_tiles=%d sk_tiles=%d sk_share=%d "
                     "grid=%d group_m=%d c_vec4=%d m_tile=%d two_unit_ctas=%d pack_a=%d pack_b=%d "
-                    "cost=%.2f reason=%s",
+                    "bm=%d bvec=%d cost=%.2f est_us=%.1f alt_us=%.1f reason=%s",
                     variant_name(p.variant), p.tiles_m, p.tiles_n, p.kt_total, p.dp_tiles,
                     p.sk_tiles, p.sk_share, p.grid, p.group_m, p.c_vec4, p.m_tile,
                     p.variant == kVarSkinny ? p.sk_two_units : 0, p.pack_a ? 1 : 0,
-                    p.pack_b ? 1 : 0, p.cost, p.reason ? p.reason : "");
+                    p.pack_b ? 1 : 0, p.mid_bm, p.b_vec, p.cost, p.est_us, p.alt_us,
+                    p.reason ? p.reason : "");
 }
 
 }  // namespace sgemm

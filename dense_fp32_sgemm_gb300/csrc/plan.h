@@ -15,6 +15,8 @@ enum Variant : int {
     kVarTile = 1,       // data-parallel only
     kVarStreamK = 2,    // data-parallel waves + stream-K tail
     kVarSkinny = 3,
+    kVarMid = 4,        // mid-size kernel, bm x 128 tiles (bm = 128 when forced)
+    kVarMid64 = 5,      // forced: the mid-size kernel with 64 x 128 tiles
 };
 
 struct PlanInput {
@@ -38,6 +40,11 @@ struct Plan {
     int m_tile, slabs;
     int sk_starts[161];
     int sk_two_units;  // CTAs whose range crosses a slab boundary
+    // mid-size kernel: tile height (128 or 64) and B copy width in floats (4 or 1)
+    int mid_bm, b_vec;
+    // estimated time of the chosen plan (microseconds) and of the best other
+    // candidate considered (0 when there was none)
+    double est_us, alt_us;
     // operands copied to 16-byte-aligned rows first (leading dimensions after the copy)
     bool pack_a, pack_b;
     int64_t lda_packed, ldb_packed;

@@ -1,7 +1,8 @@
 """Planner check over a sweep of shapes: for each shape, time the plan the
-library picks and the alternatives it could have picked (whole tiles only,
-stream-K, the 64 x 64 kernel), and report how far the automatic choice is
-from the fastest.
+library picks and the alternatives it could have picked (the tiled kernel
+with whole tiles only or with a stream-K tail, the mid-size kernel with 128-
+or 64-row tiles, the 64 x 64 kernel), and report how far the automatic choice
+is from the fastest, and how far each plan's time estimate is from its time.
 
     python -m dense_fp32_sgemm_gb300.sweep [--sizes 511,512,513,...] [--reps 30]
 
@@ -24,7 +25,8 @@ DEFAULT_SIZES = [256, 511, 512, 513, 1023, 1024, 1025, 1535, 1536, 2047, 2048, 2
                  3071, 3072, 3073, 4095, 4096, 4097]
 
 CANDIDATES = [("auto", sg.VARIANT_AUTO), ("tile", sg.VARIANT_TILE),
-              ("streamk", sg.VARIANT_STREAMK), ("generic", sg.VARIANT_GENERIC)]
+              ("streamk", sg.VARIANT_STREAMK), ("mid", sg.VARIANT_MID),
+              ("mid64", sg.VARIANT_MID64), ("generic", sg.VARIANT_GENERIC)]
 
 
 def time_launches(torch, fn, reps, flush, sink, stream):
@@ -53,7 +55,10 @@ def main():
     ap.add_argument("--shapes", default="",
                     help="extra shapes MxNxK, comma separated (leading dimensions K and N)")
     ap.add_argument("--reps", type=int, default=30)
+    ap.add_argument("--variants", default=",".join(n for n, _ in CANDIDATES),
+                    help="candidates to time (auto is always timed)")
     args = ap.parse_args()
+    chosen = set(args.variants.split(",")) | {"auto"}
     shapes = [(int(x),) * 3 for x in args.sizes.split(",") if x]
     shapes += [tuple(int(v) for v in x.split("x")) for x in args.shapes.split(",") if x]
 
@@ -70,6 +75,8 @@ def main():
         times = {}
         plans = {}
         for name, variant in CANDIDATES:
+            if name not in chosen:
+                continue
             sg.set_plan_override(variant, 0)
             try:
                 plans[name] = sg.plan_describe(M, N, K, a_addr=A.data_ptr(), b_addr=B.data_ptr(),
@@ -95,7 +102,11 @@ def main():
                "best": best, "best_us": round(times[best] * 1e6, 2),
                "auto_over_best": round(times["auto"] / times[best], 3),
                "auto_tflops": round(flops / times["auto"] / 1e12, 2),
-               "us": {k: round(v * 1e6, 2) for k, v in times.items()}}
+               "us": {k: round(v * 1e6, 2) for k, v in times.items()},
+               "est_us": {k: float(plans[k].get("est_us", 0)) for k in times},
+               "plans": {k: {f: plans[k].get(f) for f in ("variant", "bm", "grid", "dp_tiles",
+                                                           "sk_tiles", "sk_share", "kt")}
+                         for k in times}}
         rows.append(row)
         print(f"{M:5d}x{N:5d}x{K:5d} auto={row['auto']:8s} {row['auto_us']:9.2f} us "
               f"({row['auto_tflops']:6.2f} TFLOP/s)  best={best:8s} {row['best_us']:9.2f} us  "

@@ -203,9 +203,9 @@ SGEMM_API sgemm_status_t sgemm_plan_describe(int64_t M, int64_t N, int64_t K,
 /*
  * sgemm_set_plan_override -- testing and benchmarking hook, process-wide.
  * variant: -1 = automatic; otherwise one of SGEMM_VARIANT_*.
- * splits: for the stream-K variants, 0 = automatic, else the number of
- *   k-iterations each CTA takes in the stream-K region is chosen so that
- *   tiles split into about `splits` pieces.
+ * splits: for the stream-K variants (and the mid-size ones), 0 = automatic,
+ *   else the number of k-iterations each CTA takes in the stream-K region is
+ *   chosen so that tiles split into about `splits` pieces.
  * Returns SGEMM_ERR_INVALID_ARG for an unknown variant.
  */
 enum {
@@ -213,7 +213,10 @@ enum {
     SGEMM_VARIANT_GENERIC = 0,   /* any alignment: 64x64 tile, bounds-checked loads  */
     SGEMM_VARIANT_TILE = 1,      /* TMA + FFMA2 128x256 tile, whole tiles only        */
     SGEMM_VARIANT_STREAMK = 2,   /* same kernel, data-parallel waves + stream-K tail  */
-    SGEMM_VARIANT_SKINNY = 3     /* small-M streaming kernel (HBM-bound shapes)       */
+    SGEMM_VARIANT_SKINNY = 3,    /* small-M streaming kernel (HBM-bound shapes)       */
+    SGEMM_VARIANT_MID = 4,       /* cp.async + FFMA2 128x128 tile, any alignment,     */
+                                 /* data-parallel waves + stream-K tail               */
+    SGEMM_VARIANT_MID64 = 5      /* the same kernel with 64x128 tiles                 */
 };
 SGEMM_API sgemm_status_t sgemm_set_plan_override(int variant, int splits);
 

@@ -45,27 +45,27 @@ def test_quick_returns():
 
 
 def test_misaligned_operands():
-    # 1023^3: lda = ldb = 1023 break 16-byte row alignment.  The product is
-    # large enough for the tiled kernel to repay copying both operands to
-    # aligned rows first.
+    # Unaligned rows (lda = ldb = 1023): the mid-size kernel reads them with
+    # 4-byte copies, so no copy pass is planned ...
     p = plan(1023, 1023, 1023, aligned_ld=False)
-    assert p["variant"] == "streamk" and ints(p, "pack_a", "pack_b") == [1, 1]
-    # 1023 x 1025 x 513 (4.5 slices per SM) does not repay the copies
+    assert p["variant"] == "mid" and ints(p, "bvec", "pack_a", "pack_b") == [1, 0, 0]
     p = plan(1023, 1025, 513, aligned_ld=False)
-    assert p["variant"] == "generic" and ints(p, "pack_a", "pack_b") == [0, 0]
-    # only the unaligned operand is copied
-    p = plan(2048, 2048, 2048, a_addr=(1 << 20) + 4)
-    assert p["variant"] in ("tile", "streamk") and ints(p, "pack_a", "pack_b") == [1, 0]
-    # a small product, or M <= 16 (copying B would double the bytes moved),
-    # takes the bounds-checked 64 x 64 kernel instead
-    assert plan(256, 256, 256, a_addr=(1 << 20) + 4)["variant"] == "generic"
+    assert p["variant"] in ("mid", "generic") and ints(p, "pack_a", "pack_b") == [0, 0]
+    # ... B aligned keeps its 16-byte copies
+    p = plan(1023, 1024, 1023, lda=1023)
+    assert p["variant"] == "mid" and p["bvec"] == "4"
+    # M <= 16 with an unaligned operand: not the skinny kernel (TMA), and the
+    # tiled kernel's copy of B is never considered
     p = plan(16, 8192, 8191, aligned_ld=False)
-    assert p["variant"] == "generic" and ints(p, "pack_a", "pack_b") == [0, 0]
-    # forcing the tiled kernel on unaligned operands copies them
+    assert p["variant"] == "mid" and ints(p, "pack_a", "pack_b") == [0, 0]
+    # forcing the tiled kernel on unaligned operands copies only the
+    # unaligned one to aligned rows
     sg.set_plan_override(sg.VARIANT_TILE, 0)
     try:
         p = plan(300, 400, 500, b_addr=(2 << 20) + 8)
         assert p["variant"] == "tile" and ints(p, "pack_a", "pack_b") == [0, 1]
+        p = plan(2048, 2048, 2048, a_addr=(1 << 20) + 4)
+        assert ints(p, "pack_a", "pack_b") == [1, 0]
     finally:
         sg.set_plan_override(-1, 0)
 
@@ -100,12 +100,7 @@ def test_exact_waves_stay_data_parallel():
     assert ints(p, "dp_tiles", "grid") == [304, SMS]
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 32 * 700), (1000, 3000, 231), (8192, 6144, 2048),
-                                   (17, 8192, 8192), (4000, 300, 20000), (129, 257, 32 * 160),
-                                   (40, 1, 100000), (5000, 5000, 1)])
-def test_plan_invariants(M, N, K):
-    p = plan(M, N, K)
-    assert p["variant"] in ("tile", "streamk")
+def tile_invariants(p, M, N, K, forced_sk=False):
     tm, tn, kt, dp, sk, share, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles",
                                            "sk_tiles", "sk_share", "grid")
     T = tm * tn
@@ -119,25 +114,94 @@ def test_plan_invariants(M, N, K):
         # pieces per tile stay within what the idle ring combines (nine)
         assert share >= math.ceil(kt / 8)
         assert (kt + share - 2) // share + 1 <= 9
-    # the chosen cost never exceeds the data-parallel cost
-    assert float(p["cost"]) <= math.ceil(T / SMS) * kt + 1e-9
+    # the chosen cost never exceeds the data-parallel cost (a forced stream-K
+    # split takes the first candidate)
+    if not forced_sk:
+        assert float(p["cost"]) <= math.ceil(T / SMS) * kt + 1e-9
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (129, 257, 33), (1024, 1024, 64),
-                                   (2048, 2048, 16), (300, 520, 64), (768, 768, 768)])
-def test_small_products_take_the_64x64_kernel(M, N, K):
-    # At most 4 tile slices (128 x 256 x 32) per SM: the tiled kernel would
-    # idle most SMs or split its few tiles too finely.
-    assert math.ceil(M / 128) * math.ceil(N / 256) * math.ceil(K / 32) <= 4 * SMS
+def mid_invariants(p, M, N, K):
+    bm = int(p["bm"])
+    assert bm in (128, 64)
+    cps = 2 if bm == 128 else 4
+    tm, tn, kt, dp, sk, share, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles",
+                                           "sk_tiles", "sk_share", "grid")
+    T = tm * tn
+    assert tm == math.ceil(M / bm) and tn == math.ceil(N / 128) and kt == math.ceil(K / 16)
+    assert dp + sk == T
+    assert 1 <= grid <= SMS * cps
+    if sk:
+        assert dp % (SMS * cps) == 0
+        assert share * grid >= sk * kt
+        assert (kt + share - 2) // share + 1 <= 9
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 32 * 700), (1000, 3000, 231), (8192, 6144, 2048),
+                                   (17, 8192, 8192), (4000, 300, 20000), (129, 257, 32 * 160),
+                                   (40, 1, 100000), (5000, 5000, 1)])
+def test_plan_invariants(M, N, K):
+    # The tiled kernel forced whole, forced stream-K, and the mid-size kernel
+    # forced with either tile height each cover the work; the automatic plan
+    # is one of them or the 64 x 64 kernel.
+    for variant in (sg.VARIANT_TILE, sg.VARIANT_STREAMK):
+        sg.set_plan_override(variant, 0)
+        try:
+            tile_invariants(plan(M, N, K), M, N, K, forced_sk=variant == sg.VARIANT_STREAMK)
+        finally:
+            sg.set_plan_override(-1, 0)
+    for variant in (sg.VARIANT_MID, sg.VARIANT_MID64):
+        sg.set_plan_override(variant, 0)
+        try:
+            mid_invariants(plan(M, N, K), M, N, K)
+        finally:
+            sg.set_plan_override(-1, 0)
     p = plan(M, N, K)
-    assert p["variant"] == "generic" and p["reason"] == "small product"
+    if p["variant"] in ("tile", "streamk"):
+        tile_invariants(p, M, N, K)
+    elif p["variant"] == "mid":
+        mid_invariants(p, M, N, K)
+    else:
+        assert p["variant"] == "generic"
 
 
-def test_the_tiled_kernel_takes_over_above_four_slices_per_sm():
-    assert 19 * 8 * 4 == 4 * SMS
-    assert plan(128 * 19, 256 * 8, 32 * 4)["variant"] == "generic"
-    assert plan(128 * 19, 256 * 8, 32 * 4 + 1)["variant"] in ("tile", "streamk")
-    assert plan(1024, 1024, 1024)["variant"] in ("tile", "streamk")
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (129, 257, 33), (256, 256, 256),
+                                   (300, 520, 64), (511, 511, 511)])
+def test_tiny_products_take_the_64x64_kernel(M, N, K):
+    # Measured on GB300: below about 512^3 the 64 x 64 kernel's short
+    # start-up wins (128^3: 12.5 us against 20.5 on the mid-size kernel).
+    p = plan(M, N, K)
+    assert p["variant"] == "generic" and p["reason"] == "64 x 64 tiles"
+
+
+@pytest.mark.parametrize("M,N,K", [(768, 768, 768), (1024, 1024, 1024), (1000, 3000, 231),
+                                   (1024, 1024, 512)])
+def test_mid_size_products_take_the_mid_kernel(M, N, K):
+    # 128 x 128 tiles fill more SMs than 128 x 256 ones (1024^3: 59.4 us
+    # against 60.2 on the tiled kernel, 80 on the 64 x 64 one).
+    p = plan(M, N, K)
+    assert p["variant"] == "mid" and p["bm"] == "128"
+
+
+@pytest.mark.parametrize("M", [17, 24, 32, 48, 64])
+def test_short_products_take_64_row_tiles(M):
+    # 17 <= M <= 64: 64-row tiles waste at most 47 rows a tile (64 x 8192 x
+    # 8192: 173.5 us against 283 on the 128 x 256 tiled kernel).
+    p = plan(M, 8192, 8192)
+    assert p["variant"] == "mid" and p["bm"] == "64"
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 2048), (4092, 4092, 4092), (8192, 6144, 2048),
+                                   (3072, 3072, 3072), (8192, 256, 8192)])
+def test_large_aligned_products_take_the_tiled_kernel(M, N, K):
+    p = plan(M, N, K)
+    assert p["variant"] in ("tile", "streamk")
+
+
+def test_estimates_are_reported_and_ordered():
+    # The plan reports its estimate and the best other candidate's.
+    p = plan(2048, 2048, 2048)
+    est, alt = float(p["est_us"]), float(p["alt_us"])
+    assert 200 < est < 350 and alt >= est
 
 
 def test_forced_split_count():
@@ -200,9 +264,13 @@ def test_skinny_16x8192x8192_split():
 
 @pytest.mark.parametrize("M,N,K,share,grid", [(768, 768, 4096, 16, 144), (640, 640, 8192, 32, 120)])
 def test_deep_products_with_few_tiles_split_finer(M, N, K, share, grid):
-    # 18 and 15 tiles: shares of an eighth of K keep most SMs busy while each
-    # tile stays within nine pieces.
-    p = plan(M, N, K)
+    # The tiled kernel on 18 and 15 tiles: shares of an eighth of K keep most
+    # SMs busy while each tile stays within nine pieces.
+    sg.set_plan_override(sg.VARIANT_STREAMK, 0)
+    try:
+        p = plan(M, N, K)
+    finally:
+        sg.set_plan_override(-1, 0)
     assert p["variant"] == "streamk"
     assert ints(p, "sk_share", "grid") == [share, grid]
 
@@ -282,17 +350,11 @@ def test_random_plans_cover_the_work():
     for M, N, K in _random_shapes(11, 300):
         p = plan(M, N, K)
         v = p["variant"]
-        assert v in ("tile", "streamk", "generic", "skinny", "scale", "none"), (M, N, K, v)
+        assert v in ("tile", "streamk", "mid", "generic", "skinny", "scale", "none"), (M, N, K, v)
         if v in ("tile", "streamk"):
-            tm, tn, kt, dp, sk, share, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles",
-                                                   "sk_tiles", "sk_share", "grid")
-            T = tm * tn
-            assert dp + sk == T and 1 <= grid <= SMS
-            if sk:
-                assert dp % SMS == 0
-                assert share * grid >= sk * kt, (M, N, K)
-                assert (kt + share - 2) // share + 1 <= 9, (M, N, K, share)
-            assert float(p["cost"]) <= math.ceil(T / SMS) * kt + 1e-9
+            tile_invariants(p, M, N, K)
+        elif v == "mid":
+            mid_invariants(p, M, N, K)
         elif v == "skinny":
             assert M <= 16
             slabs, kt, grid = ints(p, "tiles_n", "kt", "grid")
