@@ -299,7 +299,7 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             return status_from(launch_mid(pl.mid_bm, pl.b_vec, mp, pl.grid, stream));
         }
         case kVarSkinny: {
-            const unsigned bit = 1u << (24 + pl.m_tile / 8);
+            const unsigned bit = 1u << (24 + pl.m_tile / 8);  // m_tile 8, 16, 32: bits 25, 26, 28
             if (!(d.configured & bit)) {
                 if (skinny_configure(pl.m_tile) != cudaSuccess) return SGEMM_ERR_LAUNCH;
                 d.configured |= bit;
@@ -322,7 +322,7 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             sp.timeout_ns = to ? to : kDefaultTimeoutNs;
             sp.skip_loads_from = g_skip_loads_from.load();
             Workspace *w = nullptr;
-            const size_t pbytes = (size_t)2 * pl.grid * kSkinnyMaxM * kSkinnyBN * sizeof(float);
+            const size_t pbytes = (size_t)2 * pl.grid * pl.m_tile * kSkinnyBN * sizeof(float);
             s = ensure_workspace(d, stream, pbytes, (size_t)pl.slabs, &w);
             if (s != SGEMM_OK) return s;
             sp.partials = w->partials;

@@ -1,4 +1,4 @@
-// Skinny-M FP32 GEMM (M <= 16): the decode-like regime where B is streamed
+// Skinny-M FP32 GEMM (M <= 32): the decode-like regime where B is streamed
 // from HBM once and every B element feeds only M multiply-adds, so the
 // kernel is bound by memory bandwidth, not by the FP32 pipe ("GEMM from
 // Scratch", Module 08, "The Regime That Runs LLM Inference": a tall-skinny
@@ -14,19 +14,21 @@
 // a ring of shared-memory stages completed on mbarriers, several stages
 // ahead, so enough bytes are in flight to keep HBM busy.
 //
-// One CTA of 8 warps per SM holds a 6-stage ring (with the 4-warp build, two
-// CTAs of 4 warps share an SM, 3 stages each).  Each lane owns 8 columns (two
-// groups of four, so a quarter-warp's 128-bit loads cover 32 consecutive
-// banks) and a warp the whole 256-column row.  With 16 rows of A the warps
-// form two groups of four that take alternate positions, 8 rows of each
-// block per warp; with 8 rows all 8 warps share every position, 4 rows each.
-// Either way warp w of a group takes rows w, w + W, w + 2W, ... of a block
-// (W warps in the group).  A warp rewrites only the A columns it needs
+// One CTA of 8 warps per SM holds a 6-stage ring (5 stages with a 32-row A
+// tile; with the 4-warp build, two CTAs of 4 warps share an SM, 3 stages
+// each).  Each lane owns 8 columns (two groups of four, so a quarter-warp's
+// 128-bit loads cover 32 consecutive banks) and a warp the whole 256-column
+// row.  With 16 rows of A the warps form two groups of four that take
+// alternate positions, 8 rows of each block per warp; with 32 rows the two
+// groups share every position, group g summing rows 16 g .. 16 g + 15 (so a
+// thread still holds 16 x 8 sums); with 8 rows all 8 warps share every
+// position, 4 rows each.  Either way warp w of a group takes rows w, w + W,
+// w + 2W, ... of a block (W warps in the group).  A warp rewrites only the A columns it needs
 // k-major into its own corner of shared memory, so no CTA-wide barrier is
 // needed inside a unit: warps run through the stages independently, and the
 // last warp of the group to finish with a stage (a counter in shared memory)
 // refills it with the position SSTAGES further on, which belongs to the same
-// group.  The update is the packed FP32 fma (__ffma2_rn) on pairs along m:
+// group (with split rows, the last of all eight warps).  The update is the packed FP32 fma (__ffma2_rn) on pairs along m:
 // (a_m, a_m+1) * (b_n, b_n).
 //
 // After a unit the warps' sums are added in warp order through shared
@@ -45,31 +47,37 @@ constexpr int SBN = kSkinnyBN;       // 256 columns per slab
 constexpr int SBK = kSkinnyBK;       // 32 rows of B per stage
 constexpr int WARPS = kSkinnyWarps;  // 4 or 8
 constexpr int SNT = kSkinnyThreads;
-constexpr int SSTAGES = kSkinnyStages;
 constexpr int CPL = 8;               // columns per lane: a warp covers the row
 constexpr int OWN = SBN / SNT;       // adjacent columns a thread owns after the reduction
 static_assert(32 * CPL == SBN && (OWN == 1 || OWN == 2), "warp layout");
 
 // Warp groups: with 8 warps and 16 rows of A, two groups of four warps take
-// alternate positions (8 rows of each block per warp); otherwise all warps
-// share every position.
+// alternate positions (8 rows of each block per warp); with 8 warps and 32
+// rows, two groups of four share every position and split the rows of A
+// (row_split); otherwise all warps share every position.
 template <int MT>
 struct WarpPlan {
-    static constexpr int groups = (WARPS == 8 && MT == 16) ? 2 : 1;
+    static constexpr bool row_split = (WARPS == 8 && MT == 32);
+    static constexpr int groups = (WARPS == 8 && (MT == 16 || MT == 32)) ? 2 : 1;
     static constexpr int gwarps = WARPS / groups;  // warps per group
     static constexpr int rpw = SBK / gwarps;       // rows of a block per warp
+    static constexpr int mr = row_split ? MT / groups : MT;  // rows of A a warp sums
+    // warps that read a stage before it is refilled
+    static constexpr int readers = row_split ? WARPS : gwarps;
     static_assert(rpw * gwarps == SBK, "rows per warp");
+    static_assert(MT != 32 || WARPS == 8, "32-row tiles need the 8-warp build");
 };
 
 template <int MT>
 struct SkinnyLayout {
+    static constexpr int SSTAGES = skinny_stages(MT);
     static constexpr int RPW = WarpPlan<MT>::rpw;
     static constexpr int a_floats = MT * SBK;  // M x 32, 128-byte rows, swizzled
     static constexpr int b_floats = SBK * SBN;
     static constexpr int stage_floats = a_floats + b_floats;
     static constexpr size_t stage_bytes = size_t(stage_floats) * 4;
     static_assert(stage_bytes % 1024 == 0, "stages must keep 1024-byte alignment");
-    static constexpr int at_floats = RPW * MT;  // per warp: RPW k x MT m
+    static constexpr int at_floats = RPW * WarpPlan<MT>::mr;  // per warp: RPW k x mr m
     static constexpr int RED_ROWS = 2;          // rows of M per reduction round
     static constexpr int red_floats = WARPS * RED_ROWS * SBN;
     static constexpr size_t at_off = SSTAGES * stage_bytes;
@@ -87,6 +95,7 @@ struct SkinnyLayout {
     static_assert(kSkinnyCtasPerSm * (total + 1024) <= 233472, "CTAs per SM do not fit");
 };
 
+template <int MT>
 __device__ __forceinline__ int skinny_slot(const SkinnyParams &p, int cta, int slab) {
     const int start = slab * p.kt_total;
     const int k0 = max(p.starts[cta], start) - start;
@@ -106,8 +115,10 @@ __device__ __forceinline__ int skinny_owner(const SkinnyParams &p, int u) {
     return lo;
 }
 
+// A slot holds MT rows of a slab.
+template <int MT>
 __device__ __forceinline__ const float *skinny_piece(const SkinnyParams &p, int cta, int slab) {
-    return p.partials + (size_t)skinny_slot(p, cta, slab) * (kSkinnyMaxM * SBN);
+    return p.partials + (size_t)skinny_slot<MT>(p, cta, slab) * (MT * SBN);
 }
 
 
@@ -162,6 +173,7 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
                         const __grid_constant__ CUtensorMap mapB,
                         const __grid_constant__ SkinnyParams p) {
     using L = SkinnyLayout<MT>;
+    constexpr int SSTAGES = L::SSTAGES;
     extern __shared__ __align__(1024) uint8_t smem[];
     float *stages = reinterpret_cast<float *>(smem);
     float *red = reinterpret_cast<float *>(smem + L::red_off);
@@ -176,7 +188,10 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
     float *at_w = reinterpret_cast<float *>(smem + L::at_off) + warp * L::at_floats;
     constexpr int GROUPS = WarpPlan<MT>::groups, GW = WarpPlan<MT>::gwarps;
     constexpr int RPW = WarpPlan<MT>::rpw;
+    constexpr bool ROW_SPLIT = WarpPlan<MT>::row_split;
+    constexpr int MR = WarpPlan<MT>::mr;  // rows of A this warp sums
     const int grp = warp / GW, wl = warp % GW;  // group, and warp within it
+    const int row0 = ROW_SPLIT ? grp * MR : 0;  // first of those rows
 
     const int u0 = p.starts[cta];
     const int q_total = p.starts[cta + 1] - u0;
@@ -224,14 +239,14 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
         const int k0 = u - slab * p.kt_total;
         const int k1 = min(p.kt_total, k0 + (q_total - q));
 
-        float2 acc[MT / 2][CPL];  // acc[ip][j] = (C[2ip][n_j], C[2ip+1][n_j])
+        float2 acc[MR / 2][CPL];  // acc[ip][j] = (C[row0+2ip][n_j], C[row0+2ip+1][n_j])
 #pragma unroll
-        for (int i = 0; i < MT / 2; ++i)
+        for (int i = 0; i < MR / 2; ++i)
 #pragma unroll
             for (int j = 0; j < CPL; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
         for (int kt = k0; kt < k1; ++kt, ++q) {
-            if (GROUPS > 1 && q % GROUPS != grp) continue;  // the other group's position
+            if (GROUPS > 1 && !ROW_SPLIT && q % GROUPS != grp) continue;  // the other group's
             const int s = q % SSTAGES;
             // After a timeout anywhere in the CTA (flags[0], a hint) the
             // remaining waits are skipped; the garbage computed is discarded.
@@ -243,11 +258,12 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
             }
             const float *raw = stages + s * L::stage_floats;
             const float *bs = raw + L::a_floats;
-            // This warp's A columns k = wl + GW * kk, k-major: at_w[kk * MT + m].
+            // This warp's A columns k = wl + GW * kk of its rows, k-major:
+            // at_w[kk * MR + m] = A[row0 + m][k].
 #pragma unroll
-            for (int e = lane; e < RPW * MT; e += 32) {
-                const int m = e % MT, kk = e / MT;
-                at_w[kk * MT + m] = a_elem(raw, m, wl + GW * kk);
+            for (int e = lane; e < RPW * MR; e += 32) {
+                const int m = e % MR, kk = e / MR;
+                at_w[kk * MR + m] = a_elem(raw, row0 + m, wl + GW * kk);
             }
             __syncwarp();
 
@@ -274,8 +290,8 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
                 // A values of this row: broadcast loads from the warp's own
                 // k-major copy.
 #pragma unroll
-                for (int r = 0; r < MT / 4; ++r) {
-                    const float4 a = ld_shared_f4(at_w + kk * MT + r * 4);
+                for (int r = 0; r < MR / 4; ++r) {
+                    const float4 a = ld_shared_f4(at_w + kk * MR + r * 4);
                     const float2 a01 = make_float2(a.x, a.y);
                     const float2 a23 = make_float2(a.z, a.w);
 #pragma unroll
@@ -287,11 +303,11 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
                 }
             }
             __syncwarp();
-            // Release the stage; the last warp of the group to do so refills it.
+            // Release the stage; the last of its readers refills it.
             if (lane == 0) {
                 __threadfence_block();
                 const int old = atomicAdd(&release[s], 1);
-                if (old == GW - 1) {
+                if (old == WarpPlan<MT>::readers - 1) {
                     release[s] = 0;
                     if (q + SSTAGES < q_total && !flags[0]) {
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -308,11 +324,15 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
         }
 
         // ---- add the warps' sums in warp order ----
-        // Thread t owns columns [OWN t, OWN t + OWN) and all MT rows.
+        // Thread t owns columns [OWN t, OWN t + OWN) and all MT rows.  Round
+        // r brings rows RR r .. RR r + RR - 1 of every warp's MR rows
+        // through `red`; row m of C sums the warps that hold it (all warps,
+        // or with split rows the warps of group m / MR).
         constexpr int RR = L::RED_ROWS;
+        constexpr int SUMMED = ROW_SPLIT ? GW : WARPS;  // warps holding a row
         float fin[MT][OWN];
 #pragma unroll
-        for (int r = 0; r < MT / RR; ++r) {
+        for (int r = 0; r < MR / RR; ++r) {
 #pragma unroll
             for (int i = 0; i < RR; ++i) {
                 const int m = RR * r + i;
@@ -328,24 +348,27 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
             }
             __syncthreads();
 #pragma unroll
-            for (int i = 0; i < RR; ++i) {
-                float sum[OWN], x[OWN];
-                Vec<OWN>::load(red + i * SBN + col0, sum);
+            for (int g = 0; g < WARPS / SUMMED; ++g) {
 #pragma unroll
-                for (int w = 1; w < WARPS; ++w) {
-                    Vec<OWN>::load(red + (w * RR + i) * SBN + col0, x);
+                for (int i = 0; i < RR; ++i) {
+                    float sum[OWN], x[OWN];
+                    Vec<OWN>::load(red + ((g * SUMMED) * RR + i) * SBN + col0, sum);
 #pragma unroll
-                    for (int o = 0; o < OWN; ++o) sum[o] += x[o];
+                    for (int w = 1; w < SUMMED; ++w) {
+                        Vec<OWN>::load(red + ((g * SUMMED + w) * RR + i) * SBN + col0, x);
+#pragma unroll
+                        for (int o = 0; o < OWN; ++o) sum[o] += x[o];
+                    }
+#pragma unroll
+                    for (int o = 0; o < OWN; ++o) fin[g * MR + RR * r + i][o] = sum[o];
                 }
-#pragma unroll
-                for (int o = 0; o < OWN; ++o) fin[RR * r + i][o] = sum[o];
             }
             __syncthreads();
         }
 
         bool write_c = true;
         if (!(k0 == 0 && k1 == p.kt_total)) {
-            float *slot = p.partials + (size_t)skinny_slot(p, cta, slab) * (kSkinnyMaxM * SBN);
+            float *slot = p.partials + (size_t)skinny_slot<MT>(p, cta, slab) * (MT * SBN);
 #pragma unroll
             for (int m = 0; m < MT; ++m) Vec<OWN>::store_cg(slot + m * SBN + col0, fin[m]);
             __threadfence();
@@ -387,7 +410,7 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
                                 for (int c = cc; c < cc_end; ++c) {
                                     if (c == cta) continue;
                                     bulk_load(reinterpret_cast<char *>(stages) + j * L::piece_bytes,
-                                              skinny_piece(p, c, slab), L::piece_bytes, fix_bar);
+                                              skinny_piece<MT>(p, c, slab), L::piece_bytes, fix_bar);
                                     ++j;
                                 }
                             }
@@ -434,7 +457,7 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
 #pragma unroll
                                 for (int o = 0; o < OWN; ++o) x[o] = own[m][o];
                             } else {
-                                Vec<OWN>::load_cg(skinny_piece(p, c, slab) + m * SBN + col0, x);
+                                Vec<OWN>::load_cg(skinny_piece<MT>(p, c, slab) + m * SBN + col0, x);
                             }
 #pragma unroll
                             for (int o = 0; o < OWN; ++o)
@@ -496,15 +519,22 @@ cudaError_t configure_impl() {
 
 }  // namespace
 
+// 32-row tiles exist only in the 8-warp build (two row groups of four warps).
+constexpr bool kHas32 = WARPS == 8;
+
 size_t skinny_smem_bytes(int m_tile, int /*share*/) {
     if (m_tile == 8) return SkinnyLayout<8>::total;
     if (m_tile == 16) return SkinnyLayout<16>::total;
+    if constexpr (kHas32)
+        if (m_tile == 32) return SkinnyLayout<32>::total;
     return 0;
 }
 
 cudaError_t skinny_configure(int m_tile) {
     if (m_tile == 8) return configure_impl<8>();
     if (m_tile == 16) return configure_impl<16>();
+    if constexpr (kHas32)
+        if (m_tile == 32) return configure_impl<32>();
     return cudaErrorInvalidValue;
 }
 
@@ -514,6 +544,9 @@ cudaError_t launch_skinny(int m_tile, const CUtensorMap &mapA, const CUtensorMap
         sgemm_skinny_kernel<8><<<grid, SNT, SkinnyLayout<8>::total, stream>>>(mapA, mapB, p);
     } else if (m_tile == 16) {
         sgemm_skinny_kernel<16><<<grid, SNT, SkinnyLayout<16>::total, stream>>>(mapA, mapB, p);
+    } else if (kHas32 && m_tile == 32) {
+        if constexpr (kHas32)
+            sgemm_skinny_kernel<32><<<grid, SNT, SkinnyLayout<32>::total, stream>>>(mapA, mapB, p);
     } else {
         return cudaErrorInvalidValue;
     }

@@ -142,14 +142,14 @@ cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, cons
                          int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
-// Skinny-M kernel (M <= 16): streams B once through a TMA ring together with
+// Skinny-M kernel (M <= 32): streams B once through a TMA ring together with
 // the matching 32-column slices of A (128-byte swizzled), stream-K over
 // (column slab, k) with a fixed-order reduction.  The A tensor map must use
 // CU_TENSOR_MAP_SWIZZLE_128B.
 // ---------------------------------------------------------------------------
 constexpr int kSkinnyBN = 256;   // columns per slab
 constexpr int kSkinnyBK = 32;    // B rows per TMA stage
-constexpr int kSkinnyMaxM = 16;  // rows of C the kernel covers (partial slots hold this many)
+constexpr int kSkinnyMaxM = 32;  // rows of C the kernel covers (tiles of 8, 16 or 32 rows)
 // Warps per CTA: 8 (one CTA per SM, 6 ring stages) or 4 (two CTAs per SM, 3
 // stages each).  A build constant so that both can be timed; 8 measured
 // faster on GB300 (its warps share one ring, so no CTA of an SM falls behind
@@ -162,6 +162,9 @@ static_assert(kSkinnyWarps == 4 || kSkinnyWarps == 8, "skinny kernel: 4 or 8 war
 constexpr int kSkinnyThreads = 32 * kSkinnyWarps;
 constexpr int kSkinnyCtasPerSm = kSkinnyWarps == 4 ? 2 : 1;
 constexpr int kSkinnyStages = kSkinnyWarps == 4 ? 3 : 6;
+// Ring stages of the kernel with an m_tile-row A tile: the 32-row tile's
+// stages are 36 KiB, five of them fit beside the reduction buffers.
+constexpr int skinny_stages(int m_tile) { return m_tile == 32 ? 5 : kSkinnyStages; }
 
 constexpr int kSkinnyMaxGrid = 160;  // CTAs a skinny launch may use
 // A unit end in the middle of a CTA's range (a reduction over the warps, a
@@ -185,7 +188,7 @@ struct SkinnyParams {
     long long ldc;
     int c_vec4;
     Epilogue epi;
-    float *partials;      // 2 * gridDim.x slots of kSkinnyMaxM * BN floats
+    float *partials;      // 2 * gridDim.x slots of m_tile * BN floats
     int *counters;        // one per slab
     int *err;
     unsigned long long timeout_ns;

@@ -34,11 +34,12 @@ namespace sgemm {
 namespace {
 
 constexpr int kMaxGrid = kSkinnyMaxGrid;
+constexpr int kMaxM = 16;  // rows this entry point takes (tiles of 8 or 16 rows)
 constexpr int kMaxSlabs = 4096;
 constexpr int kMaxDevices = 64;
-// The skinny kernel gives each CTA two partial slots of kSkinnyMaxM x 256
-// floats (16 KiB).
-constexpr size_t kSlotFloats = size_t(kSkinnyMaxM) * kSkinnyBN;
+// The skinny kernel gives each CTA two partial slots of m_tile x 256 floats
+// (at most 16 KiB here).
+constexpr size_t kSlotFloats = size_t(kMaxM) * kSkinnyBN;
 constexpr size_t kPartialBytes = 2 * size_t(kMaxGrid) * kSlotFloats * sizeof(float);
 constexpr size_t kCounterBytes = size_t(kMaxSlabs) * sizeof(int);
 constexpr size_t kErrOffset = kPartialBytes + kCounterBytes;
@@ -145,7 +146,7 @@ extern "C" sgemm_status_t sgemm_run_skinny_noalloc(int64_t M, int64_t N, int64_t
                     (reinterpret_cast<uintptr_t>(B) & 3u)))
         return SGEMM_ERR_INVALID_ARG;
     // Sizes and layouts this fixed buffer and kernel cannot take.
-    if (M > kSkinnyMaxM) return SGEMM_ERR_SCRATCH_LIMIT;
+    if (M > kMaxM) return SGEMM_ERR_SCRATCH_LIMIT;
     if ((N + kSkinnyBN - 1) / kSkinnyBN > kMaxSlabs) return SGEMM_ERR_SCRATCH_LIMIT;
     if (product && ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
                     lda % 4 != 0 || ldb % 4 != 0))

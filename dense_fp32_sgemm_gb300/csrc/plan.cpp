@@ -280,8 +280,10 @@ int make_plan(const PlanInput &in, Plan *pl) {
     if (want == kVarSkinny && !tma_ok) return -2;
     if (want == kVarSkinny && in.M > kSkinnyMaxM) return -3;
 
-    // M <= 16: every B element feeds at most 16 products, so the product is
-    // bound by streaming B; a 128-row tile would spend 8x the multiply-adds.
+    // M <= 32: every B element feeds at most 32 products, so the product is
+    // bound by streaming B (M <= 16) or close to it; a tile of 64 or 128 rows
+    // would spend 2-8x the multiply-adds (measured, 32 x 8192 x 8192: see the
+    // planner sweep).
     if (tma_ok && (want == kVarSkinny || (want < 0 && in.M <= kSkinnyMaxM))) {
         // Persistent grid: every CTA the SMs hold at once.
         int64_t G = (in.num_sms > 0 ? in.num_sms : 1) * kSkinnyCtasPerSm;
@@ -307,7 +309,7 @@ int make_plan(const PlanInput &in, Plan *pl) {
                     lo = mid + 1;
             }
             p.variant = kVarSkinny;
-            p.m_tile = in.M <= 8 ? 8 : 16;
+            p.m_tile = in.M <= 8 ? 8 : in.M <= 16 ? 16 : 32;
             p.slabs = (int)slabs;
             p.tiles_n = (int)slabs;
             p.tiles_m = 1;

@@ -434,7 +434,7 @@ def ceil4(x):
     return (x + 3) // 4 * 4
 
 
-@pytest.mark.parametrize("M", [1, 5, 8, 9, 16])
+@pytest.mark.parametrize("M", [1, 5, 8, 9, 16, 17, 24, 31, 32])
 @pytest.mark.parametrize("N,K", [(256, 32), (300, 70), (1030, 1000), (4096, 513),
                                  (10240, 320), (40000, 64)])
 def test_skinny_shapes(M, N, K):
@@ -442,9 +442,10 @@ def test_skinny_shapes(M, N, K):
           ldc=N + 1, label=f"skinny {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M", [16, 32, 27])
 @pytest.mark.parametrize("splits", [0, 2, 3, 7])
-def test_skinny_integers_bit_exact(splits):
-    M, N, K = 16, 1024, 96
+def test_skinny_integers_bit_exact(splits, M):
+    N, K = 1024, 96
     A, lda, B, ldb, C, ldc = inputs("ints", 17, M, N, K)
     out, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc, variant=3, splits=splits)
     want = (A.reshape(M, K).astype(np.int64) @ B.reshape(K, N).astype(np.int64)
@@ -452,8 +453,9 @@ def test_skinny_integers_bit_exact(splits):
     assert np.array_equal(out.astype(np.int64), want)
 
 
-def test_skinny_is_bitwise_deterministic():
-    M, N, K = 16, 2048, 4096
+@pytest.mark.parametrize("M", [16, 32])
+def test_skinny_is_bitwise_deterministic(M):
+    N, K = 2048, 4096
     A, lda, B, ldb, _, _ = inputs("uniform", 18, M, N, K)
     first, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N)
     for _ in range(3):
@@ -461,8 +463,9 @@ def test_skinny_is_bitwise_deterministic():
         assert np.array_equal(first, again)
 
 
-def test_skinny_wait_timeout_reports_and_recovers():
-    M, N, K = 16, 1024, 4096
+@pytest.mark.parametrize("M", [16, 32])
+def test_skinny_wait_timeout_reports_and_recovers(M):
+    N, K = 1024, 4096
     A, lda, B, ldb, _, _ = inputs("uniform", 19, M, N, K)
     dA = torch.from_numpy(A).cuda()
     dB = torch.from_numpy(B).cuda()

@@ -160,6 +160,8 @@ def test_plan_invariants(M, N, K):
         tile_invariants(p, M, N, K)
     elif p["variant"] == "mid":
         mid_invariants(p, M, N, K)
+    elif p["variant"] == "skinny":
+        assert M <= 32
     else:
         assert p["variant"] == "generic"
 
@@ -182,11 +184,22 @@ def test_mid_size_products_take_the_mid_kernel(M, N, K):
     assert p["variant"] == "mid" and p["bm"] == "128"
 
 
-@pytest.mark.parametrize("M", [17, 24, 32, 48, 64])
+@pytest.mark.parametrize("M", [33, 48, 64])
 def test_short_products_take_64_row_tiles(M):
-    # 17 <= M <= 64: 64-row tiles waste at most 47 rows a tile (64 x 8192 x
+    # 33 <= M <= 64: 64-row tiles waste at most 31 rows a tile (64 x 8192 x
     # 8192: 173.5 us against 283 on the 128 x 256 tiled kernel).
     p = plan(M, 8192, 8192)
+    assert p["variant"] == "mid" and p["bm"] == "64"
+
+
+@pytest.mark.parametrize("M", [17, 24, 32])
+def test_up_to_32_rows_stream_b_once(M):
+    # 17 <= M <= 32 with aligned operands: the skinny kernel with a 32-row A
+    # tile (two groups of warps each summing 16 rows); unaligned operands
+    # take 64-row mid-size tiles.
+    p = plan(M, 8192, 8192)
+    assert p["variant"] == "skinny" and p["m_tile"] == "32"
+    p = plan(M, 8192, 8191, aligned_ld=False)
     assert p["variant"] == "mid" and p["bm"] == "64"
 
 
@@ -233,7 +246,8 @@ UNIT_END = 5  # positions a range pays for each slab boundary it crosses
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 8192, 8192), (1, 4096, 4096), (9, 300, 72),
-                                   (8, 100000, 64), (16, 10240, 320)])
+                                   (8, 100000, 64), (16, 10240, 320), (32, 8192, 8192),
+                                   (20, 3000, 500)])
 def test_skinny_plan(M, N, K):
     # M <= 16: the streaming kernel over 256-column slabs and 32-row positions,
     # the (slab, k) plane cut into contiguous ranges, one per CTA of a
@@ -245,7 +259,7 @@ def test_skinny_plan(M, N, K):
                                                 "two_unit_ctas")
     total = slabs * kt
     assert slabs == math.ceil(N / 256) and kt == math.ceil(K / 32)
-    assert m_tile == (8 if M <= 8 else 16)
+    assert m_tile == (8 if M <= 8 else 16 if M <= 16 else 32)
     assert 1 <= grid <= SMS
     assert budget >= math.ceil(total / SMS)
     if kt >= 32:
@@ -356,7 +370,7 @@ def test_random_plans_cover_the_work():
         elif v == "mid":
             mid_invariants(p, M, N, K)
         elif v == "skinny":
-            assert M <= 16
+            assert M <= 32
             slabs, kt, grid = ints(p, "tiles_n", "kt", "grid")
             assert 1 <= grid <= SMS and slabs == math.ceil(N / 256)
 
