@@ -21,7 +21,7 @@ __all__ = [
     "sgemm_run_host", "ACT_NONE", "ACT_RELU",
     "run", "run_host", "status_string", "device_status", "plan_describe",
     "set_plan_override", "set_wait_timeout_ns", "set_tile_config",
-    "release_workspace", "probe_ffma", "probe_read", "probe_hold", "EXPORTED_SYMBOLS",
+    "release_workspace", "probe_ffma", "probe_read", "probe_hold", "probe_tf32", "EXPORTED_SYMBOLS",
     "VARIANT_AUTO", "VARIANT_GENERIC", "VARIANT_TILE", "VARIANT_STREAMK",
     "VARIANT_SKINNY", "VARIANT_MID", "VARIANT_MID64", "STATUS",
 ]
@@ -64,6 +64,7 @@ _SIGNATURES = {
     "sgemm_probe_ffma": (_int, [_int, _i64, _int, _vp, _vp]),
     "sgemm_probe_read": (_int, [_vp, _i64, _vp, _int, _vp]),
     "sgemm_probe_hold": (_int, [_i64, _vp]),
+    "sgemm_probe_tf32": (_int, [_i64, _int, _vp]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -338,6 +339,13 @@ def probe_ffma(paired: bool, iters: int, blocks: int, sink_ptr: int, stream=None
     _check(library().sgemm_probe_ffma(1 if paired else 0, int(iters), int(blocks), sink_ptr, s),
            "sgemm_probe_ffma")
     return float(blocks) * 512 * iters * 128 * 2
+
+
+def probe_tf32(iters: int, blocks: int, stream=None) -> float:
+    """Queue the tcgen05 TF32 rate probe; returns the FLOPs it performs."""
+    s = stream.cuda_stream if stream is not None else None
+    _check(library().sgemm_probe_tf32(int(iters), int(blocks), s), "sgemm_probe_tf32")
+    return float(blocks) * iters * 4 * 2 * 128 * 256 * 8
 
 
 def probe_read(buf_ptr: int, n_floats: int, sink_ptr: int, blocks: int, stream=None) -> float:

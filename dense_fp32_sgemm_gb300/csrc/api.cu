@@ -76,6 +76,7 @@ struct DeviceState {
     unsigned configured = 0;            // skinny configurations set up
     std::set<int> x3_configured;        // 3xTF32 kernel forms set up
     std::set<int> configured_tiles;     // tile configurations set up
+    bool tf32_probe_configured = false;
 };
 
 std::mutex g_mu;
@@ -809,6 +810,24 @@ sgemm_status_t sgemm_probe_read(const float *buf, int64_t n_floats, float *sink,
         return SGEMM_ERR_INVALID_ARG;
     return status_from(launch_read_probe(reinterpret_cast<const float4 *>(buf), n_floats / 4, sink,
                                          blocks, static_cast<cudaStream_t>(stream)));
+}
+
+sgemm_status_t sgemm_probe_tf32(int64_t iters, int blocks, void *stream) {
+    // At most 2^18 iterations: about 80 ms, far inside the bounded wait.
+    if (iters < 1 || iters > (int64_t(1) << 18) || blocks < 1) return SGEMM_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState *d = nullptr;
+    const sgemm_status_t s = device_state(&d);
+    if (s != SGEMM_OK) return s;
+    if (!d->tf32_probe_configured) {
+        if (tf32_probe_configure() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        d->tf32_probe_configured = true;
+    }
+    unsigned long long timeout_ns = 0;
+    int skip = -1;
+    wait_hooks(&timeout_ns, &skip);
+    return status_from(launch_tf32_probe((long long)iters, blocks, d->err, timeout_ns,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 sgemm_status_t sgemm_probe_hold(int64_t ns, void *stream) {

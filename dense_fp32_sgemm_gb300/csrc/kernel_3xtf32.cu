@@ -597,7 +597,80 @@ __global__ void __launch_bounds__(THREADS, (X3Cfg<BK, STAGES>::kCtasPerSm))
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-pipe rate probe: the TF32 dense peak the 3xTF32 kernel is judged
+// against, measured in the same run.  One CTA per SM (its shared memory
+// request leaves room for one) allocates 256 tensor-memory columns; one
+// thread issues `iters` x 4 tcgen05.mma kind::tf32 of M 128, N 256, K 8 back
+// to back into one accumulator, reading a 128 x 32 A tile and a 256 x 32 B
+// tile (128-byte-swizzled K-major rows) of scattered values in [-0.5, 0.5)
+// (zero operands would draw less power and run at a higher clock than real
+// data), commits them to an mbarrier and waits (bounded) for them before the
+// tensor memory is freed.
+// FLOPs per launch: blocks * iters * 4 * 2 * 128 * 256 * 8.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kProbeA = BM * 32 * 4, kProbeB = BN * 32 * 4;
+constexpr size_t kProbeSmem = 120 * 1024;  // > half the SM: one CTA per SM
+
+__global__ void __launch_bounds__(THREADS, 1)
+    x3_mma_probe_kernel(long long iters, int *err, unsigned long long timeout_ns) {
+    extern __shared__ unsigned char probe_raw[];
+    __shared__ uint64_t done;
+    __shared__ uint32_t tmem_slot;
+    const uint32_t raw = smem_addr(probe_raw);
+    unsigned char *smem = probe_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    float *f = reinterpret_cast<float *>(smem);
+    for (int i = tid; i < (int)((kProbeA + kProbeB) / 4); i += THREADS) {
+        const uint32_t h = (uint32_t)(i + 1) * 2654435761u;  // multiplicative hash
+        f[i] = (float)(h >> 9) * (1.0f / 8388608.0f) - 0.5f;
+    }
+    fence_proxy_async_shared();
+    if (tid == 0) {
+        mbar_init(&done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 2) tmem_alloc(&tmem_slot);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (tid == 0) {
+        const uint32_t idesc = make_idesc(BN);
+        for (long long it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_tf32(tmem, smem_desc<32>(sbase + kk * 32),
+                         smem_desc<32>(sbase + kProbeA + kk * 32), idesc, (it | kk) != 0);
+        }
+        mma_commit(&done);
+        if (!mbar_wait_bounded(&done, 0, timeout_ns)) {
+            // Let the MMAs drain (bounded) before the columns are freed.
+            atomicOr(err, kErrWaitTimeout);
+            if (!mbar_wait_bounded(&done, 0, 1000000000ull)) atomicOr(err, kErrDrainTimeout);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem);
+    }
+}
+
 }  // namespace
+
+cudaError_t tf32_probe_configure() {
+    return cudaFuncSetAttribute(x3_mma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kProbeSmem);
+}
+
+cudaError_t launch_tf32_probe(long long iters, int blocks, int *err, unsigned long long timeout_ns,
+                              cudaStream_t stream) {
+    x3_mma_probe_kernel<<<blocks, THREADS, kProbeSmem, stream>>>(iters, err, timeout_ns);
+    return cudaGetLastError();
+}
 
 namespace {
 template <int BK, int S, bool ARAW>

@@ -107,4 +107,11 @@ cudaError_t launch_x3_split(const float *A, long long lda, int M, const float *B
                             int N, int K, float *splitA, int Mp, float *splitB, int Np, int Kp,
                             int num_sms, cudaStream_t stream);
 
+// Rate probe of tcgen05.mma kind::tf32 (M 128, N 256, K 8): `blocks` CTAs, one
+// per SM, each issuing iters * 4 MMAs; 2^21 * iters * blocks flops per launch.
+// A bounded wait that gives up sets `err`.
+cudaError_t tf32_probe_configure();
+cudaError_t launch_tf32_probe(long long iters, int blocks, int *err, unsigned long long timeout_ns,
+                              cudaStream_t stream);
+
 }  // namespace sgemm

@@ -43,6 +43,19 @@ SGEMM_API sgemm_status_t sgemm_probe_read(const float *buf, int64_t n_floats, fl
                                 void *stream);
 
 /*
+ * sgemm_probe_tf32 -- the tensor pipe's TF32 dense rate, against which the
+ * 3xTF32 entry point is judged: `blocks` CTAs (one per SM: launch as many as
+ * the GPU has SMs) each issue iters * 4 back-to-back tcgen05.mma kind::tf32
+ * of M 128, N 256, K 8 into tensor memory, from zeroed shared-memory
+ * operands.  FLOPs per launch = blocks * iters * 4 * 2 * 128 * 256 * 8.  The
+ * final wait for the MMAs is bounded; if it gives up, sgemm_device_status()
+ * reports SGEMM_ERR_DEVICE_TIMEOUT.  Returns SGEMM_ERR_INVALID_ARG for
+ * iters < 1, iters > 2^18 (a launch stays near 80 ms or less) or blocks < 1,
+ * SGEMM_ERR_NO_DEVICE without an sm_103 device.
+ */
+SGEMM_API sgemm_status_t sgemm_probe_tf32(int64_t iters, int blocks, void *stream);
+
+/*
  * sgemm_probe_hold -- one thread that sleeps on the GPU global timer for `ns`
  * nanoseconds and does nothing else.  A benchmark queues it ahead of a batch
  * of timed launches so that the host has queued the whole batch before the

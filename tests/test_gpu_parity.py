@@ -350,6 +350,10 @@ def test_probes_run():
         assert flops == 152 * 512 * 100 * 128 * 2
     nbytes = sg.probe_read(buf.data_ptr(), buf.numel(), sink.data_ptr(), 152, stream)
     assert nbytes == 4 * buf.numel()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    flops = sg.probe_tf32(1000, sms, stream)
+    assert flops == sms * 1000 * 4 * 2 * 128 * 256 * 8
+    assert sg.device_status(stream) == 0
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
