@@ -331,6 +331,45 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
         constexpr int RR = L::RED_ROWS;
         constexpr int SUMMED = ROW_SPLIT ? GW : WARPS;  // warps holding a row
         float fin[MT][OWN];
+        if (q == q_total) {
+            // The CTA's final unit: every copy it issued has been consumed,
+            // so the idle ring takes all rows of every warp at once (one
+            // barrier instead of two per pair of rows; same order of sums).
+            static_assert(size_t(WARPS) * MR * SBN * 4 <= SSTAGES * L::stage_bytes,
+                          "the warps' sums fit the ring");
+            float *red_all = stages;
+#pragma unroll
+            for (int m = 0; m < MR; ++m) {
+#pragma unroll
+                for (int c = 0; c < CPL / 4; ++c) {
+                    float4 v;
+                    v.x = (m & 1) ? acc[m >> 1][4 * c + 0].y : acc[m >> 1][4 * c + 0].x;
+                    v.y = (m & 1) ? acc[m >> 1][4 * c + 1].y : acc[m >> 1][4 * c + 1].x;
+                    v.z = (m & 1) ? acc[m >> 1][4 * c + 2].y : acc[m >> 1][4 * c + 2].x;
+                    v.w = (m & 1) ? acc[m >> 1][4 * c + 3].y : acc[m >> 1][4 * c + 3].x;
+                    *reinterpret_cast<float4 *>(red_all + (warp * MR + m) * SBN + c * 128 +
+                                                lane * 4) = v;
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int g = 0; g < WARPS / SUMMED; ++g) {
+#pragma unroll
+                for (int m = 0; m < MR; ++m) {
+                    float sum[OWN], x[OWN];
+                    Vec<OWN>::load(red_all + ((g * SUMMED) * MR + m) * SBN + col0, sum);
+#pragma unroll
+                    for (int w = 1; w < SUMMED; ++w) {
+                        Vec<OWN>::load(red_all + ((g * SUMMED + w) * MR + m) * SBN + col0, x);
+#pragma unroll
+                        for (int o = 0; o < OWN; ++o) sum[o] += x[o];
+                    }
+#pragma unroll
+                    for (int o = 0; o < OWN; ++o) fin[g * MR + m][o] = sum[o];
+                }
+            }
+            __syncthreads();
+        } else {
 #pragma unroll
         for (int r = 0; r < MR / RR; ++r) {
 #pragma unroll
@@ -364,6 +403,7 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
                 }
             }
             __syncthreads();
+        }
         }
 
         bool write_c = true;
