@@ -62,8 +62,13 @@ constexpr KernelModel kMidModel = {128, kMidBN, kMidBK, 2, {0, 1.55, 2.77, 0, 0}
 // CTAs of 64 slices: 191 us).
 constexpr KernelModel kMid64Model = {64, kMidBN, kMidBK, 4, {0, 1.0, 1.5, 2.2, 2.8}, 3.0, 1.5};
 // B in 4-byte copies (rows off 16 bytes) makes a mid-size slice slower
-// (2049^3: 2.93 us per slice against 2.77 at 2048^3).
-constexpr double kMidUnalignedB = 1.06;
+// (2049^3: 2.93 us per slice against 2.77 at 2048^3) and each unit's first
+// copies slower to arrive: 1023 x 1025 x 513 (two units a CTA) took 51.2 us
+// with 297 CTAs of 8 slices and with 140 of 17, about 7 us above the aligned
+// 1024 x 1024 x 512 model.
+constexpr double kMidUnalignedB[5] = {1.06, 1.06, 1.06, 1.06, 1.06};
+constexpr double kMidUnalignedUnitUs = 3.5;
+constexpr double kNoScale[5] = {1, 1, 1, 1, 1};
 // 64 x 64 kernel, one tile per CTA and 16-k slices: 0.78 us per slice at up to
 // one CTA per SM (128^3: 12.3 us; 512^3: 30.9 us), growing with the CTAs an
 // SM holds (1024^3, 1.7 per SM: 80 us).
@@ -97,11 +102,11 @@ const char *variant_name(int v) {
 
 // Time of one CTA slice when `ctas` CTAs share `sms` SMs (at most the
 // model's CTAs per SM).
-static double slice_us(const KernelModel &m, int64_t ctas, int64_t sms) {
+static double slice_us(const KernelModel &m, int64_t ctas, int64_t sms, const double *scale) {
     int64_t c = ceil_div(ctas, sms);
     if (c < 1) c = 1;
     if (c > m.ctas_per_sm) c = m.ctas_per_sm;
-    return m.slice_us[c];
+    return m.slice_us[c] * scale[c];
 }
 
 // Tiles of the model's shape on a persistent grid of at most
@@ -110,7 +115,7 @@ static double slice_us(const KernelModel &m, int64_t ctas, int64_t sms) {
 // busiest CTA's slices plus the fix-up allowance in slices; `est_us` the
 // model's time (launch included).
 static void plan_grid(const PlanInput &in, Plan *pl, bool allow_sk, bool force_sk,
-                      const KernelModel &m, double slice_scale) {
+                      const KernelModel &m, const double *slice_scale) {
     const int64_t sms = in.num_sms > 0 ? in.num_sms : 1;
     const int64_t G = sms * m.ctas_per_sm;
     const int64_t tm = ceil_div(in.M, m.bm), tn = ceil_div(in.N, m.bn);
@@ -130,13 +135,14 @@ static void plan_grid(const PlanInput &in, Plan *pl, bool allow_sk, bool force_s
     best.sk_share = 1;
     best.grid = (int)(T < G ? T : G);
     best.cost = (double)ceil_div(T, G) * (double)KT;
-    best.est_us = kLaunchUs + best.cost * slice_us(m, best.grid, sms) * slice_scale;
+    best.est_us = kLaunchUs + best.cost * slice_us(m, best.grid, sms, slice_scale);
     best.reason = "whole tiles";
 
     const bool sk_fits = T * KT < (int64_t(1) << 30);
     if (allow_sk && sk_fits && (T % G != 0 || force_sk)) {
         const int64_t full = T / G;
-        const double piece_slices = m.piece_us / (m.slice_us[m.ctas_per_sm] * slice_scale);
+        const double piece_slices =
+            m.piece_us / (m.slice_us[m.ctas_per_sm] * slice_scale[m.ctas_per_sm]);
         for (int64_t d = full; d >= 0 && d >= full - 1; --d) {
             const int64_t dp = d * G;
             const int64_t sk_tiles = T - dp;
@@ -170,7 +176,7 @@ static void plan_grid(const PlanInput &in, Plan *pl, bool allow_sk, bool force_s
                 const int64_t grid = dp > 0 ? G : ctas;
                 const double cost = (double)d * KT + (double)sh + piece_slices * (double)extra;
                 const double est =
-                    kLaunchUs + ((double)d * KT + (double)sh) * slice_us(m, grid, sms) * slice_scale +
+                    kLaunchUs + ((double)d * KT + (double)sh) * slice_us(m, grid, sms, slice_scale) +
                     (extra > 0 ? m.fixup_us + m.piece_us * (double)extra : 0.0);
                 if (est < best.est_us || (force_sk && !taken)) {
                     best.variant = kVarStreamK;
@@ -191,7 +197,7 @@ static void plan_grid(const PlanInput &in, Plan *pl, bool allow_sk, bool force_s
 }
 
 static void plan_tile(const PlanInput &in, Plan *pl, bool allow_sk, int64_t pack_floats) {
-    plan_grid(in, pl, allow_sk, in.force_variant == kVarStreamK, kTileModel, 1.0);
+    plan_grid(in, pl, allow_sk, in.force_variant == kVarStreamK, kTileModel, kNoScale);
     if (pl->pack_a || pl->pack_b)
         pl->est_us += 2.0 * 4.0 * (double)pack_floats / kPackBytesPerUs + kPackFixedUs;
 }
@@ -201,10 +207,20 @@ static void plan_tile(const PlanInput &in, Plan *pl, bool allow_sk, int64_t pack
 static void plan_mid(const PlanInput &in, Plan *pl, int bm) {
     const bool b_ok = aligned16(in.b_addr) && in.ldb % 4 == 0;
     plan_grid(in, pl, true, in.force_splits > 0, bm == 64 ? kMid64Model : kMidModel,
-              b_ok ? 1.0 : kMidUnalignedB);
+              b_ok ? kNoScale : kMidUnalignedB);
     pl->variant = kVarMid;
     pl->mid_bm = bm;
     pl->b_vec = b_ok ? 4 : 1;
+    if (!b_ok) {
+        // Units of the busiest CTA: a stream-K range shorter than a tile
+        // usually ends in the tile after the one it starts in.
+        const int64_t units = pl->sk_tiles > 0
+                                  ? (pl->sk_share < pl->kt_total
+                                         ? 2
+                                         : (pl->sk_share + pl->kt_total - 1) / pl->kt_total + 1)
+                                  : 1;
+        pl->est_us += kMidUnalignedUnitUs * (double)units;
+    }
     pl->reason = pl->sk_tiles > 0 ? "mid tiles, stream-K tail" : "mid tiles";
 }
 
