@@ -71,8 +71,15 @@ constexpr double kMidUnalignedUnitUs = 3.5;
 constexpr double kNoScale[5] = {1, 1, 1, 1, 1};
 // 64 x 64 kernel, one tile per CTA and 16-k slices: 0.78 us per slice at up to
 // one CTA per SM (128^3: 12.3 us; 512^3: 30.9 us), growing with the CTAs an
-// SM holds (1024^3, 1.7 per SM: 80 us).
+// SM holds, first almost in proportion, then less (tiles per SM 1.7: 80 us
+// at 1024^3; 3.0: 75.5 us at 1400 x 1300 x 512; 6.7: 478 us at 2048^3;
+// 14.5: 163 us at 3000 x 3000 x 300).
 constexpr double kGenericSliceUs = 0.78;
+static double generic_scale(double tiles_per_sm) {
+    if (tiles_per_sm <= 1.0) return 1.0;
+    const double a = 0.9 * tiles_per_sm, b = 0.62 * tiles_per_sm + 0.6;
+    return a < b ? a : b;
+}
 // Copy of unaligned operands for the tiled kernel: read and write at about
 // 3 TB/s, plus its own launch.
 constexpr double kPackBytesPerUs = 3.0e6;
@@ -232,8 +239,7 @@ static void plan_generic(const PlanInput &in, Plan *pl) {
     pl->tiles_n = (int)ceil_div(in.N, kGenBN);
     pl->kt_total = (int)ceil_div(in.K, kGenBK);
     pl->grid = pl->tiles_m * pl->tiles_n;
-    const double per_sm = (double)pl->grid / (double)sms;
-    const double scale = per_sm <= 1.0 ? 1.0 : 0.4 + 0.6 * per_sm;
+    const double scale = generic_scale((double)pl->grid / (double)sms);
     pl->cost = (double)pl->kt_total;
     pl->est_us = kLaunchUs + (double)pl->kt_total * kGenericSliceUs * scale;
 }
