@@ -82,35 +82,6 @@ struct MidCfg {
     static_assert(FIX_REGIONS * FIX_REGION <= RING_FLOATS, "fix-up regions fit the ring");
 };
 
-// ---- cp.async ---------------------------------------------------------------
-// `src_bytes` below the copy size fills the rest with zeros; 0 reads nothing
-// (the address passed is then a valid one anyway).
-__device__ __forceinline__ void cp_async4(float *dst, const float *src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst)),
-                 "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async16(float *dst, const float *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)),
-                 "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ float4 lds128(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Offset (floats) of A element (m, k) in a k-major slice of BM rows: the
 // 16-byte chunk m / 4 of row k is XOR-ed with k mod 8.  A copy instruction
 // covers 16 k of two rows, and the shared-memory side of a 4-byte cp.async

@@ -29,11 +29,6 @@ static_assert(sizeof(Plan::sk_starts) / sizeof(int) == kSkinnyMaxGrid + 1,
 
 namespace {
 
-// Per extra piece of a stream-K tile of the tiled kernel, in k-iterations of
-// a tile: measured on GB300, 1024^3 with 6 pieces per tile (share 7) took
-// 63.5 us against 61.4 with 5 (share 8), one iteration less work for one
-// piece more.
-constexpr double kFixupCost = 1.5;
 
 // Time model of each kernel on GB300 (2070 MHz), fitted to CUDA-event times
 // of single launches after an L2 flush (the planner sweep):
@@ -47,20 +42,28 @@ struct KernelModel {
     double slice_us[5];  // [c]: one CTA's slice with c CTAs resident per SM
     double fixup_us;     // once, when some tile is split
     double piece_us;     // per extra piece of the most-split tile
+    double shared_fixup_us;  // once more when the split CTAs share SMs
 };
 constexpr double kLaunchUs = 6.1;
-// Tiled kernel: 2^20 multiply-adds per 128 x 256 x 32 slice, one CTA per SM
-// (2048^3: cost 57 slices, 273 us); extra pieces at kFixupCost slices.
-constexpr KernelModel kTileModel = {kTileBM, kTileBN, kTileBK, 1, {0, 4.7, 0, 0, 0}, 0.0,
-                                    kFixupCost * 4.7};
-// Mid-size kernel, 128 x 128 x 16 slices: 1.55 us alone on an SM (1024 x
-// 1024 x 512 with 128 CTAs), 2.77 us per CTA with two per SM (2048^3 with 304
-// CTAs of 108 slices: 305 us); fix-up through the ring 4 us plus 2.5 us per
-// extra piece (1024 x 1024 x 512 with 2 and 4 pieces: 37.3 and 39.4 us).
-constexpr KernelModel kMidModel = {128, kMidBN, kMidBK, 2, {0, 1.55, 2.77, 0, 0}, 4.0, 2.5};
-// 64 x 128 x 16 slices, up to four CTAs per SM (64 x 8192 x 8192 with 512
-// CTAs of 64 slices: 191 us).
-constexpr KernelModel kMid64Model = {64, kMidBN, kMidBK, 4, {0, 1.0, 1.5, 2.2, 2.8}, 3.0, 1.5};
+// Tiled kernel: 2^20 multiply-adds per 128 x 256 x 32 slice, one CTA per SM;
+// split tiles 11 us once plus 2 us per extra piece of the most-split tile
+// (fitted over twelve shapes: 1536^3 with 2 pieces 131.5 us, 2048^3 with 3
+// 273 us, 1024^3 with 4 60.4 us, 1024 x 1024 x 8192 with 6 283 us, 768 x
+// 768 x 4096 with 8 104 us, 640 x 640 x 8192 with 8 178 us).
+constexpr KernelModel kTileModel = {kTileBM, kTileBN, kTileBK, 1, {0, 4.7, 0, 0, 0}, 11.0, 2.0, 0.0};
+// Mid-size kernel, 128 x 128 x 16 slices: 1.43 us alone on an SM (512^3,
+// 768^3, 100 x 5000 x 3000, 640 x 640 x 8192), 2.65 us per CTA with two per SM
+// (2048^3 with 304 CTAs of 108 slices: 305 us; 1280^3, 4096^3); fix-up
+// through the ring 4 us plus 2.5 us per
+// extra piece (1024 x 1024 x 512 with 2 and 4 pieces: 37.3 and 39.4 us),
+// and 5 us more with two CTAs per SM, where a CTA's fix-up runs beside the
+// other's main loop (1280^3: 94.9 us, 2048 x 1024 x 1024: 96.7 us, 1400 x
+// 1300 x 512: 61 us, each with 4 pieces).
+constexpr KernelModel kMidModel = {128, kMidBN, kMidBK, 2, {0, 1.43, 2.65, 0, 0}, 4.0, 2.5, 5.0};
+// 64 x 128 x 16 slices, up to four CTAs per SM; a third or fourth CTA adds
+// no throughput (64 x 8192 x 8192: 304 CTAs of 108 slices 170 us, 456 CTAs of
+// 72 slices 211 us).
+constexpr KernelModel kMid64Model = {64, kMidBN, kMidBK, 4, {0, 1.0, 1.5, 2.65, 3.5}, 3.0, 1.5, 0.0};
 // B in 4-byte copies (rows off 16 bytes) makes a mid-size slice slower
 // (2049^3: 2.93 us per slice against 2.77 at 2048^3) and each unit's first
 // copies slower to arrive: 1023 x 1025 x 513 (two units a CTA) took 51.2 us
@@ -68,6 +71,16 @@ constexpr KernelModel kMid64Model = {64, kMidBN, kMidBK, 4, {0, 1.0, 1.5, 2.2, 2
 // 1024 x 1024 x 512 model.
 constexpr double kMidUnalignedB[5] = {1.06, 1.06, 1.06, 1.06, 1.06};
 constexpr double kMidUnalignedUnitUs = 3.5;
+// Split-K kernel: one 64 x 128 tile per CTA, one CTA per SM, slices of 64 k
+// (four groups of 16).  Per wave: a fixed part (first copies, the groups'
+// sums added through shared memory, the store) and K / 64 slices plus a
+// quarter slice for the rounding of the last one; measured 1024 x 1024 x 512
+// 31.2-32.8 us, 1024^3 53.7-54.8 us, 768 x 768 x 4096 188 us, 1024 x 1024 x
+// 8192 367 us, 3000 x 300 x 5000 237 us; B in 4-byte copies (rows off 16
+// bytes) about 1.2x a slice (1023^3 65.5 us, 1023 x 1025 x 513 38-40 us).
+constexpr double kKsSliceUs = 2.8;
+constexpr double kKsFixedUs = 3.5;
+constexpr double kKsUnalignedB = 1.2;
 constexpr double kNoScale[5] = {1, 1, 1, 1, 1};
 // 64 x 64 kernel, one tile per CTA and 16-k slices: 0.78 us per slice at up to
 // one CTA per SM (128^3: 12.3 us; 512^3: 30.9 us), growing with the CTAs an
@@ -81,11 +94,21 @@ static double generic_scale(double tiles_per_sm) {
     return a < b ? a : b;
 }
 // Copy of unaligned operands for the tiled kernel: read and write at about
-// 3 TB/s, plus its own launch.
+// 3 TB/s (2047^3: 24 us over 2048^3; 4095^3: 80 us over 4096^3), plus its
+// own launch.
 constexpr double kPackBytesPerUs = 3.0e6;
-constexpr double kPackFixedUs = 3.0;
+constexpr double kPackFixedUs = 4.0;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t gcd64(int64_t a, int64_t b) {
+    while (b) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
 
 bool aligned16(uint64_t addr) { return (addr & 15u) == 0; }
 
@@ -103,6 +126,7 @@ const char *variant_name(int v) {
         case kVarSkinny: return "skinny";
         case kVarMid: return "mid";
         case kVarMid64: return "mid64";
+        case kVarKsplit: return "ksplit";
         default: return "?";
     }
 }
@@ -176,15 +200,19 @@ static void plan_grid(const PlanInput &in, Plan *pl, bool allow_sk, bool force_s
             for (int64_t sh = share; sh <= last; ++sh) {
                 const int64_t ctas = ceil_div(total, sh);
                 if (ctas > G) continue;
-                // Most pieces any tile is cut into.
-                const int64_t pieces = (KT + sh - 2) / sh + 1;
+                // Most pieces any tile is cut into: tile t starts at offset
+                // t KT mod sh of a range, a multiple of gcd(KT, sh), so at
+                // most sh - gcd into one.
+                const int64_t pieces = ceil_div(KT + sh - gcd64(KT, sh), sh);
                 const int64_t max_pieces = pieces < ctas ? pieces : ctas;
                 const int64_t extra = max_pieces > 1 ? max_pieces - 1 : 0;
                 const int64_t grid = dp > 0 ? G : ctas;
                 const double cost = (double)d * KT + (double)sh + piece_slices * (double)extra;
                 const double est =
                     kLaunchUs + ((double)d * KT + (double)sh) * slice_us(m, grid, sms, slice_scale) +
-                    (extra > 0 ? m.fixup_us + m.piece_us * (double)extra : 0.0);
+                    (extra > 0 ? m.fixup_us + m.piece_us * (double)extra +
+                                     (grid > sms ? m.shared_fixup_us : 0.0)
+                               : 0.0);
                 if (est < best.est_us || (force_sk && !taken)) {
                     best.variant = kVarStreamK;
                     best.dp_tiles = (int)dp;
@@ -229,6 +257,34 @@ static void plan_mid(const PlanInput &in, Plan *pl, int bm) {
         pl->est_us += kMidUnalignedUnitUs * (double)units;
     }
     pl->reason = pl->sk_tiles > 0 ? "mid tiles, stream-K tail" : "mid tiles";
+}
+
+// The split-K kernel: one 64 x 128 tile per CTA over the whole K, in waves of
+// one CTA per SM.
+static void plan_ksplit(const PlanInput &in, Plan *pl) {
+    const int64_t sms = in.num_sms > 0 ? in.num_sms : 1;
+    const bool b_ok = aligned16(in.b_addr) && in.ldb % 4 == 0;
+    const int64_t tm = ceil_div(in.M, kKsBM), tn = ceil_div(in.N, kKsBN);
+    const int64_t T = tm * tn;
+    const int64_t KT = ceil_div(in.K, kKsBK);
+    pl->variant = kVarKsplit;
+    pl->tiles_m = (int)tm;
+    pl->tiles_n = (int)tn;
+    pl->kt_total = (int)KT;
+    pl->group_m = (int)(tm < 8 ? tm : 8);
+    pl->dp_tiles = (int)T;
+    pl->sk_tiles = 0;
+    pl->sk_share = 1;
+    pl->grid = (int)T;
+    pl->c_vec4 = (aligned16(in.c_addr) && in.ldc % 4 == 0) ? 1 : 0;
+    pl->mid_bm = kKsBM;
+    pl->b_vec = b_ok ? 4 : 1;
+    const int64_t waves = ceil_div(T, sms);
+    const double slices = (double)in.K / kKsBK + 0.25;
+    pl->cost = (double)waves * slices;
+    pl->est_us = kLaunchUs + (double)waves * (kKsFixedUs + slices * kKsSliceUs *
+                                                              (b_ok ? 1.0 : kKsUnalignedB));
+    pl->reason = "split-K inside the CTA";
 }
 
 // The 64 x 64 kernel: one tile per CTA over the whole K.
@@ -361,6 +417,12 @@ int make_plan(const PlanInput &in, Plan *pl) {
         *pl = p;
         return 0;
     }
+    if (want == kVarKsplit) {
+        if (ceil_div(in.M, kKsBM) * ceil_div(in.N, kKsBN) > INT32_MAX) return -2;
+        plan_ksplit(in, &p);
+        *pl = p;
+        return 0;
+    }
     // Operands the TMA cannot map (a pointer or leading dimension off 16
     // bytes) can be copied to 16-byte-aligned rows for the tiled kernel.
     const int64_t pack_floats = (a_ok ? 0 : in.M * round_up4(in.K)) +
@@ -383,13 +445,17 @@ int make_plan(const PlanInput &in, Plan *pl) {
 
     // Automatic ("Part 2", section "Selecting Among Three Kernels"): the
     // least estimated time among the tiled kernel (aligned operands, or
-    // copies of them unless M <= 16, where copying B would double the bytes
+    // copies of them unless M <= 32, where copying B would double the bytes
     // moved), the mid-size kernel with 128-row tiles and, for M <= 64, with
-    // 64-row tiles, and the 64 x 64 kernel.
-    Plan cand[4];
+    // 64-row tiles, the split-K kernel and the 64 x 64 kernel.
+    Plan cand[5];
     int n = 0;
     cand[n] = p;
     plan_mid(in, &cand[n++], 128);
+    if (ceil_div(in.M, kKsBM) * ceil_div(in.N, kKsBN) <= INT32_MAX) {
+        cand[n] = p;
+        plan_ksplit(in, &cand[n++]);
+    }
     if (in.M <= 64) {
         cand[n] = p;
         plan_mid(in, &cand[n++], 64);

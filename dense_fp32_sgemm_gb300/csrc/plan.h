@@ -17,6 +17,7 @@ enum Variant : int {
     kVarSkinny = 3,
     kVarMid = 4,        // mid-size kernel, bm x 128 tiles (bm = 128 when forced)
     kVarMid64 = 5,      // forced: the mid-size kernel with 64 x 128 tiles
+    kVarKsplit = 6,     // split-K inside the CTA: 64 x 128 tiles, one per CTA
 };
 
 struct PlanInput {
@@ -40,7 +41,8 @@ struct Plan {
     int m_tile, slabs;
     int sk_starts[161];
     int sk_two_units;  // CTAs whose range crosses a slab boundary
-    // mid-size kernel: tile height (128 or 64) and B copy width in floats (4 or 1)
+    // mid-size and split-K kernels: tile height (128 or 64) and B copy width
+    // in floats (4 or 1)
     int mid_bm, b_vec;
     // estimated time of the chosen plan (microseconds) and of the best other
     // candidate considered (0 when there was none)

@@ -1,7 +1,7 @@
 """Planner check over a sweep of shapes: for each shape, time the plan the
 library picks and the alternatives it could have picked (the tiled kernel
 with whole tiles only or with a stream-K tail, the mid-size kernel with 128-
-or 64-row tiles, the 64 x 64 kernel), and report how far the automatic choice
+or 64-row tiles, the split-K kernel, the 64 x 64 kernel), and report how far the automatic choice
 is from the fastest, and how far each plan's time estimate is from its time.
 
     python -m dense_fp32_sgemm_gb300.sweep [--sizes 511,512,513,...] [--reps 30]
@@ -26,7 +26,8 @@ DEFAULT_SIZES = [256, 511, 512, 513, 1023, 1024, 1025, 1535, 1536, 2047, 2048, 2
 
 CANDIDATES = [("auto", sg.VARIANT_AUTO), ("tile", sg.VARIANT_TILE),
               ("streamk", sg.VARIANT_STREAMK), ("mid", sg.VARIANT_MID),
-              ("mid64", sg.VARIANT_MID64), ("generic", sg.VARIANT_GENERIC)]
+              ("mid64", sg.VARIANT_MID64), ("ksplit", sg.VARIANT_KSPLIT),
+              ("generic", sg.VARIANT_GENERIC)]
 
 
 def time_launches(torch, fn, reps, flush, sink, stream):
@@ -67,6 +68,10 @@ def main():
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(64 << 20, device=dev)
     sink = torch.empty(1, device=dev)
+    # A first timing on an idle GPU reads several times too long (the clocks
+    # are still rising); 50 ms of device work first.
+    sg.probe_hold(50_000_000, stream)
+    torch.cuda.synchronize()
     rows = []
     for M, N, K in shapes:
         A = torch.rand(M, K, device=dev) - 0.5

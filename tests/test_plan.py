@@ -48,12 +48,14 @@ def test_misaligned_operands():
     # Unaligned rows (lda = ldb = 1023): the mid-size kernel reads them with
     # 4-byte copies, so no copy pass is planned ...
     p = plan(1023, 1023, 1023, aligned_ld=False)
-    assert p["variant"] == "mid" and ints(p, "bvec", "pack_a", "pack_b") == [1, 0, 0]
+    assert p["variant"] in ("mid", "ksplit") and ints(p, "bvec", "pack_a", "pack_b") == [1, 0, 0]
+    # (one wave of 64 x 128 tiles: the split-K kernel; measured 37.9 us against
+    # 45.5 on the 64 x 64 kernel and 49.9 on the mid-size one)
     p = plan(1023, 1025, 513, aligned_ld=False)
-    assert p["variant"] in ("mid", "generic") and ints(p, "pack_a", "pack_b") == [0, 0]
+    assert p["variant"] == "ksplit" and ints(p, "bvec", "pack_a", "pack_b") == [1, 0, 0]
     # ... B aligned keeps its 16-byte copies
     p = plan(1023, 1024, 1023, lda=1023)
-    assert p["variant"] == "mid" and p["bvec"] == "4"
+    assert p["variant"] in ("mid", "ksplit") and p["bvec"] == "4"
     # M <= 16 with an unaligned operand: not the skinny kernel (TMA), and the
     # tiled kernel's copy of B is never considered
     p = plan(16, 8192, 8191, aligned_ld=False)
@@ -120,6 +122,14 @@ def tile_invariants(p, M, N, K, forced_sk=False):
         assert float(p["cost"]) <= math.ceil(T / SMS) * kt + 1e-9
 
 
+def ksplit_invariants(p, M, N, K):
+    # one 64 x 128 tile per CTA over the whole K in 64-k slices
+    tm, tn, kt, dp, sk, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles", "sk_tiles", "grid")
+    assert p["bm"] == "64" and p["bvec"] in ("1", "4")
+    assert tm == math.ceil(M / 64) and tn == math.ceil(N / 128) and kt == math.ceil(K / 64)
+    assert dp == tm * tn == grid and sk == 0
+
+
 def mid_invariants(p, M, N, K):
     bm = int(p["bm"])
     assert bm in (128, 64)
@@ -155,11 +165,18 @@ def test_plan_invariants(M, N, K):
             mid_invariants(plan(M, N, K), M, N, K)
         finally:
             sg.set_plan_override(-1, 0)
+    sg.set_plan_override(sg.VARIANT_KSPLIT, 0)
+    try:
+        ksplit_invariants(plan(M, N, K), M, N, K)
+    finally:
+        sg.set_plan_override(-1, 0)
     p = plan(M, N, K)
     if p["variant"] in ("tile", "streamk"):
         tile_invariants(p, M, N, K)
     elif p["variant"] == "mid":
         mid_invariants(p, M, N, K)
+    elif p["variant"] == "ksplit":
+        ksplit_invariants(p, M, N, K)
     elif p["variant"] == "skinny":
         assert M <= 32
     else:
@@ -167,7 +184,7 @@ def test_plan_invariants(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (129, 257, 33), (256, 256, 256),
-                                   (300, 520, 64), (511, 511, 511)])
+                                   (300, 520, 64)])
 def test_tiny_products_take_the_64x64_kernel(M, N, K):
     # Measured on GB300: below about 512^3 the 64 x 64 kernel's short
     # start-up wins (128^3: 12.5 us against 20.5 on the mid-size kernel).
@@ -175,13 +192,23 @@ def test_tiny_products_take_the_64x64_kernel(M, N, K):
     assert p["variant"] == "generic" and p["reason"] == "64 x 64 tiles"
 
 
-@pytest.mark.parametrize("M,N,K", [(768, 768, 768), (1024, 1024, 1024), (1000, 3000, 231),
-                                   (1024, 1024, 512)])
+@pytest.mark.parametrize("M,N,K", [(512, 512, 512), (640, 640, 640), (768, 768, 768),
+                                   (896, 896, 896)])
 def test_mid_size_products_take_the_mid_kernel(M, N, K):
-    # 128 x 128 tiles fill more SMs than 128 x 256 ones (1024^3: 59.4 us
-    # against 60.2 on the tiled kernel, 80 on the 64 x 64 one).
+    # 128 x 128 tiles with a stream-K tail fill more SMs than 128 x 256 ones
+    # (768^3: 34.8 us against 51.2 on the tiled kernel, 43.0 on the split-K
+    # kernel, 44.5 on the 64 x 64 one).
     p = plan(M, N, K)
     assert p["variant"] == "mid" and p["bm"] == "128"
+
+
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 512), (1024, 1152, 512), (1024, 1024, 1024)])
+def test_one_wave_of_64x128_tiles_takes_the_split_k_kernel(M, N, K):
+    # 128-144 tiles of 64 x 128 fill the SMs in one wave with no partial sums
+    # in global memory (1024^3: 54.8 us against 59.4 on the mid-size kernel,
+    # 60.4 on the tiled kernel with a stream-K tail).
+    p = plan(M, N, K)
+    assert p["variant"] == "ksplit" and ksplit_invariants(p, M, N, K) is None
 
 
 @pytest.mark.parametrize("M", [33, 48, 64])
