@@ -77,6 +77,10 @@ struct DeviceState {
     std::set<int> x3_configured;        // 3xTF32 kernel forms set up
     std::set<int> configured_tiles;     // tile configurations set up
     bool tf32_probe_configured = false;
+    // Second stream for the thin edges beside the tiled kernel, forked from
+    // and joined back to the caller's stream with the two events.
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
 };
 
 std::mutex g_mu;
@@ -185,6 +189,59 @@ sgemm_status_t validate(int64_t M, int64_t N, int64_t K, float alpha, const floa
     return SGEMM_OK;
 }
 
+// Partial-sum workspace the skinny plan `pl` needs.
+size_t skinny_partial_bytes(const Plan &pl) {
+    return (size_t)2 * pl.grid * pl.m_tile * kSkinnyBN * sizeof(float);
+}
+
+// The skinny kernel on the plan `pl` (A and B 16-byte aligned, M <= 32), with
+// the workspace `w` (at least skinny_partial_bytes(pl) and pl.slabs counters).
+sgemm_status_t run_skinny(DeviceState &d, const Plan &pl, int64_t M, int64_t N, int64_t K,
+                          float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+                          float beta, float *C, int64_t ldc, const Epilogue &epi, Workspace *w,
+                          cudaStream_t stream) {
+    const unsigned bit = 1u << (24 + pl.m_tile / 8);  // m_tile 8, 16, 32: bits 25, 26, 28
+    if (!(d.configured & bit)) {
+        if (skinny_configure(pl.m_tile) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        d.configured |= bit;
+    }
+    CUtensorMap mapA, mapB;
+    sgemm_status_t s = encode_2d(&mapA, A, M, K, lda, kSkinnyBK, pl.m_tile,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != SGEMM_OK) return s;
+    s = encode_2d(&mapB, B, K, N, ldb, kSkinnyBN, kSkinnyBK);
+    if (s != SGEMM_OK) return s;
+    SkinnyParams sp;
+    sp.M = (int)M; sp.N = (int)N; sp.K = (int)K;
+    sp.slabs = pl.slabs; sp.kt_total = pl.kt_total;
+    for (int c = 0; c <= pl.grid; ++c) sp.starts[c] = pl.sk_starts[c];
+    sp.alpha = alpha; sp.beta = beta;
+    sp.A = A; sp.lda = lda; sp.C = C; sp.ldc = ldc; sp.c_vec4 = 0;
+    sp.epi = epi;
+    sp.err = d.err;
+    const unsigned long long to = g_timeout_ns.load();
+    sp.timeout_ns = to ? to : kDefaultTimeoutNs;
+    sp.skip_loads_from = g_skip_loads_from.load();
+    sp.partials = w->partials;
+    sp.counters = w->counters;
+    return status_from(launch_skinny(pl.m_tile, mapA, mapB, sp, pl.grid, stream));
+}
+
+// The narrow kernel over rows [0, M) and N <= kNarrowMaxN columns.
+sgemm_status_t run_narrow(int nn, int a_vec, int grid, int rows_per_cta, int64_t M, int64_t N,
+                          int64_t K, float alpha, const float *A, int64_t lda, const float *B,
+                          int64_t ldb, float beta, float *C, int64_t ldc, const Epilogue &epi,
+                          cudaStream_t stream) {
+    NarrowParams np;
+    np.M = (int)M; np.N = (int)N; np.K = (int)K;
+    np.alpha = alpha; np.beta = beta;
+    np.A = A; np.lda = lda; np.B = B; np.ldb = ldb; np.C = C; np.ldc = ldc;
+    np.epi = epi;
+    np.rows_per_cta = rows_per_cta;
+    np.kch = narrow_kch(K, nn);
+    return status_from(launch_narrow(nn, a_vec, np, grid, stream));
+}
+
 sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                           int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                           int64_t ldc, const Epilogue &epi, cudaStream_t stream, DeviceState &d) {
@@ -245,13 +302,31 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
                 }
                 if (launch_pack(jobs, n, d.num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
             }
+            // Thin edges left to the skinny (last edge_m rows) and narrow (last
+            // edge_n columns) kernels: the tiles cover M0 x N0.
+            const int64_t M0 = M - pl.edge_m, N0 = N - pl.edge_n;
+            Plan edge_plan = {};
+            if (pl.edge_m > 0) {
+                PlanInput ein = in;
+                ein.M = pl.edge_m;
+                ein.N = N0;
+                ein.lda = lda_use;
+                ein.ldb = ldb_use;
+                ein.a_addr = reinterpret_cast<uintptr_t>(Ause + M0 * lda_use);
+                ein.b_addr = reinterpret_cast<uintptr_t>(Buse);
+                ein.c_addr = reinterpret_cast<uintptr_t>(C + M0 * ldc);
+                ein.force_variant = kVarSkinny;
+                ein.force_splits = 0;
+                if (make_plan(ein, &edge_plan) != 0 || edge_plan.variant != kVarSkinny)
+                    return SGEMM_ERR_UNSUPPORTED;
+            }
             CUtensorMap mapA, mapB;
-            sgemm_status_t s = encode_2d(&mapA, Ause, M, K, lda_use, kTileBK, kTileBM);
+            sgemm_status_t s = encode_2d(&mapA, Ause, M0, K, lda_use, kTileBK, kTileBM);
             if (s != SGEMM_OK) return s;
-            s = encode_2d(&mapB, Buse, K, N, ldb_use, kTileBN, kTileBK);
+            s = encode_2d(&mapB, Buse, K, N0, ldb_use, kTileBN, kTileBK);
             if (s != SGEMM_OK) return s;
             TileParams tp;
-            tp.M = (int)M; tp.N = (int)N; tp.K = (int)K;
+            tp.M = (int)M0; tp.N = (int)N0; tp.K = (int)K;
             tp.tiles_m = pl.tiles_m; tp.tiles_n = pl.tiles_n; tp.kt_total = pl.kt_total;
             tp.dp_tiles = pl.dp_tiles; tp.sk_tiles = pl.sk_tiles; tp.sk_share = pl.sk_share;
             tp.group_m = pl.group_m;
@@ -262,15 +337,79 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             const unsigned long long to = g_timeout_ns.load();
             tp.timeout_ns = to ? to : kDefaultTimeoutNs;
             tp.skip_loads_from = g_skip_loads_from.load();
-            if (pl.sk_tiles > 0) {
-                Workspace *w = nullptr;
-                const size_t pbytes = (size_t)2 * pl.grid * kTileBM * kTileBN * sizeof(float);
-                s = ensure_workspace(d, stream, pbytes, (size_t)pl.sk_tiles, &w);
+            // One workspace: the tiles' stream-K slots and counters first,
+            // the bottom edge's after them (the two may run at once).
+            Workspace *w = nullptr;
+            const size_t tile_pbytes =
+                pl.sk_tiles > 0 ? (size_t)2 * pl.grid * kTileBM * kTileBN * sizeof(float) : 0;
+            const size_t tile_counters = (size_t)pl.sk_tiles;
+            if (pl.sk_tiles > 0 || pl.edge_m > 0) {
+                size_t pbytes = tile_pbytes, counters = tile_counters;
+                if (pl.edge_m > 0) {
+                    pbytes += skinny_partial_bytes(edge_plan);
+                    counters += (size_t)edge_plan.slabs;
+                }
+                s = ensure_workspace(d, stream, pbytes, counters, &w);
                 if (s != SGEMM_OK) return s;
-                tp.partials = w->partials;
-                tp.counters = w->counters;
+                if (pl.sk_tiles > 0) {
+                    tp.partials = w->partials;
+                    tp.counters = w->counters;
+                }
             }
-            return status_from(launch_tile(fm, st, tm, mapA, mapB, tp, pl.grid, stream));
+            // The edges go to a second stream forked after the copies, so
+            // that their CTAs take the SMs the tiles' last CTAs leave idle;
+            // the caller's stream waits for them before anything it queues
+            // next.  (During stream capture they stay on the caller's stream.)
+            const bool edges = pl.edge_m > 0 || pl.edge_n > 0;
+            cudaStream_t es = stream;
+            if (edges) {
+                cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+                if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+                if (cap == cudaStreamCaptureStatusNone) {
+                    if (!d.side) {
+                        if (cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) != cudaSuccess)
+                            return SGEMM_ERR_LAUNCH;
+                        if (cudaEventCreateWithFlags(&d.fork_ev, cudaEventDisableTiming) !=
+                                cudaSuccess ||
+                            cudaEventCreateWithFlags(&d.join_ev, cudaEventDisableTiming) !=
+                                cudaSuccess)
+                            return SGEMM_ERR_LAUNCH;
+                    }
+                    if (cudaEventRecord(d.fork_ev, stream) != cudaSuccess ||
+                        cudaStreamWaitEvent(d.side, d.fork_ev, 0) != cudaSuccess)
+                        return SGEMM_ERR_LAUNCH;
+                    es = d.side;
+                }
+            }
+            s = status_from(launch_tile(fm, st, tm, mapA, mapB, tp, pl.grid, stream));
+            if (s != SGEMM_OK || !edges) return s;
+            if (pl.edge_n > 0) {
+                int grid = 0, rows = 0;
+                narrow_grid(M, d.num_sms, &grid, &rows);
+                Epilogue eepi = epi;
+                if (eepi.bias) eepi.bias += N0;
+                const int a_vec =
+                    ((reinterpret_cast<uintptr_t>(Ause) & 15u) == 0 && lda_use % 4 == 0) ? 4 : 1;
+                const int nn = pl.edge_n <= 1 ? 1 : pl.edge_n <= 2 ? 2 : 4;
+                s = run_narrow(nn, a_vec, grid, rows, M, pl.edge_n, K, alpha, Ause, lda_use,
+                               Buse + N0, ldb_use, beta, C + N0, ldc, eepi, es);
+            }
+            if (s == SGEMM_OK && pl.edge_m > 0) {
+                Workspace ew = *w;
+                ew.partials = reinterpret_cast<float *>(reinterpret_cast<char *>(w->partials) +
+                                                        tile_pbytes);
+                ew.counters = w->counters + tile_counters;
+                s = run_skinny(d, edge_plan, pl.edge_m, N0, K, alpha, Ause + M0 * lda_use, lda_use,
+                               Buse, ldb_use, beta, C + M0 * ldc, ldc, epi, &ew, es);
+            }
+            if (es != stream) {
+                // Join even after a failed launch, so the caller's stream
+                // never runs ahead of work already queued on the side.
+                const bool joined = cudaEventRecord(d.join_ev, es) == cudaSuccess &&
+                                    cudaStreamWaitEvent(stream, d.join_ev, 0) == cudaSuccess;
+                if (s == SGEMM_OK && !joined) s = SGEMM_ERR_LAUNCH;
+            }
+            return s;
         }
         case kVarMid:
         case kVarMid64: {
@@ -317,36 +456,15 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             return status_from(launch_ksplit(pl.b_vec, mp, pl.grid, stream));
         }
         case kVarSkinny: {
-            const unsigned bit = 1u << (24 + pl.m_tile / 8);  // m_tile 8, 16, 32: bits 25, 26, 28
-            if (!(d.configured & bit)) {
-                if (skinny_configure(pl.m_tile) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-                d.configured |= bit;
-            }
-            CUtensorMap mapA, mapB;
-            sgemm_status_t s = encode_2d(&mapA, A, M, K, lda, kSkinnyBK, pl.m_tile,
-                                         CU_TENSOR_MAP_SWIZZLE_128B);
-            if (s != SGEMM_OK) return s;
-            s = encode_2d(&mapB, B, K, N, ldb, kSkinnyBN, kSkinnyBK);
-            if (s != SGEMM_OK) return s;
-            SkinnyParams sp;
-            sp.M = (int)M; sp.N = (int)N; sp.K = (int)K;
-            sp.slabs = pl.slabs; sp.kt_total = pl.kt_total;
-            for (int c = 0; c <= pl.grid; ++c) sp.starts[c] = pl.sk_starts[c];
-            sp.alpha = alpha; sp.beta = beta;
-            sp.A = A; sp.lda = lda; sp.C = C; sp.ldc = ldc; sp.c_vec4 = 0;
-            sp.epi = epi;
-            sp.err = d.err;
-            const unsigned long long to = g_timeout_ns.load();
-            sp.timeout_ns = to ? to : kDefaultTimeoutNs;
-            sp.skip_loads_from = g_skip_loads_from.load();
             Workspace *w = nullptr;
-            const size_t pbytes = (size_t)2 * pl.grid * pl.m_tile * kSkinnyBN * sizeof(float);
-            s = ensure_workspace(d, stream, pbytes, (size_t)pl.slabs, &w);
+            const sgemm_status_t s =
+                ensure_workspace(d, stream, skinny_partial_bytes(pl), (size_t)pl.slabs, &w);
             if (s != SGEMM_OK) return s;
-            sp.partials = w->partials;
-            sp.counters = w->counters;
-            return status_from(launch_skinny(pl.m_tile, mapA, mapB, sp, pl.grid, stream));
+            return run_skinny(d, pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, w, stream);
         }
+        case kVarNarrow:
+            return run_narrow(pl.narrow_nn, pl.a_vec, pl.grid, pl.narrow_rows, M, N, K, alpha, A,
+                              lda, B, ldb, beta, C, ldc, epi, stream);
         default:
             return SGEMM_ERR_UNSUPPORTED;
     }
@@ -752,7 +870,7 @@ sgemm_status_t sgemm_plan_describe_3xtf32(int64_t M, int64_t N, int64_t K, int64
 }
 
 sgemm_status_t sgemm_set_plan_override(int variant, int splits) {
-    if (variant < -1 || variant > SGEMM_VARIANT_KSPLIT || splits < 0) return SGEMM_ERR_INVALID_ARG;
+    if (variant < -1 || variant > SGEMM_VARIANT_NARROW || splits < 0) return SGEMM_ERR_INVALID_ARG;
     g_force_variant.store(variant);
     g_force_splits.store(splits);
     return SGEMM_OK;
@@ -801,6 +919,11 @@ sgemm_status_t sgemm_release_workspace(void) {
             if (w.second.split) cudaFree(w.second.split);
         }
         d.ws.clear();
+        if (d.side) cudaStreamDestroy(d.side);
+        if (d.fork_ev) cudaEventDestroy(d.fork_ev);
+        if (d.join_ev) cudaEventDestroy(d.join_ev);
+        d.side = nullptr;
+        d.fork_ev = d.join_ev = nullptr;
         if (d.host.A) cudaFree(d.host.A);
         if (d.host.B) cudaFree(d.host.B);
         if (d.host.C) cudaFree(d.host.C);

@@ -142,6 +142,40 @@ constexpr int kKsStages = 4;
 cudaError_t launch_ksplit(int b_vec, const MidParams &p, int grid, cudaStream_t stream);
 cudaError_t ksplit_configure(int b_vec);
 
+// ---------------------------------------------------------------------------
+// Narrow kernel: N <= kNarrowMaxN columns (also the last few columns of C
+// beside the tiled kernel).  A warp per row of A, lanes over K; B's columns
+// staged transposed in shared memory in chunks of kch k (a multiple of 128;
+// all of K when nn * (kch + 4) floats fit kNarrowSmemBytes); CTAs own
+// contiguous ranges of rows_per_cta rows.  nn: columns the kernel is built
+// for (1, 2 or 4, at least N); a_vec: 4 when A's rows are 16-byte aligned.
+// The bias of the epilogue is indexed from the first column of C passed.
+// ---------------------------------------------------------------------------
+constexpr int kNarrowMaxN = 4;
+constexpr size_t kNarrowSmemBytes = 48 * 1024;
+// Chunk of K staged at once for nn columns.
+constexpr int narrow_kch(long long K, int nn) {
+    const long long fit = ((long long)kNarrowSmemBytes / 4 / nn - 4) / 128 * 128;
+    const long long want = (K + 127) / 128 * 128;
+    return (int)(want < fit ? want : fit);
+}
+
+struct NarrowParams {
+    int M, N, K;
+    float alpha, beta;
+    const float *A;
+    long long lda;
+    const float *B;
+    long long ldb;
+    float *C;
+    long long ldc;
+    Epilogue epi;
+    int rows_per_cta;
+    int kch;  // narrow_kch(K, nn)
+};
+
+cudaError_t launch_narrow(int nn, int a_vec, const NarrowParams &p, int grid, cudaStream_t stream);
+
 // Copies of operands the TMA cannot map: rows x cols at src (leading
 // dimension ld, any 4-byte alignment) to dst with 16-byte-aligned rows of
 // ldp floats (ldp a multiple of 4, dst 16-byte aligned).  Up to two copies in

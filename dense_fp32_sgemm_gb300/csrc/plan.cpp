@@ -127,6 +127,7 @@ const char *variant_name(int v) {
         case kVarMid: return "mid";
         case kVarMid64: return "mid64";
         case kVarKsplit: return "ksplit";
+        case kVarNarrow: return "narrow";
         default: return "?";
     }
 }
@@ -287,6 +288,47 @@ static void plan_ksplit(const PlanInput &in, Plan *pl) {
     pl->reason = "split-K inside the CTA";
 }
 
+// Streaming rates of the narrow and skinny kernels (bytes of the streamed
+// operand per microsecond; 1 x 8192 x 8192 on the skinny kernel: 49 us) and
+// the cost of a kernel queued right behind another one.
+constexpr double kStreamBytesPerUs = 5.5e6;
+constexpr double kChainedLaunchUs = 2.0;
+// The narrow kernel's CTAs per SM and the time of one pass over a chunk of
+// its K when the chunk, not the streaming, sets the pace.
+constexpr int kNarrowCtasPerSm = 2;
+constexpr double kNarrowChunkUs = 0.8;
+
+// The narrow kernel (N <= kNarrowMaxN): contiguous row ranges, one warp per
+// row, CTAs of 8 warps, up to kNarrowCtasPerSm per SM.
+void narrow_grid(int64_t M, int num_sms, int *grid_out, int *rows_out) {
+    const int64_t sms = num_sms > 0 ? num_sms : 1;
+    int64_t grid = ceil_div(M, 8);
+    if (grid > sms * kNarrowCtasPerSm) grid = sms * kNarrowCtasPerSm;
+    if (grid < 1) grid = 1;
+    const int64_t rows = ceil_div(M, grid);
+    *grid_out = (int)ceil_div(M, rows);
+    *rows_out = (int)rows;
+}
+
+static void plan_narrow(const PlanInput &in, Plan *pl) {
+    int g = 0, r = 0;
+    narrow_grid(in.M, in.num_sms, &g, &r);
+    const int64_t grid = g, rows = r;
+    pl->variant = kVarNarrow;
+    pl->grid = (int)grid;
+    pl->narrow_rows = (int)rows;
+    pl->narrow_nn = in.N <= 1 ? 1 : in.N <= 2 ? 2 : 4;
+    pl->a_vec = (aligned16(in.a_addr) && in.lda % 4 == 0) ? 4 : 1;
+    pl->tiles_m = (int)grid;
+    pl->tiles_n = 1;
+    pl->kt_total = (int)ceil_div(in.K, narrow_kch(in.K, pl->narrow_nn));
+    const double stream = (double)in.M * (double)in.K * 4.0 / kStreamBytesPerUs;
+    const double passes = (double)ceil_div(rows, 8) * (double)pl->kt_total * kNarrowChunkUs;
+    pl->cost = (double)ceil_div(rows, 8) * (double)pl->kt_total;
+    pl->est_us = kLaunchUs + (stream > passes ? stream : passes);
+    pl->reason = "narrow N: stream A once";
+}
+
 // The 64 x 64 kernel: one tile per CTA over the whole K.
 static void plan_generic(const PlanInput &in, Plan *pl) {
     const int64_t sms = in.num_sms > 0 ? in.num_sms : 1;
@@ -417,6 +459,12 @@ int make_plan(const PlanInput &in, Plan *pl) {
         *pl = p;
         return 0;
     }
+    if (want == kVarNarrow) {
+        if (in.N > kNarrowMaxN) return -3;
+        plan_narrow(in, &p);
+        *pl = p;
+        return 0;
+    }
     if (want == kVarKsplit) {
         if (ceil_div(in.M, kKsBM) * ceil_div(in.N, kKsBN) > INT32_MAX) return -2;
         plan_ksplit(in, &p);
@@ -436,6 +484,34 @@ int make_plan(const PlanInput &in, Plan *pl) {
         plan_tile(in, t, allow_sk, pack_floats);
         if (!tma_ok) t->reason = "operands copied to aligned rows";
     };
+    // The tiled kernel on all but a thin last strip of rows (<= 32: the
+    // skinny kernel) and of columns (<= kNarrowMaxN: the narrow kernel), so
+    // that no tile row or column holds only a few useful elements ("Part 2",
+    // section "Selecting Among Three Kernels": at 2049 the last column of
+    // 128 x 256 tiles holds one useful column).
+    auto tile_edges_plan = [&](Plan *t) -> bool {
+        const int64_t em = in.M % kTileBM, en = in.N % kTileBN;
+        if (em + en == 0 || em > kSkinnyMaxM || en > kNarrowMaxN) return false;
+        const int64_t M0 = in.M - em, N0 = in.N - en;
+        if (M0 < kTileBM || N0 < kTileBN) return false;
+        PlanInput core = in;
+        core.M = M0;
+        core.N = N0;
+        tile_plan(t, true);  // copies, tile fields of the whole product
+        const double pack_us = (t->pack_a || t->pack_b)
+                                   ? 2.0 * 4.0 * (double)pack_floats / kPackBytesPerUs + kPackFixedUs
+                                   : 0.0;
+        plan_grid(core, t, true, false, kTileModel, kNoScale);
+        t->est_us += pack_us;
+        t->edge_m = (int)em;
+        t->edge_n = (int)en;
+        if (em > 0)
+            t->est_us += kChainedLaunchUs + (double)N0 * (double)in.K * 4.0 / kStreamBytesPerUs;
+        if (en > 0)
+            t->est_us += kChainedLaunchUs + (double)in.M * (double)in.K * 4.0 / kStreamBytesPerUs;
+        t->reason = "tiles, thin edges on the skinny/narrow kernels";
+        return true;
+    };
     if (want == kVarTile || want == kVarStreamK) {
         if (!tma_ok && !packable) return -2;
         tile_plan(&p, want != kVarTile);
@@ -448,10 +524,14 @@ int make_plan(const PlanInput &in, Plan *pl) {
     // copies of them unless M <= 32, where copying B would double the bytes
     // moved), the mid-size kernel with 128-row tiles and, for M <= 64, with
     // 64-row tiles, the split-K kernel and the 64 x 64 kernel.
-    Plan cand[5];
+    Plan cand[7];
     int n = 0;
     cand[n] = p;
     plan_mid(in, &cand[n++], 128);
+    if (in.N <= kNarrowMaxN) {
+        cand[n] = p;
+        plan_narrow(in, &cand[n++]);
+    }
     if (ceil_div(in.M, kKsBM) * ceil_div(in.N, kKsBN) <= INT32_MAX) {
         cand[n] = p;
         plan_ksplit(in, &cand[n++]);
@@ -463,6 +543,8 @@ int make_plan(const PlanInput &in, Plan *pl) {
     if (tma_ok || (packable && in.M > kSkinnyMaxM)) {
         cand[n] = p;
         tile_plan(&cand[n++], true);
+        cand[n] = p;
+        if (tile_edges_plan(&cand[n])) ++n;
     }
     cand[n] = p;
     plan_generic(in, &cand[n]);
@@ -482,11 +564,13 @@ int describe_plan(const Plan &p, char *buf, size_t len) {
     return snprintf(buf, len,
                     "variant=%s tiles_m=%d tiles_n=%d kt=%d dp_tiles=%d sk_tiles=%d sk_share=%d "
                     "grid=%d group_m=%d c_vec4=%d m_tile=%d two_unit_ctas=%d pack_a=%d pack_b=%d "
-                    "bm=%d bvec=%d cost=%.2f est_us=%.1f alt_us=%.1f reason=%s",
+                    "bm=%d bvec=%d edge_m=%d edge_n=%d narrow_nn=%d narrow_rows=%d avec=%d "
+                    "cost=%.2f est_us=%.1f alt_us=%.1f reason=%s",
                     variant_name(p.variant), p.tiles_m, p.tiles_n, p.kt_total, p.dp_tiles,
                     p.sk_tiles, p.sk_share, p.grid, p.group_m, p.c_vec4, p.m_tile,
                     p.variant == kVarSkinny ? p.sk_two_units : 0, p.pack_a ? 1 : 0,
-                    p.pack_b ? 1 : 0, p.mid_bm, p.b_vec, p.cost, p.est_us, p.alt_us,
+                    p.pack_b ? 1 : 0, p.mid_bm, p.b_vec, p.edge_m, p.edge_n, p.narrow_nn,
+                    p.narrow_rows, p.a_vec, p.cost, p.est_us, p.alt_us,
                     p.reason ? p.reason : "");
 }
 

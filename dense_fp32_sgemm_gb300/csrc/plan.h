@@ -18,6 +18,7 @@ enum Variant : int {
     kVarMid = 4,        // mid-size kernel, bm x 128 tiles (bm = 128 when forced)
     kVarMid64 = 5,      // forced: the mid-size kernel with 64 x 128 tiles
     kVarKsplit = 6,     // split-K inside the CTA: 64 x 128 tiles, one per CTA
+    kVarNarrow = 7,     // N <= kNarrowMaxN: a warp per row of A
 };
 
 struct PlanInput {
@@ -47,6 +48,13 @@ struct Plan {
     // estimated time of the chosen plan (microseconds) and of the best other
     // candidate considered (0 when there was none)
     double est_us, alt_us;
+    // tiled kernel: the last edge_m rows (<= 32, the skinny kernel) and the
+    // last edge_n columns (<= kNarrowMaxN, the narrow kernel) of C are left
+    // to other kernels; the tile counts cover the rest
+    int edge_m, edge_n;
+    // narrow kernel: columns it is built for (1, 2, 4), rows per CTA, and
+    // A's load width in floats (4 or 1)
+    int narrow_nn, narrow_rows, a_vec;
     // operands copied to 16-byte-aligned rows first (leading dimensions after the copy)
     bool pack_a, pack_b;
     int64_t lda_packed, ldb_packed;
@@ -57,6 +65,9 @@ struct Plan {
 // Returns 0 and fills `out`, or a negative value for arguments no variant
 // can take (the caller has validated sizes already).
 int make_plan(const PlanInput &in, Plan *out);
+
+// The narrow kernel's grid over M rows: CTAs and the rows each owns.
+void narrow_grid(int64_t M, int num_sms, int *grid, int *rows);
 
 // Writes a one-line key=value description of `plan`.
 int describe_plan(const Plan &plan, char *buf, size_t len);

@@ -217,8 +217,9 @@ enum {
     SGEMM_VARIANT_MID = 4,       /* cp.async + FFMA2 128x128 tile, any alignment,     */
                                  /* data-parallel waves + stream-K tail               */
     SGEMM_VARIANT_MID64 = 5,     /* the same kernel with 64x128 tiles                 */
-    SGEMM_VARIANT_KSPLIT = 6     /* cp.async + FFMA2 64x128 tile per CTA, K split     */
+    SGEMM_VARIANT_KSPLIT = 6,    /* cp.async + FFMA2 64x128 tile per CTA, K split     */
                                  /* over four warp groups inside the CTA              */
+    SGEMM_VARIANT_NARROW = 7     /* N <= 4: a warp per row of A (A x products)        */
 };
 SGEMM_API sgemm_status_t sgemm_set_plan_override(int variant, int splits);
 

@@ -219,6 +219,79 @@ def test_unaligned_operands_copied_for_the_tiled_kernel(offsets, lds, variant):
           lda=lds[0], ldb=lds[1], ldc=lds[2], variant=variant)
 
 
+# ----- narrow N (a warp per row of A) and thin edges beside the tiles ----------
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4])
+@pytest.mark.parametrize("M,K,lda_pad,off", [(1, 1, 0, 0), (9, 3, 1, 1), (40, 1024, 0, 0),
+                                             (300, 1025, 3, 0), (1000, 3000, 0, 2),
+                                             (5000, 129, 1, 3)])
+def test_narrow_kernel_integers_bit_exact(N, M, K, lda_pad, off):
+    # Every row of A against N columns of B: chunk edges of K (1024), rows
+    # that do not fill the last pass of eight, 16-byte and 4-byte loads of A.
+    A, lda, B, ldb, C, ldc = inputs("ints", 80 + N + K, M, N, K, lda=K + lda_pad, ldb=N + 1,
+                                    ldc=N + 2)
+    out, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc, offsets=(off, 1, 0), variant=7)
+    want = (A.reshape(M, lda)[:, :K].astype(np.int64) @ B.reshape(K, ldb)[:, :N].astype(np.int64)
+            + C.reshape(M, ldc)[:, :N].astype(np.int64))
+    assert np.array_equal(out.astype(np.int64), want)
+
+
+@pytest.mark.parametrize("M,N,K", [(8192, 1, 4096), (3000, 4, 2049), (64, 3, 20000), (7, 2, 5)])
+def test_narrow_kernel_floats_within_bound(M, N, K):
+    check(M, N, K, 0.5, -2.0, dist="normal", seed=90 + M, lda=K, ldb=N, ldc=N, variant=7)
+    check(M, N, K, 1.0, 0.0, dist="uniform", seed=91 + M, lda=K + 1, ldb=N + 3, ldc=N + 1,
+          offsets=(1, 0, 2))
+
+
+@pytest.mark.parametrize("M,N,K,lds,offsets,em,en", [
+    (2049, 2049, 1000, (1000, 2049, 2049), (0, 0, 0), 1, 1),  # both copied to aligned rows
+    (2050, 2052, 700, (700, 2052, 2052), (0, 0, 0), 2, 4),    # aligned: no copy
+    (2080, 2051, 1024, (1024, 2051, 2051), (0, 1, 0), 32, 3),  # B copied
+    (4128, 2051, 512, (512, 2051, 2053), (0, 1, 3), 32, 3),
+])
+def test_thin_edges_integers_bit_exact(M, N, K, lds, offsets, em, en):
+    # The automatic plan leaves the last rows to the skinny kernel and the last
+    # columns to the narrow kernel; the three kernels together give the exact
+    # sum over every element.
+    p = sg.plan_describe(M, N, K, lda=lds[0], ldb=lds[1], ldc=lds[2], a_addr=256 + 4 * offsets[0],
+                         b_addr=512 + 4 * offsets[1], c_addr=768 + 4 * offsets[2])
+    assert p["variant"] in ("tile", "streamk") and (int(p["edge_m"]), int(p["edge_n"])) == (em, en)
+    A, lda, B, ldb, C, ldc = inputs("ints", 95 + K, M, N, K, lda=lds[0], ldb=lds[1], ldc=lds[2])
+    out, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc, offsets=offsets)
+    # small integers: every partial sum is an integer below 2^24, so the FP64
+    # product (a library matmul) is the exact one
+    want = (A.reshape(M, lda)[:, :K].astype(np.float64) @ B.reshape(K, ldb)[:, :N].astype(np.float64)
+            + C.reshape(M, ldc)[:, :N].astype(np.float64))
+    assert np.array_equal(out.astype(np.float64), want)
+
+
+def test_thin_edges_floats_and_epilogue():
+    # Floats within the bound, and the bias of the last columns taken from
+    # their own columns.
+    M, N, K = 2049, 2049, 512
+    check(M, N, K, 0.75, 1.5, dist="normal", seed=97, lda=K, ldb=N, ldc=N)
+    A, lda, B, ldb, C, ldc = inputs("ints", 98, M, N, K, lda=K, ldb=N, ldc=N)
+    bias = (np.arange(N) % 37 - 18).astype(np.float32)
+    out, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc, bias=bias, activation=1)
+    want = (A.reshape(M, lda)[:, :K].astype(np.float64) @ B.reshape(K, ldb)[:, :N].astype(np.float64)
+            + C.reshape(M, ldc)[:, :N].astype(np.float64) + bias.astype(np.float64)[None, :])
+    assert np.array_equal(out.astype(np.float64), np.maximum(want, 0))
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 40, 50), (70, 1000, 9), (33, 3, 130), (5, 700, 300),
+                                   (129, 257, 1000)])
+def test_copy_pass_row_widths(M, N, K):
+    # The copy to aligned rows runs 32 to 256 threads over a row depending on
+    # its width (a block copies several short rows at once); every width, with
+    # both operands unaligned, through the tiled kernel on small integers.
+    lda, ldb, ldc = K + 1, N + 3, N + 1
+    A, lda, B, ldb, C, ldc = inputs("ints", 70 + K, M, N, K, lda=lda, ldb=ldb, ldc=ldc)
+    out, _ = run_gemm(M, N, K, 1.0, 1.0, A, lda, B, ldb, C, ldc, offsets=(1, 3, 0), variant=1)
+    want = (A.reshape(M, lda)[:, :K].astype(np.int64) @ B.reshape(K, ldb)[:, :N].astype(np.int64)
+            + C.reshape(M, ldc)[:, :N].astype(np.int64))
+    assert np.array_equal(out.astype(np.int64), want)
+
+
 @pytest.mark.parametrize("variant", [-1, 1, 2, 4, 6])
 def test_odd_workload_bit_exact(variant):
     # 1023 x 1025 x 513 with small integers, as planned and through the tiled
@@ -519,7 +592,8 @@ def test_skinny_wait_timeout_reports_and_recovers(M):
 
 @pytest.mark.parametrize("M,N,K,variant", [(16, 4096, 2048, -1), (1100, 1300, 512, 2),
                                            (300, 520, 200, 0), (1023, 1025, 513, 4),
-                                           (700, 900, 3000, 5), (1023, 1025, 513, 6)])
+                                           (700, 900, 3000, 5), (1023, 1025, 513, 6),
+                                           (2049, 2049, 1000, -1), (3000, 3, 1000, 7)])
 def test_capture_in_a_cuda_graph_and_replay(M, N, K, variant):
     # After a first call has set up the stream's workspace, sgemm_run queues
     # kernels only (no allocation, no host synchronisation), so it can be

@@ -106,7 +106,10 @@ def tile_invariants(p, M, N, K, forced_sk=False):
     tm, tn, kt, dp, sk, share, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles",
                                            "sk_tiles", "sk_share", "grid")
     T = tm * tn
-    assert tm == math.ceil(M / 128) and tn == math.ceil(N / 256) and kt == math.ceil(K / 32)
+    em, en = ints(p, "edge_m", "edge_n")  # rows and columns left to other kernels
+    assert 0 <= em <= 32 and 0 <= en <= 4
+    assert tm == math.ceil((M - em) / 128) and tn == math.ceil((N - en) / 256)
+    assert kt == math.ceil(K / 32)
     assert dp + sk == T
     assert 1 <= grid <= SMS
     if sk:
@@ -120,6 +123,14 @@ def tile_invariants(p, M, N, K, forced_sk=False):
     # split takes the first candidate)
     if not forced_sk:
         assert float(p["cost"]) <= math.ceil(T / SMS) * kt + 1e-9
+
+
+def narrow_invariants(p, M, N, K):
+    # N <= 4; contiguous row ranges covering M once, at most two CTAs per SM
+    grid, rows, nn = ints(p, "grid", "narrow_rows", "narrow_nn")
+    assert N <= 4 and nn == (1 if N == 1 else 2 if N == 2 else 4)
+    assert 1 <= grid <= 2 * SMS
+    assert rows * grid >= M and rows * (grid - 1) < M
 
 
 def ksplit_invariants(p, M, N, K):
@@ -179,6 +190,8 @@ def test_plan_invariants(M, N, K):
         ksplit_invariants(p, M, N, K)
     elif p["variant"] == "skinny":
         assert M <= 32
+    elif p["variant"] == "narrow":
+        narrow_invariants(p, M, N, K)
     else:
         assert p["variant"] == "generic"
 
@@ -391,11 +404,16 @@ def test_random_plans_cover_the_work():
     for M, N, K in _random_shapes(11, 300):
         p = plan(M, N, K)
         v = p["variant"]
-        assert v in ("tile", "streamk", "mid", "generic", "skinny", "scale", "none"), (M, N, K, v)
+        assert v in ("tile", "streamk", "mid", "ksplit", "narrow", "generic", "skinny", "scale",
+                     "none"), (M, N, K, v)
         if v in ("tile", "streamk"):
             tile_invariants(p, M, N, K)
         elif v == "mid":
             mid_invariants(p, M, N, K)
+        elif v == "ksplit":
+            ksplit_invariants(p, M, N, K)
+        elif v == "narrow":
+            narrow_invariants(p, M, N, K)
         elif v == "skinny":
             assert M <= 32
             slabs, kt, grid = ints(p, "tiles_n", "kt", "grid")
@@ -420,3 +438,38 @@ def test_random_3xtf32_plans():
             assert kps >= 16 and (splits - 1) * kps < kt
         assert ctas == math.ceil(M / 128) * math.ceil(N / bn) * splits
         assert cps == (2 if ctas > SMS else 1)
+
+
+# ----- narrow N and thin edges -------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [(8192, 1, 8192), (8192, 4, 8192), (100000, 1, 1000),
+                                   (2049, 3, 2049), (40, 2, 100)])
+def test_narrow_products_stream_a_once(M, N, K):
+    # N <= 4 (and M above the skinny kernel's 32 rows): a warp per row of A.
+    p = plan(M, N, K)
+    assert p["variant"] == "narrow"
+    narrow_invariants(p, M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K,em,en", [(2049, 2049, 2049, 1, 1), (4097, 4097, 4097, 1, 1),
+                                         (2050, 2052, 1000, 2, 4), (4096, 4097, 4096, 0, 1),
+                                         (2080, 4096, 4096, 32, 0)])
+def test_thin_edges_leave_the_tiles_whole(M, N, K, em, en):
+    # A last tile row of at most 32 rows goes to the skinny kernel and a last
+    # tile column of at most 4 columns to the narrow one; the tiled kernel
+    # covers the rest with whole 128 x 256 tiles.
+    p = plan(M, N, K)
+    assert p["variant"] in ("tile", "streamk")
+    assert ints(p, "edge_m", "edge_n") == [em, en]
+    tm, tn = ints(p, "tiles_m", "tiles_n")
+    assert tm * 128 == M - em and tn * 256 == N - en
+
+
+def test_forced_tiles_keep_their_edges():
+    # The forced tiled variants cover the whole product themselves.
+    sg.set_plan_override(sg.VARIANT_STREAMK, 0)
+    try:
+        p = plan(2049, 2049, 2049)
+    finally:
+        sg.set_plan_override(-1, 0)
+    assert ints(p, "edge_m", "edge_n", "tiles_m", "tiles_n") == [0, 0, 17, 9]
