@@ -110,7 +110,8 @@ def main():
                "us": {k: round(v * 1e6, 2) for k, v in times.items()},
                "est_us": {k: float(plans[k].get("est_us", 0)) for k in times},
                "plans": {k: {f: plans[k].get(f) for f in ("variant", "bm", "grid", "dp_tiles",
-                                                           "sk_tiles", "sk_share", "kt")}
+                                                           "sk_tiles", "sk_share", "kt", "edge_m",
+                                                           "edge_n")}
                          for k in times}}
         rows.append(row)
         print(f"{M:5d}x{N:5d}x{K:5d} auto={row['auto']:8s} {row['auto_us']:9.2f} us "
