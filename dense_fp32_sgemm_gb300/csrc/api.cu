@@ -438,10 +438,11 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             }
             return status_from(launch_mid(pl.mid_bm, pl.b_vec, mp, pl.grid, stream));
         }
-        case kVarKsplit: {
-            const int key = 2000 + pl.b_vec;
+        case kVarKsplit:
+        case kVarKsplit64: {
+            const int key = 2000 + pl.ks_bn * 10 + pl.b_vec;
             if (!d.configured_tiles.count(key)) {
-                if (ksplit_configure(pl.b_vec) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+                if (ksplit_configure(pl.b_vec, pl.ks_bn) != cudaSuccess) return SGEMM_ERR_LAUNCH;
                 d.configured_tiles.insert(key);
             }
             MidParams mp = {};
@@ -453,7 +454,7 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             mp.A = A; mp.lda = lda; mp.B = B; mp.ldb = ldb; mp.C = C; mp.ldc = ldc;
             mp.c_vec4 = pl.c_vec4;
             mp.epi = epi;
-            return status_from(launch_ksplit(pl.b_vec, mp, pl.grid, stream));
+            return status_from(launch_ksplit(pl.b_vec, pl.ks_bn, mp, pl.grid, stream));
         }
         case kVarSkinny: {
             Workspace *w = nullptr;
@@ -870,7 +871,7 @@ sgemm_status_t sgemm_plan_describe_3xtf32(int64_t M, int64_t N, int64_t K, int64
 }
 
 sgemm_status_t sgemm_set_plan_override(int variant, int splits) {
-    if (variant < -1 || variant > SGEMM_VARIANT_NARROW || splits < 0) return SGEMM_ERR_INVALID_ARG;
+    if (variant < -1 || variant > SGEMM_VARIANT_KSPLIT64 || splits < 0) return SGEMM_ERR_INVALID_ARG;
     g_force_variant.store(variant);
     g_force_splits.store(splits);
     return SGEMM_OK;

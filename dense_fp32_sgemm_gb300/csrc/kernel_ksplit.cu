@@ -9,11 +9,13 @@
 // partial tile written, a ticket, the last piece's CTA reading the others
 // back) costs several microseconds per tile, which is as much as a small
 // product's whole main loop.  Here the split stays inside one CTA: one CTA of
-// 256 threads owns a 64 x 128 tile, its four groups of 64 threads each take a
-// quarter of every slice of kKsBK k (group g the g-th quarter), and at the end
-// the four sets of sums meet in shared memory and are added in group order.  The
-// SM then holds eight warps of independent multiply-adds (two per scheduler)
-// for one tile, where a 64 x 128 tile of 64 threads would hold two.
+// 256 threads owns a 64 x 128 tile (four groups of 64 threads) or a 64 x 64
+// tile (eight groups of one warp); each group takes its part of every slice of
+// kKsBK k, and at the end the groups' sums meet in shared memory and are
+// added in group order.  The SM then holds eight warps of independent
+// multiply-adds (two per scheduler) for one tile, where a 64 x 128 tile of 64
+// threads would hold two; the 64 x 64 tile spreads small products over twice
+// as many SMs.
 //
 // Each thread keeps a 16 x 8 micro-tile of the tile's sums (warps of 64 x 64,
 // lanes 4 x 8, rows in groups of four 16 apart, columns in two groups of four
@@ -46,25 +48,34 @@ namespace sgemm {
 namespace {
 
 constexpr int BM = kKsBM;
-constexpr int BN = kKsBN;
 constexpr int BK = kKsBK;
-constexpr int KG = kKsGroups;
 constexpr int ST = kKsStages;
-constexpr int GK = BK / KG;                 // k of a slice per group
-constexpr int GT = BM * BN / (16 * 8);      // threads per group: 64
-constexpr int NT = KG * GT;                 // 256
+constexpr int NT = kKsThreads;              // 256
 constexpr int A_FLOATS = BK * BM;           // k-major: row k holds BM values
-constexpr int B_FLOATS = BK * BN;
-constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
 constexpr int A_HALVES = BK / 32;           // 32-k halves of an A row per slice
-constexpr int TILE_F4 = BM * BN / 4;        // float4 of one tile: 2048
-constexpr size_t RING_BYTES = size_t(ST) * STAGE_FLOATS * 4;
-constexpr size_t SUMS_BYTES = size_t(KG) * TILE_F4 * 16;  // the groups' sums, after the loop
-constexpr size_t SMEM_BYTES = RING_BYTES > SUMS_BYTES ? RING_BYTES : SUMS_BYTES;
-static_assert(BM == 64 && BN == 128 && (BK == 32 || BK == 64) && KG == 4,
-              "the copy and fragment maps");
-static_assert(GK % 8 == 0 && GT == 64 && NT == 256, "group layout");
-static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
+static_assert(BM == 64 && (BK == 32 || BK == 64) && NT == 256, "the copy and fragment maps");
+
+// A tile of BM x BN (BN = 128 or 64): each k-group holds one 16 x 8 micro-tile
+// of the whole tile per thread, so a group is BM * BN / 128 threads (two
+// warps or one) and there are NT / that many groups (four or eight).
+template <int BN_>
+struct KsCfg {
+    static constexpr int BN = BN_;
+    static constexpr int GT = BM * BN / (16 * 8);  // threads per group: 64 or 32
+    static constexpr int KG = NT / GT;             // groups: 4 or 8
+    static constexpr int GK = BK / KG;             // k of a slice per group
+    static constexpr int WARPS_N = BN / 64;        // warp columns of a group
+    static constexpr int B_FLOATS = BK * BN;
+    static constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
+    static constexpr int TILE_F4 = BM * BN / 4;    // float4 of one tile
+    static constexpr int ROW_F4 = BN / 4;          // float4 of one tile row
+    static constexpr size_t RING_BYTES = size_t(ST) * STAGE_FLOATS * 4;
+    static constexpr size_t SUMS_BYTES = size_t(KG) * TILE_F4 * 16;  // the groups' sums
+    static constexpr size_t SMEM_BYTES = RING_BYTES > SUMS_BYTES ? RING_BYTES : SUMS_BYTES;
+    static_assert(BN == 128 || BN == 64, "tile widths");
+    static_assert(GK % 8 == 0 && KG * GT == NT, "group layout");
+    static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
+};
 
 // Offset (floats) of A element (m, k) in a k-major slice of BM rows.
 __device__ __forceinline__ int ks_a_off(int m, int k) {
@@ -82,7 +93,7 @@ __device__ __forceinline__ void ks_tile_coords(const MidParams &p, int t, int &t
 }
 
 // Copies of k-slice ks of tile (tm, tn) into stage `st`.
-template <int BVEC>
+template <int BVEC, int BN>
 __device__ __forceinline__ void ks_issue(const MidParams &p, float *st, int tm, int tn, int ks,
                                          int tid) {
     float *sa = st;
@@ -106,30 +117,35 @@ __device__ __forceinline__ void ks_issue(const MidParams &p, float *st, int tm, 
     }
     const int n_base = tn * BN;
     if (BVEC == 4) {
-        // BK * 32 chunks of 16 bytes; chunk t + 256 q is row t / 32 + 8 q,
-        // columns 4 (t % 32) .. + 3.
-        const int n4 = (tid & 31) * 4;
+        // BK * BN / 4 chunks of 16 bytes, CPR to a row; chunk t + 256 q is
+        // row t / CPR + (256 / CPR) q, columns 4 (t % CPR) .. + 3.
+        constexpr int CPR = BN / 4;
+        constexpr int RPQ = NT / CPR;
+        const int n4 = (tid % CPR) * 4;
         const int cols = min(4, p.N - (n_base + n4));
-        const int kin0 = tid >> 5;
+        const int kin0 = tid / CPR;
         const float *src = p.B + (long long)(k_base + kin0) * p.ldb + n_base + n4;
-        const long long step = 8LL * p.ldb;
+        const long long step = (long long)RPQ * p.ldb;
 #pragma unroll
         for (int q = 0; q < BK * BN / 4 / NT; ++q) {
-            const bool ok = k_base + kin0 + 8 * q < p.K && cols > 0;
-            cp_async16(sb + (kin0 + 8 * q) * BN + n4, ok ? src : p.B, ok ? uint32_t(cols) * 4u : 0u);
+            const bool ok = k_base + kin0 + RPQ * q < p.K && cols > 0;
+            cp_async16(sb + (kin0 + RPQ * q) * BN + n4, ok ? src : p.B,
+                       ok ? uint32_t(cols) * 4u : 0u);
             src += step;
         }
     } else {
-        // BK * 128 elements; element t + 256 q is row t / 128 + 2 q, column t % 128.
-        const int n = tid & 127;
+        // BK * BN elements; element t + 256 q is row t / BN + (256 / BN) q,
+        // column t % BN.
+        constexpr int RPQ = NT / BN;
+        const int n = tid % BN;
         const bool n_ok = n_base + n < p.N;
-        const int kin0 = tid >> 7;
+        const int kin0 = tid / BN;
         const float *src = p.B + (long long)(k_base + kin0) * p.ldb + n_base + n;
-        const long long step = 2LL * p.ldb;
+        const long long step = (long long)RPQ * p.ldb;
 #pragma unroll
         for (int q = 0; q < BK * BN / NT; ++q) {
-            const bool ok = n_ok && k_base + kin0 + 2 * q < p.K;
-            cp_async4(sb + (kin0 + 2 * q) * BN + n, ok ? src : p.B, ok ? 4u : 0u);
+            const bool ok = n_ok && k_base + kin0 + RPQ * q < p.K;
+            cp_async4(sb + (kin0 + RPQ * q) * BN + n, ok ? src : p.B, ok ? 4u : 0u);
             src += step;
         }
     }
@@ -143,6 +159,7 @@ struct KsAcc {
 
 // Fragment addresses of one thread: the four A bases (one per k mod 4, the
 // XOR of row chunk ty with k mod 4) and the B base, as shared-window bytes.
+template <int BN>
 struct KsFrag {
     uint32_t pa[4];
     uint32_t pb;
@@ -186,7 +203,8 @@ __device__ __forceinline__ void ks_fma(KsAcc &acc, const float4 (&a)[4], const f
 
 // The group's GK k (k0 .. k0 + GK - 1 of the stage whose fragment bases are
 // in `f`), fully unrolled with fragments double-buffered in registers.
-__device__ __forceinline__ void ks_compute_full(const KsFrag &f, int k0, KsAcc &acc) {
+template <int GK, int BN>
+__device__ __forceinline__ void ks_compute_full(const KsFrag<BN> &f, int k0, KsAcc &acc) {
     float4 fa[2][4], fb[2][2];
     f.load(k0, 0, fa[0], fb[0]);
 #pragma unroll
@@ -197,7 +215,8 @@ __device__ __forceinline__ void ks_compute_full(const KsFrag &f, int k0, KsAcc &
 }
 
 // The first `kc` (< GK) of the group's k, one at a time (the last slice).
-__device__ __forceinline__ void ks_compute_part(const KsFrag &f, int k0, int kc, KsAcc &acc) {
+template <int BN>
+__device__ __forceinline__ void ks_compute_part(const KsFrag<BN> &f, int k0, int kc, KsAcc &acc) {
 #pragma unroll 1
     for (int k = 0; k < kc; ++k) {
         float4 a[4], b[2];
@@ -261,15 +280,18 @@ __device__ __forceinline__ void ks_store4(const MidParams &p, int m, int n, floa
     }
 }
 
-template <int BVEC>
+template <int BVEC, int BN>
 __global__ void __launch_bounds__(NT, 1) sgemm_ksplit_kernel(const __grid_constant__ MidParams p) {
+    using Cf = KsCfg<BN>;
+    constexpr int GK = Cf::GK, KG = Cf::KG, STAGE_FLOATS = Cf::STAGE_FLOATS;
+    constexpr int TILE_F4 = Cf::TILE_F4, ROW_F4 = Cf::ROW_F4;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     float *ring = reinterpret_cast<float *>(smem_raw);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int grp = warp >> 1;           // k-group
-    const int wn = warp & 1;             // warp column (64 wide) within the tile
+    const int grp = warp / Cf::WARPS_N;  // k-group
+    const int wn = warp % Cf::WARPS_N;   // warp column (64 wide) within the tile
     const int ty = lane >> 3, tx = lane & 7;
 
     int tm, tn;
@@ -278,7 +300,7 @@ __global__ void __launch_bounds__(NT, 1) sgemm_ksplit_kernel(const __grid_consta
 
 #pragma unroll
     for (int s = 0; s < ST - 1; ++s) {
-        if (s < n_slices) ks_issue<BVEC>(p, ring + s * STAGE_FLOATS, tm, tn, s, tid);
+        if (s < n_slices) ks_issue<BVEC, BN>(p, ring + s * STAGE_FLOATS, tm, tn, s, tid);
         cp_async_commit();
     }
     KsAcc acc;
@@ -288,7 +310,7 @@ __global__ void __launch_bounds__(NT, 1) sgemm_ksplit_kernel(const __grid_consta
         for (int j = 0; j < 8; ++j) acc.v[i][j] = make_float2(0.f, 0.f);
 
     // Fragment bases relative to stage 0; a stage adds s * STAGE_FLOATS * 4.
-    KsFrag f0;
+    KsFrag<BN> f0;
 #pragma unroll
     for (int x = 0; x < 4; ++x) f0.pa[x] = smem_addr(ring + ((ty ^ x) << 2));
     f0.pb = smem_addr(ring + A_FLOATS + wn * 64 + tx * 4);
@@ -304,34 +326,35 @@ __global__ void __launch_bounds__(NT, 1) sgemm_ksplit_kernel(const __grid_consta
         cp_async_wait<ST - 2>();  // this thread's copies of slice i are in
         __syncthreads();          // everyone's are; slice i - 1 is consumed
         if (i + ST - 1 < n_slices)
-            ks_issue<BVEC>(p, ring + ((i + ST - 1) % ST) * STAGE_FLOATS, tm, tn, i + ST - 1, tid);
+            ks_issue<BVEC, BN>(p, ring + ((i + ST - 1) % ST) * STAGE_FLOATS, tm, tn, i + ST - 1,
+                               tid);
         cp_async_commit();
-        KsFrag f = f0;
+        KsFrag<BN> f = f0;
         const uint32_t so = 4u * (uint32_t)((i % ST) * STAGE_FLOATS);
 #pragma unroll
         for (int x = 0; x < 4; ++x) f.pa[x] += so;
         f.pb += so;
         f.a0 += so;
         if (i < full)
-            ks_compute_full(f, k_grp, acc);
+            ks_compute_full<GK>(f, k_grp, acc);
         else if (kc_last > 0)
             ks_compute_part(f, k_grp, kc_last, acc);
     }
     cp_async_wait<0>();
     __syncthreads();  // every group is done with the ring
 
-    // The groups' sums, float4 (row, c4) of group g at S[g][row * 32 + c4].
+    // The groups' sums, float4 (row, c4) of group g at S[g][row * ROW_F4 + c4].
     float4 *S = reinterpret_cast<float4 *>(ring);
 #pragma unroll 1
     for (int e4 = 0; e4 < 32; ++e4) {
         const int ri = e4 >> 1;  // r * 4 + i
         const int row = (ri >> 2) * 16 + ty * 4 + (ri & 3);
         const int c4 = wn * 16 + (e4 & 1) * 8 + tx;
-        S[grp * TILE_F4 + row * 32 + c4] = ks_f4(acc, e4);
+        S[grp * TILE_F4 + row * ROW_F4 + c4] = ks_f4(acc, e4);
     }
     __syncthreads();
-    // Thread t adds float4 t + 256 q (q < 8) of the four groups in group
-    // order and stores it: a warp covers one row of the tile.
+    // Thread t adds float4 t + 256 q of the groups in group order and stores
+    // it: consecutive threads cover consecutive columns of a row.
     const int m0 = tm * BM, n0 = tn * BN;
 #pragma unroll 1
     for (int q = 0; q < TILE_F4 / NT; ++q) {
@@ -345,38 +368,45 @@ __global__ void __launch_bounds__(NT, 1) sgemm_ksplit_kernel(const __grid_consta
             s.z += x.z;
             s.w += x.w;
         }
-        ks_store4(p, m0 + (f >> 5), n0 + (f & 31) * 4, s);
+        ks_store4(p, m0 + f / ROW_F4, n0 + (f % ROW_F4) * 4, s);
     }
 }
 
-template <int BVEC>
+template <int BVEC, int BN>
 cudaError_t launch_impl(const MidParams &p, int grid, cudaStream_t stream) {
-    sgemm_ksplit_kernel<BVEC><<<grid, NT, SMEM_BYTES, stream>>>(p);
+    sgemm_ksplit_kernel<BVEC, BN><<<grid, NT, KsCfg<BN>::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 
-template <int BVEC>
+template <int BVEC, int BN>
 cudaError_t configure_impl() {
-    cudaError_t e = cudaFuncSetAttribute(sgemm_ksplit_kernel<BVEC>,
+    cudaError_t e = cudaFuncSetAttribute(sgemm_ksplit_kernel<BVEC, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+                                         (int)KsCfg<BN>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(sgemm_ksplit_kernel<BVEC>,
+    return cudaFuncSetAttribute(sgemm_ksplit_kernel<BVEC, BN>,
                                 cudaFuncAttributePreferredSharedMemoryCarveout,
                                 (int)cudaSharedmemCarveoutMaxShared);
 }
 
+// The instantiated forms: (B copy width, tile width).
+#define SGEMM_KS_FORMS(X) X(4, 128) X(1, 128) X(4, 64) X(1, 64)
+
 }  // namespace
 
-cudaError_t launch_ksplit(int b_vec, const MidParams &p, int grid, cudaStream_t stream) {
-    if (b_vec == 4) return launch_impl<4>(p, grid, stream);
-    if (b_vec == 1) return launch_impl<1>(p, grid, stream);
+cudaError_t launch_ksplit(int b_vec, int bn, const MidParams &p, int grid, cudaStream_t stream) {
+#define SGEMM_KS_LAUNCH(BV, BN_) \
+    if (b_vec == BV && bn == BN_) return launch_impl<BV, BN_>(p, grid, stream);
+    SGEMM_KS_FORMS(SGEMM_KS_LAUNCH)
+#undef SGEMM_KS_LAUNCH
     return cudaErrorInvalidValue;
 }
 
-cudaError_t ksplit_configure(int b_vec) {
-    if (b_vec == 4) return configure_impl<4>();
-    if (b_vec == 1) return configure_impl<1>();
+cudaError_t ksplit_configure(int b_vec, int bn) {
+#define SGEMM_KS_CONF(BV, BN_) \
+    if (b_vec == BV && bn == BN_) return configure_impl<BV, BN_>();
+    SGEMM_KS_FORMS(SGEMM_KS_CONF)
+#undef SGEMM_KS_CONF
     return cudaErrorInvalidValue;
 }
 

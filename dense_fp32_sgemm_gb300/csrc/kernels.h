@@ -124,23 +124,24 @@ cudaError_t mid_configure(int bm, int b_vec);
 constexpr int mid_ctas_per_sm(int bm) { return bm == 64 ? 4 : 2; }
 
 // ---------------------------------------------------------------------------
-// Split-K-in-CTA kernel: one CTA of 256 threads per 64 x 128 tile, in four
-// groups of 64 threads; group g takes the g-th quarter of every kKsBK-k slice
-// and keeps a 16 x 8 micro-tile of sums of the whole tile per thread; the
-// four groups' sums are added in shared memory in group order.  Copies as in
-// the mid-size kernel (cp.async of 4 or 16 bytes, any alignment), a ring of
-// kKsStages slices.  Data-parallel: one tile per CTA, one CTA per SM.
-// Takes MidParams (tiles_m, tiles_n, kt_total = ceil(K / kKsBK), group_m;
-// the stream-K fields are unused).
+// Split-K-in-CTA kernel: one CTA of 256 threads per 64 x BN tile (BN = 128:
+// four groups of 64 threads; BN = 64: eight groups of one warp); group g
+// takes the g-th part of every kKsBK-k slice and keeps a 16 x 8 micro-tile
+// of sums of the whole tile per thread; the groups' sums are added in
+// shared memory in group order.  Copies as in the mid-size kernel (cp.async
+// of 4 or 16 bytes, any alignment), a ring of kKsStages slices.
+// Data-parallel: one tile per CTA, one CTA per SM.  Takes MidParams
+// (tiles_m, tiles_n, kt_total = ceil(K / kKsBK), group_m; the stream-K
+// fields are unused).
 // ---------------------------------------------------------------------------
 constexpr int kKsBM = 64;
-constexpr int kKsBN = 128;
 constexpr int kKsBK = 64;
-constexpr int kKsGroups = 4;
 constexpr int kKsStages = 4;
+constexpr int kKsThreads = 256;
 
-cudaError_t launch_ksplit(int b_vec, const MidParams &p, int grid, cudaStream_t stream);
-cudaError_t ksplit_configure(int b_vec);
+// b_vec: 4 (B 16-byte aligned, ldb % 4 == 0) or 1; bn: 128 or 64.
+cudaError_t launch_ksplit(int b_vec, int bn, const MidParams &p, int grid, cudaStream_t stream);
+cudaError_t ksplit_configure(int b_vec, int bn);
 
 // ---------------------------------------------------------------------------
 // Narrow kernel: N <= kNarrowMaxN columns (also the last few columns of C

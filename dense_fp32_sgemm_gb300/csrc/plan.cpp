@@ -71,16 +71,22 @@ constexpr KernelModel kMid64Model = {64, kMidBN, kMidBK, 4, {0, 1.0, 1.5, 2.65, 
 // 1024 x 1024 x 512 model.
 constexpr double kMidUnalignedB[5] = {1.06, 1.06, 1.06, 1.06, 1.06};
 constexpr double kMidUnalignedUnitUs = 3.5;
-// Split-K kernel: one 64 x 128 tile per CTA, one CTA per SM, slices of 64 k
-// (four groups of 16).  Per wave: a fixed part (first copies, the groups'
-// sums added through shared memory, the store) and K / 64 slices plus a
-// quarter slice for the rounding of the last one; measured 1024 x 1024 x 512
+// Split-K kernel: one 64 x 128 (or 64 x 64) tile per CTA, one CTA per SM,
+// slices of 64 k.  Per wave: a fixed part (first copies, the groups' sums
+// added through shared memory, the store) and K / 64 slices plus a quarter
+// slice for the rounding of the last one.  64 x 128 tiles: 1024 x 1024 x 512
 // 31.2-32.8 us, 1024^3 53.7-54.8 us, 768 x 768 x 4096 188 us, 1024 x 1024 x
 // 8192 367 us, 3000 x 300 x 5000 237 us; B in 4-byte copies (rows off 16
 // bytes) about 1.2x a slice (1023^3 65.5 us, 1023 x 1025 x 513 38-40 us).
+// 64 x 64 tiles: 128^3 12.3 us, 256^3 14.8, 384^3 18.4, 512^3 23.2, 640^3
+// 24.6, 768^3 28.7; with B in 4-byte copies 1.35x a slice (255^3 18.4 us,
+// 511^3 26.6 us).
 constexpr double kKsSliceUs = 2.8;
 constexpr double kKsFixedUs = 3.5;
 constexpr double kKsUnalignedB = 1.2;
+constexpr double kKsSliceUs64 = 1.75;
+constexpr double kKsFixedUs64 = 1.5;
+constexpr double kKsUnalignedB64 = 1.35;
 constexpr double kNoScale[5] = {1, 1, 1, 1, 1};
 // 64 x 64 kernel, one tile per CTA and 16-k slices: 0.78 us per slice at up to
 // one CTA per SM (128^3: 12.3 us; 512^3: 30.9 us), growing with the CTAs an
@@ -128,6 +134,7 @@ const char *variant_name(int v) {
         case kVarMid64: return "mid64";
         case kVarKsplit: return "ksplit";
         case kVarNarrow: return "narrow";
+        case kVarKsplit64: return "ksplit64";
         default: return "?";
     }
 }
@@ -262,10 +269,10 @@ static void plan_mid(const PlanInput &in, Plan *pl, int bm) {
 
 // The split-K kernel: one 64 x 128 tile per CTA over the whole K, in waves of
 // one CTA per SM.
-static void plan_ksplit(const PlanInput &in, Plan *pl) {
+static void plan_ksplit(const PlanInput &in, Plan *pl, int bn) {
     const int64_t sms = in.num_sms > 0 ? in.num_sms : 1;
     const bool b_ok = aligned16(in.b_addr) && in.ldb % 4 == 0;
-    const int64_t tm = ceil_div(in.M, kKsBM), tn = ceil_div(in.N, kKsBN);
+    const int64_t tm = ceil_div(in.M, kKsBM), tn = ceil_div(in.N, bn);
     const int64_t T = tm * tn;
     const int64_t KT = ceil_div(in.K, kKsBK);
     pl->variant = kVarKsplit;
@@ -279,12 +286,15 @@ static void plan_ksplit(const PlanInput &in, Plan *pl) {
     pl->grid = (int)T;
     pl->c_vec4 = (aligned16(in.c_addr) && in.ldc % 4 == 0) ? 1 : 0;
     pl->mid_bm = kKsBM;
+    pl->ks_bn = bn;
     pl->b_vec = b_ok ? 4 : 1;
     const int64_t waves = ceil_div(T, sms);
     const double slices = (double)in.K / kKsBK + 0.25;
     pl->cost = (double)waves * slices;
-    pl->est_us = kLaunchUs + (double)waves * (kKsFixedUs + slices * kKsSliceUs *
-                                                              (b_ok ? 1.0 : kKsUnalignedB));
+    const double slice_us = bn == 64 ? kKsSliceUs64 * (b_ok ? 1.0 : kKsUnalignedB64)
+                                     : kKsSliceUs * (b_ok ? 1.0 : kKsUnalignedB);
+    pl->est_us = kLaunchUs + (double)waves * ((bn == 64 ? kKsFixedUs64 : kKsFixedUs) +
+                                              slices * slice_us);
     pl->reason = "split-K inside the CTA";
 }
 
@@ -465,9 +475,10 @@ int make_plan(const PlanInput &in, Plan *pl) {
         *pl = p;
         return 0;
     }
-    if (want == kVarKsplit) {
-        if (ceil_div(in.M, kKsBM) * ceil_div(in.N, kKsBN) > INT32_MAX) return -2;
-        plan_ksplit(in, &p);
+    if (want == kVarKsplit || want == kVarKsplit64) {
+        const int bn = want == kVarKsplit64 ? 64 : 128;
+        if (ceil_div(in.M, kKsBM) * ceil_div(in.N, bn) > INT32_MAX) return -2;
+        plan_ksplit(in, &p, bn);
         *pl = p;
         return 0;
     }
@@ -524,7 +535,7 @@ int make_plan(const PlanInput &in, Plan *pl) {
     // copies of them unless M <= 32, where copying B would double the bytes
     // moved), the mid-size kernel with 128-row tiles and, for M <= 64, with
     // 64-row tiles, the split-K kernel and the 64 x 64 kernel.
-    Plan cand[7];
+    Plan cand[8];
     int n = 0;
     cand[n] = p;
     plan_mid(in, &cand[n++], 128);
@@ -532,9 +543,11 @@ int make_plan(const PlanInput &in, Plan *pl) {
         cand[n] = p;
         plan_narrow(in, &cand[n++]);
     }
-    if (ceil_div(in.M, kKsBM) * ceil_div(in.N, kKsBN) <= INT32_MAX) {
+    if (ceil_div(in.M, kKsBM) * ceil_div(in.N, 64) <= INT32_MAX) {
         cand[n] = p;
-        plan_ksplit(in, &cand[n++]);
+        plan_ksplit(in, &cand[n++], 128);
+        cand[n] = p;
+        plan_ksplit(in, &cand[n++], 64);
     }
     if (in.M <= 64) {
         cand[n] = p;
@@ -564,12 +577,12 @@ int describe_plan(const Plan &p, char *buf, size_t len) {
     return snprintf(buf, len,
                     "variant=%s tiles_m=%d tiles_n=%d kt=%d dp_tiles=%d sk_tiles=%d sk_share=%d "
                     "grid=%d group_m=%d c_vec4=%d m_tile=%d two_unit_ctas=%d pack_a=%d pack_b=%d "
-                    "bm=%d bvec=%d edge_m=%d edge_n=%d narrow_nn=%d narrow_rows=%d avec=%d "
+                    "bm=%d bvec=%d ks_bn=%d edge_m=%d edge_n=%d narrow_nn=%d narrow_rows=%d avec=%d "
                     "cost=%.2f est_us=%.1f alt_us=%.1f reason=%s",
                     variant_name(p.variant), p.tiles_m, p.tiles_n, p.kt_total, p.dp_tiles,
                     p.sk_tiles, p.sk_share, p.grid, p.group_m, p.c_vec4, p.m_tile,
                     p.variant == kVarSkinny ? p.sk_two_units : 0, p.pack_a ? 1 : 0,
-                    p.pack_b ? 1 : 0, p.mid_bm, p.b_vec, p.edge_m, p.edge_n, p.narrow_nn,
+                    p.pack_b ? 1 : 0, p.mid_bm, p.b_vec, p.ks_bn, p.edge_m, p.edge_n, p.narrow_nn,
                     p.narrow_rows, p.a_vec, p.cost, p.est_us, p.alt_us,
                     p.reason ? p.reason : "");
 }

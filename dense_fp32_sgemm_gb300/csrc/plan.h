@@ -19,6 +19,7 @@ enum Variant : int {
     kVarMid64 = 5,      // forced: the mid-size kernel with 64 x 128 tiles
     kVarKsplit = 6,     // split-K inside the CTA: 64 x 128 tiles, one per CTA
     kVarNarrow = 7,     // N <= kNarrowMaxN: a warp per row of A
+    kVarKsplit64 = 8,   // forced: the split-K kernel with 64 x 64 tiles
 };
 
 struct PlanInput {
@@ -45,6 +46,8 @@ struct Plan {
     // mid-size and split-K kernels: tile height (128 or 64) and B copy width
     // in floats (4 or 1)
     int mid_bm, b_vec;
+    // split-K kernel: tile width (128 or 64)
+    int ks_bn;
     // estimated time of the chosen plan (microseconds) and of the best other
     // candidate considered (0 when there was none)
     double est_us, alt_us;

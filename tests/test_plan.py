@@ -134,10 +134,11 @@ def narrow_invariants(p, M, N, K):
 
 
 def ksplit_invariants(p, M, N, K):
-    # one 64 x 128 tile per CTA over the whole K in 64-k slices
-    tm, tn, kt, dp, sk, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles", "sk_tiles", "grid")
-    assert p["bm"] == "64" and p["bvec"] in ("1", "4")
-    assert tm == math.ceil(M / 64) and tn == math.ceil(N / 128) and kt == math.ceil(K / 64)
+    # one 64 x bn tile per CTA (bn 128 or 64) over the whole K in 64-k slices
+    tm, tn, kt, dp, sk, grid, bn = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles", "sk_tiles",
+                                        "grid", "ks_bn")
+    assert p["bm"] == "64" and p["bvec"] in ("1", "4") and bn in (128, 64)
+    assert tm == math.ceil(M / 64) and tn == math.ceil(N / bn) and kt == math.ceil(K / 64)
     assert dp == tm * tn == grid and sk == 0
 
 
@@ -176,11 +177,12 @@ def test_plan_invariants(M, N, K):
             mid_invariants(plan(M, N, K), M, N, K)
         finally:
             sg.set_plan_override(-1, 0)
-    sg.set_plan_override(sg.VARIANT_KSPLIT, 0)
-    try:
-        ksplit_invariants(plan(M, N, K), M, N, K)
-    finally:
-        sg.set_plan_override(-1, 0)
+    for variant in (sg.VARIANT_KSPLIT, sg.VARIANT_KSPLIT64):
+        sg.set_plan_override(variant, 0)
+        try:
+            ksplit_invariants(plan(M, N, K), M, N, K)
+        finally:
+            sg.set_plan_override(-1, 0)
     p = plan(M, N, K)
     if p["variant"] in ("tile", "streamk"):
         tile_invariants(p, M, N, K)
@@ -196,21 +198,29 @@ def test_plan_invariants(M, N, K):
         assert p["variant"] == "generic"
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (129, 257, 33), (256, 256, 256),
-                                   (300, 520, 64)])
+@pytest.mark.parametrize("M,N,K", [(64, 64, 64), (129, 257, 33), (300, 520, 64)])
 def test_tiny_products_take_the_64x64_kernel(M, N, K):
-    # Measured on GB300: below about 512^3 the 64 x 64 kernel's short
-    # start-up wins (128^3: 12.5 us against 20.5 on the mid-size kernel).
+    # Measured on GB300: a few short slices per tile, where the 64 x 64
+    # kernel's short start-up wins.
     p = plan(M, N, K)
     assert p["variant"] == "generic" and p["reason"] == "64 x 64 tiles"
 
 
-@pytest.mark.parametrize("M,N,K", [(512, 512, 512), (640, 640, 640), (768, 768, 768),
-                                   (896, 896, 896)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 256, 256), (512, 512, 512),
+                                   (640, 640, 640), (768, 768, 768)])
+def test_small_products_take_64x64_split_k_tiles(M, N, K):
+    # Up to one wave of 64 x 64 tiles, eight warps splitting K inside each
+    # (512^3: 23.2 us against 29.3 on the mid-size kernel and 31.5 on the
+    # 64 x 64 kernel).
+    p = plan(M, N, K)
+    assert p["variant"] == "ksplit" and p["ks_bn"] == "64"
+    ksplit_invariants(p, M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(896, 896, 896), (100, 5000, 3000), (1400, 1300, 512)])
 def test_mid_size_products_take_the_mid_kernel(M, N, K):
-    # 128 x 128 tiles with a stream-K tail fill more SMs than 128 x 256 ones
-    # (768^3: 34.8 us against 51.2 on the tiled kernel, 43.0 on the split-K
-    # kernel, 44.5 on the 64 x 64 one).
+    # 128 x 128 tiles with a stream-K tail, where 64 x 64 tiles would take two
+    # waves (896^3: 47.1 us against 49.1 on the 64 x 128 split-K kernel).
     p = plan(M, N, K)
     assert p["variant"] == "mid" and p["bm"] == "128"
 
@@ -221,7 +231,8 @@ def test_one_wave_of_64x128_tiles_takes_the_split_k_kernel(M, N, K):
     # in global memory (1024^3: 54.8 us against 59.4 on the mid-size kernel,
     # 60.4 on the tiled kernel with a stream-K tail).
     p = plan(M, N, K)
-    assert p["variant"] == "ksplit" and ksplit_invariants(p, M, N, K) is None
+    assert p["variant"] == "ksplit" and p["ks_bn"] == "128"
+    ksplit_invariants(p, M, N, K)
 
 
 @pytest.mark.parametrize("M", [33, 48, 64])
