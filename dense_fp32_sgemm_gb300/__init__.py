@@ -23,7 +23,7 @@ __all__ = [
     "set_plan_override", "set_wait_timeout_ns", "set_tile_config",
     "release_workspace", "probe_ffma", "probe_read", "probe_hold", "probe_tf32", "EXPORTED_SYMBOLS",
     "VARIANT_AUTO", "VARIANT_GENERIC", "VARIANT_TILE", "VARIANT_STREAMK",
-    "VARIANT_SKINNY", "VARIANT_MID", "VARIANT_MID64", "VARIANT_KSPLIT", "VARIANT_NARROW", "VARIANT_KSPLIT64",
+    "VARIANT_SKINNY", "VARIANT_MID", "VARIANT_MID64", "VARIANT_KSPLIT", "VARIANT_NARROW", "VARIANT_KSPLIT64", "VARIANT_SMALL",
     "STATUS",
 ]
 
@@ -34,6 +34,7 @@ STATUS = {
 }
 VARIANT_AUTO, VARIANT_GENERIC, VARIANT_TILE, VARIANT_STREAMK, VARIANT_SKINNY = -1, 0, 1, 2, 3
 VARIANT_MID, VARIANT_MID64, VARIANT_KSPLIT, VARIANT_NARROW, VARIANT_KSPLIT64 = 4, 5, 6, 7, 8
+VARIANT_SMALL = 9
 ACT_NONE, ACT_RELU = 0, 1
 
 _i64, _f32, _vp, _int = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int

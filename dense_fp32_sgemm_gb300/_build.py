@@ -21,7 +21,7 @@ LIB_NAME = "libsgemm_gb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
 SOURCES = ["api.cu", "plan.cpp", "kernel_tile.cu", "kernel_skinny.cu", "kernel_generic.cu", "kernel_mid.cu",
-           "kernel_ksplit.cu", "kernel_narrow.cu", "probes.cu", "noalloc.cu", "kernel_3xtf32.cu"]
+           "kernel_ksplit.cu", "kernel_narrow.cu", "kernel_small.cu", "probes.cu", "noalloc.cu", "kernel_3xtf32.cu"]
 HEADERS = ["device_common.cuh", "kernels.h", "kernels_3xtf32.h", "plan.h"]
 PUBLIC_HEADERS = ["sgemm.h", "sgemm_probe.h"]
 

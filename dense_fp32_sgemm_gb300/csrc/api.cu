@@ -438,6 +438,23 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             }
             return status_from(launch_mid(pl.mid_bm, pl.b_vec, mp, pl.grid, stream));
         }
+        case kVarSmall: {
+            const int key = 3000 + pl.b_vec;
+            if (!d.configured_tiles.count(key)) {
+                if (small_configure(pl.b_vec) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+                d.configured_tiles.insert(key);
+            }
+            MidParams mp = {};
+            mp.M = (int)M; mp.N = (int)N; mp.K = (int)K;
+            mp.tiles_m = pl.tiles_m; mp.tiles_n = pl.tiles_n; mp.kt_total = pl.kt_total;
+            mp.dp_tiles = pl.dp_tiles; mp.sk_tiles = 0; mp.sk_share = 1;
+            mp.group_m = 1;
+            mp.alpha = alpha; mp.beta = beta;
+            mp.A = A; mp.lda = lda; mp.B = B; mp.ldb = ldb; mp.C = C; mp.ldc = ldc;
+            mp.c_vec4 = pl.c_vec4;
+            mp.epi = epi;
+            return status_from(launch_small(pl.b_vec, mp, pl.grid, stream));
+        }
         case kVarKsplit:
         case kVarKsplit64: {
             const int key = 2000 + pl.ks_bn * 10 + pl.b_vec;
@@ -871,7 +888,7 @@ sgemm_status_t sgemm_plan_describe_3xtf32(int64_t M, int64_t N, int64_t K, int64
 }
 
 sgemm_status_t sgemm_set_plan_override(int variant, int splits) {
-    if (variant < -1 || variant > SGEMM_VARIANT_KSPLIT64 || splits < 0) return SGEMM_ERR_INVALID_ARG;
+    if (variant < -1 || variant > SGEMM_VARIANT_SMALL || splits < 0) return SGEMM_ERR_INVALID_ARG;
     g_force_variant.store(variant);
     g_force_splits.store(splits);
     return SGEMM_OK;

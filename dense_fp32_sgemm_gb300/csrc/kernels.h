@@ -177,6 +177,23 @@ struct NarrowParams {
 
 cudaError_t launch_narrow(int nn, int a_vec, const NarrowParams &p, int grid, cudaStream_t stream);
 
+// ---------------------------------------------------------------------------
+// Small-product kernel: one CTA of 256 threads per 32 x 32 tile, four groups
+// of 64 threads each taking a quarter of every kSmallBK-k slice (4 x 4 sums
+// per thread), sums added in shared memory in group order; a 3-stage cp.async
+// ring of 16 KiB slices, up to four CTAs per SM.  Takes MidParams (tiles_m,
+// tiles_n, kt_total = ceil(K / kSmallBK); tile t is row t / tiles_n, column
+// t % tiles_n).
+// ---------------------------------------------------------------------------
+constexpr int kSmallBM = 32;
+constexpr int kSmallBN = 32;
+constexpr int kSmallBK = 64;
+constexpr int kSmallStages = 3;
+constexpr int kSmallCtasPerSm = 4;
+
+cudaError_t launch_small(int b_vec, const MidParams &p, int grid, cudaStream_t stream);
+cudaError_t small_configure(int b_vec);
+
 // Copies of operands the TMA cannot map: rows x cols at src (leading
 // dimension ld, any 4-byte alignment) to dst with 16-byte-aligned rows of
 // ldp floats (ldp a multiple of 4, dst 16-byte aligned).  Up to two copies in

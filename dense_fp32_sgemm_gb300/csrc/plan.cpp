@@ -135,6 +135,7 @@ const char *variant_name(int v) {
         case kVarKsplit: return "ksplit";
         case kVarNarrow: return "narrow";
         case kVarKsplit64: return "ksplit64";
+        case kVarSmall: return "small";
         default: return "?";
     }
 }
@@ -339,6 +340,43 @@ static void plan_narrow(const PlanInput &in, Plan *pl) {
     pl->reason = "narrow N: stream A once";
 }
 
+// The small-product kernel: one 32 x 32 tile per CTA, up to
+// kSmallCtasPerSm CTAs per SM; each wave costs K / 64 slices (plus a quarter
+// for the rounding of the last) at the time of one slice with that wave's
+// CTAs per SM, fitted on GB300: 128^3 8.2 us, 256^3 10.2, 384^3 11.7 (one
+// CTA per SM), 512^3 18.4 (two), 640^3 27.0, 600 x 600 x 2000 72.4 (three),
+// 768^3 38.9, 128 x 4096 x 1024 49.9 (four), 1024^3 82.4 (four, then three).
+constexpr double kSmallFixedUs = 0.3;
+constexpr double kSmallSliceUs[kSmallCtasPerSm + 1] = {0, 0.87, 1.5, 2.07, 2.7};
+constexpr double kSmallUnalignedB = 1.2;
+
+static void plan_small(const PlanInput &in, Plan *pl) {
+    const int64_t sms = in.num_sms > 0 ? in.num_sms : 1;
+    const bool b_ok = aligned16(in.b_addr) && in.ldb % 4 == 0;
+    const int64_t tm = ceil_div(in.M, kSmallBM), tn = ceil_div(in.N, kSmallBN);
+    const int64_t T = tm * tn;
+    pl->variant = kVarSmall;
+    pl->tiles_m = (int)tm;
+    pl->tiles_n = (int)tn;
+    pl->kt_total = (int)ceil_div(in.K, kSmallBK);
+    pl->group_m = 1;
+    pl->dp_tiles = (int)T;
+    pl->sk_tiles = 0;
+    pl->sk_share = 1;
+    pl->grid = (int)T;
+    pl->c_vec4 = (aligned16(in.c_addr) && in.ldc % 4 == 0) ? 1 : 0;
+    pl->b_vec = b_ok ? 4 : 1;
+    const int64_t per_wave = sms * kSmallCtasPerSm;
+    const int64_t full = T / per_wave, rem = T % per_wave;
+    const double slices = (double)in.K / kSmallBK + 0.25;
+    const double scale = b_ok ? 1.0 : kSmallUnalignedB;
+    double t = (double)full * (kSmallFixedUs + slices * kSmallSliceUs[kSmallCtasPerSm] * scale);
+    if (rem > 0) t += kSmallFixedUs + slices * kSmallSliceUs[ceil_div(rem, sms)] * scale;
+    pl->cost = (double)(full + (rem > 0)) * slices;
+    pl->est_us = kLaunchUs + t;
+    pl->reason = "32 x 32 tiles, split K inside the CTA";
+}
+
 // The 64 x 64 kernel: one tile per CTA over the whole K.
 static void plan_generic(const PlanInput &in, Plan *pl) {
     const int64_t sms = in.num_sms > 0 ? in.num_sms : 1;
@@ -414,7 +452,11 @@ int make_plan(const PlanInput &in, Plan *pl) {
     // bound by streaming B (M <= 16) or close to it; a tile of 64 or 128 rows
     // would spend 2-8x the multiply-adds (measured, 32 x 8192 x 8192: see the
     // planner sweep).
-    if (tma_ok && (want == kVarSkinny || (want < 0 && in.M <= kSkinnyMaxM))) {
+    // Below about 2^20 elements of B the skinny kernel's start-up and fix-up
+    // outweigh the streaming (32 x 32 x 32: 14.7 us against 6.9 on the
+    // small-product kernel), so the time model chooses there.
+    const bool big_b = in.N * in.K >= (int64_t(1) << 20);
+    if (tma_ok && (want == kVarSkinny || (want < 0 && in.M <= kSkinnyMaxM && big_b))) {
         // Persistent grid: every CTA the SMs hold at once.
         int64_t G = (in.num_sms > 0 ? in.num_sms : 1) * kSkinnyCtasPerSm;
         if (G > kSkinnyMaxGrid) G = kSkinnyMaxGrid;
@@ -466,6 +508,12 @@ int make_plan(const PlanInput &in, Plan *pl) {
     }
     if (want == kVarMid || want == kVarMid64) {
         plan_mid(in, &p, want == kVarMid64 ? 64 : 128);
+        *pl = p;
+        return 0;
+    }
+    if (want == kVarSmall) {
+        if (ceil_div(in.M, kSmallBM) * ceil_div(in.N, kSmallBN) > INT32_MAX) return -2;
+        plan_small(in, &p);
         *pl = p;
         return 0;
     }
@@ -535,7 +583,7 @@ int make_plan(const PlanInput &in, Plan *pl) {
     // copies of them unless M <= 32, where copying B would double the bytes
     // moved), the mid-size kernel with 128-row tiles and, for M <= 64, with
     // 64-row tiles, the split-K kernel and the 64 x 64 kernel.
-    Plan cand[8];
+    Plan cand[9];
     int n = 0;
     cand[n] = p;
     plan_mid(in, &cand[n++], 128);
@@ -548,6 +596,10 @@ int make_plan(const PlanInput &in, Plan *pl) {
         plan_ksplit(in, &cand[n++], 128);
         cand[n] = p;
         plan_ksplit(in, &cand[n++], 64);
+    }
+    if (ceil_div(in.M, kSmallBM) * ceil_div(in.N, kSmallBN) <= INT32_MAX) {
+        cand[n] = p;
+        plan_small(in, &cand[n++]);
     }
     if (in.M <= 64) {
         cand[n] = p;

@@ -20,6 +20,7 @@ enum Variant : int {
     kVarKsplit = 6,     // split-K inside the CTA: 64 x 128 tiles, one per CTA
     kVarNarrow = 7,     // N <= kNarrowMaxN: a warp per row of A
     kVarKsplit64 = 8,   // forced: the split-K kernel with 64 x 64 tiles
+    kVarSmall = 9,      // 32 x 32 tiles, split K inside the CTA, small products
 };
 
 struct PlanInput {

@@ -27,7 +27,7 @@ DEFAULT_SIZES = [256, 511, 512, 513, 1023, 1024, 1025, 1535, 1536, 2047, 2048, 2
 CANDIDATES = [("auto", sg.VARIANT_AUTO), ("tile", sg.VARIANT_TILE),
               ("streamk", sg.VARIANT_STREAMK), ("mid", sg.VARIANT_MID),
               ("mid64", sg.VARIANT_MID64), ("ksplit", sg.VARIANT_KSPLIT),
-              ("ksplit64", sg.VARIANT_KSPLIT64),
+              ("ksplit64", sg.VARIANT_KSPLIT64), ("small", sg.VARIANT_SMALL),
               ("generic", sg.VARIANT_GENERIC)]
 
 

@@ -220,7 +220,8 @@ enum {
     SGEMM_VARIANT_KSPLIT = 6,    /* cp.async + FFMA2 64x128 tile per CTA, K split     */
                                  /* over four warp groups inside the CTA              */
     SGEMM_VARIANT_NARROW = 7,    /* N <= 4: a warp per row of A (A x products)        */
-    SGEMM_VARIANT_KSPLIT64 = 8   /* the split-K kernel with 64x64 tiles (8 k-groups)   */
+    SGEMM_VARIANT_KSPLIT64 = 8,  /* the split-K kernel with 64x64 tiles (8 k-groups)   */
+    SGEMM_VARIANT_SMALL = 9      /* 32x32 tiles, K split over four thread groups      */
 };
 SGEMM_API sgemm_status_t sgemm_set_plan_override(int variant, int splits);
 

@@ -115,7 +115,7 @@ def test_probe_argument_checks(lib):
 
 def test_hooks_validate(lib):
     with pytest.raises(sg.SgemmError):
-        sg.set_plan_override(sg.VARIANT_KSPLIT64 + 1, 0)
+        sg.set_plan_override(sg.VARIANT_SMALL + 1, 0)
     with pytest.raises(sg.SgemmError):
         sg.set_tile_config(2, 4, 16)
     with pytest.raises(sg.SgemmError):

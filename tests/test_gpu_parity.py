@@ -94,7 +94,8 @@ def test_cublas_fp32_meets_the_same_bound():
 # ----- exact integer inputs: every variant must be bit-exact ---------------------
 
 @pytest.mark.parametrize("variant,splits", [(0, 0), (1, 0), (2, 2), (2, 3), (2, 4), (-1, 0),
-                                            (4, 0), (4, 2), (4, 3), (5, 0), (5, 4), (6, 0), (8, 0)])
+                                            (4, 0), (4, 2), (4, 3), (5, 0), (5, 4), (6, 0), (8, 0),
+                                            (9, 0)])
 @pytest.mark.parametrize("M,N,K", [(64, 64, 64), (300, 520, 64), (129, 257, 40)])
 def test_small_integers_bit_exact(variant, splits, M, N, K):
     Kp = (K + 3) // 4 * 4
@@ -115,8 +116,9 @@ SIZES = [1, 3, 8, 31, 33, 127, 129, 255, 257]
 
 # Automatic plan, the tiled kernel whole (1) and split (2), the mid-size
 # kernel with 128-row (4) and 64-row (5) tiles and the split-K kernel (6) on
-# the same edges (8: the split-K kernel with 64-column tiles).
-@pytest.mark.parametrize("variant", [-1, 1, 2, 4, 5, 6, 8])
+# the same edges (8: the split-K kernel with 64-column tiles; 9: the small-
+# product kernel).
+@pytest.mark.parametrize("variant", [-1, 1, 2, 4, 5, 6, 8, 9])
 @pytest.mark.parametrize("M", [1, 33, 129, 257])
 @pytest.mark.parametrize("N", [1, 31, 255, 257])
 @pytest.mark.parametrize("K", [1, 8, 127])
@@ -126,14 +128,14 @@ def test_ragged_shapes_aligned_ld(M, N, K, variant):
           variant=variant)
 
 
-@pytest.mark.parametrize("variant", [-1, 0, 4, 5, 6, 8])
+@pytest.mark.parametrize("variant", [-1, 0, 4, 5, 6, 8, 9])
 @pytest.mark.parametrize("M,N,K", [(3, 5, 7), (33, 255, 31), (257, 129, 127), (130, 300, 65)])
 def test_ragged_shapes_odd_ld(M, N, K, variant):
     check(M, N, K, 1.0, 0.0, dist="uniform", seed=5, lda=K + 1, ldb=N + 3, ldc=N + 5,
           variant=variant)
 
 
-@pytest.mark.parametrize("variant", [-1, 0, 4, 5, 6, 8])
+@pytest.mark.parametrize("variant", [-1, 0, 4, 5, 6, 8, 9])
 @pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 1)])
 def test_misaligned_pointers(offsets, variant):
     check(200, 300, 100, 1.0, 1.0, seed=6, offsets=offsets, lda=104, ldb=300, ldc=300,
@@ -143,7 +145,7 @@ def test_misaligned_pointers(offsets, variant):
 # ----- the mid-size kernel: any alignment, copies of 4 or 16 bytes -------------
 
 @pytest.mark.parametrize("variant,splits", [(4, 0), (4, 2), (4, 5), (5, 0), (5, 3), (6, 0),
-                                            (8, 0)])
+                                            (8, 0), (9, 0)])
 @pytest.mark.parametrize("offsets,lds", [
     ((0, 0, 0), (516, 1028, 1028)),      # aligned: 16-byte copies of B
     ((1, 0, 0), (513, 1028, 1025)),      # A and C unaligned, B aligned
@@ -162,7 +164,7 @@ def test_mid_kernel_any_alignment_integers_bit_exact(variant, splits, offsets, l
     assert np.array_equal(out.astype(np.int64), want)
 
 
-@pytest.mark.parametrize("variant", [4, 5, 6, 8])
+@pytest.mark.parametrize("variant", [4, 5, 6, 8, 9])
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 4097, 3), (65, 129, 17), (128, 128, 16),
                                    (200, 2000, 1500), (17, 8192, 4096), (3000, 300, 5000)])
 def test_mid_kernel_floats_within_bound(variant, M, N, K):
@@ -179,7 +181,7 @@ def test_mid_kernel_stream_k_is_bitwise_deterministic():
         assert np.array_equal(first, again)
 
 
-@pytest.mark.parametrize("variant", [6, 8])
+@pytest.mark.parametrize("variant", [6, 8, 9])
 def test_split_k_kernel_is_bitwise_deterministic(variant):
     # The groups' sums are added in group order, whatever the timing.
     M, N, K = 1000, 1100, 2500
@@ -190,7 +192,7 @@ def test_split_k_kernel_is_bitwise_deterministic(variant):
         assert np.array_equal(first, again)
 
 
-@pytest.mark.parametrize("variant", [6, 8])
+@pytest.mark.parametrize("variant", [6, 8, 9])
 @pytest.mark.parametrize("K", [1, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 129])
 def test_split_k_kernel_every_k_remainder(K, variant):
     # Each k-group takes 16 (eight groups: 8) of every 64-k slice; in the last
@@ -470,6 +472,7 @@ EPI_CASES = [  # (M, N, K, variant, splits): every kernel and the alpha == 0 pat
     (257, 1030, 2048, -1, 0), (9, 1030, 1000, 3, 0), (16, 1024, 96, 3, 2),
     (300, 520, 256, 4, 0), (301, 1030, 700, 4, 3), (40, 1030, 500, 5, 2),
     (300, 520, 256, 6, 0), (1023, 1030, 513, 6, 0), (300, 520, 256, 8, 0), (129, 70, 70, 8, 0),
+    (130, 300, 96, 9, 0), (33, 65, 200, 9, 0),
 ]
 
 
@@ -597,7 +600,7 @@ def test_skinny_wait_timeout_reports_and_recovers(M):
                                            (300, 520, 200, 0), (1023, 1025, 513, 4),
                                            (700, 900, 3000, 5), (1023, 1025, 513, 6),
                                            (2049, 2049, 1000, -1), (3000, 3, 1000, 7),
-                                           (513, 515, 500, 8)])
+                                           (513, 515, 500, 8), (200, 300, 150, 9)])
 def test_capture_in_a_cuda_graph_and_replay(M, N, K, variant):
     # After a first call has set up the stream's workspace, sgemm_run queues
     # kernels only (no allocation, no host synchronisation), so it can be

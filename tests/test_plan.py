@@ -125,6 +125,13 @@ def tile_invariants(p, M, N, K, forced_sk=False):
         assert float(p["cost"]) <= math.ceil(T / SMS) * kt + 1e-9
 
 
+def small_invariants(p, M, N, K):
+    # one 32 x 32 tile per CTA over the whole K in 64-k slices
+    tm, tn, kt, dp, sk, grid = ints(p, "tiles_m", "tiles_n", "kt", "dp_tiles", "sk_tiles", "grid")
+    assert tm == math.ceil(M / 32) and tn == math.ceil(N / 32) and kt == math.ceil(K / 64)
+    assert dp == tm * tn == grid and sk == 0 and p["bvec"] in ("1", "4")
+
+
 def narrow_invariants(p, M, N, K):
     # N <= 4; contiguous row ranges covering M once, at most two CTAs per SM
     grid, rows, nn = ints(p, "grid", "narrow_rows", "narrow_nn")
@@ -183,6 +190,11 @@ def test_plan_invariants(M, N, K):
             ksplit_invariants(plan(M, N, K), M, N, K)
         finally:
             sg.set_plan_override(-1, 0)
+    sg.set_plan_override(sg.VARIANT_SMALL, 0)
+    try:
+        small_invariants(plan(M, N, K), M, N, K)
+    finally:
+        sg.set_plan_override(-1, 0)
     p = plan(M, N, K)
     if p["variant"] in ("tile", "streamk"):
         tile_invariants(p, M, N, K)
@@ -194,24 +206,28 @@ def test_plan_invariants(M, N, K):
         assert M <= 32
     elif p["variant"] == "narrow":
         narrow_invariants(p, M, N, K)
+    elif p["variant"] == "small":
+        small_invariants(p, M, N, K)
     else:
         assert p["variant"] == "generic"
 
 
-@pytest.mark.parametrize("M,N,K", [(64, 64, 64), (129, 257, 33), (300, 520, 64)])
-def test_tiny_products_take_the_64x64_kernel(M, N, K):
-    # Measured on GB300: a few short slices per tile, where the 64 x 64
-    # kernel's short start-up wins.
+@pytest.mark.parametrize("M,N,K", [(64, 64, 64), (129, 257, 33), (300, 520, 64), (128, 128, 128),
+                                   (256, 256, 256), (512, 512, 512), (32, 32, 32)])
+def test_small_products_take_the_32x32_kernel(M, N, K):
+    # Measured on GB300: 32 x 32 tiles spread small products over the most
+    # SMs, four CTAs to an SM (128^3: 8.2 us against 12.3 on 64 x 64 split-K
+    # tiles and 12.6 on the 64 x 64 kernel; 512^3: 18.4 against 22.5).
     p = plan(M, N, K)
-    assert p["variant"] == "generic" and p["reason"] == "64 x 64 tiles"
+    assert p["variant"] == "small"
+    small_invariants(p, M, N, K)
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 256, 256), (512, 512, 512),
-                                   (640, 640, 640), (768, 768, 768)])
+@pytest.mark.parametrize("M,N,K", [(640, 640, 640), (768, 768, 768), (128, 4096, 1024)])
 def test_small_products_take_64x64_split_k_tiles(M, N, K):
-    # Up to one wave of 64 x 64 tiles, eight warps splitting K inside each
-    # (512^3: 23.2 us against 29.3 on the mid-size kernel and 31.5 on the
-    # 64 x 64 kernel).
+    # From about four 32 x 32 tiles per SM, 64 x 64 tiles with eight warps
+    # splitting K (768^3: 28.7 us against 38.9 on 32 x 32 tiles and 34.8 on
+    # the mid-size kernel).
     p = plan(M, N, K)
     assert p["variant"] == "ksplit" and p["ks_bn"] == "64"
     ksplit_invariants(p, M, N, K)
@@ -296,7 +312,7 @@ def test_forced_generic():
 UNIT_END = 6  # positions a range pays for each slab boundary it crosses
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 8192, 8192), (1, 4096, 4096), (9, 300, 72),
+@pytest.mark.parametrize("M,N,K", [(16, 8192, 8192), (1, 4096, 4096), (9, 3000, 720),
                                    (8, 100000, 64), (16, 10240, 320), (32, 8192, 8192),
                                    (20, 3000, 500)])
 def test_skinny_plan(M, N, K):
@@ -415,8 +431,8 @@ def test_random_plans_cover_the_work():
     for M, N, K in _random_shapes(11, 300):
         p = plan(M, N, K)
         v = p["variant"]
-        assert v in ("tile", "streamk", "mid", "ksplit", "narrow", "generic", "skinny", "scale",
-                     "none"), (M, N, K, v)
+        assert v in ("tile", "streamk", "mid", "ksplit", "narrow", "small", "generic", "skinny",
+                     "scale", "none"), (M, N, K, v)
         if v in ("tile", "streamk"):
             tile_invariants(p, M, N, K)
         elif v == "mid":
@@ -425,6 +441,8 @@ def test_random_plans_cover_the_work():
             ksplit_invariants(p, M, N, K)
         elif v == "narrow":
             narrow_invariants(p, M, N, K)
+        elif v == "small":
+            small_invariants(p, M, N, K)
         elif v == "skinny":
             assert M <= 32
             slabs, kt, grid = ints(p, "tiles_n", "kt", "grid")
