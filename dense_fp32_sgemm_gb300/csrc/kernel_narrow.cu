@@ -13,12 +13,15 @@
 // (b[j][k]), all of K at once when it fits (else in chunks), and read back
 // with 128-bit loads.
 //
-// A CTA of 8 warps owns a contiguous range of rows and walks it in passes of
-// eight rows; a pass walks K in steps of 1024, each lane's loads of the next
-// step in flight while the current one is multiplied (32 values of A a
-// lane; loads issued one 128-k group at a time and waited for before the
-// next read 2.7 TB/s at 8192 x 1 x 8192).  Barriers come only where a new
-// chunk of B is staged.  A lane keeps N sums over its k (in increasing k), and the
+// A CTA of 8 warps owns a contiguous range of rows, taken in groups of up to
+// four passes of eight; for each staged chunk of B every pass of a group
+// walks the chunk in steps of 1024 k, each lane's loads of the next step in flight
+// while the current one is multiplied (32 values of A a lane; loads issued
+// one 128-k group at a time and waited for before the next read 2.7 TB/s at
+// 8192 x 1 x 8192).  Barriers come only where a new chunk of B is staged: once
+// per CTA when K fits one chunk, else once per chunk and group (staging per
+// pass read 110 us at 8192 x 4 x 8192); a lane's k are the same, and taken in
+// the same order, however K is chunked.  A lane keeps N sums over its k (in increasing k), and the
 // warp adds its lanes' sums with a fixed butterfly of shuffles, so the result
 // does not depend on timing.  No CTA depends on another.
 
@@ -75,6 +78,8 @@ __device__ __forceinline__ void narrow_stage_b(const NarrowParams &p, float *bs,
     }
 }
 
+constexpr int PMAX = 4;  // passes of eight rows that share one staging of B
+
 template <int NN, int AVEC>
 __global__ void __launch_bounds__(NTH) sgemm_narrow_kernel(const __grid_constant__ NarrowParams p) {
     extern __shared__ __align__(16) float bs[];  // bs[j * (kch + 4) + kk] = B[k0 + kk][j]
@@ -84,24 +89,37 @@ __global__ void __launch_bounds__(NTH) sgemm_narrow_kernel(const __grid_constant
     const int kch = p.kch;
     const int chunks = (p.K + kch - 1) / kch;
     const int brow = kch + 4;
-    // One chunk (K <= kch): B is staged once for every pass of the CTA.
+    // One chunk (K <= kch): B is staged once for every row of the CTA.
     if (chunks == 1) {
         narrow_stage_b<NN>(p, bs, 0, kch);
         __syncthreads();
     }
 
+    // Groups of up to PMAX passes of eight rows (uniform over the CTA).
 #pragma unroll 1
-    for (long long base = r0; base < r1; base += NW) {  // uniform over the CTA
-        const long long row = base + warp;
-        const bool active = row < r1;
-        const float *arow = p.A + (active ? row : r0) * p.lda;
-        float acc[NN];
+    for (long long g0 = r0; g0 < r1; g0 += PMAX * NW) {
+        const int npass = (int)min((long long)PMAX, (r1 - g0 + NW - 1) / NW);
+        // Pass ps takes row g0 + 8 ps + warp of this warp.
+        const float *arow[PMAX];
+        bool act[PMAX];
 #pragma unroll
-        for (int j = 0; j < NN; ++j) acc[j] = 0.0f;
-        // Steps of STEP k; the next step's loads are issued before this
-        // step's multiply-adds (and before a chunk's barriers and staging).
+        for (int ps = 0; ps < PMAX; ++ps) {
+            const long long row = g0 + ps * NW + warp;
+            act[ps] = ps < npass && row < r1;
+            arow[ps] = p.A + (act[ps] ? row : r0) * p.lda;
+        }
+        float acc[PMAX][NN];
+#pragma unroll
+        for (int ps = 0; ps < PMAX; ++ps)
+#pragma unroll
+            for (int j = 0; j < NN; ++j) acc[ps][j] = 0.0f;
+
+        // Steps of STEP k: for every chunk of B, every pass walks the chunk;
+        // the next step's loads are issued before this step's multiply-adds
+        // (and before a chunk's barriers and staging), so B is staged once
+        // per chunk for the group's rows.
         float4 a_next[KI];
-        if (active) narrow_load_a<AVEC>(arow, min(STEP, min(kch, p.K)), lane, a_next);
+        if (act[0]) narrow_load_a<AVEC>(arow[0], min(STEP, min(kch, p.K)), lane, a_next);
 
 #pragma unroll 1
         for (int c = 0; c < chunks; ++c) {
@@ -112,52 +130,66 @@ __global__ void __launch_bounds__(NTH) sgemm_narrow_kernel(const __grid_constant
                 narrow_stage_b<NN>(p, bs, k0, kch);
                 __syncthreads();
             }
+#pragma unroll
+            for (int ps = 0; ps < PMAX; ++ps) {
+                if (ps >= npass) break;  // uniform over the CTA
 #pragma unroll 1
-            for (int s0 = 0; s0 < kn; s0 += STEP) {
-                float4 a[KI];
+                for (int s0 = 0; s0 < kn; s0 += STEP) {
+                    float4 a[KI];
 #pragma unroll
-                for (int i = 0; i < KI; ++i) a[i] = a_next[i];
-                if (active) {
-                    if (s0 + STEP < kn)
-                        narrow_load_a<AVEC>(arow + k0 + s0 + STEP, min(STEP, kn - s0 - STEP), lane,
-                                            a_next);
-                    else if (c + 1 < chunks)
-                        narrow_load_a<AVEC>(arow + k0 + kch, min(STEP, min(kch, p.K - k0 - kch)),
-                                            lane, a_next);
+                    for (int i = 0; i < KI; ++i) a[i] = a_next[i];
+                    if (s0 + STEP < kn) {
+                        if (act[ps])
+                            narrow_load_a<AVEC>(arow[ps] + k0 + s0 + STEP,
+                                                min(STEP, kn - s0 - STEP), lane, a_next);
+                    } else if (ps + 1 < npass) {
+                        if (ps + 1 < PMAX && act[ps + 1])
+                            narrow_load_a<AVEC>(arow[ps + 1] + k0, min(STEP, kn), lane, a_next);
+                    } else if (c + 1 < chunks) {
+                        if (act[0])
+                            narrow_load_a<AVEC>(arow[0] + k0 + kch,
+                                                min(STEP, min(kch, p.K - k0 - kch)), lane, a_next);
+                    }
+                    if (act[ps]) {
 #pragma unroll
-                    for (int i = 0; i < KI; ++i) {
-                        // Groups past the chunk's end hold zeros of A; they
-                        // are skipped (uniform over the warp), so that every
-                        // read of bs stays inside row j of the chunk.
-                        if (s0 + 128 * i >= kn) break;
-                        const int kk = s0 + 4 * lane + 128 * i;
+                        for (int i = 0; i < KI; ++i) {
+                            // Groups past the chunk's end hold zeros of A;
+                            // they are skipped (uniform over the warp), so
+                            // that every read of bs stays inside row j.
+                            if (s0 + 128 * i >= kn) break;
+                            const int kk = s0 + 4 * lane + 128 * i;
 #pragma unroll
-                        for (int j = 0; j < NN; ++j) {
-                            const float4 b = ld_shared_f4(bs + j * brow + kk);
-                            acc[j] = __fmaf_rn(a[i].x, b.x, acc[j]);
-                            acc[j] = __fmaf_rn(a[i].y, b.y, acc[j]);
-                            acc[j] = __fmaf_rn(a[i].z, b.z, acc[j]);
-                            acc[j] = __fmaf_rn(a[i].w, b.w, acc[j]);
+                            for (int j = 0; j < NN; ++j) {
+                                const float4 b = ld_shared_f4(bs + j * brow + kk);
+                                acc[ps][j] = __fmaf_rn(a[i].x, b.x, acc[ps][j]);
+                                acc[ps][j] = __fmaf_rn(a[i].y, b.y, acc[ps][j]);
+                                acc[ps][j] = __fmaf_rn(a[i].z, b.z, acc[ps][j]);
+                                acc[ps][j] = __fmaf_rn(a[i].w, b.w, acc[ps][j]);
+                            }
                         }
                     }
                 }
             }
         }
-        // The lanes' sums, added by a fixed butterfly (every lane ends with
-        // the same total).
+        // Per row: the lanes' sums added by a fixed butterfly (every lane
+        // ends with the same total); lane j stores column j.
 #pragma unroll
-        for (int j = 0; j < NN; ++j)
+        for (int ps = 0; ps < PMAX; ++ps) {
+            if (ps >= npass) break;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
-        // Lane j stores column j.
-        float mine = acc[0];
+            for (int j = 0; j < NN; ++j)
 #pragma unroll
-        for (int j = 1; j < NN; ++j) mine = lane == j ? acc[j] : mine;
-        if (active && lane < NN && lane < p.N) {
-            float *c = p.C + row * p.ldc + lane;
-            float v = p.alpha * mine;
-            if (p.beta != 0.0f) v = __fmaf_rn(p.beta, *c, v);
-            *c = apply_epilogue(v, p.epi, lane);
+                for (int off = 16; off > 0; off >>= 1)
+                    acc[ps][j] += __shfl_xor_sync(0xffffffffu, acc[ps][j], off);
+            float mine = acc[ps][0];
+#pragma unroll
+            for (int j = 1; j < NN; ++j) mine = lane == j ? acc[ps][j] : mine;
+            if (act[ps] && lane < NN && lane < p.N) {
+                float *c = p.C + (g0 + ps * NW + warp) * p.ldc + lane;
+                float v = p.alpha * mine;
+                if (p.beta != 0.0f) v = __fmaf_rn(p.beta, *c, v);
+                *c = apply_epilogue(v, p.epi, lane);
+            }
         }
     }
 }
