@@ -50,6 +50,8 @@ WORKLOADS = {
     "s6_skinny": "sgemm 16x8192x8192 fp32 row-major alpha=1 beta=0 A,B U[-1,1)",
     "s1_128": "sgemm 128x128x128 fp32 row-major alpha=1 beta=0 A,B U[-1,1)",
     "s7_gemv": "sgemm 1x8192x8192 fp32 row-major alpha=1 beta=0 A,B U[-1,1) (GEMV)",
+    "s8_2049": "sgemm 2049x2049x2049 fp32 row-major alpha=1 beta=0 A,B U[-1,1)",
+    "s9_ax": "sgemm 8192x1x8192 fp32 row-major alpha=1 beta=0 A,B U[-1,1) (A x)",
 }
 METRIC = "SGEMM GFLOP/s at 4092^3 and 2048^3 FP32; % of GB300 FP32 FFMA peak"
 FP32_LANES_PER_SM = 128
@@ -525,7 +527,8 @@ def gpu_arm(args, ws, rank, local):
     # ---- the other workloads, timed the same way (fewer steps) ----
     if not args.no_secondary:
         others = []
-        for other in ("s3_4092", "s4_rect", "s5_odd", "s6_skinny", "s7_gemv", "s1_128"):
+        for other in ("s3_4092", "s4_rect", "s5_odd", "s6_skinny", "s7_gemv", "s1_128", "s8_2049",
+                      "s9_ax"):
             if other == name:
                 continue
             cfgo, _, _, _, dAo, dBo, dCo = device_inputs(other)
@@ -538,7 +541,7 @@ def gpu_arm(args, ws, rank, local):
                    "value": round(flops_of(cfgo) / mo / 1e9, 2), "unit": "GFLOP/s",
                    "ms_per_step": round(mo * 1e3, 4)}
             ao = flops_of(cfgo) / mo / 1e12
-            if other in ("s6_skinny", "s7_gemv"):
+            if other in ("s6_skinny", "s7_gemv", "s9_ax"):
                 nbytes = algorithmic_bytes(cfgo)
                 ent["roofline"] = {"bound": "hbm", "achieved": round(nbytes / mo / 1e9, 1),
                                    "peak": hbm_peak, "unit": "GB/s",
@@ -636,7 +639,8 @@ def with_summary_last(result, name):
     only the tail of the line still sees each workload's rate and fraction."""
     short = {"s1_128": "s1 128^3", "s2_2048": "s2 2048^3", "s3_4092": "s3 4092^3",
              "s4_rect": "s4 8192x6144x2048", "s5_odd": "s5 1023x1025x513",
-             "s6_skinny": "s6 16x8192x8192", "s7_gemv": "gemv 1x8192x8192"}
+             "s6_skinny": "s6 16x8192x8192", "s7_gemv": "gemv 1x8192x8192",
+             "s8_2049": "2049^3", "s9_ax": "Ax 8192x1x8192"}
     by_text = {v: k for k, v in WORKLOADS.items()}
     summary = {}
 

@@ -184,6 +184,11 @@ CONFIGS = {
     "s6_skinny": dict(M=16, N=8192, K=8192, alpha=1.0, beta=0.0, dist="uniform"),
     # one row of A: the decode-step GEMV (matrix-vector) case of the skinny regime
     "s7_gemv": dict(M=1, N=8192, K=8192, alpha=1.0, beta=0.0, dist="uniform"),
+    # one past the tile size in every dimension (the last tile row and column
+    # hold one useful row or column)
+    "s8_2049": dict(M=2049, N=2049, K=2049, alpha=1.0, beta=0.0, dist="uniform"),
+    # one column of B: the matrix-vector product A x
+    "s9_ax": dict(M=8192, N=1, K=8192, alpha=1.0, beta=0.0, dist="uniform"),
 }
 CONFIG_SEEDS = {name: 1000 + i for i, name in enumerate(CONFIGS)}
 

@@ -59,10 +59,11 @@ def check(M, N, K, alpha, beta, dist="uniform", seed=1, lda=None, ldb=None, ldc=
     return out
 
 
-# ----- the six workloads at full size, launched as the benchmark launches them ---
+# ----- every workload at full size, launched as the benchmark launches them ------
 
 @pytest.mark.parametrize("name", [
-    "s1_128", "s2_2048", "s3_4092", "s4_rect", "s5_odd", "s6_skinny", "s7_gemv",
+    "s1_128", "s2_2048", "s3_4092", "s4_rect", "s5_odd", "s6_skinny", "s7_gemv", "s8_2049",
+    "s9_ax",
 ])
 def test_workload_full_size(name):
     # Every element of every workload, launched as the benchmark launches it.
