@@ -452,10 +452,11 @@ int make_plan(const PlanInput &in, Plan *pl) {
     // bound by streaming B (M <= 16) or close to it; a tile of 64 or 128 rows
     // would spend 2-8x the multiply-adds (measured, 32 x 8192 x 8192: see the
     // planner sweep).
-    // Below about 2^20 elements of B the skinny kernel's start-up and fix-up
+    // Below about 2^21 elements of B the skinny kernel's start-up and fix-up
     // outweigh the streaming (32 x 32 x 32: 14.7 us against 6.9 on the
-    // small-product kernel), so the time model chooses there.
-    const bool big_b = in.N * in.K >= (int64_t(1) << 20);
+    // small-product kernel; 16 x 1024 x 1024: 21.5 against 20.5), so the time
+    // model chooses there.
+    const bool big_b = in.N * in.K >= (int64_t(1) << 21);
     if (tma_ok && (want == kVarSkinny || (want < 0 && in.M <= kSkinnyMaxM && big_b))) {
         // Persistent grid: every CTA the SMs hold at once.
         int64_t G = (in.num_sms > 0 ? in.num_sms : 1) * kSkinnyCtasPerSm;

@@ -314,7 +314,7 @@ UNIT_END = 6  # positions a range pays for each slab boundary it crosses
 
 @pytest.mark.parametrize("M,N,K", [(16, 8192, 8192), (1, 4096, 4096), (9, 3000, 720),
                                    (8, 100000, 64), (16, 10240, 320), (32, 8192, 8192),
-                                   (20, 3000, 500)])
+                                   (20, 3000, 800)])
 def test_skinny_plan(M, N, K):
     # M <= 16: the streaming kernel over 256-column slabs and 32-row positions,
     # the (slab, k) plane cut into contiguous ranges, one per CTA of a
