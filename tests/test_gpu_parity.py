@@ -387,7 +387,8 @@ def test_host_entry_point():
 
 
 @pytest.mark.parametrize("M,N,K,alpha,beta,blocks", [(3000, 1030, 4100, 0.5, 2.0, 4),
-                                                    (2048, 2056, 2048, 1.0, 0.0, 2)])
+                                                    (2048, 2056, 2048, 1.0, 0.0, 2),
+                                                    (2049, 2049, 2049, 1.0, 0.5, 2)])
 def test_host_entry_point_in_row_blocks(M, N, K, alpha, beta, blocks):
     # Large enough that the host entry point copies and computes row blocks in
     # a pipeline (4 blocks with a ragged last one; 2 blocks); pinned host
@@ -399,6 +400,30 @@ def test_host_entry_point_in_row_blocks(M, N, K, alpha, beta, blocks):
     sg.run_host(Ah, Bh, Ch, alpha=alpha, beta=beta)
     ref, bound = reference(M, N, K, alpha, beta, A, lda, B, ldb, C if beta else None, ldc)
     assert_within(Ch.numpy(), ref, bound, "sgemm_run_host in row blocks")
+
+
+def test_thin_edges_on_two_streams_at_once():
+    # Two streams, each with a product whose last row and column go to the
+    # edge kernels on the library's second stream: each result is its own.
+    M, N, K = 2049, 2049, 1000
+    outs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    data = []
+    for i, st in enumerate(streams):
+        A, lda, B, ldb, _, _ = inputs("ints", 120 + i, M, N, K, lda=K, ldb=N)
+        dA = torch.from_numpy(A).cuda()
+        dB = torch.from_numpy(B).cuda()
+        dC = torch.full((M * N,), float("nan"), device="cuda")
+        data.append((A, B, dA, dB, dC))
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for (A, B, dA, dB, dC), st in zip(data, streams):
+            assert sg.sgemm_run(M, N, K, 1.0, dA.data_ptr(), K, dB.data_ptr(), N, 0.0,
+                                dC.data_ptr(), N, st.cuda_stream) == 0
+    torch.cuda.synchronize()
+    for A, B, dA, dB, dC in data:
+        want = A.reshape(M, K).astype(np.float64) @ B.reshape(K, N).astype(np.float64)
+        assert np.array_equal(dC.cpu().numpy().reshape(M, N).astype(np.float64), want)
 
 
 def test_torch_binding_with_strided_rows():
