@@ -80,6 +80,7 @@ struct SkinnyLayout {
     static constexpr int at_floats = RPW * WarpPlan<MT>::mr;  // per warp: RPW k x mr m
     static constexpr int RED_ROWS = 2;          // rows of M per reduction round
     static constexpr int red_floats = WARPS * RED_ROWS * SBN;
+
     static constexpr size_t at_off = SSTAGES * stage_bytes;
     static constexpr size_t red_off = at_off + size_t(WARPS) * at_floats * 4;
     static constexpr size_t bar_off = red_off + size_t(red_floats) * 4;  // SSTAGES + 1 barriers
@@ -90,6 +91,7 @@ struct SkinnyLayout {
     // Fix-up through the idle ring: one piece is MT rows of a slot.
     static constexpr uint32_t piece_bytes = uint32_t(MT) * SBN * 4;
     static constexpr int ring_pieces = int(SSTAGES * stage_bytes / piece_bytes);
+
     static_assert(total <= 232448, "exceeds the 227 KB of shared memory a CTA may use");
     // The CTAs of one SM must fit its 228 KB together with 1 KB reserved each.
     static_assert(kSkinnyCtasPerSm * (total + 1024) <= 233472, "CTAs per SM do not fit");
@@ -166,6 +168,52 @@ struct Vec<2> {
         __stcg(reinterpret_cast<float2 *>(p), make_float2(v[0], v[1]));
     }
 };
+
+// Adds the warps' sums in warp order through `buf`, RR of each warp's rows
+// at a time.  Thread t ends with all MT rows of columns [OWN t, OWN t + OWN)
+// in fin; row m sums the warps that hold it (all warps, or with split rows
+// the warps of group m / MR).  Starts and ends with `buf` free to reuse.
+template <int MT, int RR>
+__device__ __forceinline__ void reduce_warps(const float2 (&acc)[WarpPlan<MT>::mr / 2][CPL],
+                                             float *buf, float (&fin)[MT][OWN], int warp, int lane,
+                                             int col0) {
+    constexpr int MR = WarpPlan<MT>::mr;
+    constexpr int SUMMED = WarpPlan<MT>::row_split ? WarpPlan<MT>::gwarps : WARPS;
+#pragma unroll
+    for (int r = 0; r < MR / RR; ++r) {
+#pragma unroll
+        for (int i = 0; i < RR; ++i) {
+            const int m = RR * r + i;
+#pragma unroll
+            for (int c = 0; c < CPL / 4; ++c) {
+                float4 v;
+                v.x = (m & 1) ? acc[m >> 1][4 * c + 0].y : acc[m >> 1][4 * c + 0].x;
+                v.y = (m & 1) ? acc[m >> 1][4 * c + 1].y : acc[m >> 1][4 * c + 1].x;
+                v.z = (m & 1) ? acc[m >> 1][4 * c + 2].y : acc[m >> 1][4 * c + 2].x;
+                v.w = (m & 1) ? acc[m >> 1][4 * c + 3].y : acc[m >> 1][4 * c + 3].x;
+                *reinterpret_cast<float4 *>(buf + (warp * RR + i) * SBN + c * 128 + lane * 4) = v;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int g = 0; g < WARPS / SUMMED; ++g) {
+#pragma unroll
+            for (int i = 0; i < RR; ++i) {
+                float sum[OWN], x[OWN];
+                Vec<OWN>::load(buf + ((g * SUMMED) * RR + i) * SBN + col0, sum);
+#pragma unroll
+                for (int w = 1; w < SUMMED; ++w) {
+                    Vec<OWN>::load(buf + ((g * SUMMED + w) * RR + i) * SBN + col0, x);
+#pragma unroll
+                    for (int o = 0; o < OWN; ++o) sum[o] += x[o];
+                }
+#pragma unroll
+                for (int o = 0; o < OWN; ++o) fin[g * MR + RR * r + i][o] = sum[o];
+            }
+        }
+        __syncthreads();
+    }
+}
 
 template <int MT>
 __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
@@ -324,97 +372,28 @@ __global__ void __launch_bounds__(SNT, kSkinnyCtasPerSm)
         }
 
         // ---- add the warps' sums in warp order ----
-        // Thread t owns columns [OWN t, OWN t + OWN) and all MT rows.  Round
-        // r brings rows RR r .. RR r + RR - 1 of every warp's MR rows
-        // through `red`; row m of C sums the warps that hold it (all warps,
-        // or with split rows the warps of group m / MR).
-        constexpr int RR = L::RED_ROWS;
-        constexpr int SUMMED = ROW_SPLIT ? GW : WARPS;  // warps holding a row
+        // The final unit has no copies outstanding, so the idle ring takes
+        // all rows of every warp at once (one barrier instead of two per
+        // pair of rows); other units use `red`, two rows per round.  (Same
+        // order of sums either way.)
+        static_assert(size_t(WARPS) * MR * SBN * 4 <= SSTAGES * L::stage_bytes,
+                      "the warps' sums fit the ring");
         float fin[MT][OWN];
-        if (q == q_total) {
-            // The CTA's final unit: every copy it issued has been consumed,
-            // so the idle ring takes all rows of every warp at once (one
-            // barrier instead of two per pair of rows; same order of sums).
-            static_assert(size_t(WARPS) * MR * SBN * 4 <= SSTAGES * L::stage_bytes,
-                          "the warps' sums fit the ring");
-            float *red_all = stages;
-#pragma unroll
-            for (int m = 0; m < MR; ++m) {
-#pragma unroll
-                for (int c = 0; c < CPL / 4; ++c) {
-                    float4 v;
-                    v.x = (m & 1) ? acc[m >> 1][4 * c + 0].y : acc[m >> 1][4 * c + 0].x;
-                    v.y = (m & 1) ? acc[m >> 1][4 * c + 1].y : acc[m >> 1][4 * c + 1].x;
-                    v.z = (m & 1) ? acc[m >> 1][4 * c + 2].y : acc[m >> 1][4 * c + 2].x;
-                    v.w = (m & 1) ? acc[m >> 1][4 * c + 3].y : acc[m >> 1][4 * c + 3].x;
-                    *reinterpret_cast<float4 *>(red_all + (warp * MR + m) * SBN + c * 128 +
-                                                lane * 4) = v;
-                }
-            }
-            __syncthreads();
-#pragma unroll
-            for (int g = 0; g < WARPS / SUMMED; ++g) {
-#pragma unroll
-                for (int m = 0; m < MR; ++m) {
-                    float sum[OWN], x[OWN];
-                    Vec<OWN>::load(red_all + ((g * SUMMED) * MR + m) * SBN + col0, sum);
-#pragma unroll
-                    for (int w = 1; w < SUMMED; ++w) {
-                        Vec<OWN>::load(red_all + ((g * SUMMED + w) * MR + m) * SBN + col0, x);
-#pragma unroll
-                        for (int o = 0; o < OWN; ++o) sum[o] += x[o];
-                    }
-#pragma unroll
-                    for (int o = 0; o < OWN; ++o) fin[g * MR + m][o] = sum[o];
-                }
-            }
-            __syncthreads();
-        } else {
-#pragma unroll
-        for (int r = 0; r < MR / RR; ++r) {
-#pragma unroll
-            for (int i = 0; i < RR; ++i) {
-                const int m = RR * r + i;
-#pragma unroll
-                for (int c = 0; c < CPL / 4; ++c) {
-                    float4 v;
-                    v.x = (m & 1) ? acc[m >> 1][4 * c + 0].y : acc[m >> 1][4 * c + 0].x;
-                    v.y = (m & 1) ? acc[m >> 1][4 * c + 1].y : acc[m >> 1][4 * c + 1].x;
-                    v.z = (m & 1) ? acc[m >> 1][4 * c + 2].y : acc[m >> 1][4 * c + 2].x;
-                    v.w = (m & 1) ? acc[m >> 1][4 * c + 3].y : acc[m >> 1][4 * c + 3].x;
-                    *reinterpret_cast<float4 *>(red + (warp * RR + i) * SBN + c * 128 + lane * 4) = v;
-                }
-            }
-            __syncthreads();
-#pragma unroll
-            for (int g = 0; g < WARPS / SUMMED; ++g) {
-#pragma unroll
-                for (int i = 0; i < RR; ++i) {
-                    float sum[OWN], x[OWN];
-                    Vec<OWN>::load(red + ((g * SUMMED) * RR + i) * SBN + col0, sum);
-#pragma unroll
-                    for (int w = 1; w < SUMMED; ++w) {
-                        Vec<OWN>::load(red + ((g * SUMMED + w) * RR + i) * SBN + col0, x);
-#pragma unroll
-                        for (int o = 0; o < OWN; ++o) sum[o] += x[o];
-                    }
-#pragma unroll
-                    for (int o = 0; o < OWN; ++o) fin[g * MR + RR * r + i][o] = sum[o];
-                }
-            }
-            __syncthreads();
-        }
-        }
+        if (q == q_total)
+            reduce_warps<MT, MR>(acc, stages, fin, warp, lane, col0);
+        else
+            reduce_warps<MT, L::RED_ROWS>(acc, red, fin, warp, lane, col0);
 
+        const bool partial = !(k0 == 0 && k1 == p.kt_total);
+        const int c_first = partial ? skinny_owner(p, slab * p.kt_total) : cta;
+        const int c_last = partial ? skinny_owner(p, slab * p.kt_total + p.kt_total - 1) : cta;
         bool write_c = true;
-        if (!(k0 == 0 && k1 == p.kt_total)) {
+        if (partial) {
             float *slot = p.partials + (size_t)skinny_slot<MT>(p, cta, slab) * (MT * SBN);
 #pragma unroll
             for (int m = 0; m < MT; ++m) Vec<OWN>::store_cg(slot + m * SBN + col0, fin[m]);
             __threadfence();
             __syncthreads();
-            const int c_first = skinny_owner(p, slab * p.kt_total);
-            const int c_last = skinny_owner(p, slab * p.kt_total + p.kt_total - 1);
             if (tid == 0) {
                 const int old = atomicAdd(&p.counters[slab], 1);
                 flags[1] = (old == c_last - c_first) ? 1 : 0;
