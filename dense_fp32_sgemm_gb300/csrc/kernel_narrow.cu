@@ -66,16 +66,27 @@ __device__ __forceinline__ void narrow_load_a(const float *a_step, int kn, int l
 }
 
 // B[k0 .. k0 + kch) transposed into bs (row stride kch + 4), zeros past K
-// and past N.  Element e = (kk, j), j fastest: consecutive threads read
-// consecutive columns of one row of B.
+// and past N, with 4-byte asynchronous copies (a source size of 0 writes the
+// zero): they take no registers, so all of a thread's copies are in flight
+// at once, and the chunk costs about one L2 round trip.  Thread t copies
+// column t % NN of rows t / NN, t / NN + NTH / NN, ...; consecutive threads
+// read consecutive columns of one row of B.  Returns once this thread's
+// copies have landed; the caller's barrier publishes them.
 template <int NN>
 __device__ __forceinline__ void narrow_stage_b(const NarrowParams &p, float *bs, int k0, int kch) {
+    static_assert(NTH % NN == 0, "a thread keeps its column");
+    constexpr int KSTEP = NTH / NN;  // rows of B between a thread's copies
     const int kn = min(kch, p.K - k0);
-    for (int e = threadIdx.x; e < kch * NN; e += NTH) {
-        const int kk = e / NN, j = e - (e / NN) * NN;
-        bs[j * (kch + 4) + kk] =
-            (kk < kn && j < p.N) ? __ldg(p.B + (long long)(k0 + kk) * p.ldb + j) : 0.0f;
+    const int j = threadIdx.x % NN;
+    const bool col_ok = j < p.N;
+    float *dst = bs + j * (kch + 4);
+    const float *src = p.B + (long long)k0 * p.ldb + j;
+    for (int kk = threadIdx.x / NN; kk < kch; kk += KSTEP) {
+        const bool ok = col_ok && kk < kn;
+        cp_async4(dst + kk, ok ? src + (long long)kk * p.ldb : p.B, ok ? 4u : 0u);
     }
+    cp_async_commit();
+    cp_async_wait<0>();
 }
 
 constexpr int PMAX = 4;  // passes of eight rows that share one staging of B
