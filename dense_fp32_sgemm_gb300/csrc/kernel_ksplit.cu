@@ -344,8 +344,11 @@ __global__ void __launch_bounds__(NT, 1) sgemm_ksplit_kernel(const __grid_consta
     __syncthreads();  // every group is done with the ring
 
     // The groups' sums, float4 (row, c4) of group g at S[g][row * ROW_F4 + c4].
+    // (Unrolled: each store takes its sums straight from registers; through
+    // the rolled switch of ks_f4 the write took 2.6 us at 1023 x 1025 x 513,
+    // unrolled 0.5 us.)
     float4 *S = reinterpret_cast<float4 *>(ring);
-#pragma unroll 1
+#pragma unroll
     for (int e4 = 0; e4 < 32; ++e4) {
         const int ri = e4 >> 1;  // r * 4 + i
         const int row = (ri >> 2) * 16 + ty * 4 + (ri & 3);

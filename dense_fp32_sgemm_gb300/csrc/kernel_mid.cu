@@ -371,12 +371,23 @@ __global__ void __launch_bounds__(MidCfg<BM>::NT, mid_ctas_per_sm(BM))
         }
 
         const int m0 = tm * BM, n0 = tn * MBN;
+        // The thread's sums go to its own part of the idle ring (float4 e4
+        // at e4 * NT + t, unrolled, straight from registers) and leave from
+        // there in rolled loops: a rolled loop over the registers needs a
+        // switch per float4 (2.6 us for a 64 x 128 tile in the split-K
+        // kernel), and fully unrolled stores make long code that runs once.
+        // No copy is in flight; the barrier waits for the last slice's reads.
+        __syncthreads();
+        float4 *own = reinterpret_cast<float4 *>(ring) + tid;
+        static_assert(Cf::TILE_FLOATS <= Cf::RING_FLOATS, "a tile of sums fits the ring");
+#pragma unroll
+        for (int e4 = 0; e4 < Cf::E4; ++e4) own[e4 * Cf::NT] = mid_f4(acc, e4);
         if (k0 == 0 && k1 == p.kt_total) {
-            // Whole tile: store straight from registers (a rolled loop: code
-            // that runs once per unit stays short).
+            // Whole tile: store.  (The next unit's barrier keeps these reads
+            // ahead of its copies.)
 #pragma unroll 1
             for (int e4 = 0; e4 < Cf::E4; ++e4)
-                mid_store4(p, m0 + mid_row<BM>(tid, e4), n0 + mid_col<BM>(tid, e4), mid_f4(acc, e4));
+                mid_store4(p, m0 + mid_row<BM>(tid, e4), n0 + mid_col<BM>(tid, e4), own[e4 * Cf::NT]);
             continue;
         }
         // Part of a stream-K tile: publish the piece (float4 e4 of thread t
@@ -386,7 +397,7 @@ __global__ void __launch_bounds__(MidCfg<BM>::NT, mid_ctas_per_sm(BM))
         float4 *slot = reinterpret_cast<float4 *>(p.partials +
                                                   (size_t)mid_slot(p, cta, t_sk) * Cf::TILE_FLOATS);
 #pragma unroll 1
-        for (int e4 = 0; e4 < Cf::E4; ++e4) __stcg(slot + e4 * Cf::NT + tid, mid_f4(acc, e4));
+        for (int e4 = 0; e4 < Cf::E4; ++e4) __stcg(slot + e4 * Cf::NT + tid, own[e4 * Cf::NT]);
         __threadfence();
         __syncthreads();  // also: every thread is done with the ring
         const int c_first = (t_sk * p.kt_total) / p.sk_share;
