@@ -228,10 +228,15 @@ sgemm_status_t run_skinny(DeviceState &d, const Plan &pl, int64_t M, int64_t N, 
 }
 
 // The narrow kernel over rows [0, M) and N <= kNarrowMaxN columns.
-sgemm_status_t run_narrow(int nn, int a_vec, int grid, int rows_per_cta, int64_t M, int64_t N,
-                          int64_t K, float alpha, const float *A, int64_t lda, const float *B,
-                          int64_t ldb, float beta, float *C, int64_t ldc, const Epilogue &epi,
-                          cudaStream_t stream) {
+sgemm_status_t run_narrow(DeviceState &d, int nn, int a_vec, int grid, int rows_per_cta, int64_t M,
+                          int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                          const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                          const Epilogue &epi, cudaStream_t stream) {
+    const int key = 4000 + nn * 10 + a_vec;
+    if (!d.configured_tiles.count(key)) {
+        if (narrow_configure(nn, a_vec) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        d.configured_tiles.insert(key);
+    }
     NarrowParams np;
     np.M = (int)M; np.N = (int)N; np.K = (int)K;
     np.alpha = alpha; np.beta = beta;
@@ -391,7 +396,7 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
                 const int a_vec =
                     ((reinterpret_cast<uintptr_t>(Ause) & 15u) == 0 && lda_use % 4 == 0) ? 4 : 1;
                 const int nn = pl.edge_n <= 1 ? 1 : pl.edge_n <= 2 ? 2 : 4;
-                s = run_narrow(nn, a_vec, grid, rows, M, pl.edge_n, K, alpha, Ause, lda_use,
+                s = run_narrow(d, nn, a_vec, grid, rows, M, pl.edge_n, K, alpha, Ause, lda_use,
                                Buse + N0, ldb_use, beta, C + N0, ldc, eepi, es);
             }
             if (s == SGEMM_OK && pl.edge_m > 0) {
@@ -481,7 +486,7 @@ sgemm_status_t run_locked(int64_t M, int64_t N, int64_t K, float alpha, const fl
             return run_skinny(d, pl, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, w, stream);
         }
         case kVarNarrow:
-            return run_narrow(pl.narrow_nn, pl.a_vec, pl.grid, pl.narrow_rows, M, N, K, alpha, A,
+            return run_narrow(d, pl.narrow_nn, pl.a_vec, pl.grid, pl.narrow_rows, M, N, K, alpha, A,
                               lda, B, ldb, beta, C, ldc, epi, stream);
         default:
             return SGEMM_ERR_UNSUPPORTED;

@@ -213,7 +213,23 @@ cudaError_t launch_impl(const NarrowParams &p, int grid, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <int NN, int AVEC>
+cudaError_t configure_impl() {
+    return cudaFuncSetAttribute(sgemm_narrow_kernel<NN, AVEC>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kNarrowSmemBytes);
+}
+
 }  // namespace
+
+cudaError_t narrow_configure(int nn, int a_vec) {
+#define SGEMM_NARROW_CONF(NN_, AV_) \
+    if (nn == NN_ && a_vec == AV_) return configure_impl<NN_, AV_>();
+    SGEMM_NARROW_CONF(1, 4) SGEMM_NARROW_CONF(1, 1)
+    SGEMM_NARROW_CONF(2, 4) SGEMM_NARROW_CONF(2, 1)
+    SGEMM_NARROW_CONF(4, 4) SGEMM_NARROW_CONF(4, 1)
+#undef SGEMM_NARROW_CONF
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_narrow(int nn, int a_vec, const NarrowParams &p, int grid, cudaStream_t stream) {
 #define SGEMM_NARROW_LAUNCH(NN_, AV_) \

@@ -153,7 +153,7 @@ cudaError_t ksplit_configure(int b_vec, int bn);
 // The bias of the epilogue is indexed from the first column of C passed.
 // ---------------------------------------------------------------------------
 constexpr int kNarrowMaxN = 4;
-constexpr size_t kNarrowSmemBytes = 48 * 1024;
+constexpr size_t kNarrowSmemBytes = 96 * 1024;  // two CTAs per SM fit with it
 // Chunk of K staged at once for nn columns.
 constexpr int narrow_kch(long long K, int nn) {
     const long long fit = ((long long)kNarrowSmemBytes / 4 / nn - 4) / 128 * 128;
@@ -176,6 +176,8 @@ struct NarrowParams {
 };
 
 cudaError_t launch_narrow(int nn, int a_vec, const NarrowParams &p, int grid, cudaStream_t stream);
+// Lets the form (nn, a_vec) use kNarrowSmemBytes of dynamic shared memory.
+cudaError_t narrow_configure(int nn, int a_vec);
 
 // ---------------------------------------------------------------------------
 // Small-product kernel: one CTA of 256 threads per 32 x 32 tile, four groups

@@ -43,14 +43,22 @@ struct KernelModel {
     double fixup_us;     // once, when some tile is split
     double piece_us;     // per extra piece of the most-split tile
     double shared_fixup_us;  // once more when the split CTAs share SMs
+    // Whole tiles only (no stream-K tail): slice time x dp_slice_scale and
+    // dp_wave_us more per wave of tiles (first copies, the store).
+    double dp_slice_scale;
+    double dp_wave_us;
 };
 constexpr double kLaunchUs = 6.1;
 // Tiled kernel: 2^20 multiply-adds per 128 x 256 x 32 slice, one CTA per SM;
 // split tiles 11 us once plus 2 us per extra piece of the most-split tile
 // (fitted over twelve shapes: 1536^3 with 2 pieces 131.5 us, 2048^3 with 3
 // 273 us, 1024^3 with 4 60.4 us, 1024 x 1024 x 8192 with 6 283 us, 768 x
-// 768 x 4096 with 8 104 us, 640 x 640 x 8192 with 8 178 us).
-constexpr KernelModel kTileModel = {kTileBM, kTileBN, kTileBK, 1, {0, 4.7, 0, 0, 0}, 11.0, 2.0, 0.0};
+// 768 x 4096 with 8 104 us, 640 x 640 x 8192 with 8 178 us).  Whole tiles
+// without a tail: 4.56 us a slice and 18 us a wave (one wave: 1000 x 3000 x
+// 231 66.5 us, 1024^3 172.3, 2048^3 317.4, 768 x 768 x 4096 608.3, 1024 x
+// 1024 x 8192 1190.9; two: 2049^3 635.9).
+constexpr KernelModel kTileModel = {kTileBM, kTileBN, kTileBK, 1, {0, 4.7, 0, 0, 0}, 11.0, 2.0, 0.0,
+                                    4.56 / 4.7, 18.0};
 // Mid-size kernel, 128 x 128 x 16 slices: 1.43 us alone on an SM (512^3,
 // 768^3, 100 x 5000 x 3000, 640 x 640 x 8192), 2.65 us per CTA with two per SM
 // (2048^3 with 304 CTAs of 108 slices: 305 us; 1280^3, 4096^3); fix-up
@@ -59,11 +67,13 @@ constexpr KernelModel kTileModel = {kTileBM, kTileBN, kTileBK, 1, {0, 4.7, 0, 0,
 // and 5 us more with two CTAs per SM, where a CTA's fix-up runs beside the
 // other's main loop (1280^3: 94.9 us, 2048 x 1024 x 1024: 96.7 us, 1400 x
 // 1300 x 512: 61 us, each with 4 pieces).
-constexpr KernelModel kMidModel = {128, kMidBN, kMidBK, 2, {0, 1.43, 2.65, 0, 0}, 4.0, 2.5, 5.0};
+constexpr KernelModel kMidModel = {128, kMidBN, kMidBK, 2, {0, 1.43, 2.65, 0, 0}, 4.0, 2.5, 5.0,
+                                   1.0, 0.0};
 // 64 x 128 x 16 slices, up to four CTAs per SM; a third or fourth CTA adds
 // no throughput (64 x 8192 x 8192: 304 CTAs of 108 slices 170 us, 456 CTAs of
 // 72 slices 211 us).
-constexpr KernelModel kMid64Model = {64, kMidBN, kMidBK, 4, {0, 1.0, 1.5, 2.65, 3.5}, 3.0, 1.5, 0.0};
+constexpr KernelModel kMid64Model = {64, kMidBN, kMidBK, 4, {0, 1.0, 1.5, 2.65, 3.5}, 3.0, 1.5, 0.0,
+                                     1.0, 0.0};
 // B in 4-byte copies (rows off 16 bytes) makes a mid-size slice slower
 // (2049^3: 2.93 us per slice against 2.77 at 2048^3) and each unit's first
 // copies slower to arrive: 1023 x 1025 x 513 (two units a CTA) took 51.2 us
@@ -75,18 +85,17 @@ constexpr double kMidUnalignedUnitUs = 3.5;
 // slices of 64 k.  Per wave: a fixed part (first copies, the groups' sums
 // added through shared memory, the store) and K / 64 slices plus a quarter
 // slice for the rounding of the last one.  64 x 128 tiles: 1024 x 1024 x 512
-// 31.2-32.8 us, 1024^3 53.7-54.8 us, 768 x 768 x 4096 188 us, 1024 x 1024 x
-// 8192 367 us, 3000 x 300 x 5000 237 us; B in 4-byte copies (rows off 16
-// bytes) about 1.2x a slice (1023^3 65.5 us, 1023 x 1025 x 513 38-40 us).
-// 64 x 64 tiles: 128^3 12.3 us, 256^3 14.8, 384^3 18.4, 512^3 23.2, 640^3
-// 24.6, 768^3 28.7; with B in 4-byte copies 1.35x a slice (255^3 18.4 us,
-// 511^3 26.6 us).
-constexpr double kKsSliceUs = 2.8;
-constexpr double kKsFixedUs = 3.5;
-constexpr double kKsUnalignedB = 1.2;
-constexpr double kKsSliceUs64 = 1.75;
+// 29.3 us, 640^3 34.8, 1024^3 52.0, 768 x 768 x 4096 188 us, 1024 x 1024 x
+// 8192 365 us; B in 4-byte copies (rows off 16 bytes) about 1.25x a slice
+// (1023^3 63.5 us, 1023 x 1025 x 513 35.7 us).  64 x 64 tiles: 512^3 21.2
+// us, 640^3 22.5, 768^3 26.6, 1024^3 (two waves) 60.1; with B in 4-byte
+// copies 1.3x a slice (511^3 24.6 us, 1023^3 71.7, 1025^3 72.5).
+constexpr double kKsSliceUs = 2.82;
+constexpr double kKsFixedUs = 1.0;
+constexpr double kKsUnalignedB = 1.25;
+constexpr double kKsSliceUs64 = 1.55;
 constexpr double kKsFixedUs64 = 1.5;
-constexpr double kKsUnalignedB64 = 1.35;
+constexpr double kKsUnalignedB64 = 1.3;
 constexpr double kNoScale[5] = {1, 1, 1, 1, 1};
 // 64 x 64 kernel, one tile per CTA and 16-k slices: 0.78 us per slice at up to
 // one CTA per SM (128^3: 12.3 us; 512^3: 30.9 us), growing with the CTAs an
@@ -175,7 +184,9 @@ static void plan_grid(const PlanInput &in, Plan *pl, bool allow_sk, bool force_s
     best.sk_share = 1;
     best.grid = (int)(T < G ? T : G);
     best.cost = (double)ceil_div(T, G) * (double)KT;
-    best.est_us = kLaunchUs + best.cost * slice_us(m, best.grid, sms, slice_scale);
+    best.est_us = kLaunchUs +
+                  best.cost * slice_us(m, best.grid, sms, slice_scale) * m.dp_slice_scale +
+                  (double)ceil_div(T, G) * m.dp_wave_us;
     best.reason = "whole tiles";
 
     const bool sk_fits = T * KT < (int64_t(1) << 30);
@@ -215,6 +226,8 @@ static void plan_grid(const PlanInput &in, Plan *pl, bool allow_sk, bool force_s
                 const int64_t pieces = ceil_div(KT + sh - gcd64(KT, sh), sh);
                 const int64_t max_pieces = pieces < ctas ? pieces : ctas;
                 const int64_t extra = max_pieces > 1 ? max_pieces - 1 : 0;
+                // A share that splits no tile is the whole-tile plan again.
+                if (extra == 0 && !force_sk) continue;
                 const int64_t grid = dp > 0 ? G : ctas;
                 const double cost = (double)d * KT + (double)sh + piece_slices * (double)extra;
                 const double est =

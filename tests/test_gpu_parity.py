@@ -242,8 +242,10 @@ def test_narrow_kernel_integers_bit_exact(N, M, K, lda_pad, off):
     assert np.array_equal(out.astype(np.int64), want)
 
 
-@pytest.mark.parametrize("M,N,K", [(8192, 1, 4096), (3000, 4, 2049), (64, 3, 20000), (7, 2, 5)])
+@pytest.mark.parametrize("M,N,K", [(8192, 1, 4096), (3000, 4, 2049), (64, 3, 20000), (7, 2, 5),
+                                   (40, 2, 30000), (33, 1, 50000)])
 def test_narrow_kernel_floats_within_bound(M, N, K):
+    # K of 20000-50000 takes several chunks of B for every column count.
     check(M, N, K, 0.5, -2.0, dist="normal", seed=90 + M, lda=K, ldb=N, ldc=N, variant=7)
     check(M, N, K, 1.0, 0.0, dist="uniform", seed=91 + M, lda=K + 1, ldb=N + 3, ldc=N + 1,
           offsets=(1, 0, 2))
