@@ -83,3 +83,18 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_timing_rule_follows_the_operand_size():
+    # Workloads whose operands are larger than L2 (129 MB) run back to back
+    # without a flush; the others are flushed before every step.  The rule
+    # and the config note the line carries agree, and both arms share them.
+    streamed = {n for n in bench.WORKLOADS if bench.streams_past_l2(bench.datagen.CONFIGS[n])}
+    assert {"s3_4092", "s4_rect", "s6_skinny", "s7_gemv", "s9_ax"} <= streamed
+    assert not streamed & {"s1_128", "s2_2048", "s5_odd", "s8_2049"}
+    for n in bench.WORKLOADS:
+        cfg = bench.datagen.CONFIGS[n]
+        big = bench.algorithmic_bytes(cfg) > bench.L2_BYTES_GB300
+        assert (n in streamed) == big
+        note = bench.workload_config(n)["l2"]
+        assert ("back to back" in note) == big and ("flushed before every timed step" in note) != big
