@@ -226,8 +226,8 @@ __device__ __forceinline__ void ks_compute_part(const KsFrag<BN> &f, int k0, int
 }
 
 // Float4 number e4 (0..31) of a thread's sums: row e4 / 2 of its sixteen,
-// columns (e4 % 2) * 32 + tx * 4 .. + 3.  A switch keeps the sums in
-// registers while the caller's loop over e4 stays rolled.
+// columns (e4 % 2) * 32 + tx * 4 .. + 3.  Called with e4 known after
+// unrolling, the switch folds away and the sums stay in registers.
 __device__ __forceinline__ float4 ks_f4(const KsAcc &acc, int e4) {
     switch (e4) {
 #define SGEMM_KS_E4(E)                                                                     \

@@ -246,8 +246,8 @@ __device__ __forceinline__ void compute_slice(const float *st, MidAcc &acc, int 
 }
 
 // Float4 number e4 (0..31) of a thread's sums: row e4 / 2 of its sixteen,
-// columns (e4 % 2) * 32 + tx * 4 .. + 3.  A switch keeps the sums in
-// registers while a caller's loop over e4 stays rolled.
+// columns (e4 % 2) * 32 + tx * 4 .. + 3.  Called with e4 known after
+// unrolling, the switch folds away and the sums stay in registers.
 __device__ __forceinline__ float4 mid_f4(const MidAcc &acc, int e4) {
     switch (e4) {
 #define SGEMM_MID_E4(E)                                                                     \
