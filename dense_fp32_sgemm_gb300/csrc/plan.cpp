@@ -71,8 +71,9 @@ constexpr KernelModel kMidModel = {128, kMidBN, kMidBK, 2, {0, 1.43, 2.65, 0, 0}
                                    1.0, 0.0};
 // 64 x 128 x 16 slices, up to four CTAs per SM; a third or fourth CTA adds
 // no throughput (64 x 8192 x 8192: 304 CTAs of 108 slices 170 us, 456 CTAs of
-// 72 slices 211 us).
-constexpr KernelModel kMid64Model = {64, kMidBN, kMidBK, 4, {0, 1.0, 1.5, 2.65, 3.5}, 3.0, 1.5, 0.0,
+// 72 slices 211 us); 3 us per extra piece (40 x 40 x 4000, one tile in eight
+// pieces: 64.3 us).
+constexpr KernelModel kMid64Model = {64, kMidBN, kMidBK, 4, {0, 1.0, 1.5, 2.65, 3.5}, 3.0, 3.0, 0.0,
                                      1.0, 0.0};
 // B in 4-byte copies (rows off 16 bytes) makes a mid-size slice slower
 // (2049^3: 2.93 us per slice against 2.77 at 2048^3) and each unit's first
