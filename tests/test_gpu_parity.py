@@ -500,7 +500,7 @@ EPI_CASES = [  # (M, N, K, variant, splits): every kernel and the alpha == 0 pat
     (257, 1030, 2048, -1, 0), (9, 1030, 1000, 3, 0), (16, 1024, 96, 3, 2),
     (300, 520, 256, 4, 0), (301, 1030, 700, 4, 3), (40, 1030, 500, 5, 2),
     (300, 520, 256, 6, 0), (1023, 1030, 513, 6, 0), (300, 520, 256, 8, 0), (129, 70, 70, 8, 0),
-    (130, 300, 96, 9, 0), (33, 65, 200, 9, 0),
+    (130, 300, 96, 9, 0), (33, 65, 200, 9, 0), (500, 3, 300, 7, 0), (64, 4, 3000, 7, 0),
 ]
 
 
