@@ -193,6 +193,18 @@ def test_split_k_kernel_is_bitwise_deterministic(variant):
         assert np.array_equal(first, again)
 
 
+@pytest.mark.parametrize("M,N,K,variant", [(3000, 4, 20000, 7), (2050, 2052, 700, -1)])
+def test_narrow_and_thin_edge_plans_are_bitwise_deterministic(M, N, K, variant):
+    # The narrow kernel's lanes add their k in a fixed order and the warp adds
+    # the lanes by a fixed butterfly; a thin-edge plan runs three kernels on
+    # two streams, each deterministic, with no shared output element.
+    A, lda, B, ldb, _, _ = inputs("uniform", 64, M, N, K, lda=K, ldb=N)
+    first, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, variant=variant)
+    for _ in range(3):
+        again, _ = run_gemm(M, N, K, 1.0, 0.0, A, lda, B, ldb, None, N, variant=variant)
+        assert np.array_equal(first, again)
+
+
 @pytest.mark.parametrize("variant", [6, 8, 9])
 @pytest.mark.parametrize("K", [1, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 129])
 def test_split_k_kernel_every_k_remainder(K, variant):
