@@ -213,6 +213,9 @@ cudaError_t launch_impl(const NarrowParams &p, int grid, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// No carveout preference: A's 16-byte loads go through L1, and with the
+// largest shared-memory carveout (L1 shrunk to its minimum) 8192 x 1 x 8192
+// took 53.2 us against 49.2, 8192 x 4 x 8192 67.6 against 58.9.
 template <int NN, int AVEC>
 cudaError_t configure_impl() {
     return cudaFuncSetAttribute(sgemm_narrow_kernel<NN, AVEC>,
