@@ -36,6 +36,21 @@ constexpr int NTH = NW * 32;
 constexpr int KI = 8;            // 4-k groups a lane loads per step
 constexpr int STEP = 128 * KI;   // k per step of a warp: 1024
 
+// The full steps' 16-byte loads of A, which is read once: through the
+// non-coherent path without allocating in L1 (8192 x 1 x 8192: 47.1-48.1 us
+// against 48.8-49.1 with L1 allocation; 8192 x 4 x 8192 57.3-57.6 against
+// 58.9).  Volatile, so that no load is moved ahead
+// of the check that the whole step lies inside the row.  The bounds-checked
+// loads of a row's last step keep __ldg: as volatile predicated loads they made
+// 100000 x 1 x 1000 (every row a single short step) 88 us against 73.
+__device__ __forceinline__ float4 ld_stream_f4(const float *p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 // A lane's A values of one step: a[i] holds k = 4 lane + 128 i + (0..3) of
 // the step (zeros past kn).  Full steps load without bounds checks, so all KI
 // loads of a lane are in flight together.
@@ -47,7 +62,7 @@ __device__ __forceinline__ void narrow_load_a(const float *a_step, int kn, int l
         for (int i = 0; i < KI; ++i) {
             const float *q = a_step + 4 * lane + 128 * i;
             if (AVEC == 4) {
-                a[i] = __ldg(reinterpret_cast<const float4 *>(q));
+                a[i] = ld_stream_f4(q);
             } else {
                 a[i] = make_float4(__ldg(q), __ldg(q + 1), __ldg(q + 2), __ldg(q + 3));
             }
