@@ -121,6 +121,10 @@ def tile_invariants(p, M, N, K, forced_sk=False):
         # pieces per tile stay within what the idle ring combines (nine)
         assert share >= math.ceil(kt / 8)
         assert (kt + share - 2) // share + 1 <= 9
+        # an automatic stream-K tail splits some tile: a share of whole tiles
+        # is the whole-tile plan, which carries its own cost per wave
+        if not forced_sk:
+            assert share % kt != 0
     # the chosen cost never exceeds the data-parallel cost (a forced stream-K
     # split takes the first candidate)
     if not forced_sk:
