@@ -50,24 +50,24 @@ struct KernelModel {
 };
 constexpr double kLaunchUs = 6.1;
 // Tiled kernel: 2^20 multiply-adds per 128 x 256 x 32 slice, one CTA per SM;
-// split tiles 11 us once plus 2 us per extra piece of the most-split tile
+// split tiles 14 us once plus 2 us per extra piece of the most-split tile
 // (fitted over twelve shapes: 1536^3 with 2 pieces 131.5 us, 2048^3 with 3
 // 273 us, 1024^3 with 4 60.4 us, 1024 x 1024 x 8192 with 6 283 us, 768 x
 // 768 x 4096 with 8 104 us, 640 x 640 x 8192 with 8 178 us).  Whole tiles
 // without a tail: 4.56 us a slice and 18 us a wave (one wave: 1000 x 3000 x
 // 231 66.5 us, 1024^3 172.3, 2048^3 317.4, 768 x 768 x 4096 608.3, 1024 x
 // 1024 x 8192 1190.9; two: 2049^3 635.9).
-constexpr KernelModel kTileModel = {kTileBM, kTileBN, kTileBK, 1, {0, 4.7, 0, 0, 0}, 11.0, 2.0, 0.0,
+constexpr KernelModel kTileModel = {kTileBM, kTileBN, kTileBK, 1, {0, 4.7, 0, 0, 0}, 14.0, 2.0, 0.0,
                                     4.56 / 4.7, 18.0};
 // Mid-size kernel, 128 x 128 x 16 slices: 1.43 us alone on an SM (512^3,
-// 768^3, 100 x 5000 x 3000, 640 x 640 x 8192), 2.65 us per CTA with two per SM
+// 768^3, 100 x 5000 x 3000, 640 x 640 x 8192), 2.58 us per CTA with two per SM
 // (2048^3 with 304 CTAs of 108 slices: 305 us; 1280^3, 4096^3); fix-up
 // through the ring 4 us plus 2.5 us per
 // extra piece (1024 x 1024 x 512 with 2 and 4 pieces: 37.3 and 39.4 us),
 // and 5 us more with two CTAs per SM, where a CTA's fix-up runs beside the
 // other's main loop (1280^3: 94.9 us, 2048 x 1024 x 1024: 96.7 us, 1400 x
 // 1300 x 512: 61 us, each with 4 pieces).
-constexpr KernelModel kMidModel = {128, kMidBN, kMidBK, 2, {0, 1.43, 2.65, 0, 0}, 4.0, 2.5, 5.0,
+constexpr KernelModel kMidModel = {128, kMidBN, kMidBK, 2, {0, 1.43, 2.58, 0, 0}, 4.0, 2.5, 5.0,
                                    1.0, 0.0};
 // 64 x 128 x 16 slices, up to four CTAs per SM; a third or fourth CTA adds
 // no throughput (64 x 8192 x 8192: 304 CTAs of 108 slices 170 us, 456 CTAs of
@@ -87,16 +87,16 @@ constexpr double kMidUnalignedUnitUs = 3.5;
 // added through shared memory, the store) and K / 64 slices plus a quarter
 // slice for the rounding of the last one.  64 x 128 tiles: 1024 x 1024 x 512
 // 29.3 us, 640^3 34.8, 1024^3 52.0, 768 x 768 x 4096 188 us, 1024 x 1024 x
-// 8192 365 us; B in 4-byte copies (rows off 16 bytes) about 1.25x a slice
-// (1023^3 63.5 us, 1023 x 1025 x 513 35.7 us).  64 x 64 tiles: 512^3 21.2
-// us, 640^3 22.5, 768^3 26.6, 1024^3 (two waves) 60.1; with B in 4-byte
-// copies 1.3x a slice (511^3 24.6 us, 1023^3 71.7, 1025^3 72.5).
+// 8192 365 us; B in 4-byte copies (rows off 16 bytes) about 1.18x a slice
+// (1023^3 60-61 us, 1023 x 1025 x 513 35.3 us).  64 x 64 tiles: 512^3 21.2
+// us, 640^3 22.5, 768^3 26.6, 1024^3 (two waves) 60.1, 768 x 768 x 4096
+// 112; with B in 4-byte copies 1.15x a slice (511^3 24.6 us, 1025^3 67.6).
 constexpr double kKsSliceUs = 2.82;
 constexpr double kKsFixedUs = 1.0;
-constexpr double kKsUnalignedB = 1.25;
-constexpr double kKsSliceUs64 = 1.55;
+constexpr double kKsUnalignedB = 1.18;
+constexpr double kKsSliceUs64 = 1.6;
 constexpr double kKsFixedUs64 = 1.5;
-constexpr double kKsUnalignedB64 = 1.3;
+constexpr double kKsUnalignedB64 = 1.15;
 constexpr double kNoScale[5] = {1, 1, 1, 1, 1};
 // 64 x 64 kernel, one tile per CTA and 16-k slices: 0.78 us per slice at up to
 // one CTA per SM (128^3: 12.3 us; 512^3: 30.9 us), growing with the CTAs an
